@@ -1,0 +1,186 @@
+"""The fp64 CPU oracle for the ragged-M grouped GEMM (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s ``cpu_baseline``
+and ``--impl reference`` legs may import this package.  The CUDA library never
+imports, links or calls it, and it imports nothing from the CUDA library: the
+two sides share only the seeded input generators in
+``ragged_grouped_gemm_02_gb300.workloads``, which hold none of the method's
+arithmetic.
+
+The arithmetic lives in ``rgg_oracle.c`` (plain C, fp64, OpenMP); this module
+compiles it with gcc on first use and wraps it with numpy.  Every function
+cites the page passage it follows; see the header of ``rgg_oracle.c``.
+
+Inputs are numpy arrays of bf16 *bit patterns* (``uint16``), so the oracle sees
+exactly the bf16-rounded values the GPU receives.
+
+Parity status: every function here is pinned by ``tests/test_oracle.py``
+against the pages' printed figures, exact rational arithmetic, a library
+special case, integer-exact cases and the invariants the pages fix.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rgg_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "librgg_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ORACLE_OK = 0
+ORACLE_ERR_INVALID_ARG = 1
+ORACLE_ERR_BAD_OFFSETS = 4
+
+
+def build(force: bool = False) -> str:
+    """Compile ``rgg_oracle.c`` into ``librgg_oracle.so`` next to it."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-std=c11",
+           "-Wall", "-Wextra", "-o", tmp, _SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64 = ctypes.c_int32, ctypes.c_int64
+        lib.rgg_oracle_check_offsets.argtypes = [P, ctypes.c_int, i64]
+        lib.rgg_oracle_check_offsets.restype = ctypes.c_int
+        lib.rgg_oracle_grouped_gemm.argtypes = [P, P, P, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
+        lib.rgg_oracle_grouped_gemm.restype = ctypes.c_int
+        lib.rgg_oracle_grouped_gemm_points.argtypes = [P, P, P, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int,
+                                                       P, P, i64, P, ctypes.c_int]
+        lib.rgg_oracle_grouped_gemm_points.restype = ctypes.c_int
+        lib.rgg_oracle_tile_list.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, i64]
+        lib.rgg_oracle_tile_list.restype = i64
+        lib.rgg_oracle_row_utilisation.argtypes = [P, ctypes.c_int, ctypes.c_int]
+        lib.rgg_oracle_row_utilisation.restype = ctypes.c_double
+        lib.rgg_oracle_max_threads.argtypes = []
+        lib.rgg_oracle_max_threads.restype = ctypes.c_int
+        del i32
+        _lib = lib
+        return lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _as_bits(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("bf16 operands are passed as uint16 bit patterns, got %s" % a.dtype)
+    return a
+
+
+def _as_offsets(off) -> np.ndarray:
+    off = np.ascontiguousarray(np.asarray(off, dtype=np.int64))
+    if off.ndim != 1 or off.size < 2:
+        raise ValueError("group offsets must be a 1-D array of E+1 entries")
+    if off.min() < -(2 ** 31) or off.max() >= 2 ** 31:
+        raise ValueError("group offsets must fit int32")
+    return off.astype(np.int32)
+
+
+def max_threads() -> int:
+    return int(_load().rgg_oracle_max_threads())
+
+
+def check_offsets(off, M_tot: int) -> int:
+    """0 when the offsets are valid (0 <= off[0] <= ... <= off[E] <= M_tot), else 4."""
+    off = _as_offsets(off)
+    return int(_load().rgg_oracle_check_offsets(_ptr(off), off.size - 1, int(M_tot)))
+
+
+def grouped_gemm(X_bits: np.ndarray, W_bits: np.ndarray, off, nthreads: int = 0,
+                 out: np.ndarray | None = None) -> np.ndarray:
+    """Y = X_e . W_e for every expert, in fp64 (worklog, "What I am measuring").
+
+    X_bits: uint16 [M_tot, K]; W_bits: uint16 [E, K, N]; off: int [E+1].
+    Rows that belong to no expert keep the value they had in ``out`` (NaN
+    when ``out`` is not given), so tests can see that nothing wrote them.
+    """
+    X_bits, W_bits, off = _as_bits(X_bits), _as_bits(W_bits), _as_offsets(off)
+    if X_bits.ndim != 2 or W_bits.ndim != 3:
+        raise ValueError("X must be [M_tot, K] and W [E, K, N]")
+    M_tot, K = X_bits.shape
+    E, K2, N = W_bits.shape
+    if K2 != K or off.size != E + 1:
+        raise ValueError("shape mismatch: X %s, W %s, offsets %d" % (X_bits.shape, W_bits.shape, off.size))
+    if out is None:
+        out = np.full((M_tot, N), np.nan, dtype=np.float64)
+    if out.shape != (M_tot, N) or out.dtype != np.float64 or not out.flags.c_contiguous:
+        raise ValueError("out must be a C-contiguous float64 [M_tot, N] array")
+    rc = _load().rgg_oracle_grouped_gemm(_ptr(X_bits), _ptr(W_bits), _ptr(off), E, M_tot, K, N,
+                                         _ptr(out), int(nthreads))
+    if rc != ORACLE_OK:
+        raise OracleError("oracle rejected the arguments (code %d)" % rc)
+    return out
+
+
+def grouped_gemm_points(X_bits: np.ndarray, W_bits: np.ndarray, off, rows, cols,
+                        nthreads: int = 0) -> np.ndarray:
+    """The same definition at chosen outputs (rows[p], cols[p]) only; NaN where
+    the row belongs to no expert."""
+    X_bits, W_bits, off = _as_bits(X_bits), _as_bits(W_bits), _as_offsets(off)
+    M_tot, K = X_bits.shape
+    E, _, N = W_bits.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int32))
+    if rows.shape != cols.shape or rows.ndim != 1:
+        raise ValueError("rows and cols must be 1-D and of equal length")
+    out = np.empty(rows.size, dtype=np.float64)
+    rc = _load().rgg_oracle_grouped_gemm_points(_ptr(X_bits), _ptr(W_bits), _ptr(off), E, M_tot, K, N,
+                                                _ptr(rows), _ptr(cols), rows.size, _ptr(out), int(nthreads))
+    if rc != ORACLE_OK:
+        raise OracleError("oracle rejected the arguments (code %d)" % rc)
+    return out
+
+
+def tile_list(off, N: int, BM: int, BN: int) -> np.ndarray:
+    """The worklog's flat tile list (section 2): int32 [T, 4] rows of
+    (expert, row0, rows, col0), expert-major, then M tile, then N tile."""
+    off = _as_offsets(off)
+    lib = _load()
+    T = lib.rgg_oracle_tile_list(_ptr(off), off.size - 1, int(N), int(BM), int(BN), None, 0)
+    if T < 0:
+        raise OracleError("oracle rejected the tile-list arguments")
+    desc = np.zeros((max(T, 1), 4), dtype=np.int32)
+    T2 = lib.rgg_oracle_tile_list(_ptr(off), off.size - 1, int(N), int(BM), int(BN), _ptr(desc), T)
+    assert T2 == T
+    return desc[:T]
+
+
+def tile_count(off, N: int, BM: int, BN: int) -> int:
+    off = _as_offsets(off)
+    T = _load().rgg_oracle_tile_list(_ptr(off), off.size - 1, int(N), int(BM), int(BN), None, 0)
+    if T < 0:
+        raise OracleError("oracle rejected the tile-list arguments")
+    return int(T)
+
+
+def row_utilisation(off, BM: int) -> float:
+    """eta of worklog section 2.1: sum m_e / (BM * sum ceil(m_e / BM))."""
+    off = _as_offsets(off)
+    v = _load().rgg_oracle_row_utilisation(_ptr(off), off.size - 1, int(BM))
+    if v < 0:
+        raise OracleError("oracle rejected the row-utilisation arguments")
+    return float(v)

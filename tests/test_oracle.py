@@ -1,0 +1,262 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+The oracle is only trusted because these tests tie it to things other than
+itself:
+
+* figures the worklog prints ("Grouped GEMM for Imbalanced Experts on
+  Blackwell: A WIP Worklog"): descriptor counts, the s=1.2 skew extremes,
+  eta waste percentages, eta-scaled estimates (tests/golden/worklog_figures.json);
+* a hand-worked tile list for the 4-expert case, written out below from the
+  enumeration rule of the worklog's section 2;
+* exact rational arithmetic on tiny inputs (the fp64 sum must sit within the
+  textbook error bound of the exact value);
+* a library special case (one expert is a plain GEMM: numpy float64 matmul);
+* integer-valued inputs, where every partial sum is an exact integer and the
+  result must equal numpy's int64 product bit for bit;
+* the invariants the pages fix: experts are independent GEMMs, rows of no
+  expert are untouched, permuting the experts permutes the output blocks.
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from ragged_grouped_gemm_02_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worklog_figures.json")
+
+
+def _figures():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def _counts(routing, M, E=64):
+    if routing == "uniform":
+        return np.full(E, M // E, dtype=np.int64)
+    if routing == "worklog_skew":
+        return wl.power_law_counts_first_experts(M, E, 1.2)
+    raise ValueError(routing)
+
+
+# ----------------------------------------------------------------- tile list
+
+@pytest.mark.parametrize("entry", _figures()["tile_counts"], ids=lambda e: "%s-%d-%dx%d" % (
+    e["routing"], e["M"], e["BM"], e["BN"]))
+def test_tile_counts_match_worklog(oracle_mod, entry):
+    off = wl.offsets_from_counts(_counts(entry["routing"], entry["M"], entry["E"]))
+    assert oracle_mod.tile_count(off, entry["N"], entry["BM"], entry["BN"]) == entry["tiles"], entry["cite"]
+    assert oracle_mod.tile_list(off, entry["N"], entry["BM"], entry["BN"]).shape[0] == entry["tiles"]
+
+
+def test_skew_split_extremes_match_worklog():
+    f = _figures()["skew_extremes"]
+    c = wl.power_law_counts_first_experts(f["M"], f["E"], f["s"])
+    assert c.sum() == f["M"]
+    assert c.max() == f["max_rows"] and c.min() == f["min_rows"], f["cite"]
+    # the skew is monotone in the expert index
+    assert (np.diff(c) <= 0).all()
+
+
+def test_tiny_tile_list_worked_by_hand(oracle_mod):
+    # m = [37, 0, 64, 155], N = 512, BM = BN = 128 -> offsets [0, 37, 37, 101, 256].
+    # Worklog section 2: for e, for mt < ceil(m_e/BM), for nt < ceil(N/BN):
+    #   {e, off[e] + mt*BM, min(BM, m_e - mt*BM), nt*BN}
+    # expert 0: one M tile of 37 rows; expert 1: nothing; expert 2: one tile of
+    # 64 rows starting at row 37; expert 3: rows 101..228 (128) then 229..255 (27).
+    expected = []
+    for e, row0, rows in [(0, 0, 37), (2, 37, 64), (3, 101, 128), (3, 229, 27)]:
+        for col0 in (0, 128, 256, 384):
+            expected.append((e, row0, rows, col0))
+    got = oracle_mod.tile_list([0, 37, 37, 101, 256], 512, 128, 128)
+    assert [tuple(r) for r in got.tolist()] == expected
+    # the same experts with BM = 64, BN = 256: expert 3 now splits into rows
+    # 101..164, 165..228 and 229..255 (27), each over the N tiles at 0 and 256
+    expected = []
+    for e, row0, rows in [(0, 0, 37), (2, 37, 64), (3, 101, 64), (3, 165, 64), (3, 229, 27)]:
+        for col0 in (0, 256):
+            expected.append((e, row0, rows, col0))
+    got = oracle_mod.tile_list([0, 37, 37, 101, 256], 512, 64, 256)
+    assert [tuple(r) for r in got.tolist()] == expected
+
+
+def test_tile_list_edge_cases(oracle_mod):
+    # all experts empty: no tiles at all
+    assert oracle_mod.tile_count([0, 0, 0, 0], 512, 128, 128) == 0
+    assert oracle_mod.tile_list([0, 0, 0], 512, 64, 128).shape == (0, 4)
+    # N not a multiple of BN: the last N tile is partial but still one tile
+    t = oracle_mod.tile_list([0, 1], 520, 128, 256)
+    assert [tuple(r) for r in t.tolist()] == [(0, 0, 1, 0), (0, 0, 1, 256), (0, 0, 1, 512)]
+    # exact multiples produce no empty trailing tile
+    t = oracle_mod.tile_list([0, 128, 384], 128, 128, 128)
+    assert [tuple(r) for r in t.tolist()] == [(0, 0, 128, 0), (1, 128, 128, 0), (1, 256, 128, 0)]
+    # rows beyond off[E] (spare rows) are never tiled
+    assert oracle_mod.tile_count([5, 10], 64, 64, 64) == 1
+    assert oracle_mod.tile_list([5, 10], 64, 64, 64).tolist() == [[0, 5, 5, 0]]
+
+
+def test_tile_list_rejects_bad_offsets(oracle_mod):
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.tile_list([0, 10, 5], 64, 64, 64)
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.tile_list([-1, 10], 64, 64, 64)
+
+
+# --------------------------------------------------------- row utilisation
+
+@pytest.mark.parametrize("entry", _figures()["eta_waste_percent"], ids=lambda e: "%s-%d-BM%d" % (
+    e["routing"], e["M"], e["BM"]))
+def test_eta_waste_matches_worklog(oracle_mod, entry):
+    off = wl.offsets_from_counts(_counts(entry["routing"], entry["M"]))
+    eta = oracle_mod.row_utilisation(off, entry["BM"])
+    assert round(100.0 * (1.0 - eta), 1) == entry["waste"], entry["cite"]
+
+
+@pytest.mark.parametrize("entry", _figures()["eta_estimates"], ids=lambda e: "%s-%d" % (e["routing"], e["M"]))
+def test_eta_scaled_estimate_matches_worklog(oracle_mod, entry):
+    off = wl.offsets_from_counts(_counts(entry["routing"], entry["M"]))
+    eta = oracle_mod.row_utilisation(off, entry["BM"])
+    assert round(eta, 3) == entry["eta_3dp"], entry["cite"]
+    assert round(entry["balanced_tflops"] * round(eta, 3), 1) == entry["estimate"], entry["cite"]
+
+
+def test_eta_edge_cases(oracle_mod):
+    assert oracle_mod.row_utilisation([0, 0, 0], 128) == 1.0
+    assert oracle_mod.row_utilisation([0, 128, 256], 128) == 1.0
+    assert oracle_mod.row_utilisation([0, 1], 128) == 1.0 / 128
+
+
+# ------------------------------------------------------------- the product
+
+def _exact(x_bits, w_bits, off):
+    """Exact rational Y for tiny inputs, the definition with Fractions."""
+    M, K = x_bits.shape
+    E, _, N = w_bits.shape
+    xf = x_bits.astype(np.uint32) << 16
+    wf = w_bits.astype(np.uint32) << 16
+    xv = xf.view(np.float32)
+    wv = wf.view(np.float32)
+    out = {}
+    absum = {}
+    for e in range(E):
+        for i in range(off[e], off[e + 1]):
+            for j in range(N):
+                terms = [Fraction(float(xv[i, k])) * Fraction(float(wv[e, k, j])) for k in range(K)]
+                out[(i, j)] = sum(terms, Fraction(0))
+                absum[(i, j)] = sum(abs(t) for t in terms)
+    return out, absum
+
+
+def test_matches_exact_rational_arithmetic(oracle_mod):
+    inp = wl.make_custom([2, 0, 3, 1], K=24, N=10, seed=11, spare_rows=2)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    Y = oracle_mod.grouped_gemm(xb, wb, inp.offsets)
+    exact, absum = _exact(xb, wb, inp.offsets)
+    K = xb.shape[1]
+    for (i, j), v in exact.items():
+        bound = K * 2.0 ** -52 * float(absum[(i, j)]) + 1e-300
+        assert abs(Y[i, j] - float(v)) <= bound, (i, j, Y[i, j], float(v))
+    # the two spare rows belong to no expert and keep the NaN canary
+    assert np.isnan(Y[6:]).all()
+
+
+def test_single_expert_is_plain_gemm(oracle_mod):
+    inp = wl.make_custom([77], K=96, N=40, seed=12)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    Y = oracle_mod.grouped_gemm(xb, wb, inp.offsets)
+    ref = inp.X.double().numpy() @ inp.W[0].double().numpy()
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_integer_inputs_are_exact(oracle_mod):
+    # entries in {-2..2}, K = 64: every partial sum is an integer of magnitude <= 256
+    counts = [3, 0, 9, 1, 5]
+    inp = wl.make_custom(counts, K=64, N=24, seed=13, integer_valued=True)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    Y = oracle_mod.grouped_gemm(xb, wb, inp.offsets)
+    Xi = inp.X.to(torch.int64).numpy()
+    Wi = inp.W.to(torch.int64).numpy()
+    off = inp.offsets
+    for e in range(len(counts)):
+        ref = Xi[off[e]:off[e + 1]] @ Wi[e]
+        assert np.array_equal(Y[off[e]:off[e + 1]], ref.astype(np.float64))
+
+
+def test_experts_are_independent_gemms(oracle_mod):
+    counts = [5, 0, 17, 3]
+    inp = wl.make_custom(counts, K=40, N=32, seed=14)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    Y = oracle_mod.grouped_gemm(xb, wb, inp.offsets)
+    off = inp.offsets
+    for e in range(len(counts)):
+        if counts[e] == 0:
+            continue
+        Ye = oracle_mod.grouped_gemm(np.ascontiguousarray(xb[off[e]:off[e + 1]]),
+                                     np.ascontiguousarray(wb[e:e + 1]), [0, counts[e]])
+        assert np.array_equal(Y[off[e]:off[e + 1]], Ye)
+
+
+def test_permuting_experts_permutes_blocks(oracle_mod):
+    counts = np.array([4, 9, 0, 6, 2])
+    inp = wl.make_custom(counts, K=32, N=16, seed=15)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    Y = oracle_mod.grouped_gemm(xb, wb, inp.offsets)
+    perm = np.array([3, 0, 4, 2, 1])
+    off = inp.offsets
+    xp = np.concatenate([xb[off[p]:off[p + 1]] for p in perm])
+    wp = np.ascontiguousarray(wb[perm])
+    offp = wl.offsets_from_counts(counts[perm])
+    Yp = oracle_mod.grouped_gemm(xp, wp, offp)
+    for new_e, old_e in enumerate(perm):
+        assert np.array_equal(Yp[offp[new_e]:offp[new_e + 1]], Y[off[old_e]:off[old_e + 1]])
+
+
+def test_rows_of_no_expert_untouched(oracle_mod):
+    # offsets may start after row 0 and end before M_tot; those rows are nobody's
+    inp = wl.make_custom([4, 3], K=16, N=8, seed=16, spare_rows=5)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    off = np.array([2, 6, 9], dtype=np.int32)
+    Y = oracle_mod.grouped_gemm(xb, wb, off)
+    assert np.isnan(Y[:2]).all() and np.isnan(Y[9:]).all()
+    assert not np.isnan(Y[2:9]).any()
+    # a preset output keeps its values outside the experts
+    out = np.full(Y.shape, -7.0)
+    oracle_mod.grouped_gemm(xb, wb, off, out=out)
+    assert (out[:2] == -7.0).all() and (out[9:] == -7.0).all()
+
+
+def test_points_equal_full_product(oracle_mod):
+    counts = [6, 0, 11, 2]
+    inp = wl.make_custom(counts, K=48, N=20, seed=17, spare_rows=3)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    Y = oracle_mod.grouped_gemm(xb, wb, inp.offsets)
+    rng = np.random.default_rng(0)
+    rows = rng.integers(0, xb.shape[0], 200)
+    cols = rng.integers(0, 20, 200)
+    P = oracle_mod.grouped_gemm_points(xb, wb, inp.offsets, rows, cols)
+    ref = Y[rows, cols]
+    assert np.array_equal(np.isnan(P), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(P[ok], ref[ok])
+
+
+@pytest.mark.parametrize("off,M", [([0, 5, 3], 8), ([0, 4, 9], 8), ([-1, 2, 3], 8)])
+def test_bad_offsets_rejected(oracle_mod, off, M):
+    inp = wl.make_custom([1, 1], K=8, N=8, seed=18, spare_rows=M - 2)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    assert oracle_mod.check_offsets(off, M) == oracle_mod.ORACLE_ERR_BAD_OFFSETS
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.grouped_gemm(xb, wb, off)
+
+
+def test_k_not_multiple_of_tile_and_odd_n(oracle_mod):
+    # shapes the pages never use (K=264, N=520) still follow the definition
+    inp = wl.make_custom([3, 2], K=264, N=520, seed=19)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    Y = oracle_mod.grouped_gemm(xb, wb, inp.offsets)
+    Xd, Wd = inp.X.double().numpy(), inp.W.double().numpy()
+    np.testing.assert_allclose(Y[:3], Xd[:3] @ Wd[0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(Y[3:], Xd[3:] @ Wd[1], rtol=1e-12, atol=1e-12)

@@ -1,0 +1,152 @@
+"""Plant plausible mistakes in copies of the oracle and check the pins catch them.
+
+Each case edits one line of a private copy of oracle/rgg_oracle.c (a dropped
+term, a transposed operand, a wrong expert, a flipped sign, a shifted row
+range, a wrong tile rule, a wrong rounding in eta), compiles the copy with gcc
+into a temporary directory and runs the same kinds of checks that
+tests/test_oracle.py applies to the real oracle.  Every mutant must fail at
+least one of them, and the unmutated copy must pass all of them.  All of this
+runs on the CPU.
+"""
+import ctypes
+import json
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+from ragged_grouped_gemm_02_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "rgg_oracle.c")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "worklog_figures.json")
+
+MUTANTS = {
+    "dropped_last_k": ("for (int k = 0; k < K; ++k) {", "for (int k = 0; k < K - 1; ++k) {"),
+    "transposed_w": ("acc[j] += x * bf16_bits_to_f64(wrow[j]);",
+                     "acc[j] += x * bf16_bits_to_f64(We[(int64_t)j * K + k]);"),
+    "wrong_expert": ("const uint16_t* We = W + (int64_t)e * K * N;\n        #pragma omp parallel",
+                     "const uint16_t* We = W + (int64_t)((e + 1) % E) * K * N;\n        #pragma omp parallel"),
+    "flipped_sign": ("acc[j] += x * bf16_bits_to_f64(wrow[j]);", "acc[j] -= x * bf16_bits_to_f64(wrow[j]);"),
+    "skipped_first_row": ("const int64_t row_begin = off[e], row_end = off[e + 1];",
+                          "const int64_t row_begin = off[e] + (off[e + 1] > off[e] ? 1 : 0), row_end = off[e + 1];"),
+    "x_row_of_next_expert": ("const double x = bf16_bits_to_f64(X[i * K + k]);",
+                             "const double x = bf16_bits_to_f64(X[((i + 1) % M_tot) * K + k]);"),
+    "tile_rows_not_clipped": ("desc[4 * count + 2] = (int32_t)(left < BM ? left : BM);",
+                              "desc[4 * count + 2] = (int32_t)BM;"),
+    "tile_row0_off_by_tile": ("desc[4 * count + 1] = (int32_t)(off[e] + mt * BM);",
+                              "desc[4 * count + 1] = (int32_t)(off[e] + mt * BN);"),
+    "tile_count_floor": ("const int64_t m_tiles = ceil_div64(m_e, BM);", "const int64_t m_tiles = m_e / BM;"),
+    "eta_floor": ("scheduled_tiles += ceil_div64(m_e, BM);", "scheduled_tiles += m_e / BM + 1;"),
+}
+
+
+def _build(tmp_path, name, mutation):
+    src = open(SRC).read()
+    if mutation is not None:
+        old, new = mutation
+        assert src.count(old) == 1, "mutation anchor for %s not unique" % name
+        src = src.replace(old, new)
+    c = tmp_path / ("%s.c" % name)
+    so = tmp_path / ("lib%s.so" % name)
+    c.write_text(src)
+    subprocess.run(["gcc", "-O1", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-std=c11",
+                    "-o", str(so), str(c)], check=True)
+    lib = ctypes.CDLL(str(so))
+    P = ctypes.c_void_p
+    lib.rgg_oracle_grouped_gemm.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P,
+                                            ctypes.c_int]
+    lib.rgg_oracle_grouped_gemm.restype = ctypes.c_int
+    lib.rgg_oracle_tile_list.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                                         ctypes.c_int64]
+    lib.rgg_oracle_tile_list.restype = ctypes.c_int64
+    lib.rgg_oracle_row_utilisation.argtypes = [P, ctypes.c_int, ctypes.c_int]
+    lib.rgg_oracle_row_utilisation.restype = ctypes.c_double
+    return lib
+
+
+def _gemm(lib, xb, wb, off):
+    M, K = xb.shape
+    E, _, N = wb.shape
+    off = np.ascontiguousarray(off, dtype=np.int32)
+    Y = np.full((M, N), np.nan)
+    rc = lib.rgg_oracle_grouped_gemm(xb.ctypes.data, wb.ctypes.data, off.ctypes.data, E, M, K, N,
+                                     Y.ctypes.data, 1)
+    assert rc == 0
+    return Y
+
+
+def _tiles(lib, off, N, BM, BN):
+    off = np.ascontiguousarray(off, dtype=np.int32)
+    T = lib.rgg_oracle_tile_list(off.ctypes.data, off.size - 1, N, BM, BN, None, 0)
+    d = np.zeros((max(T, 1), 4), dtype=np.int32)
+    lib.rgg_oracle_tile_list(off.ctypes.data, off.size - 1, N, BM, BN, d.ctypes.data, T)
+    return [tuple(r) for r in d[:T].tolist()]
+
+
+def _product_checks_pass(lib):
+    # library special case: one expert
+    inp = wl.make_custom([9], K=40, N=24, seed=21)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    Y = _gemm(lib, xb, wb, inp.offsets)
+    if not np.allclose(Y, inp.X.double().numpy() @ inp.W[0].double().numpy(), rtol=1e-12, atol=1e-12):
+        return False
+    # integer-exact, several experts with an empty one and spare rows
+    counts = [3, 0, 5, 2]
+    inp = wl.make_custom(counts, K=32, N=16, seed=22, integer_valued=True, spare_rows=2)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    Y = _gemm(lib, xb, wb, inp.offsets)
+    Xi, Wi, off = inp.X.to(torch.int64).numpy(), inp.W.to(torch.int64).numpy(), inp.offsets
+    for e in range(len(counts)):
+        if not np.array_equal(Y[off[e]:off[e + 1]], (Xi[off[e]:off[e + 1]] @ Wi[e]).astype(np.float64)):
+            return False
+    return bool(np.isnan(Y[off[-1]:]).all())
+
+
+def _tile_checks_pass(lib):
+    expected = []
+    for e, row0, rows in [(0, 0, 37), (2, 37, 64), (3, 101, 128), (3, 229, 27)]:
+        for col0 in (0, 128, 256, 384):
+            expected.append((e, row0, rows, col0))
+    if _tiles(lib, [0, 37, 37, 101, 256], 512, 128, 128) != expected:
+        return False
+    expected = []
+    for e, row0, rows in [(0, 0, 37), (2, 37, 64), (3, 101, 64), (3, 165, 64), (3, 229, 27)]:
+        for col0 in (0, 256):
+            expected.append((e, row0, rows, col0))
+    if _tiles(lib, [0, 37, 37, 101, 256], 512, 64, 256) != expected:
+        return False
+    figs = json.load(open(GOLDEN))
+    for entry in figs["tile_counts"]:
+        c = (np.full(64, entry["M"] // 64) if entry["routing"] == "uniform"
+             else wl.power_law_counts_first_experts(entry["M"], 64, 1.2))
+        if len(_tiles(lib, wl.offsets_from_counts(c), entry["N"], entry["BM"], entry["BN"])) != entry["tiles"]:
+            return False
+    return True
+
+
+def _eta_checks_pass(lib):
+    figs = json.load(open(GOLDEN))
+    for entry in figs["eta_waste_percent"]:
+        c = (np.full(64, entry["M"] // 64) if entry["routing"] == "uniform"
+             else wl.power_law_counts_first_experts(entry["M"], 64, 1.2))
+        off = np.ascontiguousarray(wl.offsets_from_counts(c))
+        eta = lib.rgg_oracle_row_utilisation(off.ctypes.data, 64, entry["BM"])
+        if round(100.0 * (1.0 - eta), 1) != entry["waste"]:
+            return False
+    return True
+
+
+def _all_pass(lib):
+    return _product_checks_pass(lib) and _tile_checks_pass(lib) and _eta_checks_pass(lib)
+
+
+def test_unmutated_copy_passes(tmp_path):
+    assert _all_pass(_build(tmp_path, "clean", None))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    assert not _all_pass(_build(tmp_path, name, MUTANTS[name])), "pins missed mutant %s" % name
