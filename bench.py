@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 ragged-M grouped GEMM (one JSON line per run).
+
+A step is one launch of the whole hot path: Y_e = X_e . W_e for every expert
+of one batch of synthetic input (offsets -> tile list -> TMA -> tcgen05 ->
+epilogue, all inside the kernel).  The metric is useful TFLOP/s,
+2 * M_tot * K * N / t ("Grouped GEMM for Imbalanced Experts on Blackwell: A WIP
+Worklog", section 1), with t measured on the device with CUDA events.
+
+Default workload: the small-decode, weight-bound configuration -- 32 experts
+x 16 rows, K = 6144, N = 4096 (the decode example of "Pearl's grouped GEMM
+kernel for MoE models, explained", "Why MoE needs a grouped GEMM").  Its
+inputs (1.6 GB of weights) are larger than the 129 MB L2, so no flush is
+needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+experts of one GPU under expert parallelism, no data-path collective: weak
+scaling); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from ragged_grouped_gemm_02_gb300 import workloads as wl  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+CSRC = os.path.join(ROOT, "ragged_grouped_gemm_02_gb300", "csrc")
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "useful TFLOP/s (2*M_tot*K*N/t) and HBM GB/s, as % of GB300 roofline"
+# The worklog's own figure for this exact metric and workload (B300, k2 with
+# two stages, uniform routing 16k rows): context, another machine's number.
+PAGE_NUMBERS = {"uniform": 440.1}
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default="decode", choices=sorted(wl.WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--bm", type=int, default=0)
+    p.add_argument("--bn", type=int, default=0)
+    p.add_argument("--stages", type=int, default=0)
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_setup(backend):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(CSRC, "*"))):
+        if path.endswith((".cu", ".cuh", ".h")):
+            h.update(os.path.basename(path).encode())
+            with open(path, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel sources and this workload; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_hash") != kernel_source_hash():
+        return None
+    entry = t.get("workloads", {}).get(workload)
+    return None if entry is None else int(entry["bytes_per_launch"])
+
+
+def work_of(counts, K, N):
+    M = int(np.sum(counts))
+    active = int(np.count_nonzero(counts))
+    flops = 2.0 * M * K * N
+    # each active expert's weights once, X and Y once, the offsets
+    bytes_ = 2.0 * (active * K * N + M * K + M * N) + 4.0 * (len(counts) + 1)
+    return flops, bytes_
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="rgg_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            phys = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+            idx = phys[self.dev] if self.dev < len(phys) and phys[self.dev] != "" else str(self.dev)
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", idx], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def oracle_cpu_rate(inp, budget_s=12.0):
+    """The fp64 oracle as it stands, on the host cores, over a bounded sample
+    of the workload: the first experts' complete rows (all N columns), about
+    `budget_s` of work.  Returns (TFLOP/s, sample description, threads)."""
+    import oracle
+    oracle.build()
+    counts = inp.counts
+    K, N = inp.X.shape[1], inp.W.shape[2]
+    threads = oracle.max_threads()
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    # calibrate on one expert's rows (or 16 rows)
+    e0 = int(np.argmax(counts > 0))
+    r = int(min(counts[e0], 16))
+    t0 = time.perf_counter()
+    oracle.grouped_gemm(np.ascontiguousarray(xb[inp.offsets[e0]:inp.offsets[e0] + r]), wb[e0:e0 + 1], [0, r])
+    rate = 2.0 * r * K * N / max(time.perf_counter() - t0, 1e-6)
+    want = budget_s * rate
+    e_take, flops = 0, 0.0
+    while e_take < len(counts) and (flops < want or flops == 0.0):
+        flops += 2.0 * counts[e_take] * K * N
+        e_take += 1
+    rows = int(inp.offsets[e_take])
+    off = inp.offsets[:e_take + 1]
+    t0 = time.perf_counter()
+    oracle.grouped_gemm(np.ascontiguousarray(xb[:rows]), np.ascontiguousarray(wb[:e_take]), off)
+    dt = time.perf_counter() - t0
+    sample = "experts 0..%d of %d (%d of %d rows, all %d columns), %.1f GFLOP in %.2f s" % (
+        e_take - 1, len(counts), rows, int(counts.sum()), N, flops / 1e9, dt)
+    return flops / dt / 1e12, sample, threads
+
+
+# --------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import ragged_grouped_gemm_02_gb300 as rgg
+    from ragged_grouped_gemm_02_gb300 import _build
+
+    world, rank, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(wl.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank}))
+    K, N, E = w.K, w.N, w.E
+    M_tot = inp.X.shape[0]
+    flops, bytes_ = work_of(inp.counts, K, N)
+    X, W = inp.X.to(dev), inp.W.to(dev)
+    off = torch.from_numpy(inp.offsets).to(dev)
+    Y = torch.empty(M_tot, N, dtype=torch.bfloat16, device=dev)
+    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages)
+    plan = rgg.rgg_plan(E, M_tot, K, N, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
+                        **opts)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rgg.rgg_grouped_gemm(X, W, off, Y, stream=stream, **opts)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    # warm-up: at least W steps and about a second of GPU work, so the clock
+    # record covers the GPU under load
+    t_begin = time.time()
+    n_warm = 0
+    while n_warm < max(3, args.warmup) or time.time() - t_begin < 1.0:
+        step()
+        n_warm += 1
+        if n_warm % 64 == 0:
+            torch.cuda.synchronize(dev)
+    status = rgg.rgg_query_status(local, stream)
+    if status != rgg.RGG_OK:
+        raise RuntimeError("device status after warm-up: %s" % rgg.rgg_status_string(status))
+
+    K_steps = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(K_steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    status = rgg.rgg_query_status(local, stream)
+    if status != rgg.RGG_OK:
+        raise RuntimeError("device status after the timed region: %s" % rgg.rgg_status_string(status))
+    total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # end to end through the public API: pinned host X and offsets in, Y out, every step
+    e2e = None
+    if not args.no_e2e:
+        hX = inp.X.pin_memory()
+        hoff = torch.from_numpy(inp.offsets).pin_memory()
+        hY = torch.empty(M_tot, N, dtype=torch.bfloat16).pin_memory()
+        dX = torch.empty_like(X)
+        doff = torch.empty_like(off)
+        for _ in range(3):
+            dX.copy_(hX, non_blocking=True)
+            doff.copy_(hoff, non_blocking=True)
+            rgg.rgg_grouped_gemm(dX, W, doff, Y, stream=stream, **opts)
+            hY.copy_(Y, non_blocking=True)
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e_start.record(stream)
+        for _ in range(K_steps):
+            dX.copy_(hX, non_blocking=True)
+            doff.copy_(hoff, non_blocking=True)
+            rgg.rgg_grouped_gemm(dX, W, doff, Y, stream=stream, **opts)
+            hY.copy_(Y, non_blocking=True)
+        e_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
+        e2e = {"value": round(flops * K_steps * world / (e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(hX.numel() * 2 + hoff.numel() * 4),
+               "d2h_bytes_per_step": int(hY.numel() * 2), "ms_per_step": round(e_ms / K_steps, 4),
+               "weights": "resident in HBM (model parameters); not copied per step"}
+
+    peaks = load_peaks()
+    t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": round(bytes_ / (launch_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": round(flops / (launch_ms / 1e3) / 1e12, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = measured_traffic(args.workload)
+    roof["peak_source"] = peaks["source"]
+    roof["algorithmic_per_launch"] = {"flops": flops, "bytes": bytes_}
+    roof["launch_ms"] = round(launch_ms, 5)
+    roof["hbm_gbs"] = round(bytes_ / (launch_ms / 1e3) / 1e9, 1)
+    roof["hbm_frac"] = round(bytes_ / (launch_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
+    roof["tensor_frac"] = round(flops / (launch_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, threads = oracle_cpu_rate(inp)
+        cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
+
+    value = flops * K_steps * world / (total_ms / 1e3) / 1e12
+    page = PAGE_NUMBERS.get(args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K_steps,
+        "warmup": n_warm, "ms_per_step": round(total_ms / K_steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": round(value / page, 4) if page else None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/K) weights)",
+        "config": {"workload": args.workload, "E": E, "K": K, "N": N, "M_tot": M_tot,
+                   "routing": w.routing, "note": w.note, "accumulate": "fp32", "out": "bf16",
+                   "l2": "inputs larger than L2 (%.0f MB > 129 MB), no flush" % (bytes_ / 1e6)
+                   if bytes_ > L2_BYTES else "inputs smaller than L2: back-to-back launches",
+                   "plan": plan, "parallelism": "expert replicas x%d" % world},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": K_steps, "impl": "ours",
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores: each step is a bounded
+    sample of the workload (the first rows of expert 0, all N columns), sized
+    so the whole run takes about a minute."""
+    world, rank, _ = dist_setup("gloo")
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w)
+    K, N = w.K, w.N
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    e0 = int(np.argmax(inp.counts > 0))
+    r0 = int(inp.offsets[e0])
+    # calibrate: one row
+    t0 = time.perf_counter()
+    oracle.grouped_gemm(np.ascontiguousarray(xb[r0:r0 + 1]), wb[e0:e0 + 1], [0, 1])
+    per_row = max(time.perf_counter() - t0, 1e-6)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(inp.counts[e0], budget / per_row)))
+    sub_x = np.ascontiguousarray(xb[r0:r0 + rows])
+    sub_w = np.ascontiguousarray(wb[e0:e0 + 1])
+    for _ in range(args.warmup):
+        oracle.grouped_gemm(sub_x, sub_w, [0, rows])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.grouped_gemm(sub_x, sub_w, [0, rows])
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * K * N * args.steps
+    value = flops / dt / 1e12
+    sample = "%d rows of expert %d (all %d columns, K=%d) per step" % (rows, e0, N, K)
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "E": w.E, "K": K, "N": N, "M_tot": int(inp.counts.sum())},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/*
+ * rgg.h -- C ABI of the GB300 (sm_103a) ragged-M grouped GEMM library (librgg.so).
+ *
+ * The operation (sources cited by page title and section):
+ *
+ *   "Grouped GEMM for Imbalanced Experts on Blackwell: A WIP Worklog",
+ *   "What I am measuring" and section 2 "The Grouped Problem and the flat tile
+ *   list": after routing, the rows of X are grouped by expert and one launch
+ *   computes E independent products  Y_e = X_e . W_e,  [m_e, K] x [K, N],
+ *   where m_e is known only at run time and may be zero.  "Grouped GEMM"
+ *   (InferenceX glossary), "Technical definition": independent matrix
+ *   multiplications with different row counts in one launch.
+ *
+ * Data layout (all row-major, all device memory, all owned by the caller):
+ *   X             bf16 [M_tot, K]      rows grouped by expert
+ *   W             bf16 [E, K, N]       expert e's weight is W[e], N contiguous
+ *   group_offsets int32 [E + 1]        expert e owns rows [off[e], off[e+1])
+ *   Y             bf16 [M_tot, N]      written only on rows some expert owns
+ * Accumulation is fp32; each output is rounded once to bf16 (nearest even).
+ *
+ * Offsets are valid when 0 <= off[0] <= off[1] <= ... <= off[E] <= M_tot.
+ * Rows outside [off[0], off[E]) belong to no expert and are never written.
+ * The library reads the offsets on the device only, so the routed row counts
+ * never have to reach the host.
+ *
+ * Errors: arguments the host can check are checked before anything is
+ * launched and reported by the return value.  What only the device can see
+ * (invalid offsets, a pipeline wait that ran past its time limit) is recorded
+ * in a status word owned by the handle and reported by rgg_query_status();
+ * a launch that finds invalid offsets writes nothing to Y.  Nothing traps.
+ *
+ * Streams: every launching call is asynchronous on the given stream (a
+ * cudaStream_t passed as void*; NULL is the legacy default stream).
+ * rgg_grouped_gemm allocates nothing per call.
+ */
+#ifndef RGG_H
+#define RGG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rgg_status {
+    RGG_OK = 0,
+    RGG_ERR_INVALID_ARG = 1,     /* null pointer, bad size, misaligned pointer, unsupported option value */
+    RGG_ERR_UNSUPPORTED = 2,     /* a valid request this build cannot run (no sm_103 device, E too large, ...) */
+    RGG_ERR_CUDA = 3,            /* a CUDA runtime / driver call failed; see rgg_last_cuda_error() */
+    RGG_ERR_BAD_OFFSETS = 4,     /* device-detected: group offsets not valid; nothing was written */
+    RGG_ERR_DEVICE_TIMEOUT = 5,  /* device-detected: a pipeline wait exceeded the time limit; Y is incomplete */
+    RGG_ERR_CAPACITY = 6         /* rgg_export_tiles: more tiles than the output capacity (count still exact) */
+} rgg_status;
+
+typedef struct rgg_handle rgg_handle;
+
+/* Tuning overrides; a zeroed struct (or a NULL pointer) means "choose automatically". */
+typedef struct rgg_options {
+    int bm;                      /* rows per tile: 0 = auto, or 64, 128 */
+    int bn;                      /* columns per tile: 0 = auto, or 128, 192, 256 */
+    int stages;                  /* shared-memory ring depth: 0 = as many as fit, else 2..16 */
+    int max_ctas;                /* persistent CTAs: 0 = one per SM, else an upper bound */
+    uint64_t timeout_ns;         /* limit of any single pipeline wait: 0 = 2 s */
+    const int32_t* host_counts;  /* optional HOST copy of m_e[E] to guide the tile shape; NULL = use M_tot/E */
+    int debug_flags;             /* 0 in normal use.  RGG_DEBUG_PRODUCER_STALL makes the load pipeline issue
+                                    nothing, so the first MMA wait can only end by its time limit: a test of the
+                                    bounded waits, which then report RGG_ERR_DEVICE_TIMEOUT */
+} rgg_options;
+
+#define RGG_DEBUG_PRODUCER_STALL 1
+
+/* The configuration a call would use (see rgg_plan). */
+typedef struct rgg_plan_info {
+    int bm, bn, bk;              /* tile rows, tile columns, K per pipeline stage */
+    int stages;                  /* ring depth */
+    int grid;                    /* persistent CTAs launched */
+    int threads;                 /* threads per CTA */
+    int smem_bytes;              /* dynamic shared memory per CTA */
+    int tmem_cols;               /* TMEM columns allocated per CTA (two accumulator buffers) */
+    int64_t max_tiles;           /* upper bound on the flat tile count for these sizes */
+} rgg_plan_info;
+
+/*
+ * Create a handle bound to CUDA device `device`: queries the SM count and the
+ * shared-memory limit, checks for compute capability 10.3 (sm_103), and
+ * allocates the device status word (the only device allocation the library
+ * makes, once per handle).  On success *out owns the handle; release it with
+ * rgg_destroy.  Returns RGG_ERR_UNSUPPORTED on any other GPU.
+ */
+rgg_status rgg_create(rgg_handle** out, int device);
+
+/* Free the handle and its status word.  NULL is ignored. */
+void rgg_destroy(rgg_handle* h);
+
+/*
+ * Y_e = X_e . W_e for every expert e, in one kernel launch on `stream`
+ * (Worklog section 2 and section 7 "Next: tcgen05 and adaptive BM"): a
+ * persistent, warp-specialized tcgen05 kernel walks the flat tile list it
+ * builds from group_offsets.
+ *
+ * X, W, Y: device pointers, 16-byte aligned.  group_offsets: device int32
+ * [E+1].  Requirements: 1 <= E <= 4096, 0 <= M_tot < 2^31, K >= 8 and
+ * N >= 8 with K % 8 == 0 and N % 8 == 0 (the 16-byte row-stride rule of the
+ * tensor-memory accelerator).  `opt` may be NULL.
+ *
+ * Returns RGG_OK once the launch is queued.  Invalid offsets or a device
+ * timeout are reported later by rgg_query_status.  The call allocates
+ * nothing and only reads the offsets on the device.
+ */
+rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const int32_t* group_offsets,
+                            void* Y, int E, int64_t M_tot, int K, int N, void* stream,
+                            const rgg_options* opt);
+
+/*
+ * The flat tile list the kernel walks, written out for checking (Worklog
+ * section 2, "Source -- k1/common.cuh . k1/harness.cu"): descriptors
+ * {expert, row0, rows, col0} in expert-major, M-tile, N-tile order, built on
+ * the device by the same code the GEMM kernel uses.
+ *
+ * desc_out: device int32 [4 * cap] (may be NULL when cap == 0).
+ * n_tiles_out: device int32 [1], receives the total tile count T (also when
+ * T > cap, in which case only the first cap descriptors are written and the
+ * status word records RGG_ERR_CAPACITY).  bm in {64, 128}, bn in
+ * {128, 192, 256}.  Asynchronous on `stream`; invalid offsets are reported by
+ * rgg_query_status (T is then written as -1).
+ */
+rgg_status rgg_export_tiles(rgg_handle* h, const int32_t* group_offsets, int E, int64_t M_tot, int N,
+                            int bm, int bn, int32_t* desc_out, int64_t cap, int32_t* n_tiles_out,
+                            void* stream);
+
+/*
+ * Synchronize `stream`, read the device status word, reset it to RGG_OK and
+ * return what it held (RGG_OK when no launch reported a problem).  Host-side
+ * CUDA failures return RGG_ERR_CUDA.
+ */
+rgg_status rgg_query_status(rgg_handle* h, void* stream);
+
+/*
+ * The configuration rgg_grouped_gemm would choose for these sizes on a GPU
+ * with `num_sms` SMs and `smem_optin` bytes of opt-in shared memory per block
+ * (pass 0 for both to use GB300's 152 and 232448).  Pure host code: needs no
+ * GPU.  The tile shape follows the Worklog's section 6 and section 7 point
+ * that BM must be chosen from the expert sizes, and the Pearl article's
+ * 64-row tiles where experts average 64 rows or fewer ("Four changes").
+ */
+rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N,
+                    const rgg_options* opt, rgg_plan_info* out);
+
+/* A static, human-readable name for a status code. */
+const char* rgg_status_string(rgg_status s);
+
+/* The text of the last CUDA error seen by this library on this thread ("" if none). */
+const char* rgg_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RGG_H */

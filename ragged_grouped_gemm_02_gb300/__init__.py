@@ -1,1 +1,231 @@
-"""GB300-native ragged-M grouped GEMM (placeholder; the binding follows)."""
+"""GB300-native ragged-M grouped GEMM.
+
+``Y_e = X_e . W_e`` for every expert e in one launch of a persistent,
+warp-specialized tcgen05 kernel (see include/rgg.h for the full contract).
+
+This module is a thin ctypes binding over ``librgg.so``: it turns torch
+tensors into device pointers and the current CUDA stream into a handle, and
+raises on a non-OK status.  Every step of the computation runs in the CUDA
+library; there is no CPU or PyTorch fallback.  Build the library with
+``python -c "import __graft_entry__ as g; g.build()"`` (or
+``python ragged_grouped_gemm_02_gb300/_build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "RggError", "rgg_grouped_gemm", "rgg_export_tiles", "rgg_query_status", "rgg_plan",
+    "rgg_status_string", "library_path", "load_library", "EXPORTED_SYMBOLS",
+    "RGG_OK", "RGG_ERR_INVALID_ARG", "RGG_ERR_UNSUPPORTED", "RGG_ERR_CUDA", "RGG_ERR_BAD_OFFSETS",
+    "RGG_ERR_DEVICE_TIMEOUT", "RGG_ERR_CAPACITY",
+]
+
+RGG_OK = 0
+RGG_ERR_INVALID_ARG = 1
+RGG_ERR_UNSUPPORTED = 2
+RGG_ERR_CUDA = 3
+RGG_ERR_BAD_OFFSETS = 4
+RGG_ERR_DEVICE_TIMEOUT = 5
+RGG_ERR_CAPACITY = 6
+RGG_DEBUG_PRODUCER_STALL = 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "librgg.so")
+
+# The C ABI entry points declared in include/rgg.h.
+EXPORTED_SYMBOLS = (
+    "rgg_create", "rgg_destroy", "rgg_grouped_gemm", "rgg_export_tiles", "rgg_query_status",
+    "rgg_plan", "rgg_status_string", "rgg_last_cuda_error",
+)
+
+
+class RggError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(what)
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("stages", ctypes.c_int),
+                ("max_ctas", ctypes.c_int), ("timeout_ns", ctypes.c_uint64), ("host_counts", ctypes.c_void_p),
+                ("debug_flags", ctypes.c_int)]
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int), ("stages", ctypes.c_int),
+                ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("tmem_cols", ctypes.c_int), ("max_tiles", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+_handles: dict[int, ctypes.c_void_p] = {}
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load librgg.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("librgg.so is not built (%s): run __graft_entry__.build() first" % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        lib.rgg_create.argtypes = [ctypes.POINTER(ctypes.c_void_p), I]
+        lib.rgg_create.restype = I
+        lib.rgg_destroy.argtypes = [P]
+        lib.rgg_destroy.restype = None
+        lib.rgg_grouped_gemm.argtypes = [P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
+        lib.rgg_grouped_gemm.restype = I
+        lib.rgg_export_tiles.argtypes = [P, P, I, I64, I, I, I, P, I64, P, P]
+        lib.rgg_export_tiles.restype = I
+        lib.rgg_query_status.argtypes = [P, P]
+        lib.rgg_query_status.restype = I
+        lib.rgg_plan.argtypes = [I, I, I, I64, I, I, ctypes.POINTER(_Options), ctypes.POINTER(_PlanInfo)]
+        lib.rgg_plan.restype = I
+        lib.rgg_status_string.argtypes = [I]
+        lib.rgg_status_string.restype = ctypes.c_char_p
+        lib.rgg_last_cuda_error.argtypes = []
+        lib.rgg_last_cuda_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def rgg_status_string(status: int) -> str:
+    return load_library().rgg_status_string(int(status)).decode()
+
+
+def _raise(status: int, call: str):
+    lib = load_library()
+    msg = "%s: %s" % (call, lib.rgg_status_string(status).decode())
+    if status == RGG_ERR_CUDA:
+        msg += " [%s]" % lib.rgg_last_cuda_error().decode()
+    raise RggError(status, msg)
+
+
+def _handle(device: int) -> ctypes.c_void_p:
+    lib = load_library()
+    with _lock:
+        h = _handles.get(device)
+        if h is None:
+            h = ctypes.c_void_p()
+            s = lib.rgg_create(ctypes.byref(h), int(device))
+            if s != RGG_OK:
+                _raise(s, "rgg_create(device=%d)" % device)
+            _handles[device] = h
+        return h
+
+
+def _options(bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0):
+    opt = _Options(int(bm), int(bn), int(stages), int(max_ctas), int(timeout_ns), None, int(debug_flags))
+    keep = None
+    if host_counts is not None:
+        import numpy as np
+        keep = np.ascontiguousarray(np.asarray(host_counts, dtype=np.int32))
+        opt.host_counts = keep.ctypes.data
+    return opt, keep
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
+                     host_counts=None, debug_flags=0, stream=None, check=False):
+    """Y_e = X_e . W_e for every expert (one kernel launch, asynchronous).
+
+    X: bf16 CUDA [M_tot, K]; W: bf16 CUDA [E, K, N]; group_offsets: int32
+    CUDA [E+1]; Y: optional bf16 CUDA [M_tot, N] (allocated uninitialised when
+    omitted: rows that belong to no expert are never written).  Keyword
+    options map to ``rgg_options``.  ``check=True`` synchronises the stream
+    and raises if the device reported bad offsets or a timeout.
+    """
+    import torch
+    if not (X.is_cuda and W.is_cuda and group_offsets.is_cuda):
+        raise ValueError("X, W and group_offsets must be CUDA tensors")
+    if X.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or group_offsets.dtype != torch.int32:
+        raise TypeError("X and W must be bf16 and group_offsets int32")
+    if X.dim() != 2 or W.dim() != 3 or group_offsets.dim() != 1:
+        raise ValueError("X must be [M_tot, K], W [E, K, N] and group_offsets [E+1]")
+    if not (X.is_contiguous() and W.is_contiguous() and group_offsets.is_contiguous()):
+        raise ValueError("X, W and group_offsets must be contiguous")
+    M_tot, K = X.shape
+    E, K2, N = W.shape
+    if K2 != K or group_offsets.numel() != E + 1:
+        raise ValueError("shape mismatch: X %s, W %s, offsets %d" % (tuple(X.shape), tuple(W.shape),
+                                                                     group_offsets.numel()))
+    device = X.device.index if X.device.index is not None else torch.cuda.current_device()
+    if Y is None:
+        Y = torch.empty(M_tot, N, dtype=torch.bfloat16, device=X.device)
+    elif Y.shape != (M_tot, N) or Y.dtype != torch.bfloat16 or not Y.is_contiguous() or not Y.is_cuda:
+        raise ValueError("Y must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
+    lib = load_library()
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags)
+    st = _stream_ptr(stream, device)
+    s = lib.rgg_grouped_gemm(_handle(device), X.data_ptr(), W.data_ptr(), group_offsets.data_ptr(), Y.data_ptr(),
+                             E, M_tot, K, N, st, ctypes.byref(opt))
+    del keep
+    if s != RGG_OK:
+        _raise(s, "rgg_grouped_gemm")
+    if check:
+        s = lib.rgg_query_status(_handle(device), st)
+        if s != RGG_OK:
+            _raise(s, "rgg_grouped_gemm (device status)")
+    return Y
+
+
+def rgg_export_tiles(group_offsets, M_tot: int, N: int, bm: int, bn: int, cap: int | None = None, stream=None):
+    """The flat tile list the kernel walks, built on the device by the same
+    code: returns (int32 CPU tensor [min(T, cap), 4] of (expert, row0, rows,
+    col0), T).  Raises if the device rejects the offsets."""
+    import torch
+    E = group_offsets.numel() - 1
+    device = group_offsets.device.index if group_offsets.device.index is not None else torch.cuda.current_device()
+    if cap is None:
+        cap = (M_tot // bm + E) * (-(-N // bn))
+    desc = torch.empty(max(cap, 1) * 4, dtype=torch.int32, device=group_offsets.device)
+    n = torch.empty(1, dtype=torch.int32, device=group_offsets.device)
+    lib = load_library()
+    st = _stream_ptr(stream, device)
+    s = lib.rgg_export_tiles(_handle(device), group_offsets.data_ptr(), E, int(M_tot), int(N), int(bm), int(bn),
+                             desc.data_ptr(), int(cap), n.data_ptr(), st)
+    if s != RGG_OK:
+        _raise(s, "rgg_export_tiles")
+    s = lib.rgg_query_status(_handle(device), st)
+    T = int(n.item())
+    if s not in (RGG_OK, RGG_ERR_CAPACITY):
+        _raise(s, "rgg_export_tiles (device status)")
+    return desc[: 4 * min(T, cap)].view(-1, 4).cpu(), T
+
+
+def rgg_query_status(device: int | None = None, stream=None) -> int:
+    """Synchronise the stream, return and clear the device status word."""
+    import torch
+    if device is None:
+        device = torch.cuda.current_device()
+    return int(load_library().rgg_query_status(_handle(device), _stream_ptr(stream, device)))
+
+
+def rgg_plan(E: int, M_tot: int, K: int, N: int, *, num_sms: int = 0, smem_optin: int = 0, bm=0, bn=0,
+             stages=0, max_ctas=0, host_counts=None) -> dict:
+    """The launch configuration rgg_grouped_gemm would use (host-only)."""
+    lib = load_library()
+    opt, keep = _options(bm, bn, stages, max_ctas, 0, host_counts)
+    info = _PlanInfo()
+    s = lib.rgg_plan(int(num_sms), int(smem_optin), int(E), int(M_tot), int(K), int(N), ctypes.byref(opt),
+                     ctypes.byref(info))
+    del keep
+    if s != RGG_OK:
+        _raise(s, "rgg_plan")
+    return {f: getattr(info, f) for f, _ in _PlanInfo._fields_}

@@ -1,0 +1,378 @@
+// rgg_api.cu -- the C ABI of librgg.so (declared in include/rgg.h): argument
+// checks, the tile-shape planner, TMA descriptor encoding and the launches.
+//
+// The planner follows "Grouped GEMM for Imbalanced Experts on Blackwell: A
+// WIP Worklog", section 6 ("BM therefore has to be selected from both the
+// expert sizes and the rate each tile shape achieves") and section 7 (choose
+// BM from the expert-size distribution), and "Pearl's grouped GEMM kernel for
+// MoE models, explained", "Four changes, three of them measured" (64-row
+// tiles where experts average 64 rows or fewer).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "rgg.h"
+#include "rgg_internal.h"
+
+struct rgg_handle {
+    int device;
+    int num_sms;
+    int smem_optin;
+    int32_t* d_status;
+};
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+
+constexpr int kDefaultSms = 152;
+constexpr int kDefaultSmemOptin = 232448;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+rgg_status cuda_failure(cudaError_t err, const char* what) {
+    g_last_cuda_error = std::string(what) + ": " + cudaGetErrorName(err) + " (" + cudaGetErrorString(err) + ")";
+    return RGG_ERR_CUDA;
+}
+
+// Makes `device` current for the scope of a call and restores the caller's.
+class DeviceScope {
+public:
+    explicit DeviceScope(int device) {
+        if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+        if (prev_ != device) err_ = cudaSetDevice(device);
+    }
+    ~DeviceScope() {
+        int cur = -1;
+        if (prev_ >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev_) cudaSetDevice(prev_);
+    }
+    cudaError_t error() const { return err_; }
+
+private:
+    int prev_ = -1;
+    cudaError_t err_ = cudaSuccess;
+};
+
+using EncodeTiledFn = decltype(&cuTensorMapEncodeTiled);
+
+EncodeTiledFn encode_tiled_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Plan {
+    int bm, bn, stages, grid;
+    int smem_bytes;
+    int64_t max_tiles;
+};
+
+// Upper bound on the flat tile count: sum_e ceil(m_e/BM) <= floor(M_tot/BM) + E.
+int64_t tile_bound(int E, int64_t M_tot, int N, int bm, int bn) {
+    return (M_tot / bm + E) * ceil_div(N, bn);
+}
+
+rgg_status check_sizes(int E, int64_t M_tot, int K, int N) {
+    if (E < 1 || E > rgg::kMaxExperts) return E < 1 ? RGG_ERR_INVALID_ARG : RGG_ERR_UNSUPPORTED;
+    if (M_tot < 0 || M_tot >= (int64_t(1) << 31)) return RGG_ERR_INVALID_ARG;
+    if (K < 8 || N < 8 || (K % 8) != 0 || (N % 8) != 0) return RGG_ERR_INVALID_ARG;
+    return RGG_OK;
+}
+
+rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N, const rgg_options* opt,
+                     Plan* out) {
+    rgg_status s = check_sizes(E, M_tot, K, N);
+    if (s != RGG_OK) return s;
+    if (num_sms <= 0) num_sms = kDefaultSms;
+    if (smem_optin <= 0) smem_optin = kDefaultSmemOptin;
+    const int want_bm = opt ? opt->bm : 0;
+    const int want_bn = opt ? opt->bn : 0;
+    const int want_stages = opt ? opt->stages : 0;
+    const int max_ctas = opt ? opt->max_ctas : 0;
+    if (want_bm != 0 && want_bm != 64 && want_bm != 128) return RGG_ERR_INVALID_ARG;
+    if (want_bn != 0 && want_bn != 128 && want_bn != 192 && want_bn != 256) return RGG_ERR_INVALID_ARG;
+    if (want_stages != 0 && (want_stages < 2 || want_stages > rgg::kMaxStages)) return RGG_ERR_INVALID_ARG;
+    if (max_ctas < 0) return RGG_ERR_INVALID_ARG;
+    const int grid_cap = max_ctas > 0 ? std::min(max_ctas, num_sms) : num_sms;
+
+    // Per-expert M tiles at each BM: exact with host counts, else the
+    // balanced estimate E * ceil(avg / BM).
+    auto m_tiles = [&](int bm) -> int64_t {
+        if (opt && opt->host_counts) {
+            int64_t t = 0;
+            for (int e = 0; e < E; ++e) t += ceil_div(std::max<int64_t>(0, opt->host_counts[e]), bm);
+            return t;
+        }
+        const int64_t avg = ceil_div(M_tot, E);
+        return static_cast<int64_t>(E) * ceil_div(avg, bm);
+    };
+
+    // BM: 64-row tiles when experts average 64 rows or fewer (counting only
+    // experts that have rows, when the counts are known).
+    int bm = want_bm;
+    if (bm == 0) {
+        double avg = static_cast<double>(M_tot) / E;
+        if (opt && opt->host_counts) {
+            int64_t rows = 0, busy = 0;
+            for (int e = 0; e < E; ++e)
+                if (opt->host_counts[e] > 0) {
+                    rows += opt->host_counts[e];
+                    ++busy;
+                }
+            avg = busy ? static_cast<double>(rows) / busy : 0.0;
+        }
+        bm = (avg <= 64.0) ? 64 : 128;
+    }
+
+    // BN: fewest waves of persistent work, a tile costing about (BN + 64)
+    // units (MMA and weight bytes scale with BN, plus a fixed per-tile cost);
+    // ties go to the wider tile.
+    int bn = want_bn;
+    if (bn == 0) {
+        const int64_t mt = std::max<int64_t>(1, m_tiles(bm));
+        int64_t best = INT64_MAX;
+        for (int cand : {256, 192, 128}) {
+            const int64_t tiles = mt * ceil_div(N, cand);
+            const int64_t waves = ceil_div(tiles, grid_cap);
+            const int64_t cost = waves * (cand + 64);
+            if (cost < best) {
+                best = cost;
+                bn = cand;
+            }
+        }
+    }
+
+    const int64_t max_tiles = tile_bound(E, M_tot, N, bm, bn);
+    if (max_tiles >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
+
+    const rgg::SmemPlan probe = rgg::smem_plan(bm, bn, 0, E);
+    const int64_t per_stage = static_cast<int64_t>(bm + bn) * 128 + 16;  // tiles + two barriers
+    const int64_t room = static_cast<int64_t>(smem_optin) - 1024 - probe.total - 64;
+    int fit = static_cast<int>(std::min<int64_t>(rgg::kMaxStages, room / per_stage));
+    int stages = want_stages ? want_stages : fit;
+    if (stages < 2 || stages > fit) return RGG_ERR_UNSUPPORTED;
+
+    const rgg::SmemPlan sp = rgg::smem_plan(bm, bn, stages, E);
+    // Ask for more than half of the SM's shared memory so that exactly one CTA
+    // (and one 2 x BN-column TMEM allocation) lives on each SM.
+    const int smem = std::max<int>(static_cast<int>(sp.total) + 1024, smem_optin / 2 + 1024);
+    if (smem > smem_optin) return RGG_ERR_UNSUPPORTED;
+
+    out->bm = bm;
+    out->bn = bn;
+    out->stages = stages;
+    out->grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(grid_cap, max_tiles)));
+    out->smem_bytes = smem;
+    out->max_tiles = max_tiles;
+    return RGG_OK;
+}
+
+rgg_status encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K, int N, int bm,
+                       CUtensorMap* tx, CUtensorMap* tw) {
+    EncodeTiledFn encode = encode_tiled_fn();
+    if (!encode) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled is not available from the driver";
+        return RGG_ERR_CUDA;
+    }
+    // X: 2-D {K, M_tot}, box {64, BM}: one 128-byte swizzle row per tile row.
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M_tot)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bm)};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r = encode(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            g_last_cuda_error = "cuTensorMapEncodeTiled(X) failed with CUresult " + std::to_string(static_cast<int>(r));
+            return RGG_ERR_CUDA;
+        }
+    }
+    // W: 3-D {N, K, E}, box {64, 64, 1}: one 64-column panel of 64 K rows.
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K),
+                                    static_cast<cuuint64_t>(E)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(N) * K * 2};
+        const cuuint32_t box[3] = {64, 64, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = encode(tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            g_last_cuda_error = "cuTensorMapEncodeTiled(W) failed with CUresult " + std::to_string(static_cast<int>(r));
+            return RGG_ERR_CUDA;
+        }
+    }
+    return RGG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rgg_status_string(rgg_status s) {
+    switch (s) {
+        case RGG_OK: return "RGG_OK";
+        case RGG_ERR_INVALID_ARG: return "RGG_ERR_INVALID_ARG: invalid argument";
+        case RGG_ERR_UNSUPPORTED: return "RGG_ERR_UNSUPPORTED: request not supported by this build or device";
+        case RGG_ERR_CUDA: return "RGG_ERR_CUDA: a CUDA call failed";
+        case RGG_ERR_BAD_OFFSETS: return "RGG_ERR_BAD_OFFSETS: group offsets are not valid; nothing was written";
+        case RGG_ERR_DEVICE_TIMEOUT: return "RGG_ERR_DEVICE_TIMEOUT: a device pipeline wait exceeded its limit";
+        case RGG_ERR_CAPACITY: return "RGG_ERR_CAPACITY: more tiles than the output capacity";
+    }
+    return "unknown rgg_status";
+}
+
+const char* rgg_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+rgg_status rgg_create(rgg_handle** out, int device) {
+    if (!out) return RGG_ERR_INVALID_ARG;
+    *out = nullptr;
+    int count = 0;
+    cudaError_t err = cudaGetDeviceCount(&count);
+    if (err != cudaSuccess) return cuda_failure(err, "cudaGetDeviceCount");
+    if (device < 0 || device >= count) return RGG_ERR_INVALID_ARG;
+    int major = 0, minor = 0, sms = 0, smem = 0;
+    if ((err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device)) != cudaSuccess)
+        return cuda_failure(err, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3) {
+        g_last_cuda_error = "librgg is built for sm_103a; device " + std::to_string(device) + " is sm_" +
+                            std::to_string(major) + std::to_string(minor);
+        return RGG_ERR_UNSUPPORTED;
+    }
+    DeviceScope scope(device);
+    if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
+    int32_t* status = nullptr;
+    if ((err = cudaMalloc(&status, 256)) != cudaSuccess) return cuda_failure(err, "cudaMalloc(status)");
+    if ((err = cudaMemset(status, 0, 256)) != cudaSuccess) {
+        cudaFree(status);
+        return cuda_failure(err, "cudaMemset(status)");
+    }
+    rgg_handle* h = new rgg_handle;
+    h->device = device;
+    h->num_sms = sms;
+    h->smem_optin = smem;
+    h->d_status = status;
+    *out = h;
+    return RGG_OK;
+}
+
+void rgg_destroy(rgg_handle* h) {
+    if (!h) return;
+    {
+        DeviceScope scope(h->device);
+        cudaFree(h->d_status);
+    }
+    delete h;
+}
+
+rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N, const rgg_options* opt,
+                    rgg_plan_info* out) {
+    if (!out) return RGG_ERR_INVALID_ARG;
+    Plan p;
+    rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, N, opt, &p);
+    if (s != RGG_OK) return s;
+    out->bm = p.bm;
+    out->bn = p.bn;
+    out->bk = rgg::kBK;
+    out->stages = p.stages;
+    out->grid = p.grid;
+    out->threads = rgg::kThreads;
+    out->smem_bytes = p.smem_bytes;
+    out->tmem_cols = (2 * p.bn <= 256) ? 256 : 512;
+    out->max_tiles = p.max_tiles;
+    return RGG_OK;
+}
+
+rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const int32_t* group_offsets, void* Y,
+                            int E, int64_t M_tot, int K, int N, void* stream, const rgg_options* opt) {
+    if (!h || !group_offsets || !W) return RGG_ERR_INVALID_ARG;
+    rgg_status s = check_sizes(E, M_tot, K, N);
+    if (s != RGG_OK) return s;
+    if (M_tot > 0 && (!X || !Y)) return RGG_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(group_offsets, 4) || (M_tot > 0 && (!aligned(X, 16) || !aligned(Y, 16))))
+        return RGG_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceScope scope(h->device);
+    if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
+
+    if (M_tot == 0) {
+        cudaError_t err = rgg::launch_validate_offsets(group_offsets, E, M_tot, h->d_status, st);
+        return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
+    }
+
+    Plan p;
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p);
+    if (s != RGG_OK) return s;
+
+    CUtensorMap tx, tw;
+    s = encode_maps(X, W, E, M_tot, K, N, p.bm, &tx, &tw);
+    if (s != RGG_OK) return s;
+
+    rgg::GemmArgs a;
+    a.offsets = group_offsets;
+    a.Y = static_cast<__nv_bfloat16*>(Y);
+    a.status = h->d_status;
+    a.M_tot = M_tot;
+    a.E = E;
+    a.K = K;
+    a.N = N;
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(K, rgg::kBK));
+    a.n_tiles_n = static_cast<int32_t>(ceil_div(N, p.bn));
+    a.stages = p.stages;
+    a.y_vec32 = ((N % 16) == 0 && aligned(Y, 32)) ? 1 : 0;
+    a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+    a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
+
+    cudaError_t err = (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tw, a)
+                                    : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tw, a);
+    return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm launch");
+}
+
+rgg_status rgg_export_tiles(rgg_handle* h, const int32_t* group_offsets, int E, int64_t M_tot, int N, int bm,
+                            int bn, int32_t* desc_out, int64_t cap, int32_t* n_tiles_out, void* stream) {
+    if (!h || !group_offsets || !n_tiles_out || cap < 0 || (cap > 0 && !desc_out)) return RGG_ERR_INVALID_ARG;
+    if (E < 1 || E > rgg::kMaxExperts || M_tot < 0 || M_tot >= (int64_t(1) << 31) || N < 1)
+        return RGG_ERR_INVALID_ARG;
+    if ((bm != 64 && bm != 128) || (bn != 128 && bn != 192 && bn != 256)) return RGG_ERR_INVALID_ARG;
+    if (tile_bound(E, M_tot, N, bm, bn) >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
+    DeviceScope scope(h->device);
+    if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
+    cudaError_t err = rgg::launch_export_tiles(group_offsets, E, M_tot, N, bm, bn, desc_out, cap, n_tiles_out,
+                                               h->d_status, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? RGG_OK : cuda_failure(err, "export_tiles launch");
+}
+
+rgg_status rgg_query_status(rgg_handle* h, void* stream) {
+    if (!h) return RGG_ERR_INVALID_ARG;
+    DeviceScope scope(h->device);
+    if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t value = 0;
+    cudaError_t err = cudaMemcpyAsync(&value, h->d_status, sizeof(value), cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaMemsetAsync(h->d_status, 0, sizeof(int32_t), st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return cuda_failure(err, "rgg_query_status");
+    return static_cast<rgg_status>(value);
+}
+
+}  // extern "C"

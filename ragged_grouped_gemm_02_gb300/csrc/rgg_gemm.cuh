@@ -1,0 +1,339 @@
+// rgg_gemm.cuh -- the persistent, warp-specialized tcgen05 grouped GEMM kernel.
+//
+// Sources (by page title and section):
+//  * "Grouped GEMM for Imbalanced Experts on Blackwell: A WIP Worklog":
+//    section 2 (one flat, expert-major tile list; a tile owns its full K
+//    reduction; partial tiles run the full MMA loop and mask their stores),
+//    section 5 (TMA loads into a multistage shared-memory ring connected by
+//    full/empty mbarriers with phase parity; 128-byte swizzle; a producer warp
+//    separate from the math), section 7 (tcgen05: operands read from shared
+//    memory through descriptors, the accumulator in TMEM, one thread issuing
+//    the MMA for the CTA; BM chosen from the expert sizes).
+//  * "Pearl's grouped GEMM kernel for MoE models, explained", "Four changes,
+//    three of them measured": results go from registers straight to global
+//    memory with 256-bit stores; 64-row tiles on a single CTA; the
+//    accumulator's two halves are synchronised separately so one tile's
+//    epilogue overlaps the next tile's main loop.
+//
+// CTA = 192 threads, one CTA per SM, persistent over tiles t = cta, cta+grid..
+//   warp 0   : TMA producer (one lane)          smem ring  <- X tile, W tile
+//   warp 1   : TMEM owner + MMA issuer (one lane) TMEM acc <- tcgen05.mma
+//   warps 2-5: epilogue                          Y        <- TMEM via registers
+// The TMEM accumulator holds two BN-column buffers; acc_full/acc_empty
+// barriers per buffer let the epilogue of tile i run under the MMAs of i+1.
+//
+// Operand layouts in shared memory (both written by TMA with 128B swizzle):
+//   A (X rows, K-major): BM rows x 64 K = BM x 128 B per stage; 8-row groups
+//     1024 B apart.  A K step of 16 elements is +32 B on the start address.
+//   B (W, N-major = "MN-major"): BN/64 panels of 64 columns; a panel is 64 K
+//     rows x 128 B (8 KiB).  LBO = panel stride (8 KiB), SBO = 1024 B (8 K rows).
+//     A K step of 16 is +16 rows = +2048 B on the start address.
+//
+// Every wait is bounded by a global-timer limit.  On expiry the thread raises
+// a CTA-wide abort flag and writes RGG_ERR_DEVICE_TIMEOUT to the status word;
+// every role then leaves its loop, waits (again bounded) for its own
+// in-flight copies or MMAs, and TMEM is freed before the CTA exits.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "rgg_ptx.cuh"
+#include "rgg_tiles.cuh"
+
+namespace rgg {
+
+constexpr int kStatusTimeout = 5;
+constexpr int kStatusBadOffsets = 4;
+constexpr int kStatusCapacity = 6;
+constexpr int kMaxStages = 16;
+constexpr int kThreads = 192;
+constexpr int kEpilogueWarps = 4;
+constexpr int kBK = 64;                  // K elements per stage = one 128-byte swizzle row
+constexpr uint32_t kPanelBytes = 64 * 128;  // one 64-column W panel of 64 K rows
+constexpr uint64_t kDrainLimitNs = 2000000000ull;  // teardown waits for copies/MMAs already issued
+constexpr int32_t kDebugProducerStall = 1;  // test hook: the producer issues nothing
+
+struct GemmArgs {
+    const int32_t* offsets;  // device int32 [E+1]
+    __nv_bfloat16* Y;        // device bf16 [M_tot, N]
+    int32_t* status;         // device status word
+    int64_t M_tot;
+    int32_t E, K, N;
+    int32_t num_k_blocks;    // ceil(K / 64)
+    int32_t n_tiles_n;       // ceil(N / BN)
+    int32_t stages;
+    int32_t y_vec32;         // 1: rows of Y are 32-byte aligned (256-bit stores)
+    int32_t debug_flags;     // 0 in normal use; kDebugProducerStall for failure-detection tests
+    uint64_t timeout_ns;
+};
+
+// Shared-memory carve-up shared by the host planner and the kernel.  Offsets
+// are from a 1024-byte aligned base; the host adds 1024 bytes of slack for
+// aligning the dynamic shared-memory window.
+struct SmemPlan {
+    uint32_t a_stage, b_stage, a_off, b_off, bar_off, misc_off, off_off, pre_off, total;
+};
+
+__host__ __device__ inline SmemPlan smem_plan(int BM, int BN, int stages, int E) {
+    SmemPlan p;
+    p.a_stage = static_cast<uint32_t>(BM) * 128u;
+    p.b_stage = static_cast<uint32_t>(BN) * 128u;
+    p.a_off = 0;
+    p.b_off = p.a_off + stages * p.a_stage;
+    p.bar_off = p.b_off + stages * p.b_stage;          // full[S], empty[S], acc_full[2], acc_empty[2], drain
+    p.misc_off = p.bar_off + 8u * (2u * stages + 5u);   // tmem base, abort flag (16 B reserved)
+    p.off_off = p.misc_off + 16u;
+    p.pre_off = p.off_off + 4u * static_cast<uint32_t>(E + 1);
+    p.total = p.pre_off + 4u * static_cast<uint32_t>(E + 1);
+    return p;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                              int32_t* status, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1u;
+            atomicCAS(status, 0, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// Used only while tearing down after an abort: waits for the barrier without
+// looking at the abort flag, still bounded by the time limit.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    return true;
+}
+
+template <int BM, int BN>
+struct TileConfig {
+    static_assert(BM == 64 || BM == 128, "tcgen05 cta_group::1 tiles are 64 or 128 rows");
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN is a multiple of one 64-column panel, at most 256");
+    static constexpr uint32_t kTmemCols = (2 * BN <= 256) ? 256u : 512u;  // two accumulator buffers
+    static constexpr uint32_t kStageTx = static_cast<uint32_t>((BM + BN) * kBK * 2);
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*b_mn_major=*/true);
+};
+
+template <int BM, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                        const GemmArgs args) {
+    using Cfg = TileConfig<BM, BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int E = args.E;
+    const int S = args.stages;
+
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const SmemPlan sp = smem_plan(BM, BN, S, E);
+    const uint32_t a0 = base + sp.a_off;
+    const uint32_t b0 = base + sp.b_off;
+    const uint32_t bars = base + sp.bar_off;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+    auto accf_bar = [&](int a) { return bars + 8u * (2 * S + a); };
+    auto acce_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + sp.misc_off);
+    int32_t* s_off = reinterpret_cast<int32_t*>(gbase + sp.off_off);
+    int32_t* s_pre = reinterpret_cast<int32_t*>(gbase + sp.pre_off);
+
+    // S1: group offsets -> validated per-expert tile prefix.
+    if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
+        if (threadIdx.x == 0) atomicCAS(args.status, 0, kStatusBadOffsets);
+        return;
+    }
+    if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
+    __syncthreads();
+    const int32_t T = s_pre[E];
+    if (static_cast<int32_t>(blockIdx.x) >= T) return;  // uniform over the CTA
+
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), kEpilogueWarps);
+        }
+        mbar_init(drain_bar, 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmap_x);
+        tma_prefetch_map(&tmap_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&misc[0]), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+
+    const uint32_t tmem_base = misc[0];
+    volatile uint32_t* abort_flag = &misc[1];
+    const int KB = args.num_k_blocks;
+    const int nN = args.n_tiles_n;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- S4: TMA producer
+        if (lane == 0 && (args.debug_flags & kDebugProducerStall) == 0) {
+            int st = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
+                const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_or_abort(empty_bar(st), ph ^ 1u, abort_flag, args.status, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(st), Cfg::kStageTx);
+                    tma_load_2d(a0 + st * sp.a_stage, &tmap_x, full_bar(st), kb * kBK, c.row0);
+#pragma unroll
+                    for (int p = 0; p < BN / 64; ++p)
+                        tma_load_3d(b0 + st * sp.b_stage + p * kPanelBytes, &tmap_w, full_bar(st), c.col0 + 64 * p,
+                                    kb * kBK, c.expert);
+                    ++issued;
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let the copies already issued land before the CTA can exit.
+                const uint32_t n = issued < static_cast<uint32_t>(S) ? issued : static_cast<uint32_t>(S);
+                for (uint32_t i = issued - n; i < issued; ++i)
+                    wait_bounded(full_bar(static_cast<int>(i % S)), (i / S) & 1u, kDrainLimitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ S5: MMA issuer
+        if (lane == 0) {
+            int st = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t acc_ph = 0;
+            bool ok = true;
+            for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
+                if (!wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, args.status, args.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_or_abort(full_bar(st), ph, abort_flag, args.status, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_st = a0 + st * sp.a_stage;
+                    const uint32_t b_st = b0 + st * sp.b_stage;
+#pragma unroll
+                    for (int j = 0; j < kBK / 16; ++j) {
+                        const uint64_t ad = sw128_desc(a_st + 32u * j, 16u, 1024u);
+                        const uint64_t bd = sw128_desc(b_st + 2048u * j, kPanelBytes, 1024u);
+                        mma_bf16_ss(d_tmem, ad, bd, Cfg::kIdesc, (kb | j) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(st));  // frees the stage once these MMAs have read it
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(accf_bar(acc));      // accumulator buffer ready for the epilogue
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_ph ^= 1u;
+                }
+            }
+            if (!ok) {
+                mma_commit(drain_bar);
+                wait_bounded(drain_bar, 0u, kDrainLimitNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- S6: epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        const int r_local = (BM == 128) ? (q * 32 + lane) : (q * 16 + (lane & 15));
+        const bool lane_has_row = (BM == 128) || (lane < 16);
+        const int N = args.N;
+        int acc = 0;
+        uint32_t acc_ph = 0;
+        for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
+            const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+            bool ok = wait_or_abort(accf_bar(acc), acc_ph, abort_flag, args.status, args.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            const bool row_ok = lane_has_row && (r_local < c.rows);
+            __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0;
+#pragma unroll 1
+            for (int cc = 0; cc < BN; cc += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int col = c.col0 + cc + 16 * h;
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
+                        __nv_bfloat16* dst = yrow + cc + 16 * h;
+                        if (col + 16 <= N) {
+                            if (args.y_vec32) {
+                                st_global_v8(dst, w);
+                            } else {
+                                st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                                st_global_v4(dst + 8, w[4], w[5], w[6], w[7]);
+                            }
+                        } else if (col + 8 <= N) {
+                            st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(acc));
+            if (++acc == 2) {
+                acc = 0;
+                acc_ph ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+}  // namespace rgg

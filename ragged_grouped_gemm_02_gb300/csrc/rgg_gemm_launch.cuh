@@ -1,0 +1,20 @@
+// rgg_gemm_launch.cuh -- the host-side launch of one grouped_gemm_kernel
+// instantiation (included by the per-BM translation units).
+#pragma once
+
+#include "rgg_internal.h"
+
+namespace rgg {
+
+template <int BM, int BN>
+cudaError_t launch_gemm_instance(int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
+                                 const CUtensorMap& tmap_w, const GemmArgs& args) {
+    auto kernel = grouped_gemm_kernel<BM, BN>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    kernel<<<grid, kThreads, smem, stream>>>(tmap_x, tmap_w, args);
+    return cudaGetLastError();
+}
+
+}  // namespace rgg

@@ -1,0 +1,30 @@
+// rgg_internal.h -- launch entry points shared between the C ABI layer
+// (rgg_api.cu) and the translation units that instantiate the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "rgg_gemm.cuh"
+
+namespace rgg {
+
+// Grouped GEMM kernels, one translation unit per BM.  `bn` is 128, 192 or
+// 256.  Returns cudaErrorInvalidValue for a shape with no instantiation.
+cudaError_t launch_gemm_bm128(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
+                              const CUtensorMap& tmap_w, const GemmArgs& args);
+cudaError_t launch_gemm_bm64(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
+                             const CUtensorMap& tmap_w, const GemmArgs& args);
+
+// The flat tile list written out by the same device code the GEMM uses.
+cudaError_t launch_export_tiles(const int32_t* offsets, int E, int64_t M_tot, int N, int bm, int bn,
+                                int32_t* desc, int64_t cap, int32_t* n_tiles, int32_t* status,
+                                cudaStream_t stream);
+
+// Offsets check alone (used when there are no rows to multiply).
+cudaError_t launch_validate_offsets(const int32_t* offsets, int E, int64_t M_tot, int32_t* status,
+                                    cudaStream_t stream);
+
+}  // namespace rgg

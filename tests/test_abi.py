@@ -1,0 +1,148 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry
+point include/rgg.h declares, and its host-only logic (the planner, argument
+checks, status strings) behaves as documented.  No compute call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ragged_grouped_gemm_02_gb300 as rgg
+from ragged_grouped_gemm_02_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return rgg.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(rgg_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    assert set(rgg.EXPORTED_SYMBOLS) <= names
+    assert "rgg_grouped_gemm" in names and "rgg_export_tiles" in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), "librgg.so does not export %s" % name
+
+
+def test_library_has_no_runtime_cuda_dependency():
+    # the CUDA runtime is linked statically; the library loads on a machine
+    # without a GPU or a driver and reaches the driver only when called
+    import subprocess
+    out = subprocess.run(["ldd", rgg.library_path()], capture_output=True, text=True).stdout
+    assert "libcudart" not in out and "libcuda.so" not in out
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = rgg.rgg_status_string(code)
+        assert s.startswith("RGG_")
+    assert rgg.rgg_status_string(99) == "unknown rgg_status"
+
+
+def test_null_handle_is_rejected_without_touching_cuda(lib):
+    P = ctypes.c_void_p
+    s = lib.rgg_grouped_gemm(None, P(16), P(16), P(16), P(16), 4, 256, 256, 512, None, None)
+    assert s == rgg.RGG_ERR_INVALID_ARG
+    assert lib.rgg_query_status(None, None) == rgg.RGG_ERR_INVALID_ARG
+    assert lib.rgg_export_tiles(None, P(16), 4, 256, 512, 128, 128, None, 0, P(16), None) == rgg.RGG_ERR_INVALID_ARG
+
+
+def test_create_without_a_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    s = lib.rgg_create(ctypes.byref(h), 0)
+    assert s in (rgg.RGG_ERR_CUDA, rgg.RGG_ERR_INVALID_ARG)
+    assert not h.value
+
+
+# ------------------------------------------------------------------ planner
+
+def test_plan_small_decode_uses_64_row_tiles(lib):
+    # 16 rows per expert: the Pearl article's 64-row tiles where experts average <= 64 rows
+    p = rgg.rgg_plan(32, 512, 6144, 4096)
+    assert p["bm"] == 64 and p["bk"] == 64 and p["threads"] == 192
+    assert p["grid"] == 152 and 2 <= p["stages"] <= 16
+    assert p["smem_bytes"] <= 232448
+
+
+def test_plan_large_groups_use_128_row_tiles(lib):
+    p = rgg.rgg_plan(64, 16384, 1024, 2688)
+    assert p["bm"] == 128
+    assert p["bn"] in (128, 192, 256)
+    assert p["tmem_cols"] == (256 if p["bn"] == 128 else 512)
+
+
+def test_plan_stages_fill_shared_memory(lib):
+    for bm, bn in [(64, 128), (64, 256), (128, 128), (128, 192), (128, 256)]:
+        p = rgg.rgg_plan(64, 16384, 1024, 2688, bm=bm, bn=bn)
+        stage = (bm + bn) * 128
+        assert p["bm"] == bm and p["bn"] == bn
+        # one more stage would not fit
+        assert p["stages"] == 16 or (p["stages"] + 1) * stage + 1024 > 232448 - 8 * 65 - 200
+        # more than half the SM's shared memory: one CTA (one TMEM allocation) per SM
+        assert p["smem_bytes"] > 232448 // 2
+
+
+def test_plan_host_counts_guide_bm(lib):
+    # most experts tiny, but the routed rows average > 64 over busy experts
+    counts = [0] * 60 + [1000, 1000, 1000, 1000]
+    assert rgg.rgg_plan(64, 4000, 1024, 2688, host_counts=counts)["bm"] == 128
+    counts = [16] * 32
+    assert rgg.rgg_plan(32, 512, 6144, 4096, host_counts=counts)["bm"] == 64
+
+
+def test_plan_grid_never_exceeds_tiles_or_sms(lib):
+    p = rgg.rgg_plan(4, 256, 256, 512)
+    assert p["max_tiles"] == (256 // p["bm"] + 4) * (-(-512 // p["bn"]))
+    assert p["grid"] <= min(152, p["max_tiles"])
+    assert rgg.rgg_plan(4, 256, 256, 512, max_ctas=3)["grid"] == 3
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, num_sms=148)["grid"] == 148
+
+
+@pytest.mark.parametrize("kw", [dict(E=0), dict(K=12), dict(N=100), dict(K=4), dict(M_tot=-1),
+                                dict(M_tot=2 ** 31)])
+def test_plan_rejects_bad_sizes(lib, kw):
+    args = dict(E=4, M_tot=256, K=256, N=512)
+    args.update(kw)
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_plan(args["E"], args["M_tot"], args["K"], args["N"])
+    assert ei.value.status == rgg.RGG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(bm=32), dict(bn=64), dict(stages=1), dict(stages=17), dict(max_ctas=-1)])
+def test_plan_rejects_bad_options(lib, kw):
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_plan(4, 256, 256, 512, **kw)
+    assert ei.value.status == rgg.RGG_ERR_INVALID_ARG
+
+
+def test_plan_rejects_too_many_experts(lib):
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_plan(4097, 4097, 256, 512)
+    assert ei.value.status == rgg.RGG_ERR_UNSUPPORTED
+
+
+def test_plan_too_many_stages_for_shared_memory(lib):
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_plan(64, 16384, 1024, 2688, bm=128, bn=256, stages=16)
+    assert ei.value.status == rgg.RGG_ERR_UNSUPPORTED

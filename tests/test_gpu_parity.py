@@ -1,0 +1,258 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, on a GB300.
+
+Tolerance (the contract the method states): |gpu - oracle| <= 1e-2 * max(1, |oracle|)
+elementwise, the oracle in fp64 and not rounded to bf16.  Integer-valued
+inputs with K <= 64 are exact in fp32 and in bf16, so there the GPU must
+equal the oracle bit for bit; that also pins the TMEM lane-to-row mapping,
+the swizzled operand layouts and the row/column masks.  The flat tile list
+must match the oracle's enumeration exactly.
+
+Rows that belong to no expert are pre-filled with a NaN canary bit pattern
+and must still hold it afterwards.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ragged_grouped_gemm_02_gb300 as rgg
+from ragged_grouped_gemm_02_gb300 import _build
+from ragged_grouped_gemm_02_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+CANARY = 0x7FC1  # a bf16 NaN the kernel never produces
+RTOL = 1e-2
+SHAPES = [(64, 128), (64, 192), (64, 256), (128, 128), (128, 192), (128, 256)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    _build.build()
+    oracle.build()
+    assert rgg.load_library() is not None
+    return torch.device("cuda:0")
+
+
+def _canary(M, N):
+    return torch.full((M, N), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+
+
+def _run(inp, offsets=None, **opts):
+    off = inp.offsets if offsets is None else np.asarray(offsets, dtype=np.int32)
+    X = inp.X.cuda()
+    W = inp.W.cuda()
+    d_off = torch.from_numpy(off).cuda()
+    Y = _canary(X.shape[0], W.shape[2])
+    rgg.rgg_grouped_gemm(X, W, d_off, Y, check=True, **opts)
+    torch.cuda.synchronize()
+    return Y.cpu()
+
+
+def _assert_untouched(Y, rows):
+    bits = Y.view(torch.int16)[rows]
+    assert bool((bits == CANARY).all()), "rows that belong to no expert were written"
+
+
+def _assert_close(Y, ref, rows):
+    y = Y[rows].double().numpy()
+    r = ref[rows]
+    err = np.abs(y - r)
+    bound = RTOL * np.maximum(1.0, np.abs(r))
+    bad = np.argwhere(~(err <= bound))
+    assert bad.size == 0, "%d outputs out of tolerance; first %s: gpu %r oracle %r" % (
+        bad.shape[0], bad[0].tolist(), y[tuple(bad[0])], r[tuple(bad[0])])
+
+
+def _full_parity(inp, offsets=None, **opts):
+    off = inp.offsets if offsets is None else np.asarray(offsets, dtype=np.int32)
+    Y = _run(inp, off, **opts)
+    ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), off)
+    M = inp.X.shape[0]
+    covered = np.zeros(M, dtype=bool)
+    covered[off[0]:off[-1]] = True
+    _assert_close(Y, ref, covered)
+    if (~covered).any():
+        _assert_untouched(Y, torch.from_numpy(~covered))
+    return Y, ref
+
+
+# ---------------------------------------------------------------- small cases
+
+@pytest.mark.parametrize("bm,bn", SHAPES)
+def test_tiny_config_every_tile_shape(bm, bn):
+    _full_parity(wl.make_inputs("tiny"), bm=bm, bn=bn)
+
+
+def test_tiny_config_auto_plan():
+    _full_parity(wl.make_inputs("tiny"))
+
+
+@pytest.mark.parametrize("bm,bn", SHAPES)
+@pytest.mark.parametrize("N", [512, 520])
+def test_integer_inputs_bit_exact(bm, bn, N):
+    # ragged counts around the tile sizes, an empty expert, spare rows at the end;
+    # N = 520 leaves a half 16-column chunk (128-bit store path)
+    counts = [3, 0, 130, 64, 1, 200, 65, 127]
+    inp = wl.make_custom(counts, K=64, N=N, seed=31, integer_valued=True, spare_rows=5)
+    Y = _run(inp, bm=bm, bn=bn)
+    ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
+    M_used = int(inp.offsets[-1])
+    assert np.array_equal(Y[:M_used].double().numpy(), ref[:M_used]), "integer case not bit-exact"
+    _assert_untouched(Y, slice(M_used, None))
+
+
+@pytest.mark.parametrize("bm,bn", [(64, 256), (128, 192), (128, 128)])
+def test_ragged_random_k_and_n_tails(bm, bn):
+    # K = 264 (a 8-wide K tail), N = 640 (not a multiple of 192 or 256), sizes around 64/128
+    counts = [0, 1, 63, 64, 65, 127, 128, 129, 300, 0, 17]
+    inp = wl.make_custom(counts, K=264, N=640, seed=32)
+    _full_parity(inp, bm=bm, bn=bn)
+
+
+def test_ragged_random_auto_plan_many_tiles():
+    counts = [500, 3, 0, 257, 1024, 77, 129, 2, 640, 64]
+    inp = wl.make_custom(counts, K=512, N=1024, seed=33)
+    _full_parity(inp)
+
+
+def test_offsets_need_not_cover_all_rows():
+    # experts own rows [7, 7 + 150); rows before and after belong to nobody
+    inp = wl.make_custom([40, 60, 50], K=128, N=256, seed=34, spare_rows=20)
+    off = np.array([7, 47, 107, 157], dtype=np.int32)
+    _full_parity(inp, offsets=off, bm=128, bn=128)
+    _full_parity(inp, offsets=off, bm=64, bn=256)
+
+
+def test_all_experts_empty_writes_nothing():
+    inp = wl.make_custom([0, 0, 0], K=64, N=128, seed=35, spare_rows=50)
+    Y = _run(inp)
+    _assert_untouched(Y, slice(None))
+
+
+def test_zero_rows():
+    X = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(2, 64, 128, dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    rgg.rgg_grouped_gemm(X, W, torch.zeros(3, dtype=torch.int32, device="cuda"), Y, check=True)
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_grouped_gemm(X, W, torch.tensor([0, 1, 1], dtype=torch.int32, device="cuda"), Y, check=True)
+    assert ei.value.status == rgg.RGG_ERR_BAD_OFFSETS
+
+
+@pytest.mark.parametrize("off", [[0, 50, 40, 100], [0, 50, 60, 101], [-1, 50, 60, 100]])
+def test_bad_offsets_rejected_and_nothing_written(off):
+    inp = wl.make_custom([50, 10, 40], K=64, N=128, seed=36)
+    X, W = inp.X.cuda(), inp.W.cuda()
+    Y = _canary(100, 128)
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_grouped_gemm(X, W, torch.tensor(off, dtype=torch.int32, device="cuda"), Y, check=True)
+    assert ei.value.status == rgg.RGG_ERR_BAD_OFFSETS
+    _assert_untouched(Y.cpu(), slice(None))
+    # the context is still usable and the status word was cleared
+    _full_parity(inp)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    # the producer issues nothing, so the first MMA wait can only end by its limit
+    inp = wl.make_inputs("tiny")
+    X, W = inp.X.cuda(), inp.W.cuda()
+    off = torch.from_numpy(inp.offsets).cuda()
+    Y = _canary(256, 512)
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_grouped_gemm(X, W, off, Y, check=True, timeout_ns=20_000_000,
+                             debug_flags=rgg.RGG_DEBUG_PRODUCER_STALL)
+    assert ei.value.status == rgg.RGG_ERR_DEVICE_TIMEOUT
+    assert rgg.rgg_query_status() == rgg.RGG_OK
+    _full_parity(inp)
+
+
+def test_non_default_stream_and_determinism():
+    inp = wl.make_custom([100, 0, 37, 300], K=256, N=384, seed=37)
+    X, W = inp.X.cuda(), inp.W.cuda()
+    off = torch.from_numpy(inp.offsets).cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        Y1 = rgg.rgg_grouped_gemm(X, W, off)
+        Y2 = rgg.rgg_grouped_gemm(X, W, off)
+    s.synchronize()
+    assert rgg.rgg_query_status(stream=s) == rgg.RGG_OK
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
+    _assert_close(Y1.cpu(), ref, slice(None))
+
+
+# --------------------------------------------------------------- tile list
+
+def _export_matches_oracle(off, M_tot, N, bm, bn):
+    d_off = torch.from_numpy(np.asarray(off, dtype=np.int32)).cuda()
+    desc, T = rgg.rgg_export_tiles(d_off, M_tot, N, bm, bn)
+    ref = oracle.tile_list(off, N, bm, bn)
+    assert T == ref.shape[0]
+    assert np.array_equal(desc.numpy(), ref)
+
+
+@pytest.mark.parametrize("bm,bn", SHAPES)
+@pytest.mark.parametrize("name", ["tiny", "decode", "uniform", "skew16k", "skew2k", "prefill",
+                                  "worklog_skew16k", "decode_sweep_m1", "decode_sweep_m256"])
+def test_tile_list_bit_exact(name, bm, bn):
+    w = wl.WORKLOADS[name]
+    counts = wl.workload_counts(w)
+    _export_matches_oracle(wl.offsets_from_counts(counts), int(counts.sum()), w.N, bm, bn)
+
+
+def test_tile_list_edge_cases():
+    _export_matches_oracle([0, 0, 0], 10, 512, 128, 128)
+    _export_matches_oracle([3, 3, 10, 10, 11], 20, 520, 64, 256)
+    off = wl.offsets_from_counts(np.random.default_rng(5).integers(0, 300, 4096))
+    _export_matches_oracle(off, int(off[-1]), 4096, 128, 256)
+
+
+def test_tile_list_capacity():
+    off = np.array([0, 37, 37, 101, 256], dtype=np.int32)
+    d_off = torch.from_numpy(off).cuda()
+    desc, T = rgg.rgg_export_tiles(d_off, 256, 512, 128, 128, cap=5)
+    ref = oracle.tile_list(off, 512, 128, 128)
+    assert T == 16 and desc.shape == (5, 4)
+    assert np.array_equal(desc.numpy(), ref[:5])
+
+
+# --------------------------------------------------------- full-size configs
+
+FULL = ["decode", "uniform", "skew16k", "skew2k", "prefill"] + [
+    "decode_sweep_m%d" % m for m in (1, 4, 8, 32, 64, 128, 256)]
+
+
+def _sample_points(off, N, rng, per_expert=4, extra=2000):
+    rows, cols = [], []
+    E = off.size - 1
+    for e in range(E):
+        if off[e + 1] > off[e]:
+            for r in (off[e], off[e + 1] - 1):
+                rows += [r] * per_expert
+                cols += list(rng.integers(0, N, per_expert - 1)) + [N - 1]
+    rr = rng.integers(off[0], off[-1], extra)
+    rows += list(rr)
+    cols += list(rng.integers(0, N, extra))
+    return np.asarray(rows, dtype=np.int64), np.asarray(cols, dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_config_sampled(name):
+    inp = wl.make_inputs(name)
+    X, W = inp.X.cuda(), inp.W.cuda()
+    off = torch.from_numpy(inp.offsets).cuda()
+    Y = rgg.rgg_grouped_gemm(X, W, off, check=True)  # the launch configuration the benchmark times
+    torch.cuda.synchronize()
+    # a property that holds at any size: every output of a routed row is finite
+    assert bool(torch.isfinite(Y).all())
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    rows, cols = _sample_points(inp.offsets, inp.W.shape[2], rng)
+    ref = oracle.grouped_gemm_points(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets, rows, cols)
+    got = Y[torch.from_numpy(rows).cuda(), torch.from_numpy(cols.astype(np.int64)).cuda()].double().cpu().numpy()
+    err = np.abs(got - ref)
+    bound = RTOL * np.maximum(1.0, np.abs(ref))
+    assert (err <= bound).all(), "max err %.4g at %d" % (err.max(), int(np.argmax(err - bound)))
