@@ -63,6 +63,8 @@ def parse_args():
     p.add_argument("--bm", type=int, default=0)
     p.add_argument("--bn", type=int, default=0)
     p.add_argument("--stages", type=int, default=0)
+    p.add_argument("--profile", action="store_true",
+                   help="for ncu: --warmup launches then one more, no timing, no CPU work after")
     return p.parse_args()
 
 
@@ -222,6 +224,28 @@ def oracle_cpu_rate(inp, budget_s=12.0):
 
 
 # --------------------------------------------------------------- our arm
+
+def run_profile(args):
+    """A short, fixed launch sequence for ncu captures: `--warmup` launches,
+    then one more (capture it with -s <warmup> -c 1)."""
+    import ragged_grouped_gemm_02_gb300 as rgg
+    from ragged_grouped_gemm_02_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    inp = wl.make_inputs(args.workload)
+    X, W = inp.X.to(dev), inp.W.to(dev)
+    off = torch.from_numpy(inp.offsets).to(dev)
+    Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device=dev)
+    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages)
+    for _ in range(args.warmup + 1):
+        rgg.rgg_grouped_gemm(X, W, off, Y, **opts)
+    torch.cuda.synchronize(dev)
+    status = rgg.rgg_query_status(0)
+    plan = rgg.rgg_plan(inp.workload.E, X.shape[0], inp.workload.K, inp.workload.N, **opts)
+    print(json.dumps({"profile": args.workload, "launches": args.warmup + 1, "status": status, "plan": plan}))
+    if status != rgg.RGG_OK:
+        raise SystemExit(1)
+
 
 def run_ours(args):
     import ragged_grouped_gemm_02_gb300 as rgg
@@ -407,7 +431,9 @@ def run_reference(args):
 
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -57,7 +57,8 @@ typedef struct rgg_handle rgg_handle;
 
 /* Tuning overrides; a zeroed struct (or a NULL pointer) means "choose automatically". */
 typedef struct rgg_options {
-    int bm;                      /* rows per tile: 0 = auto, or 64, 128 */
+    int bm;                      /* rows per tile: 0 = auto, or 64, 128, or 256 = a CTA pair on two SMs
+                                    (tcgen05 cta_group::2, 128 rows per CTA; BN must then be 128 or 256) */
     int bn;                      /* columns per tile: 0 = auto, or 128, 192, 256 */
     int stages;                  /* shared-memory ring depth: 0 = as many as fit, else 2..16 */
     int max_ctas;                /* persistent CTAs: 0 = one per SM, else an upper bound */
@@ -121,7 +122,7 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
  * desc_out: device int32 [4 * cap] (may be NULL when cap == 0).
  * n_tiles_out: device int32 [1], receives the total tile count T (also when
  * T > cap, in which case only the first cap descriptors are written and the
- * status word records RGG_ERR_CAPACITY).  bm in {64, 128}, bn in
+ * status word records RGG_ERR_CAPACITY).  bm in {64, 128, 256}, bn in
  * {128, 192, 256}.  Asynchronous on `stream`; invalid offsets are reported by
  * rgg_query_status (T is then written as -1).
  */

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "librgg.so")
 
-SOURCES = ["rgg_api.cu", "rgg_aux.cu", "rgg_gemm_bm128.cu", "rgg_gemm_bm64.cu"]
+SOURCES = ["rgg_api.cu", "rgg_aux.cu", "rgg_gemm_bm128.cu", "rgg_gemm_bm64.cu", "rgg_gemm_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

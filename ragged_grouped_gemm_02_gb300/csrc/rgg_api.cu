@@ -105,11 +105,12 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     const int want_bn = opt ? opt->bn : 0;
     const int want_stages = opt ? opt->stages : 0;
     const int max_ctas = opt ? opt->max_ctas : 0;
-    if (want_bm != 0 && want_bm != 64 && want_bm != 128) return RGG_ERR_INVALID_ARG;
+    if (want_bm != 0 && want_bm != 64 && want_bm != 128 && want_bm != 256) return RGG_ERR_INVALID_ARG;
     if (want_bn != 0 && want_bn != 128 && want_bn != 192 && want_bn != 256) return RGG_ERR_INVALID_ARG;
+    if (want_bm == 256 && want_bn == 192) return RGG_ERR_INVALID_ARG;  // pair tiles split BN in whole panels
     if (want_stages != 0 && (want_stages < 2 || want_stages > rgg::kMaxStages)) return RGG_ERR_INVALID_ARG;
     if (max_ctas < 0) return RGG_ERR_INVALID_ARG;
-    const int grid_cap = max_ctas > 0 ? std::min(max_ctas, num_sms) : num_sms;
+    int grid_cap = max_ctas > 0 ? std::min(max_ctas, num_sms) : num_sms;
 
     // Per-expert M tiles at each BM: exact with host counts, else the
     // balanced estimate E * ceil(avg / BM).
@@ -139,6 +140,9 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         }
         bm = (avg <= 64.0) ? 64 : 128;
     }
+    const bool pair = (bm == 256);
+    // A CTA pair (256-row tile) counts as one unit of persistent work.
+    const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;
 
     // BN: fewest waves of persistent work, a tile costing about (BN + 64)
     // units (MMA and weight bytes scale with BN, plus a fixed per-tile cost);
@@ -148,8 +152,9 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         const int64_t mt = std::max<int64_t>(1, m_tiles(bm));
         int64_t best = INT64_MAX;
         for (int cand : {256, 192, 128}) {
+            if (pair && cand == 192) continue;
             const int64_t tiles = mt * ceil_div(N, cand);
-            const int64_t waves = ceil_div(tiles, grid_cap);
+            const int64_t waves = ceil_div(tiles, units);
             const int64_t cost = waves * (cand + 64);
             if (cost < best) {
                 best = cost;
@@ -161,14 +166,17 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     const int64_t max_tiles = tile_bound(E, M_tot, N, bm, bn);
     if (max_tiles >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
 
-    const rgg::SmemPlan probe = rgg::smem_plan(bm, bn, 0, E);
-    const int64_t per_stage = static_cast<int64_t>(bm + bn) * 128 + 16;  // tiles + two barriers
+    // Per-CTA tile extents: a pair CTA holds 128 rows of A and half of B.
+    const int cta_m = pair ? 128 : bm;
+    const int cta_n = pair ? bn / 2 : bn;
+    const rgg::SmemPlan probe = rgg::smem_plan(cta_m, cta_n, 0, E);
+    const int64_t per_stage = static_cast<int64_t>(cta_m + cta_n) * 128 + 16;  // tiles + two barriers
     const int64_t room = static_cast<int64_t>(smem_optin) - 1024 - probe.total - 64;
     int fit = static_cast<int>(std::min<int64_t>(rgg::kMaxStages, room / per_stage));
     int stages = want_stages ? want_stages : fit;
     if (stages < 2 || stages > fit) return RGG_ERR_UNSUPPORTED;
 
-    const rgg::SmemPlan sp = rgg::smem_plan(bm, bn, stages, E);
+    const rgg::SmemPlan sp = rgg::smem_plan(cta_m, cta_n, stages, E);
     // Ask for more than half of the SM's shared memory so that exactly one CTA
     // (and one 2 x BN-column TMEM allocation) lives on each SM.
     const int smem = std::max<int>(static_cast<int>(sp.total) + 1024, smem_optin / 2 + 1024);
@@ -177,7 +185,8 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     out->bm = bm;
     out->bn = bn;
     out->stages = stages;
-    out->grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(grid_cap, max_tiles)));
+    out->grid = pair ? static_cast<int>(2 * std::max<int64_t>(1, std::min<int64_t>(units, max_tiles)))
+                     : static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(grid_cap, max_tiles)));
     out->smem_bytes = smem;
     out->max_tiles = max_tiles;
     return RGG_OK;
@@ -190,11 +199,11 @@ rgg_status encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K
         g_last_cuda_error = "cuTensorMapEncodeTiled is not available from the driver";
         return RGG_ERR_CUDA;
     }
-    // X: 2-D {K, M_tot}, box {64, BM}: one 128-byte swizzle row per tile row.
+    // X: 2-D {K, M_tot}, box {64, rows per CTA}: one 128-byte swizzle row per tile row.
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M_tot)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bm)};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bm > 128 ? 128 : bm)};
         const cuuint32_t estr[2] = {1, 1};
         CUresult r = encode(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -298,7 +307,7 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->grid = p.grid;
     out->threads = rgg::kThreads;
     out->smem_bytes = p.smem_bytes;
-    out->tmem_cols = (2 * p.bn <= 256) ? 256 : 512;
+    out->tmem_cols = (p.bm == 256 || 2 * p.bn > 256) ? 512 : 256;
     out->max_tiles = p.max_tiles;
     return RGG_OK;
 }
@@ -343,8 +352,9 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
     a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
 
-    cudaError_t err = (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tw, a)
-                                    : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tw, a);
+    cudaError_t err = (p.bm == 256)   ? rgg::launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tw, a)
+                      : (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tw, a)
+                                      : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm launch");
 }
 
@@ -353,7 +363,7 @@ rgg_status rgg_export_tiles(rgg_handle* h, const int32_t* group_offsets, int E, 
     if (!h || !group_offsets || !n_tiles_out || cap < 0 || (cap > 0 && !desc_out)) return RGG_ERR_INVALID_ARG;
     if (E < 1 || E > rgg::kMaxExperts || M_tot < 0 || M_tot >= (int64_t(1) << 31) || N < 1)
         return RGG_ERR_INVALID_ARG;
-    if ((bm != 64 && bm != 128) || (bn != 128 && bn != 192 && bn != 256)) return RGG_ERR_INVALID_ARG;
+    if ((bm != 64 && bm != 128 && bm != 256) || (bn != 128 && bn != 192 && bn != 256)) return RGG_ERR_INVALID_ARG;
     if (tile_bound(E, M_tot, N, bm, bn) >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
     DeviceScope scope(h->device);
     if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");

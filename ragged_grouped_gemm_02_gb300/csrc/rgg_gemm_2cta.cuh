@@ -1,0 +1,290 @@
+// rgg_gemm_2cta.cuh -- the CTA-pair (tcgen05 cta_group::2) variant for large
+// expert groups: 256-row tiles computed by two CTAs on neighbouring SMs.
+//
+// "Pearl's grouped GEMM kernel for MoE models, explained", "Four changes,
+// three of them measured", describes a baseline library that offers its
+// smaller tiles only in a two-block mode; for large groups the pair mode is
+// the natural shape on Blackwell: one tcgen05.mma of M = 256 reads the A rows
+// of both CTAs (128 each) and the B columns of both CTAs (BN/2 each) and
+// writes each CTA's 128 accumulator rows into that CTA's TMEM.  Each CTA
+// therefore loads only half of the weight tile per stage, which halves the
+// shared-memory fill per FLOP compared with one CTA holding the whole
+// 128 x BN tile.  No TMA multicast is used: every CTA loads its own boxes.
+//
+// Roles (both CTAs run the same code, rank = %cluster_ctarank):
+//   warp 0 lane 0 : producer.  Waits its own empty[s]; the leader (rank 0)
+//                   arms its full[s] for both CTAs' bytes; both CTAs' TMA
+//                   loads complete on the leader's full[s].
+//   warp 1        : allocates the pair's TMEM in both CTAs; lane 0 of the
+//                   leader issues every MMA and commits to the empty /
+//                   acc_full barriers of both CTAs at once (multicast).
+//   warps 2-5     : epilogue of the CTA's own 128 rows; they arrive on the
+//                   leader's acc_empty (8 arrivals: 4 warps x 2 CTAs).
+// All waits are bounded; an abort raised in either CTA is mirrored into the
+// other CTA's flag so the pair leaves its loops together.
+#pragma once
+
+#include "rgg_gemm.cuh"
+
+namespace rgg {
+
+template <int BN>
+struct PairConfig {
+    static_assert(BN == 128 || BN == 256, "pair tiles split BN into two whole 64-column panel sets");
+    static constexpr int kHalfN = BN / 2;           // B columns held by each CTA
+    static constexpr int kPanels = kHalfN / 64;
+    static constexpr uint32_t kTmemCols = 512;      // two BN-column fp32 buffers (BN <= 256)
+    static constexpr uint32_t kStageBytesPerCta = static_cast<uint32_t>((128 + kHalfN) * kBK * 2);
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(256, BN, /*b_mn_major=*/true);
+};
+
+__device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                   uint32_t peer_flag_cluster, int32_t* status, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1u;
+            st_shared_cluster_u32(peer_flag_cluster, 1u);
+            atomicCAS(status, 0, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) {
+    }
+}
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                             const GemmArgs args) {
+    using Cfg = PairConfig<BN>;
+    constexpr int BM = 256;  // rows per pair tile
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int E = args.E;
+    const int S = args.stages;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t pair = cluster_id_x();
+    const uint32_t npairs = cluster_count_x();
+
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const SmemPlan sp = smem_plan(128, Cfg::kHalfN, S, E);
+    const uint32_t a0 = base + sp.a_off;
+    const uint32_t b0 = base + sp.b_off;
+    const uint32_t bars = base + sp.bar_off;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+    auto accf_bar = [&](int a) { return bars + 8u * (2 * S + a); };
+    auto acce_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + sp.misc_off);
+    int32_t* s_off = reinterpret_cast<int32_t*>(gbase + sp.off_off);
+    int32_t* s_pre = reinterpret_cast<int32_t*>(gbase + sp.pre_off);
+
+    // S1, identical in both CTAs, so every early exit below is pair-uniform.
+    if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
+        if (threadIdx.x == 0 && rank == 0) atomicCAS(args.status, 0, kStatusBadOffsets);
+        return;
+    }
+    if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
+    __syncthreads();
+    const int32_t T = s_pre[E];
+    if (static_cast<int32_t>(pair) >= T) return;
+
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), 2 * kEpilogueWarps);
+        }
+        mbar_init(drain_bar, 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmap_x);
+        tma_prefetch_map(&tmap_w);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(&misc[0]), Cfg::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
+    tc_fence_after_sync();
+
+    const uint32_t tmem_base = misc[0];
+    volatile uint32_t* abort_flag = &misc[1];
+    const uint32_t peer_flag = map_to_rank(smem_addr(&misc[1]), rank ^ 1u);
+    const int KB = args.num_k_blocks;
+    const int nN = args.n_tiles_n;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- S4: TMA producer
+        if (lane == 0 && (args.debug_flags & kDebugProducerStall) == 0) {
+            int st = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int32_t t = pair; ok && t < T; t += npairs) {
+                const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+                const int32_t a_row = c.row0 + 128 * static_cast<int32_t>(rank);
+                const int32_t b_col = c.col0 + Cfg::kHalfN * static_cast<int32_t>(rank);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!pair_wait_or_abort(empty_bar(st), ph ^ 1u, abort_flag, peer_flag, args.status,
+                                            args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_leader = map_to_rank(full_bar(st), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(st), 2u * Cfg::kStageBytesPerCta);
+                    tma_load_2d_pair(a0 + st * sp.a_stage, &tmap_x, full_leader, kb * kBK, a_row);
+#pragma unroll
+                    for (int p = 0; p < Cfg::kPanels; ++p)
+                        tma_load_3d_pair(b0 + st * sp.b_stage + p * kPanelBytes, &tmap_w, full_leader, b_col + 64 * p,
+                                         kb * kBK, c.expert);
+                    ++issued;
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // The leader's full barriers count both CTAs' bytes: it waits
+                // for the stages it armed; the peer gives its copies a grace
+                // period (they land in microseconds).
+                if (rank == 0) {
+                    const uint32_t n = issued < static_cast<uint32_t>(S) ? issued : static_cast<uint32_t>(S);
+                    for (uint32_t i = issued - n; i < issued; ++i)
+                        wait_bounded(full_bar(static_cast<int>(i % S)), (i / S) & 1u, kDrainLimitNs);
+                } else {
+                    spin_ns(200000ull);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------- S5: MMA issuer (leader only)
+        if (lane == 0 && rank == 0) {
+            int st = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t acc_ph = 0;
+            bool ok = true;
+            for (int32_t t = pair; ok && t < T; t += npairs) {
+                if (!pair_wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, peer_flag, args.status,
+                                        args.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!pair_wait_or_abort(full_bar(st), ph, abort_flag, peer_flag, args.status, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_st = a0 + st * sp.a_stage;
+                    const uint32_t b_st = b0 + st * sp.b_stage;
+#pragma unroll
+                    for (int j = 0; j < kBK / 16; ++j) {
+                        const uint64_t ad = sw128_desc(a_st + 32u * j, 16u, 1024u);
+                        const uint64_t bd = sw128_desc(b_st + 2048u * j, kPanelBytes, 1024u);
+                        mma_bf16_ss_pair(d_tmem, ad, bd, Cfg::kIdesc, (kb | j) != 0 ? 1u : 0u);
+                    }
+                    mma_commit_pair(empty_bar(st), 0x3);
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair(accf_bar(acc), 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_ph ^= 1u;
+                }
+            }
+            if (!ok) {
+                mma_commit_pair(drain_bar, 0x1);
+                wait_bounded(drain_bar, 0u, kDrainLimitNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- S6: epilogue
+        const int q = warp & 3;
+        const int r_local = 128 * static_cast<int>(rank) + q * 32 + lane;
+        const int N = args.N;
+        int acc = 0;
+        uint32_t acc_ph = 0;
+        for (int32_t t = pair; t < T; t += npairs) {
+            const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+            bool ok = pair_wait_or_abort(accf_bar(acc), acc_ph, abort_flag, peer_flag, args.status, args.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            const bool row_ok = r_local < c.rows;
+            __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0;
+#pragma unroll 1
+            for (int cc = 0; cc < BN; cc += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int col = c.col0 + cc + 16 * h;
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
+                        __nv_bfloat16* dst = yrow + cc + 16 * h;
+                        if (col + 16 <= N) {
+                            if (args.y_vec32) {
+                                st_global_v8(dst, w);
+                            } else {
+                                st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                                st_global_v4(dst + 8, w[4], w[5], w[6], w[7]);
+                            }
+                        } else if (col + 8 <= N) {
+                            st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar(acc), 0));
+            if (++acc == 2) {
+                acc = 0;
+                acc_ph ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    cluster_sync_all();  // neither CTA leaves while the pair's MMAs or arrivals may touch it
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+}  // namespace rgg

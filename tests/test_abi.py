@@ -146,3 +146,17 @@ def test_plan_too_many_stages_for_shared_memory(lib):
     with pytest.raises(rgg.RggError) as ei:
         rgg.rgg_plan(64, 16384, 1024, 2688, bm=128, bn=256, stages=16)
     assert ei.value.status == rgg.RGG_ERR_UNSUPPORTED
+
+
+def test_plan_cta_pair_mode(lib):
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, bm=256, bn=256)
+    assert p["bm"] == 256 and p["bn"] == 256 and p["tmem_cols"] == 512
+    assert p["grid"] % 2 == 0 and p["grid"] <= 152
+    # each CTA holds 128 rows of X and half of the weight tile per stage
+    stage = (128 + 128) * 128
+    assert p["stages"] == 16 or (p["stages"] + 1) * stage + 1024 > 232448 - 8 * 65 - 200
+    p = rgg.rgg_plan(4, 256, 256, 512, bm=256, bn=128)
+    assert p["grid"] == 2 * min(76, (256 // 256 + 4) * 4)
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_plan(64, 16384, 1024, 2688, bm=256, bn=192)
+    assert ei.value.status == rgg.RGG_ERR_INVALID_ARG

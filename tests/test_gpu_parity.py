@@ -26,6 +26,8 @@ pytestmark = pytest.mark.gpu
 CANARY = 0x7FC1  # a bf16 NaN the kernel never produces
 RTOL = 1e-2
 SHAPES = [(64, 128), (64, 192), (64, 256), (128, 128), (128, 192), (128, 256)]
+# 256-row tiles computed by a CTA pair (tcgen05 cta_group::2)
+PAIR_SHAPES = [(256, 128), (256, 256)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -82,7 +84,7 @@ def _full_parity(inp, offsets=None, **opts):
 
 # ---------------------------------------------------------------- small cases
 
-@pytest.mark.parametrize("bm,bn", SHAPES)
+@pytest.mark.parametrize("bm,bn", SHAPES + PAIR_SHAPES)
 def test_tiny_config_every_tile_shape(bm, bn):
     _full_parity(wl.make_inputs("tiny"), bm=bm, bn=bn)
 
@@ -91,7 +93,7 @@ def test_tiny_config_auto_plan():
     _full_parity(wl.make_inputs("tiny"))
 
 
-@pytest.mark.parametrize("bm,bn", SHAPES)
+@pytest.mark.parametrize("bm,bn", SHAPES + PAIR_SHAPES)
 @pytest.mark.parametrize("N", [512, 520])
 def test_integer_inputs_bit_exact(bm, bn, N):
     # ragged counts around the tile sizes, an empty expert, spare rows at the end;
@@ -105,7 +107,7 @@ def test_integer_inputs_bit_exact(bm, bn, N):
     _assert_untouched(Y, slice(M_used, None))
 
 
-@pytest.mark.parametrize("bm,bn", [(64, 256), (128, 192), (128, 128)])
+@pytest.mark.parametrize("bm,bn", [(64, 256), (128, 192), (128, 128), (256, 256), (256, 128)])
 def test_ragged_random_k_and_n_tails(bm, bn):
     # K = 264 (a 8-wide K tail), N = 640 (not a multiple of 192 or 256), sizes around 64/128
     counts = [0, 1, 63, 64, 65, 127, 128, 129, 300, 0, 17]
@@ -125,6 +127,7 @@ def test_offsets_need_not_cover_all_rows():
     off = np.array([7, 47, 107, 157], dtype=np.int32)
     _full_parity(inp, offsets=off, bm=128, bn=128)
     _full_parity(inp, offsets=off, bm=64, bn=256)
+    _full_parity(inp, offsets=off, bm=256, bn=256)
 
 
 def test_all_experts_empty_writes_nothing():
@@ -156,18 +159,19 @@ def test_bad_offsets_rejected_and_nothing_written(off):
     _full_parity(inp)
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("bm", [64, 128, 256])
+def test_bounded_wait_reports_timeout_and_context_survives(bm):
     # the producer issues nothing, so the first MMA wait can only end by its limit
     inp = wl.make_inputs("tiny")
     X, W = inp.X.cuda(), inp.W.cuda()
     off = torch.from_numpy(inp.offsets).cuda()
     Y = _canary(256, 512)
     with pytest.raises(rgg.RggError) as ei:
-        rgg.rgg_grouped_gemm(X, W, off, Y, check=True, timeout_ns=20_000_000,
+        rgg.rgg_grouped_gemm(X, W, off, Y, check=True, timeout_ns=20_000_000, bm=bm,
                              debug_flags=rgg.RGG_DEBUG_PRODUCER_STALL)
     assert ei.value.status == rgg.RGG_ERR_DEVICE_TIMEOUT
     assert rgg.rgg_query_status() == rgg.RGG_OK
-    _full_parity(inp)
+    _full_parity(inp, bm=bm)
 
 
 def test_non_default_stream_and_determinism():
@@ -195,7 +199,7 @@ def _export_matches_oracle(off, M_tot, N, bm, bn):
     assert np.array_equal(desc.numpy(), ref)
 
 
-@pytest.mark.parametrize("bm,bn", SHAPES)
+@pytest.mark.parametrize("bm,bn", SHAPES + PAIR_SHAPES)
 @pytest.mark.parametrize("name", ["tiny", "decode", "uniform", "skew16k", "skew2k", "prefill",
                                   "worklog_skew16k", "decode_sweep_m1", "decode_sweep_m256"])
 def test_tile_list_bit_exact(name, bm, bn):
@@ -256,3 +260,19 @@ def test_full_size_config_sampled(name):
     err = np.abs(got - ref)
     bound = RTOL * np.maximum(1.0, np.abs(ref))
     assert (err <= bound).all(), "max err %.4g at %d" % (err.max(), int(np.argmax(err - bound)))
+
+
+@pytest.mark.parametrize("name", ["uniform", "prefill"])
+def test_full_size_pair_mode_sampled(name):
+    # the CTA-pair tiles on the large-group workloads
+    inp = wl.make_inputs(name)
+    X, W = inp.X.cuda(), inp.W.cuda()
+    off = torch.from_numpy(inp.offsets).cuda()
+    Y = rgg.rgg_grouped_gemm(X, W, off, check=True, bm=256, bn=256)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(Y).all())
+    rng = np.random.default_rng(zlib.crc32(name.encode()) + 1)
+    rows, cols = _sample_points(inp.offsets, inp.W.shape[2], rng)
+    ref = oracle.grouped_gemm_points(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets, rows, cols)
+    got = Y[torch.from_numpy(rows).cuda(), torch.from_numpy(cols.astype(np.int64)).cuda()].double().cpu().numpy()
+    assert (np.abs(got - ref) <= RTOL * np.maximum(1.0, np.abs(ref))).all()
