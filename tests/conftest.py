@@ -11,6 +11,7 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103a) GPU and the built CUDA library")
     config.addinivalue_line("markers", "slow: takes more than a few seconds on the CPU")
+    config.addinivalue_line("markers", "pair: runs the CTA-pair (cta_group::2) kernel")
 
 
 @pytest.fixture(scope="session")

@@ -27,7 +27,7 @@ CANARY = 0x7FC1  # a bf16 NaN the kernel never produces
 RTOL = 1e-2
 SHAPES = [(64, 128), (64, 192), (64, 256), (128, 128), (128, 192), (128, 256)]
 # 256-row tiles computed by a CTA pair (tcgen05 cta_group::2)
-PAIR_SHAPES = [(256, 128), (256, 256)]
+PAIR_SHAPES = [pytest.param(256, 128, marks=pytest.mark.pair), pytest.param(256, 256, marks=pytest.mark.pair)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -107,7 +107,7 @@ def test_integer_inputs_bit_exact(bm, bn, N):
     _assert_untouched(Y, slice(M_used, None))
 
 
-@pytest.mark.parametrize("bm,bn", [(64, 256), (128, 192), (128, 128), (256, 256), (256, 128)])
+@pytest.mark.parametrize("bm,bn", [(64, 256), (128, 192), (128, 128)] + PAIR_SHAPES)
 def test_ragged_random_k_and_n_tails(bm, bn):
     # K = 264 (a 8-wide K tail), N = 640 (not a multiple of 192 or 256), sizes around 64/128
     counts = [0, 1, 63, 64, 65, 127, 128, 129, 300, 0, 17]
@@ -127,6 +127,12 @@ def test_offsets_need_not_cover_all_rows():
     off = np.array([7, 47, 107, 157], dtype=np.int32)
     _full_parity(inp, offsets=off, bm=128, bn=128)
     _full_parity(inp, offsets=off, bm=64, bn=256)
+
+
+@pytest.mark.pair
+def test_offsets_need_not_cover_all_rows_pair():
+    inp = wl.make_custom([40, 60, 50], K=128, N=256, seed=34, spare_rows=20)
+    off = np.array([7, 47, 107, 157], dtype=np.int32)
     _full_parity(inp, offsets=off, bm=256, bn=256)
 
 
@@ -159,7 +165,7 @@ def test_bad_offsets_rejected_and_nothing_written(off):
     _full_parity(inp)
 
 
-@pytest.mark.parametrize("bm", [64, 128, 256])
+@pytest.mark.parametrize("bm", [64, 128, pytest.param(256, marks=pytest.mark.pair)])
 def test_bounded_wait_reports_timeout_and_context_survives(bm):
     # the producer issues nothing, so the first MMA wait can only end by its limit
     inp = wl.make_inputs("tiny")
@@ -262,6 +268,7 @@ def test_full_size_config_sampled(name):
     assert (err <= bound).all(), "max err %.4g at %d" % (err.max(), int(np.argmax(err - bound)))
 
 
+@pytest.mark.pair
 @pytest.mark.parametrize("name", ["uniform", "prefill"])
 def test_full_size_pair_mode_sampled(name):
     # the CTA-pair tiles on the large-group workloads
