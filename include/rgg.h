@@ -154,6 +154,42 @@ const char* rgg_status_string(rgg_status s);
 /* The text of the last CUDA error seen by this library on this thread ("" if none). */
 const char* rgg_last_cuda_error(void);
 
+/*
+ * rgg_grouped_gemm_noalloc -- the same product as rgg_grouped_gemm (default
+ * options, same kernel and tile plan) for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this entry point.
+ *
+ * Who needs it: code that must not call cudaMalloc where it runs the GEMM --
+ * an inference-engine plugin whose execute step may not allocate, code running
+ * while a stream is captured into a CUDA graph in global capture mode (where
+ * cudaMalloc is refused), a process whose device memory all belongs to a pool
+ * allocator.  rgg_grouped_gemm needs a handle, and rgg_create allocates the
+ * handle's status word.  This call takes no handle and allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Scratch: the kernel's only scratch (its 4-byte status word) lives in a
+ * file-scope device array of 256 bytes that every GPU which loads librgg.so
+ * holds until the process exits.  The scratch need does not grow with the
+ * problem, so only the kernel's own limits bound a call (1 <= E <= 4096,
+ * 0 <= M_tot < 2^31, K and N multiples of 8): other sizes are rejected with
+ * RGG_ERR_INVALID_ARG or RGG_ERR_UNSUPPORTED before anything is launched.
+ *
+ * The call runs on the current CUDA device.  Its first call on a device sets
+ * up that device (it looks up the array's device address with
+ * cudaGetSymbolAddress and reads the SM count); make that first call before
+ * any stream capture.  Each call clears the status word, launches the kernel
+ * and, when status_out is not NULL, copies the final status word into
+ * *status_out (device memory or pinned host memory, int32): RGG_OK,
+ * RGG_ERR_BAD_OFFSETS or RGG_ERR_DEVICE_TIMEOUT, valid once the stream has
+ * reached that point.  All calls share the one status word, so calls that
+ * overlap on the GPU (other streams, other threads) race on it.
+ *
+ * Arguments, layouts and ownership as for rgg_grouped_gemm; asynchronous on
+ * `stream` (a cudaStream_t, NULL = legacy default stream).
+ */
+rgg_status rgg_grouped_gemm_noalloc(const void* X, const void* W, const int32_t* group_offsets, void* Y,
+                                    int E, int64_t M_tot, int K, int N, int32_t* status_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,7 +17,7 @@ import os
 import threading
 
 __all__ = [
-    "RggError", "rgg_grouped_gemm", "rgg_export_tiles", "rgg_query_status", "rgg_plan",
+    "RggError", "rgg_grouped_gemm", "rgg_grouped_gemm_noalloc", "rgg_export_tiles", "rgg_query_status", "rgg_plan",
     "rgg_status_string", "library_path", "load_library", "EXPORTED_SYMBOLS",
     "RGG_OK", "RGG_ERR_INVALID_ARG", "RGG_ERR_UNSUPPORTED", "RGG_ERR_CUDA", "RGG_ERR_BAD_OFFSETS",
     "RGG_ERR_DEVICE_TIMEOUT", "RGG_ERR_CAPACITY",
@@ -38,7 +38,7 @@ _LIB_PATH = os.path.join(_PKG, "librgg.so")
 # The C ABI entry points declared in include/rgg.h.
 EXPORTED_SYMBOLS = (
     "rgg_create", "rgg_destroy", "rgg_grouped_gemm", "rgg_export_tiles", "rgg_query_status",
-    "rgg_plan", "rgg_status_string", "rgg_last_cuda_error",
+    "rgg_plan", "rgg_status_string", "rgg_last_cuda_error", "rgg_grouped_gemm_noalloc",
 )
 
 
@@ -95,6 +95,8 @@ def load_library() -> ctypes.CDLL:
         lib.rgg_status_string.restype = ctypes.c_char_p
         lib.rgg_last_cuda_error.argtypes = []
         lib.rgg_last_cuda_error.restype = ctypes.c_char_p
+        lib.rgg_grouped_gemm_noalloc.argtypes = [P, P, P, P, I, I64, I, I, P, P]
+        lib.rgg_grouped_gemm_noalloc.restype = I
         _lib = lib
         return lib
 
@@ -182,6 +184,28 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
         s = lib.rgg_query_status(_handle(device), st)
         if s != RGG_OK:
             _raise(s, "rgg_grouped_gemm (device status)")
+    return Y
+
+
+def rgg_grouped_gemm_noalloc(X, W, group_offsets, Y=None, status_out=None, stream=None):
+    """The same product through the entry point that allocates nothing (no
+    handle; the kernel's status word lives in a fixed device array inside
+    librgg.so).  For callers that cannot allocate device memory where they run
+    the GEMM.  ``status_out``: optional int32 CUDA tensor [1] that receives the
+    device status once the stream reaches it.  Y, if omitted, is allocated
+    here by torch -- pass it in to allocate nothing."""
+    import torch
+    M_tot, K = X.shape
+    E, _, N = W.shape
+    if Y is None:
+        Y = torch.empty(M_tot, N, dtype=torch.bfloat16, device=X.device)
+    device = X.device.index if X.device.index is not None else torch.cuda.current_device()
+    st = _stream_ptr(stream, device)
+    s = load_library().rgg_grouped_gemm_noalloc(X.data_ptr(), W.data_ptr(), group_offsets.data_ptr(), Y.data_ptr(),
+                                                E, M_tot, K, N,
+                                                status_out.data_ptr() if status_out is not None else None, st)
+    if s != RGG_OK:
+        _raise(s, "rgg_grouped_gemm_noalloc")
     return Y
 
 

@@ -233,6 +233,20 @@ rgg_status encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K
 
 }  // namespace
 
+namespace rgg {
+
+// Host helpers shared with the other C-ABI translation unit (rgg_noalloc.cu).
+rgg_status host_encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K, int N, int bm,
+                            CUtensorMap* tx, CUtensorMap* tw) {
+    return encode_maps(X, W, E, M_tot, K, N, bm, tx, tw);
+}
+
+rgg_status host_cuda_failure(cudaError_t err, const char* what) { return cuda_failure(err, what); }
+
+void host_set_last_error(const char* what) { g_last_cuda_error = what; }
+
+}  // namespace rgg
+
 extern "C" {
 
 const char* rgg_status_string(rgg_status s) {

@@ -7,6 +7,7 @@
 
 #include <cstdint>
 
+#include "rgg.h"
 #include "rgg_gemm.cuh"
 
 namespace rgg {
@@ -27,6 +28,14 @@ cudaError_t launch_gemm_pair(int bn, int grid, size_t smem, cudaStream_t stream,
 cudaError_t launch_export_tiles(const int32_t* offsets, int E, int64_t M_tot, int N, int bm, int bn,
                                 int32_t* desc, int64_t cap, int32_t* n_tiles, int32_t* status,
                                 cudaStream_t stream);
+
+// Host helpers defined in rgg_api.cu: the X / W tensor maps for a tile of
+// `bm` rows (256 = a CTA pair, 128 rows per CTA), and the thread-local text
+// behind rgg_last_cuda_error().
+rgg_status host_encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K, int N, int bm,
+                            CUtensorMap* tx, CUtensorMap* tw);
+rgg_status host_cuda_failure(cudaError_t err, const char* what);
+void host_set_last_error(const char* what);
 
 // Offsets check alone (used when there are no rows to multiply).
 cudaError_t launch_validate_offsets(const int32_t* offsets, int E, int64_t M_tot, int32_t* status,
