@@ -63,6 +63,8 @@ def parse_args():
     p.add_argument("--bm", type=int, default=0)
     p.add_argument("--bn", type=int, default=0)
     p.add_argument("--stages", type=int, default=0)
+    p.add_argument("--tail64", type=int, default=0, help="0 auto, 1 on, -1 off")
+    p.add_argument("--prefetch-kb", type=int, default=0, help="L2 lookahead in K blocks: 0 auto, -1 off")
     p.add_argument("--profile", action="store_true",
                    help="for ncu: --warmup launches then one more, no timing, no CPU work after")
     return p.parse_args()
@@ -236,7 +238,7 @@ def run_profile(args):
     X, W = inp.X.to(dev), inp.W.to(dev)
     off = torch.from_numpy(inp.offsets).to(dev)
     Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device=dev)
-    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages)
+    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64, prefetch_kb=args.prefetch_kb)
     for _ in range(args.warmup + 1):
         rgg.rgg_grouped_gemm(X, W, off, Y, **opts)
     torch.cuda.synchronize(dev)
@@ -263,7 +265,7 @@ def run_ours(args):
     X, W = inp.X.to(dev), inp.W.to(dev)
     off = torch.from_numpy(inp.offsets).to(dev)
     Y = torch.empty(M_tot, N, dtype=torch.bfloat16, device=dev)
-    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages)
+    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64, prefetch_kb=args.prefetch_kb)
     plan = rgg.rgg_plan(E, M_tot, K, N, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
                         **opts)
     stream = torch.cuda.current_stream(dev)

@@ -67,6 +67,10 @@ typedef struct rgg_options {
     int debug_flags;             /* 0 in normal use.  RGG_DEBUG_PRODUCER_STALL makes the load pipeline issue
                                     nothing, so the first MMA wait can only end by its time limit: a test of the
                                     bounded waits, which then report RGG_ERR_DEVICE_TIMEOUT */
+    int tail64;                  /* 128-row tiles: 0 = auto (on), 1 = on, -1 = off.  A tile that holds the last
+                                    <= 64 rows of its expert runs as a 64-row MMA with a 64-row X box */
+    int prefetch_kb;             /* L2 prefetch lookahead, in 64-wide K blocks of a CTA's walk: 0 = auto,
+                                    -1 = off, else 1..64 */
 } rgg_options;
 
 #define RGG_DEBUG_PRODUCER_STALL 1
@@ -80,6 +84,8 @@ typedef struct rgg_plan_info {
     int smem_bytes;              /* dynamic shared memory per CTA */
     int tmem_cols;               /* TMEM columns allocated per CTA (two accumulator buffers) */
     int64_t max_tiles;           /* upper bound on the flat tile count for these sizes */
+    int tail64;                  /* 1 when tail tiles of <= 64 rows run as 64-row MMAs */
+    int prefetch_kb;             /* L2 prefetch lookahead in K blocks (0 = off) */
 } rgg_plan_info;
 
 /*

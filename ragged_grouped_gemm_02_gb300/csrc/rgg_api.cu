@@ -81,6 +81,8 @@ struct Plan {
     int bm, bn, stages, grid;
     int smem_bytes;
     int64_t max_tiles;
+    int tail64;       // 1: tail tiles of <= 64 rows run as 64-row MMAs (128-row tiles only)
+    int prefetch_kb;  // L2 lookahead in K blocks, 0 = off
 };
 
 // Upper bound on the flat tile count: sum_e ceil(m_e/BM) <= floor(M_tot/BM) + E.
@@ -110,6 +112,9 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (want_bm == 256 && want_bn == 192) return RGG_ERR_INVALID_ARG;  // pair tiles split BN in whole panels
     if (want_stages != 0 && (want_stages < 2 || want_stages > rgg::kMaxStages)) return RGG_ERR_INVALID_ARG;
     if (max_ctas < 0) return RGG_ERR_INVALID_ARG;
+    const int want_tail = opt ? opt->tail64 : 0;
+    const int want_pf = opt ? opt->prefetch_kb : 0;
+    if (want_tail < -1 || want_tail > 1 || want_pf < -1 || want_pf > 64) return RGG_ERR_INVALID_ARG;
     int grid_cap = max_ctas > 0 ? std::min(max_ctas, num_sms) : num_sms;
 
     // Per-expert M tiles at each BM: exact with host counts, else the
@@ -189,11 +194,13 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
                      : static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(grid_cap, max_tiles)));
     out->smem_bytes = smem;
     out->max_tiles = max_tiles;
+    out->tail64 = (bm == 128 && want_tail != -1) ? 1 : 0;
+    out->prefetch_kb = want_pf > 0 ? want_pf : 0;
     return RGG_OK;
 }
 
 rgg_status encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K, int N, int bm,
-                       CUtensorMap* tx, CUtensorMap* tw) {
+                       CUtensorMap* tx, CUtensorMap* tx64, CUtensorMap* tw) {
     EncodeTiledFn encode = encode_tiled_fn();
     if (!encode) {
         g_last_cuda_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -210,6 +217,16 @@ rgg_status encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) {
             g_last_cuda_error = "cuTensorMapEncodeTiled(X) failed with CUresult " + std::to_string(static_cast<int>(r));
+            return RGG_ERR_CUDA;
+        }
+        // The same X with a 64-row box, for tiles that hold 64 rows or fewer.
+        const cuuint32_t box64[2] = {64, 64};
+        r = encode(tx64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box64, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            g_last_cuda_error = "cuTensorMapEncodeTiled(X, 64 rows) failed with CUresult " +
+                                std::to_string(static_cast<int>(r));
             return RGG_ERR_CUDA;
         }
     }
@@ -237,8 +254,8 @@ namespace rgg {
 
 // Host helpers shared with the other C-ABI translation unit (rgg_noalloc.cu).
 rgg_status host_encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K, int N, int bm,
-                            CUtensorMap* tx, CUtensorMap* tw) {
-    return encode_maps(X, W, E, M_tot, K, N, bm, tx, tw);
+                            CUtensorMap* tx, CUtensorMap* tx64, CUtensorMap* tw) {
+    return encode_maps(X, W, E, M_tot, K, N, bm, tx, tx64, tw);
 }
 
 rgg_status host_cuda_failure(cudaError_t err, const char* what) { return cuda_failure(err, what); }
@@ -323,6 +340,8 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->smem_bytes = p.smem_bytes;
     out->tmem_cols = (p.bm == 256 || 2 * p.bn > 256) ? 512 : 256;
     out->max_tiles = p.max_tiles;
+    out->tail64 = p.tail64;
+    out->prefetch_kb = p.prefetch_kb;
     return RGG_OK;
 }
 
@@ -347,8 +366,8 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
     s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p);
     if (s != RGG_OK) return s;
 
-    CUtensorMap tx, tw;
-    s = encode_maps(X, W, E, M_tot, K, N, p.bm, &tx, &tw);
+    CUtensorMap tx, tx64, tw;
+    s = encode_maps(X, W, E, M_tot, K, N, p.bm, &tx, &tx64, &tw);
     if (s != RGG_OK) return s;
 
     rgg::GemmArgs a;
@@ -365,10 +384,12 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
     a.y_vec32 = ((N % 16) == 0 && aligned(Y, 32)) ? 1 : 0;
     a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
+    a.tail64 = p.tail64;
+    a.prefetch_kb = p.prefetch_kb;
 
     cudaError_t err = (p.bm == 256)   ? rgg::launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tw, a)
-                      : (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tw, a)
-                                      : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tw, a);
+                      : (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+                                      : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm launch");
 }
 

@@ -66,6 +66,8 @@ struct GemmArgs {
     int32_t stages;
     int32_t y_vec32;         // 1: rows of Y are 32-byte aligned (256-bit stores)
     int32_t debug_flags;     // 0 in normal use; kDebugProducerStall for failure-detection tests
+    int32_t tail64;          // 1: tiles holding <= 64 rows run as 64-row MMAs (128-row kernels)
+    int32_t prefetch_kb;     // L2 prefetch lookahead in K blocks (0 = off)
     uint64_t timeout_ns;
 };
 
@@ -121,13 +123,23 @@ struct TileConfig {
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN is a multiple of one 64-column panel, at most 256");
     static constexpr uint32_t kTmemCols = (2 * BN <= 256) ? 256u : 512u;  // two accumulator buffers
     static constexpr uint32_t kStageTx = static_cast<uint32_t>((BM + BN) * kBK * 2);
+    static constexpr uint32_t kStageTx64 = static_cast<uint32_t>((64 + BN) * kBK * 2);  // 64-row tail tile
     static constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*b_mn_major=*/true);
+    static constexpr uint32_t kIdesc64 = idesc_bf16_f32(64, BN, /*b_mn_major=*/true);
 };
+
+// A 128-row tile whose rows are the last <= 64 of its expert runs as a
+// 64-row MMA (the "tail64" mode): the tile list is unchanged, only the MMA
+// height, the X box and the epilogue's TMEM lane mapping follow the tile.
+template <int BM>
+__device__ __forceinline__ bool runs_as_64_rows(const GemmArgs& args, const TileCoord& c) {
+    return BM == 64 || (args.tail64 != 0 && c.rows <= 64);
+}
 
 template <int BM, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                        const GemmArgs args) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
+                        const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
     using Cfg = TileConfig<BM, BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
@@ -177,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmap_x);
+        tma_prefetch_map(&tmap_x64);
         tma_prefetch_map(&tmap_w);
     }
     if (warp == 1) {
@@ -199,15 +212,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = true;
+            const int PD = args.prefetch_kb;  // L2 lookahead, in K blocks of this CTA's walk
+            int32_t t_ahead = -1;
+            TileCoord c_ahead = {0, 0, 0, 0};
             for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
                 const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+                const bool half = runs_as_64_rows<BM>(args, c);
+                const uint32_t tx_bytes = half ? Cfg::kStageTx64 : Cfg::kStageTx;
+                const CUtensorMap* xmap = (BM == 128 && half) ? &tmap_x64 : &tmap_x;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_or_abort(empty_bar(st), ph ^ 1u, abort_flag, args.status, args.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(st), Cfg::kStageTx);
-                    tma_load_2d(a0 + st * sp.a_stage, &tmap_x, full_bar(st), kb * kBK, c.row0);
+                    mbar_arrive_expect_tx(full_bar(st), tx_bytes);
+                    tma_load_2d(a0 + st * sp.a_stage, xmap, full_bar(st), kb * kBK, c.row0);
 #pragma unroll
                     for (int p = 0; p < BN / 64; ++p)
                         tma_load_3d(b0 + st * sp.b_stage + p * kPanelBytes, &tmap_w, full_bar(st), c.col0 + 64 * p,
@@ -216,6 +235,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (++st == S) {
                         st = 0;
                         ph ^= 1u;
+                    }
+                    if (PD > 0) {
+                        // Warm L2 with the boxes this CTA will load PD K blocks from
+                        // now, so HBM latency overlaps more MMA work than the ring holds.
+                        int kb_a = kb + PD;
+                        int32_t t_a = t;
+                        while (kb_a >= KB) {
+                            kb_a -= KB;
+                            t_a += gridDim.x;
+                        }
+                        if (t_a < T) {
+                            if (t_a != t_ahead) {
+                                c_ahead = decode_tile(s_off, s_pre, E, BM, BN, nN, t_a);
+                                t_ahead = t_a;
+                            }
+#pragma unroll
+                            for (int p = 0; p < BN / 64; ++p)
+                                tma_prefetch_l2_3d(&tmap_w, c_ahead.col0 + 64 * p, kb_a * kBK, c_ahead.expert);
+                            tma_prefetch_l2_2d(runs_as_64_rows<BM>(args, c_ahead) ? &tmap_x64 : &tmap_x,
+                                               kb_a * kBK, c_ahead.row0);
+                        }
                     }
                 }
             }
@@ -236,6 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_ph = 0;
             bool ok = true;
             for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
+                const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+                const uint32_t idesc = runs_as_64_rows<BM>(args, c) ? Cfg::kIdesc64 : Cfg::kIdesc;
                 if (!wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, args.status, args.timeout_ns)) {
                     ok = false;
                     break;
@@ -254,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < kBK / 16; ++j) {
                         const uint64_t ad = sw128_desc(a_st + 32u * j, 16u, 1024u);
                         const uint64_t bd = sw128_desc(b_st + 2048u * j, kPanelBytes, 1024u);
-                        mma_bf16_ss(d_tmem, ad, bd, Cfg::kIdesc, (kb | j) != 0 ? 1u : 0u);
+                        mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
                     }
                     mma_commit(empty_bar(st));  // frees the stage once these MMAs have read it
                     if (++st == S) {
@@ -278,19 +320,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------- S6: epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
-        const int r_local = (BM == 128) ? (q * 32 + lane) : (q * 16 + (lane & 15));
-        const bool lane_has_row = (BM == 128) || (lane < 16);
         const int N = args.N;
         int acc = 0;
         uint32_t acc_ph = 0;
         for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
             const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+            // M = 128: tile row 32q + lane sits in TMEM lane 32q + lane.  M = 64:
+            // tile row 16q + i sits in TMEM lane 32q + i (i < 16).
+            const bool half = runs_as_64_rows<BM>(args, c);
+            const int r_local = half ? (q * 16 + (lane & 15)) : (q * 32 + lane);
             bool ok = wait_or_abort(accf_bar(acc), acc_ph, abort_flag, args.status, args.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            const bool row_ok = lane_has_row && (r_local < c.rows);
+            const bool row_ok = (!half || lane < 16) && (r_local < c.rows);
             __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0;
 #pragma unroll 1
             for (int cc = 0; cc < BN; cc += 32) {

@@ -8,12 +8,12 @@ namespace rgg {
 
 template <int BM, int BN>
 cudaError_t launch_gemm_instance(int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
-                                 const CUtensorMap& tmap_w, const GemmArgs& args) {
+                                 const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args) {
     auto kernel = grouped_gemm_kernel<BM, BN>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kernel<<<grid, kThreads, smem, stream>>>(tmap_x, tmap_w, args);
+    kernel<<<grid, kThreads, smem, stream>>>(tmap_x, tmap_x64, tmap_w, args);
     return cudaGetLastError();
 }
 

@@ -13,11 +13,12 @@
 namespace rgg {
 
 // Grouped GEMM kernels, one translation unit per BM.  `bn` is 128, 192 or
-// 256.  Returns cudaErrorInvalidValue for a shape with no instantiation.
+// 256.  tmap_x64 is X with a 64-row box (tail tiles of 128-row kernels).
+// Returns cudaErrorInvalidValue for a shape with no instantiation.
 cudaError_t launch_gemm_bm128(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
-                              const CUtensorMap& tmap_w, const GemmArgs& args);
+                              const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 cudaError_t launch_gemm_bm64(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
-                             const CUtensorMap& tmap_w, const GemmArgs& args);
+                             const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 
 // CTA-pair kernel (256-row tiles, clusters of two): `bn` is 128 or 256 and
 // `grid` is even.
@@ -30,10 +31,10 @@ cudaError_t launch_export_tiles(const int32_t* offsets, int E, int64_t M_tot, in
                                 cudaStream_t stream);
 
 // Host helpers defined in rgg_api.cu: the X / W tensor maps for a tile of
-// `bm` rows (256 = a CTA pair, 128 rows per CTA), and the thread-local text
-// behind rgg_last_cuda_error().
+// `bm` rows (256 = a CTA pair, 128 rows per CTA) plus X with a 64-row box,
+// and the thread-local text behind rgg_last_cuda_error().
 rgg_status host_encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K, int N, int bm,
-                            CUtensorMap* tx, CUtensorMap* tw);
+                            CUtensorMap* tx, CUtensorMap* tx64, CUtensorMap* tw);
 rgg_status host_cuda_failure(cudaError_t err, const char* what);
 void host_set_last_error(const char* what);
 

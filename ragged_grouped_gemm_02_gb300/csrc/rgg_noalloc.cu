@@ -115,8 +115,8 @@ extern "C" rgg_status rgg_grouped_gemm_noalloc(const void* X, const void* W, con
     if (M_tot == 0) {
         err = rgg::launch_validate_offsets(group_offsets, E, M_tot, dev.scratch, st);
     } else {
-        CUtensorMap tx, tw;
-        s = rgg::host_encode_maps(X, W, E, M_tot, K, N, plan.bm, &tx, &tw);
+        CUtensorMap tx, tx64, tw;
+        s = rgg::host_encode_maps(X, W, E, M_tot, K, N, plan.bm, &tx, &tx64, &tw);
         if (s != RGG_OK) return s;
         rgg::GemmArgs a;
         a.offsets = group_offsets;
@@ -131,10 +131,12 @@ extern "C" rgg_status rgg_grouped_gemm_noalloc(const void* X, const void* W, con
         a.stages = plan.stages;
         a.y_vec32 = ((N % 16) == 0 && aligned(Y, 32)) ? 1 : 0;
         a.debug_flags = 0;
+        a.tail64 = plan.tail64;
+        a.prefetch_kb = plan.prefetch_kb;
         a.timeout_ns = 2000000000ull;
         err = (plan.bm == 256)   ? rgg::launch_gemm_pair(plan.bn, plan.grid, plan.smem_bytes, st, tx, tw, a)
-              : (plan.bm == 128) ? rgg::launch_gemm_bm128(plan.bn, plan.grid, plan.smem_bytes, st, tx, tw, a)
-                                 : rgg::launch_gemm_bm64(plan.bn, plan.grid, plan.smem_bytes, st, tx, tw, a);
+              : (plan.bm == 128) ? rgg::launch_gemm_bm128(plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a)
+                                 : rgg::launch_gemm_bm64(plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a);
     }
     if (err != cudaSuccess) return rgg::host_cuda_failure(err, "rgg_grouped_gemm_noalloc: launch");
     if (status_out) {

@@ -107,6 +107,20 @@ def test_integer_inputs_bit_exact(bm, bn, N):
     _assert_untouched(Y, slice(M_used, None))
 
 
+@pytest.mark.parametrize("bm,bn", SHAPES + PAIR_SHAPES)
+@pytest.mark.parametrize("tail64,prefetch_kb", [(0, 0), (-1, 0), (1, 3)])
+def test_integer_inputs_bit_exact_modes(bm, bn, tail64, prefetch_kb):
+    # 64-row tail tiles on and off, and the L2 lookahead (with K = 64 the
+    # lookahead crosses tile boundaries every step)
+    counts = [3, 0, 130, 64, 1, 200, 65, 127, 129]
+    inp = wl.make_custom(counts, K=64, N=384, seed=38, integer_valued=True, spare_rows=3)
+    Y = _run(inp, bm=bm, bn=bn, tail64=tail64, prefetch_kb=prefetch_kb)
+    ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
+    M_used = int(inp.offsets[-1])
+    assert np.array_equal(Y[:M_used].double().numpy(), ref[:M_used])
+    _assert_untouched(Y, slice(M_used, None))
+
+
 @pytest.mark.parametrize("bm,bn", [(64, 256), (128, 192), (128, 128)] + PAIR_SHAPES)
 def test_ragged_random_k_and_n_tails(bm, bn):
     # K = 264 (a 8-wide K tail), N = 640 (not a multiple of 192 or 256), sizes around 64/128
@@ -115,10 +129,11 @@ def test_ragged_random_k_and_n_tails(bm, bn):
     _full_parity(inp, bm=bm, bn=bn)
 
 
-def test_ragged_random_auto_plan_many_tiles():
+@pytest.mark.parametrize("prefetch_kb", [0, 8])
+def test_ragged_random_auto_plan_many_tiles(prefetch_kb):
     counts = [500, 3, 0, 257, 1024, 77, 129, 2, 640, 64]
     inp = wl.make_custom(counts, K=512, N=1024, seed=33)
-    _full_parity(inp)
+    _full_parity(inp, prefetch_kb=prefetch_kb)
 
 
 def test_offsets_need_not_cover_all_rows():
