@@ -44,7 +44,7 @@ def build(force: bool = False) -> str:
         return _LIB_PATH
     tmp = _LIB_PATH + ".tmp%d" % os.getpid()
     cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-std=c11",
-           "-Wall", "-Wextra", "-o", tmp, _SRC]
+           "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -69,6 +69,11 @@ def _load():
         lib.rgg_oracle_tile_list.restype = i64
         lib.rgg_oracle_row_utilisation.argtypes = [P, ctypes.c_int, ctypes.c_int]
         lib.rgg_oracle_row_utilisation.restype = ctypes.c_double
+        lib.rgg_oracle_grouped_swiglu.argtypes = [P, P, P, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, P,
+                                                  ctypes.c_int]
+        lib.rgg_oracle_grouped_swiglu.restype = ctypes.c_int
+        lib.rgg_oracle_silu.argtypes = [ctypes.c_double]
+        lib.rgg_oracle_silu.restype = ctypes.c_double
         lib.rgg_oracle_max_threads.argtypes = []
         lib.rgg_oracle_max_threads.restype = ctypes.c_int
         del i32
@@ -150,6 +155,32 @@ def grouped_gemm_points(X_bits: np.ndarray, W_bits: np.ndarray, off, rows, cols,
     out = np.empty(rows.size, dtype=np.float64)
     rc = _load().rgg_oracle_grouped_gemm_points(_ptr(X_bits), _ptr(W_bits), _ptr(off), E, M_tot, K, N,
                                                 _ptr(rows), _ptr(cols), rows.size, _ptr(out), int(nthreads))
+    if rc != ORACLE_OK:
+        raise OracleError("oracle rejected the arguments (code %d)" % rc)
+    return out
+
+
+def silu(z: float) -> float:
+    """silu(z) = z / (1 + exp(-z)) in fp64, as the fused oracle applies it."""
+    return float(_load().rgg_oracle_silu(float(z)))
+
+
+def grouped_swiglu(X_bits: np.ndarray, W13_bits: np.ndarray, off, nthreads: int = 0,
+                   out: np.ndarray | None = None) -> np.ndarray:
+    """H = silu(X_e . W13_e[:, :N]) * (X_e . W13_e[:, N:]) per expert, fp64.
+
+    W13_bits: uint16 [E, K, 2N] (gate columns first, then up columns).
+    Rows of no expert keep their value in ``out`` (NaN when not given)."""
+    X_bits, W13_bits, off = _as_bits(X_bits), _as_bits(W13_bits), _as_offsets(off)
+    M_tot, K = X_bits.shape
+    E, K2, N2 = W13_bits.shape
+    if K2 != K or off.size != E + 1 or N2 % 2 != 0:
+        raise ValueError("shape mismatch: X %s, W13 %s, offsets %d" % (X_bits.shape, W13_bits.shape, off.size))
+    N = N2 // 2
+    if out is None:
+        out = np.full((M_tot, N), np.nan, dtype=np.float64)
+    rc = _load().rgg_oracle_grouped_swiglu(_ptr(X_bits), _ptr(W13_bits), _ptr(off), E, M_tot, K, N, _ptr(out),
+                                           int(nthreads))
     if rc != ORACLE_OK:
         raise OracleError("oracle rejected the arguments (code %d)" % rc)
     return out

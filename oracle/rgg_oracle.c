@@ -41,6 +41,7 @@
  * no multiply-add is fused and the k-ordered fp64 sum is the same on every
  * host architecture).
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -155,6 +156,54 @@ int rgg_oracle_grouped_gemm_points(const uint16_t* X, const uint16_t* W, const i
         for (int k = 0; k < K; ++k)
             acc += bf16_bits_to_f64(X[i * K + k]) * bf16_bits_to_f64(We[(int64_t)k * N + j]);
         out[p] = acc;
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * The fused gate-up projection of an expert FFN with its activation: the
+ * worklog ("What I am measuring"; section 7 "Scope of these results") leaves
+ * out "the activation" that follows the grouped GEMM, and the Pearl article
+ * ("What the 15% measures") benchmarks the gate and up projections of
+ * GLM 5.3, DeepSeek V4 Pro and Kimi K3, models whose experts gate with SiLU
+ * (SwiGLU).  Reading: W13 is bf16 [E, K, 2N] whose columns [0, N) are the
+ * gate projection and [N, 2N) the up projection, and for every row i of
+ * expert e and column j < N
+ *
+ *     g = sum_k x[i,k] w13[e,k,j],  u = sum_k x[i,k] w13[e,k,N+j]   (fp64, k increasing)
+ *     H[i, j] = silu(g) * u,        silu(z) = z / (1 + exp(-z)).
+ *
+ * H is double [M_tot, N]; rows of no expert are untouched.
+ */
+static double silu_f64(double z) { return z / (1.0 + exp(-z)); }
+
+double rgg_oracle_silu(double z) { return silu_f64(z); }
+
+int rgg_oracle_grouped_swiglu(const uint16_t* X, const uint16_t* W13, const int32_t* off, int E, int64_t M_tot,
+                              int K, int N, double* H, int nthreads) {
+    if (X == NULL || W13 == NULL || H == NULL || K < 1 || N < 1) return ORACLE_ERR_INVALID_ARG;
+    int rc = rgg_oracle_check_offsets(off, E, M_tot);
+    if (rc != ORACLE_OK) return rc;
+    set_threads(nthreads);
+    const int64_t N2 = 2 * (int64_t)N;
+    for (int e = 0; e < E; ++e) {
+        const int64_t row_begin = off[e], row_end = off[e + 1];
+        const uint16_t* We = W13 + (int64_t)e * K * N2;
+        #pragma omp parallel
+        {
+            double* acc = (double*)malloc(sizeof(double) * (size_t)N2);
+            #pragma omp for schedule(dynamic, 1)
+            for (int64_t i = row_begin; i < row_end; ++i) {
+                for (int64_t j = 0; j < N2; ++j) acc[j] = 0.0;
+                for (int k = 0; k < K; ++k) {
+                    const double x = bf16_bits_to_f64(X[i * K + k]);
+                    const uint16_t* wrow = We + (int64_t)k * N2;
+                    for (int64_t j = 0; j < N2; ++j) acc[j] += x * bf16_bits_to_f64(wrow[j]);
+                }
+                for (int j = 0; j < N; ++j) H[i * N + j] = silu_f64(acc[j]) * acc[N + j];
+            }
+            free(acc);
+        }
     }
     return ORACLE_OK;
 }

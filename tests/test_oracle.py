@@ -260,3 +260,49 @@ def test_k_not_multiple_of_tile_and_odd_n(oracle_mod):
     Xd, Wd = inp.X.double().numpy(), inp.W.double().numpy()
     np.testing.assert_allclose(Y[:3], Xd[:3] @ Wd[0], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(Y[3:], Xd[3:] @ Wd[1], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------- fused gate-up + SiLU activation
+
+def test_silu_closed_forms(oracle_mod):
+    # silu(0) = 0; the logistic function at 1 is 1 / (1 + 1/e) = 0.7310585786300049
+    assert oracle_mod.silu(0.0) == 0.0
+    assert abs(oracle_mod.silu(1.0) - 0.7310585786300049) < 1e-15
+    # sigma(z) + sigma(-z) = 1, hence silu(z) - silu(-z) = z (catches sign slips)
+    for z in (-7.5, -1.25, 0.3, 2.0, 11.0):
+        assert abs((oracle_mod.silu(z) - oracle_mod.silu(-z)) - z) < 1e-12 * max(1.0, abs(z))
+    # far tails: silu(z) -> z for large z, -> 0 for very negative z
+    assert abs(oracle_mod.silu(40.0) - 40.0) < 1e-12
+    assert abs(oracle_mod.silu(-40.0)) < 1e-15
+
+
+def test_swiglu_equals_gated_product_of_the_grouped_gemm(oracle_mod):
+    # the fused result is silu(gate) * up, each being the (pinned) grouped GEMM
+    # of the gate and up halves of W13
+    counts = [4, 0, 9, 3]
+    N = 24
+    inp = wl.make_custom(counts, K=40, N=2 * N, seed=61, spare_rows=2)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    H = oracle_mod.grouped_swiglu(xb, wb, inp.offsets)
+    G = oracle_mod.grouped_gemm(xb, np.ascontiguousarray(wb[:, :, :N]), inp.offsets)
+    U = oracle_mod.grouped_gemm(xb, np.ascontiguousarray(wb[:, :, N:]), inp.offsets)
+    M_used = int(inp.offsets[-1])
+    silu = np.vectorize(oracle_mod.silu)
+    np.testing.assert_allclose(H[:M_used], silu(G[:M_used]) * U[:M_used], rtol=1e-14, atol=1e-14)
+    assert np.isnan(H[M_used:]).all()
+
+
+def test_swiglu_integer_inputs_against_exact_products(oracle_mod):
+    # integer-valued inputs: gate and up are exact integers (numpy int64), so
+    # H must equal silu(g) * u computed from them to fp64 rounding
+    counts = [2, 5, 0, 1]
+    N = 16
+    inp = wl.make_custom(counts, K=32, N=2 * N, seed=62, integer_valued=True)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    H = oracle_mod.grouped_swiglu(xb, wb, inp.offsets)
+    Xi, Wi, off = inp.X.to(torch.int64).numpy(), inp.W.to(torch.int64).numpy(), inp.offsets
+    for e in range(len(counts)):
+        g = (Xi[off[e]:off[e + 1]] @ Wi[e][:, :N]).astype(np.float64)
+        u = (Xi[off[e]:off[e + 1]] @ Wi[e][:, N:]).astype(np.float64)
+        ref = g / (1.0 + np.exp(-g)) * u
+        np.testing.assert_allclose(H[off[e]:off[e + 1]], ref, rtol=1e-14, atol=1e-12)

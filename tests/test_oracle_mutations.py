@@ -40,20 +40,27 @@ MUTANTS = {
                               "desc[4 * count + 1] = (int32_t)(off[e] + mt * BN);"),
     "tile_count_floor": ("const int64_t m_tiles = ceil_div64(m_e, BM);", "const int64_t m_tiles = m_e / BM;"),
     "eta_floor": ("scheduled_tiles += ceil_div64(m_e, BM);", "scheduled_tiles += m_e / BM + 1;"),
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "gate_up_swapped": ("H[i * N + j] = silu_f64(acc[j]) * acc[N + j];",
+                        "H[i * N + j] = silu_f64(acc[N + j]) * acc[j];"),
+    "swiglu_plain_product": ("H[i * N + j] = silu_f64(acc[j]) * acc[N + j];",
+                             "H[i * N + j] = acc[j] * acc[N + j];"),
 }
 
 
 def _build(tmp_path, name, mutation):
     src = open(SRC).read()
     if mutation is not None:
+        # the same slip everywhere the line occurs (the fused function repeats
+        # the GEMM's inner loop)
         old, new = mutation
-        assert src.count(old) == 1, "mutation anchor for %s not unique" % name
+        assert src.count(old) >= 1, "mutation anchor for %s not found" % name
         src = src.replace(old, new)
     c = tmp_path / ("%s.c" % name)
     so = tmp_path / ("lib%s.so" % name)
     c.write_text(src)
     subprocess.run(["gcc", "-O1", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-std=c11",
-                    "-o", str(so), str(c)], check=True)
+                    "-o", str(so), str(c), "-lm"], check=True)
     lib = ctypes.CDLL(str(so))
     P = ctypes.c_void_p
     lib.rgg_oracle_grouped_gemm.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P,
@@ -64,6 +71,11 @@ def _build(tmp_path, name, mutation):
     lib.rgg_oracle_tile_list.restype = ctypes.c_int64
     lib.rgg_oracle_row_utilisation.argtypes = [P, ctypes.c_int, ctypes.c_int]
     lib.rgg_oracle_row_utilisation.restype = ctypes.c_double
+    lib.rgg_oracle_grouped_swiglu.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P,
+                                              ctypes.c_int]
+    lib.rgg_oracle_grouped_swiglu.restype = ctypes.c_int
+    lib.rgg_oracle_silu.argtypes = [ctypes.c_double]
+    lib.rgg_oracle_silu.restype = ctypes.c_double
     return lib
 
 
@@ -139,8 +151,32 @@ def _eta_checks_pass(lib):
     return True
 
 
+def _swiglu_checks_pass(lib):
+    # closed forms of the activation, then integer inputs against exact gate / up products
+    if lib.rgg_oracle_silu(0.0) != 0.0 or abs(lib.rgg_oracle_silu(1.0) - 0.7310585786300049) > 1e-15:
+        return False
+    if abs((lib.rgg_oracle_silu(2.0) - lib.rgg_oracle_silu(-2.0)) - 2.0) > 1e-12:
+        return False
+    counts, N = [2, 0, 3], 8
+    inp = wl.make_custom(counts, K=16, N=2 * N, seed=63, integer_valued=True)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    off = np.ascontiguousarray(inp.offsets, dtype=np.int32)
+    H = np.full((xb.shape[0], N), np.nan)
+    if lib.rgg_oracle_grouped_swiglu(xb.ctypes.data, wb.ctypes.data, off.ctypes.data, len(counts), xb.shape[0],
+                                     16, N, H.ctypes.data, 1) != 0:
+        return False
+    Xi, Wi = inp.X.to(torch.int64).numpy(), inp.W.to(torch.int64).numpy()
+    for e in range(len(counts)):
+        g = (Xi[off[e]:off[e + 1]] @ Wi[e][:, :N]).astype(np.float64)
+        u = (Xi[off[e]:off[e + 1]] @ Wi[e][:, N:]).astype(np.float64)
+        if not np.allclose(H[off[e]:off[e + 1]], g / (1.0 + np.exp(-g)) * u, rtol=1e-13, atol=1e-12):
+            return False
+    return True
+
+
 def _all_pass(lib):
-    return _product_checks_pass(lib) and _tile_checks_pass(lib) and _eta_checks_pass(lib)
+    return (_product_checks_pass(lib) and _tile_checks_pass(lib) and _eta_checks_pass(lib)
+            and _swiglu_checks_pass(lib))
 
 
 def test_unmutated_copy_passes(tmp_path):
