@@ -74,6 +74,11 @@ def _load():
         lib.rgg_oracle_grouped_swiglu.restype = ctypes.c_int
         lib.rgg_oracle_silu.argtypes = [ctypes.c_double]
         lib.rgg_oracle_silu.restype = ctypes.c_double
+        lib.rgg_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.rgg_oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.rgg_oracle_grouped_gemm_fp8.argtypes = [P, P, P, P, P, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int,
+                                                    P, ctypes.c_int]
+        lib.rgg_oracle_grouped_gemm_fp8.restype = ctypes.c_int
         lib.rgg_oracle_max_threads.argtypes = []
         lib.rgg_oracle_max_threads.restype = ctypes.c_int
         del i32
@@ -181,6 +186,37 @@ def grouped_swiglu(X_bits: np.ndarray, W13_bits: np.ndarray, off, nthreads: int 
         out = np.full((M_tot, N), np.nan, dtype=np.float64)
     rc = _load().rgg_oracle_grouped_swiglu(_ptr(X_bits), _ptr(W13_bits), _ptr(off), E, M_tot, K, N, _ptr(out),
                                            int(nthreads))
+    if rc != ORACLE_OK:
+        raise OracleError("oracle rejected the arguments (code %d)" % rc)
+    return out
+
+
+def e4m3_to_f64(code: int) -> float:
+    """The value of one FP8 E4M3 code (sign, 4-bit exponent with bias 7, 3-bit mantissa)."""
+    return float(_load().rgg_oracle_e4m3_to_f64(int(code) & 0xFF))
+
+
+def grouped_gemm_fp8(X8: np.ndarray, W8: np.ndarray, sx: np.ndarray, sw: np.ndarray, off, nthreads: int = 0,
+                     out: np.ndarray | None = None) -> np.ndarray:
+    """Y[i, j] = sx[i] * sw[e, j] * sum_k x8[i, k] w8[e, k, j] in fp64.
+
+    X8: uint8 E4M3 codes [M_tot, K]; W8: uint8 E4M3 codes [E, K, N];
+    sx: float32 [M_tot]; sw: float32 [E, N]; off: int [E+1]."""
+    X8 = np.ascontiguousarray(X8)
+    W8 = np.ascontiguousarray(W8)
+    if X8.dtype != np.uint8 or W8.dtype != np.uint8:
+        raise TypeError("FP8 operands are passed as uint8 codes")
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    off = _as_offsets(off)
+    M_tot, K = X8.shape
+    E, K2, N = W8.shape
+    if K2 != K or off.size != E + 1 or sx.shape != (M_tot,) or sw.shape != (E, N):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = np.full((M_tot, N), np.nan, dtype=np.float64)
+    rc = _load().rgg_oracle_grouped_gemm_fp8(_ptr(X8), _ptr(W8), _ptr(sx), _ptr(sw), _ptr(off), E, M_tot, K, N,
+                                             _ptr(out), int(nthreads))
     if rc != ORACLE_OK:
         raise OracleError("oracle rejected the arguments (code %d)" % rc)
     return out

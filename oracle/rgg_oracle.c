@@ -208,6 +208,59 @@ int rgg_oracle_grouped_swiglu(const uint16_t* X, const uint16_t* W13, const int3
     return ORACLE_OK;
 }
 
+/*
+ * FP8 grouped GEMM.  The Pearl article ("What the 15% measures") says the
+ * optimized kernel will be released with Pearl's FP8 scheme but does not
+ * describe it.  Reading taken (the plainest one that keeps the K loop free of
+ * scales): X and W hold FP8 E4M3 codes, X with one fp32 scale per row and W
+ * with one fp32 scale per (expert, output column), so that
+ *
+ *     Y[i, j] = sx[i] * sw[e, j] * sum_k x8[i, k] * w8[e, k, j]      (fp64, k increasing)
+ *
+ * for every row i of expert e.  E4M3 (sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities, S.1111.111 = NaN): a code with exponent
+ * field 0 is the subnormal m/8 * 2^-6, otherwise (1 + m/8) * 2^(e-7); decoding
+ * to double is exact.
+ */
+static double e4m3_to_f64(uint8_t b) {
+    const int s = b >> 7, e = (b >> 3) & 0xF, m = b & 7;
+    if (e == 0xF && m == 7) return NAN;
+    const double v = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+double rgg_oracle_e4m3_to_f64(uint8_t code) { return e4m3_to_f64(code); }
+
+int rgg_oracle_grouped_gemm_fp8(const uint8_t* X8, const uint8_t* W8, const float* sx, const float* sw,
+                                const int32_t* off, int E, int64_t M_tot, int K, int N, double* Y, int nthreads) {
+    if (X8 == NULL || W8 == NULL || sx == NULL || sw == NULL || Y == NULL || K < 1 || N < 1)
+        return ORACLE_ERR_INVALID_ARG;
+    int rc = rgg_oracle_check_offsets(off, E, M_tot);
+    if (rc != ORACLE_OK) return rc;
+    set_threads(nthreads);
+    for (int e = 0; e < E; ++e) {
+        const int64_t row_begin = off[e], row_end = off[e + 1];
+        const uint8_t* We = W8 + (int64_t)e * K * N;
+        const float* swe = sw + (int64_t)e * N;
+        #pragma omp parallel
+        {
+            double* acc = (double*)malloc(sizeof(double) * (size_t)N);
+            #pragma omp for schedule(dynamic, 1)
+            for (int64_t i = row_begin; i < row_end; ++i) {
+                for (int j = 0; j < N; ++j) acc[j] = 0.0;
+                for (int k = 0; k < K; ++k) {
+                    const double x = e4m3_to_f64(X8[i * K + k]);
+                    const uint8_t* wrow = We + (int64_t)k * N;
+                    for (int j = 0; j < N; ++j) acc[j] += x * e4m3_to_f64(wrow[j]);
+                }
+                for (int j = 0; j < N; ++j) Y[i * N + j] = (double)sx[i] * (double)swe[j] * acc[j];
+            }
+            free(acc);
+        }
+    }
+    return ORACLE_OK;
+}
+
 static int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 /*

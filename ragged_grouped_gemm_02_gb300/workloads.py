@@ -207,6 +207,60 @@ def make_custom(counts, K: int, N: int, seed: int, integer_valued: bool = False,
     return Inputs(X, W, offsets_from_counts(counts), counts, w)
 
 
+@dataclass
+class Fp8Inputs:
+    X8: torch.Tensor         # float8_e4m3fn [M_tot, K], CPU
+    W8: torch.Tensor         # float8_e4m3fn [E, K, N], CPU
+    sx: torch.Tensor         # float32 [M_tot]: row i of X is X8[i] * sx[i]
+    sw: torch.Tensor         # float32 [E, N]: column j of W[e] is W8[e][:, j] * sw[e, j]
+    offsets: np.ndarray
+    counts: np.ndarray
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_fp8(X: torch.Tensor, W: torch.Tensor):
+    """Per-row (X) and per-(expert, column) (W) amax scaling into FP8 E4M3
+    codes with torch's round-to-nearest conversion.  Input preparation only:
+    the grouped GEMM receives the codes and the scales."""
+    Xf, Wf = X.float(), W.float()
+    sx = (Xf.abs().amax(dim=1) / E4M3_MAX).clamp_min(1e-12)
+    sw = (Wf.abs().amax(dim=1) / E4M3_MAX).clamp_min(1e-12)            # [E, N]
+    X8 = (Xf / sx[:, None]).to(torch.float8_e4m3fn)
+    W8 = (Wf / sw[:, None, :]).to(torch.float8_e4m3fn)
+    return X8, W8, sx.float(), sw.float()
+
+
+def make_fp8_inputs(w: Workload | str) -> Fp8Inputs:
+    """A workload's inputs drawn as for the bf16 path (same seed and routing),
+    then quantised to E4M3 with per-row / per-column scales."""
+    inp = make_inputs(w)
+    X8, W8, sx, sw = quantize_fp8(inp.X, inp.W)
+    return Fp8Inputs(X8, W8, sx, sw, inp.offsets, inp.counts)
+
+
+def make_fp8_custom(counts, K: int, N: int, seed: int, integer_valued: bool = False, spare_rows: int = 0):
+    """Explicit-count FP8 inputs; ``integer_valued`` gives codes of {-2..2}
+    with every scale 1, so every partial sum is an exact integer."""
+    inp = make_custom(counts, K, N, seed, integer_valued=integer_valued, spare_rows=spare_rows)
+    if integer_valued:
+        X8 = inp.X.float().to(torch.float8_e4m3fn)
+        W8 = inp.W.float().to(torch.float8_e4m3fn)
+        sx = torch.ones(inp.X.shape[0], dtype=torch.float32)
+        sw = torch.ones(inp.W.shape[0], inp.W.shape[2], dtype=torch.float32)
+    else:
+        X8, W8, sx, sw = quantize_fp8(inp.X, inp.W)
+    return Fp8Inputs(X8, W8, sx, sw, inp.offsets, inp.counts)
+
+
+def fp8_codes(t: torch.Tensor) -> np.ndarray:
+    """The uint8 codes of a float8_e4m3fn CPU tensor (what the oracle reads)."""
+    if t.dtype != torch.float8_e4m3fn:
+        raise TypeError("expected a float8_e4m3fn tensor")
+    return t.contiguous().view(torch.uint8).numpy()
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """The uint16 bit patterns of a bf16 CPU tensor (what the oracle reads)."""
     if t.dtype != torch.bfloat16:

@@ -262,6 +262,55 @@ def test_k_not_multiple_of_tile_and_odd_n(oracle_mod):
     np.testing.assert_allclose(Y[3:], Xd[3:] @ Wd[1], rtol=1e-12, atol=1e-12)
 
 
+# ------------------------------------------------------------ FP8 (E4M3)
+
+def test_e4m3_decoder_matches_library_for_every_code(oracle_mod):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e4m3fn).float().double().numpy()
+    mine = np.array([oracle_mod.e4m3_to_f64(c) for c in range(256)])
+    nan = np.isnan(lib)
+    assert np.array_equal(nan, np.isnan(mine)) and nan.sum() == 2  # 0x7F and 0xFF
+    assert np.array_equal(mine[~nan], lib[~nan])
+    # format landmarks: largest finite 448, smallest subnormal 2^-9, one = 0x38
+    assert oracle_mod.e4m3_to_f64(0x7E) == 448.0 and oracle_mod.e4m3_to_f64(0x01) == 2.0 ** -9
+    assert oracle_mod.e4m3_to_f64(0x38) == 1.0 and oracle_mod.e4m3_to_f64(0xB8) == -1.0
+
+
+def test_fp8_integer_codes_are_exact(oracle_mod):
+    counts = [3, 0, 9, 1, 5]
+    f = wl.make_fp8_custom(counts, K=64, N=24, seed=81, integer_valued=True)
+    Y = oracle_mod.grouped_gemm_fp8(wl.fp8_codes(f.X8), wl.fp8_codes(f.W8), f.sx.numpy(), f.sw.numpy(), f.offsets)
+    Xi = f.X8.float().to(torch.int64).numpy()
+    Wi = f.W8.float().to(torch.int64).numpy()
+    off = f.offsets
+    for e in range(len(counts)):
+        assert np.array_equal(Y[off[e]:off[e + 1]], (Xi[off[e]:off[e + 1]] @ Wi[e]).astype(np.float64))
+
+
+def test_fp8_single_expert_is_scaled_plain_gemm(oracle_mod):
+    f = wl.make_fp8_custom([33], K=96, N=40, seed=82)
+    Y = oracle_mod.grouped_gemm_fp8(wl.fp8_codes(f.X8), wl.fp8_codes(f.W8), f.sx.numpy(), f.sw.numpy(), f.offsets)
+    ref = (f.X8.double().numpy() @ f.W8[0].double().numpy()) * np.outer(f.sx.double().numpy(),
+                                                                         f.sw[0].double().numpy())
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_scales_factor_per_row_and_per_expert_column(oracle_mod):
+    counts = [4, 0, 6, 2]
+    f = wl.make_fp8_custom(counts, K=32, N=16, seed=83)
+    X8, W8 = wl.fp8_codes(f.X8), wl.fp8_codes(f.W8)
+    sx, sw = f.sx.numpy().copy(), f.sw.numpy().copy()
+    Y = oracle_mod.grouped_gemm_fp8(X8, W8, sx, sw, f.offsets)
+    sx2, sw2 = sx.copy(), sw.copy()
+    sx2[5] *= 2.0                 # row 5 belongs to expert 2
+    sw2[2, 3] *= 4.0              # column 3 of expert 2 only
+    Y2 = oracle_mod.grouped_gemm_fp8(X8, W8, sx2, sw2, f.offsets)
+    expect = Y.copy()
+    expect[5] *= 2.0
+    expect[4:10, 3] *= 4.0
+    np.testing.assert_allclose(Y2, expect, rtol=1e-15, atol=0)
+
+
 # ------------------------------------------- fused gate-up + SiLU activation
 
 def test_silu_closed_forms(oracle_mod):

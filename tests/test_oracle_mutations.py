@@ -45,6 +45,9 @@ MUTANTS = {
                         "H[i * N + j] = silu_f64(acc[N + j]) * acc[j];"),
     "swiglu_plain_product": ("H[i * N + j] = silu_f64(acc[j]) * acc[N + j];",
                              "H[i * N + j] = acc[j] * acc[N + j];"),
+    "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "fp8_scale_ignores_expert": ("const float* swe = sw + (int64_t)e * N;", "const float* swe = sw;"),
 }
 
 
@@ -174,9 +177,40 @@ def _swiglu_checks_pass(lib):
     return True
 
 
+def _fp8_checks_pass(lib):
+    lib.rgg_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.rgg_oracle_e4m3_to_f64.restype = ctypes.c_double
+    P = ctypes.c_void_p
+    lib.rgg_oracle_grouped_gemm_fp8.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                                ctypes.c_int, P, ctypes.c_int]
+    lib.rgg_oracle_grouped_gemm_fp8.restype = ctypes.c_int
+    # every code against the library's own E4M3 conversion
+    lib_vals = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    mine = np.array([lib.rgg_oracle_e4m3_to_f64(c) for c in range(256)])
+    ok = ~np.isnan(lib_vals)
+    if not np.array_equal(mine[ok], lib_vals[ok]):
+        return False
+    # two experts with distinct column scales against the scaled plain product
+    f = wl.make_fp8_custom([3, 4], K=16, N=8, seed=84)
+    X8, W8 = wl.fp8_codes(f.X8), wl.fp8_codes(f.W8)
+    sx, sw = f.sx.numpy(), f.sw.numpy()
+    off = np.ascontiguousarray(f.offsets, dtype=np.int32)
+    Y = np.full((7, 8), np.nan)
+    if lib.rgg_oracle_grouped_gemm_fp8(X8.ctypes.data, W8.ctypes.data, sx.ctypes.data, sw.ctypes.data,
+                                       off.ctypes.data, 2, 7, 16, 8, Y.ctypes.data, 1) != 0:
+        return False
+    Xd, Wd = f.X8.double().numpy(), f.W8.double().numpy()
+    for e in range(2):
+        ref = (Xd[off[e]:off[e + 1]] @ Wd[e]) * np.outer(sx[off[e]:off[e + 1]].astype(np.float64),
+                                                         sw[e].astype(np.float64))
+        if not np.allclose(Y[off[e]:off[e + 1]], ref, rtol=1e-12, atol=1e-12):
+            return False
+    return True
+
+
 def _all_pass(lib):
     return (_product_checks_pass(lib) and _tile_checks_pass(lib) and _eta_checks_pass(lib)
-            and _swiglu_checks_pass(lib))
+            and _swiglu_checks_pass(lib) and _fp8_checks_pass(lib))
 
 
 def test_unmutated_copy_passes(tmp_path):
