@@ -65,6 +65,10 @@ def parse_args():
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--tail64", type=int, default=0, help="0 auto, 1 on, -1 off")
     p.add_argument("--prefetch-kb", type=int, default=0, help="L2 lookahead in K blocks: 0 auto, -1 off")
+    p.add_argument("--op", default="gemm", choices=["gemm", "swiglu", "fp8"],
+                   help="gemm: Y = X.W; swiglu: the workload's weights read as [gate | up], "
+                        "H = silu(X.W_gate) * (X.W_up) with N/2 output columns; fp8: the same draws "
+                        "quantised to E4M3 with per-row / per-column scales")
     p.add_argument("--profile", action="store_true",
                    help="for ncu: --warmup launches then one more, no timing, no CPU work after")
     return p.parse_args()
@@ -194,7 +198,7 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def oracle_cpu_rate(inp, budget_s=12.0):
+def oracle_cpu_rate(inp, budget_s=12.0, op="gemm", scales=None):
     """The fp64 oracle as it stands, on the host cores, over a bounded sample
     of the workload: the first experts' complete rows (all N columns), about
     `budget_s` of work.  Returns (TFLOP/s, sample description, threads)."""
@@ -203,12 +207,24 @@ def oracle_cpu_rate(inp, budget_s=12.0):
     counts = inp.counts
     K, N = inp.X.shape[1], inp.W.shape[2]
     threads = oracle.max_threads()
-    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    if op == "fp8":
+        xb, wb = wl.fp8_codes(inp.X), wl.fp8_codes(inp.W)
+        sxn, swn = scales[0].numpy(), scales[1].numpy()
+
+        def fn(x, w, off, r0=0, e0=0):
+            return oracle.grouped_gemm_fp8(x, w, sxn[r0:r0 + x.shape[0]], swn[e0:e0 + w.shape[0]], off)
+    else:
+        xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+        base = oracle.grouped_swiglu if op == "swiglu" else oracle.grouped_gemm
+
+        def fn(x, w, off, r0=0, e0=0):
+            return base(x, w, off)
     # calibrate on one expert's rows (or 16 rows)
     e0 = int(np.argmax(counts > 0))
     r = int(min(counts[e0], 16))
+    r0 = int(inp.offsets[e0])
     t0 = time.perf_counter()
-    oracle.grouped_gemm(np.ascontiguousarray(xb[inp.offsets[e0]:inp.offsets[e0] + r]), wb[e0:e0 + 1], [0, r])
+    fn(np.ascontiguousarray(xb[r0:r0 + r]), np.ascontiguousarray(wb[e0:e0 + 1]), [0, r], r0, e0)
     rate = 2.0 * r * K * N / max(time.perf_counter() - t0, 1e-6)
     want = budget_s * rate
     e_take, flops = 0, 0.0
@@ -218,7 +234,7 @@ def oracle_cpu_rate(inp, budget_s=12.0):
     rows = int(inp.offsets[e_take])
     off = inp.offsets[:e_take + 1]
     t0 = time.perf_counter()
-    oracle.grouped_gemm(np.ascontiguousarray(xb[:rows]), np.ascontiguousarray(wb[:e_take]), off)
+    fn(np.ascontiguousarray(xb[:rows]), np.ascontiguousarray(wb[:e_take]), off)
     dt = time.perf_counter() - t0
     sample = "experts 0..%d of %d (%d of %d rows, all %d columns), %.1f GFLOP in %.2f s" % (
         e_take - 1, len(counts), rows, int(counts.sum()), N, flops / 1e9, dt)
@@ -238,7 +254,8 @@ def run_profile(args):
     X, W = inp.X.to(dev), inp.W.to(dev)
     off = torch.from_numpy(inp.offsets).to(dev)
     Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device=dev)
-    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64, prefetch_kb=args.prefetch_kb)
+    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64, prefetch_kb=args.prefetch_kb,
+                host_counts=inp.counts)
     for _ in range(args.warmup + 1):
         rgg.rgg_grouped_gemm(X, W, off, Y, **opts)
     torch.cuda.synchronize(dev)
@@ -262,16 +279,36 @@ def run_ours(args):
     K, N, E = w.K, w.N, w.E
     M_tot = inp.X.shape[0]
     flops, bytes_ = work_of(inp.counts, K, N)
+    fused = args.op == "swiglu"
+    N_out = N // 2 if fused else N
+    if fused:  # the output is half as wide; the weight bytes and MMA work are the same
+        bytes_ -= 2.0 * M_tot * (N - N_out)
+    gemm = rgg.rgg_grouped_gemm_swiglu if fused else rgg.rgg_grouped_gemm
+    if args.op == "fp8":
+        # the same draws quantised to E4M3 with per-row / per-column scales:
+        # X and W stream at one byte per element, scales are fp32
+        X8, W8, sx, sw = wl.quantize_fp8(inp.X, inp.W)
+        active = int(np.count_nonzero(inp.counts))
+        bytes_ = (1.0 * (active * K * N + M_tot * K) + 2.0 * M_tot * N + 4.0 * (M_tot + E * N)
+                  + 4.0 * (E + 1))
+        sx_d, sw_d = sx.to(dev), sw.to(dev)
+        inp.X, inp.W = X8, W8
+
+        def gemm(Xd, Wd, offd, Yd, **kw):
+            return rgg.rgg_grouped_gemm_fp8(Xd, Wd, sx_d, sw_d, offd, Yd, **kw)
     X, W = inp.X.to(dev), inp.W.to(dev)
     off = torch.from_numpy(inp.offsets).to(dev)
-    Y = torch.empty(M_tot, N, dtype=torch.bfloat16, device=dev)
-    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64, prefetch_kb=args.prefetch_kb)
-    plan = rgg.rgg_plan(E, M_tot, K, N, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
-                        **opts)
+    Y = torch.empty(M_tot, N_out, dtype=torch.bfloat16, device=dev)
+    # The tile shape is planned from the routed counts, known on the host as in
+    # the worklog's harness; the kernel itself reads the offsets on the device.
+    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64, prefetch_kb=args.prefetch_kb,
+                host_counts=inp.counts)
+    plan = rgg.rgg_plan(E, M_tot, K, N_out, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
+                        op=args.op, **opts)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        rgg.rgg_grouped_gemm(X, W, off, Y, stream=stream, **opts)
+        gemm(X, W, off, Y, stream=stream, **opts)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -313,13 +350,13 @@ def run_ours(args):
     if not args.no_e2e:
         hX = inp.X.pin_memory()
         hoff = torch.from_numpy(inp.offsets).pin_memory()
-        hY = torch.empty(M_tot, N, dtype=torch.bfloat16).pin_memory()
+        hY = torch.empty(M_tot, N_out, dtype=torch.bfloat16).pin_memory()
         dX = torch.empty_like(X)
         doff = torch.empty_like(off)
         for _ in range(3):
             dX.copy_(hX, non_blocking=True)
             doff.copy_(hoff, non_blocking=True)
-            rgg.rgg_grouped_gemm(dX, W, doff, Y, stream=stream, **opts)
+            gemm(dX, W, doff, Y, stream=stream, **opts)
             hY.copy_(Y, non_blocking=True)
         e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
@@ -328,38 +365,41 @@ def run_ours(args):
         for _ in range(K_steps):
             dX.copy_(hX, non_blocking=True)
             doff.copy_(hoff, non_blocking=True)
-            rgg.rgg_grouped_gemm(dX, W, doff, Y, stream=stream, **opts)
+            gemm(dX, W, doff, Y, stream=stream, **opts)
             hY.copy_(Y, non_blocking=True)
         e_end.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
         e_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
         e2e = {"value": round(flops * K_steps * world / (e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(hX.numel() * 2 + hoff.numel() * 4),
+               "h2d_bytes_per_step": int(hX.numel() * hX.element_size() + hoff.numel() * 4),
                "d2h_bytes_per_step": int(hY.numel() * 2), "ms_per_step": round(e_ms / K_steps, 4),
                "weights": "resident in HBM (model parameters); not copied per step"}
 
     peaks = load_peaks()
     t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
-    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    # a contraction is measured against the peak of its own operand type: FP8
+    # takes the measured bf16 peak times the nominal fp8/bf16 ratio (2)
+    tc_peak = peaks["bf16_tflops"] * (2.0 if args.op == "fp8" else 1.0)
+    t_tc = flops / (tc_peak * 1e12)
     if t_hbm >= t_tc:
         roof = {"bound": "hbm", "achieved": round(bytes_ / (launch_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     else:
         roof = {"bound": "tensor", "achieved": round(flops / (launch_ms / 1e3) / 1e12, 1),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+                "peak": tc_peak, "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = measured_traffic(args.workload)
-    roof["peak_source"] = peaks["source"]
+    roof["peak_source"] = peaks["source"] + (" bf16 x 2 (nominal fp8/bf16 ratio)" if args.op == "fp8" else "")
     roof["algorithmic_per_launch"] = {"flops": flops, "bytes": bytes_}
     roof["launch_ms"] = round(launch_ms, 5)
     roof["hbm_gbs"] = round(bytes_ / (launch_ms / 1e3) / 1e9, 1)
     roof["hbm_frac"] = round(bytes_ / (launch_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
-    roof["tensor_frac"] = round(flops / (launch_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4)
+    roof["tensor_frac"] = round(flops / (launch_ms / 1e3) / 1e12 / tc_peak, 4)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, threads = oracle_cpu_rate(inp)
+        v, sample, threads = oracle_cpu_rate(inp, op=args.op, scales=(sx, sw) if args.op == "fp8" else None)
         cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
 
     value = flops * K_steps * world / (total_ms / 1e3) / 1e12
@@ -367,13 +407,17 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K_steps,
         "warmup": n_warm, "ms_per_step": round(total_ms / K_steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": round(value / page, 4) if page else None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": round(value / page, 4) if page and args.op == "gemm" else None,
+        "dtype": "e4m3" if args.op == "fp8" else "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,1/K) weights)",
-        "config": {"workload": args.workload, "E": E, "K": K, "N": N, "M_tot": M_tot,
+        "config": {"workload": args.workload + ("" if args.op == "gemm" else "+" + args.op), "op": args.op,
+                   "E": E, "K": K,
+                   "N": N_out, "weight_columns": N, "M_tot": M_tot,
                    "routing": w.routing, "note": w.note, "accumulate": "fp32", "out": "bf16",
                    "l2": "inputs larger than L2 (%.0f MB > 129 MB), no flush" % (bytes_ / 1e6)
                    if bytes_ > L2_BYTES else "inputs smaller than L2: back-to-back launches",
-                   "plan": plan, "parallelism": "expert replicas x%d" % world},
+                   "plan": plan, "plan_from": "host-side routed counts (tile shape only)",
+                   "parallelism": "expert replicas x%d" % world},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": K_steps, "impl": "ours",
     }

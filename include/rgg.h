@@ -71,6 +71,9 @@ typedef struct rgg_options {
                                     <= 64 rows of its expert runs as a 64-row MMA with a 64-row X box */
     int prefetch_kb;             /* L2 prefetch lookahead, in 64-wide K blocks of a CTA's walk: 0 = auto,
                                     -1 = off, else 1..64 */
+    int op;                      /* for rgg_plan only: 0 = plan rgg_grouped_gemm, 1 = plan
+                                    rgg_grouped_gemm_swiglu (then N is the output width), 2 = plan
+                                    rgg_grouped_gemm_fp8 */
 } rgg_options;
 
 #define RGG_DEBUG_PRODUCER_STALL 1
@@ -118,6 +121,49 @@ void rgg_destroy(rgg_handle* h);
 rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const int32_t* group_offsets,
                             void* Y, int E, int64_t M_tot, int K, int N, void* stream,
                             const rgg_options* opt);
+
+/*
+ * The fused gate-up projection of an expert FFN with its activation, in one
+ * launch: for every expert e and every row i it owns,
+ *     H[i, j] = silu(g) * u,  g = X[i,:] . W13[e][:, j],  u = X[i,:] . W13[e][:, N + j],
+ * silu(z) = z / (1 + exp(-z)), for 0 <= j < N.  The Worklog ("What I am
+ * measuring", section 7 "Scope of these results") leaves this activation out
+ * of its measured GEMM; the Pearl article ("What the 15% measures") times the
+ * gate and up projections.  The pages do not name the activation; SiLU
+ * gating (SwiGLU) is the reading taken.
+ *
+ * W13: bf16 [E, K, 2N] (gate columns [0, N), up columns [N, 2N)); H: bf16
+ * [M_tot, N].  Each tile loads BN/2 gate and the matching BN/2 up columns,
+ * one MMA of width BN puts both in TMEM, and the epilogue forms silu(g) * u in
+ * fp32 before rounding once to bf16.  Tiles are 1-CTA (rgg_options.bm 0, 64
+ * or 128; bn 0, 128 or 256, the MMA width).  Other arguments, requirements
+ * (N % 8 == 0 here is the output width) and errors as for rgg_grouped_gemm.
+ */
+rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13, const int32_t* group_offsets,
+                                   void* H, int E, int64_t M_tot, int K, int N, void* stream,
+                                   const rgg_options* opt);
+
+/*
+ * FP8 grouped GEMM: for every row i of expert e and every column j,
+ *     Y[i, j] = sx[i] * sw[e, j] * sum_k x8[i, k] * w8[e, k, j]
+ * with X8 and W8 holding FP8 E4M3 codes (the OCP "E4M3FN" format).  The Pearl
+ * article ("What the 15% measures") refers to Pearl's FP8 scheme without
+ * describing it; the reading taken keeps the K loop free of scales: one fp32
+ * scale per row of X and one per (expert, output column) of W, applied to the
+ * fp32 accumulator in the epilogue, the result rounded once to bf16.  The MMA
+ * is tcgen05.mma kind::f8f6f4 (K = 32 per instruction); a shared-memory stage
+ * holds 128 K elements (one 128-byte swizzle row), so X and W stream at half
+ * the bytes of the bf16 path.
+ *
+ * X8: uint8 codes [M_tot, K]; W8: uint8 codes [E, K, N]; sx: fp32 [M_tot];
+ * sw: fp32 [E, N] (16-byte aligned); Y: bf16 [M_tot, N].  K and N are
+ * multiples of 16 (the 16-byte row-stride rule for one-byte elements).  Tiles
+ * are 1-CTA (rgg_options.bm 0, 64 or 128; bn 0, 128 or 256).  Other
+ * arguments and errors as for rgg_grouped_gemm.
+ */
+rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, const float* sx, const float* sw,
+                                const int32_t* group_offsets, void* Y, int E, int64_t M_tot, int K, int N,
+                                void* stream, const rgg_options* opt);
 
 /*
  * The flat tile list the kernel walks, written out for checking (Worklog

@@ -17,7 +17,7 @@ import os
 import threading
 
 __all__ = [
-    "RggError", "rgg_grouped_gemm", "rgg_grouped_gemm_noalloc", "rgg_export_tiles", "rgg_query_status", "rgg_plan",
+    "RggError", "rgg_grouped_gemm", "rgg_grouped_gemm_swiglu", "rgg_grouped_gemm_noalloc", "rgg_export_tiles", "rgg_query_status", "rgg_plan",
     "rgg_status_string", "library_path", "load_library", "EXPORTED_SYMBOLS",
     "RGG_OK", "RGG_ERR_INVALID_ARG", "RGG_ERR_UNSUPPORTED", "RGG_ERR_CUDA", "RGG_ERR_BAD_OFFSETS",
     "RGG_ERR_DEVICE_TIMEOUT", "RGG_ERR_CAPACITY",
@@ -38,7 +38,8 @@ _LIB_PATH = os.path.join(_PKG, "librgg.so")
 # The C ABI entry points declared in include/rgg.h.
 EXPORTED_SYMBOLS = (
     "rgg_create", "rgg_destroy", "rgg_grouped_gemm", "rgg_export_tiles", "rgg_query_status",
-    "rgg_plan", "rgg_status_string", "rgg_last_cuda_error", "rgg_grouped_gemm_noalloc",
+    "rgg_plan", "rgg_status_string", "rgg_last_cuda_error", "rgg_grouped_gemm_noalloc", "rgg_grouped_gemm_swiglu",
+    "rgg_grouped_gemm_fp8",
 )
 
 
@@ -51,7 +52,8 @@ class RggError(RuntimeError):
 class _Options(ctypes.Structure):
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("stages", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("timeout_ns", ctypes.c_uint64), ("host_counts", ctypes.c_void_p),
-                ("debug_flags", ctypes.c_int), ("tail64", ctypes.c_int), ("prefetch_kb", ctypes.c_int)]
+                ("debug_flags", ctypes.c_int), ("tail64", ctypes.c_int), ("prefetch_kb", ctypes.c_int),
+                ("op", ctypes.c_int)]
 
 
 class _PlanInfo(ctypes.Structure):
@@ -96,6 +98,10 @@ def load_library() -> ctypes.CDLL:
         lib.rgg_status_string.restype = ctypes.c_char_p
         lib.rgg_last_cuda_error.argtypes = []
         lib.rgg_last_cuda_error.restype = ctypes.c_char_p
+        lib.rgg_grouped_gemm_swiglu.argtypes = [P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
+        lib.rgg_grouped_gemm_swiglu.restype = I
+        lib.rgg_grouped_gemm_fp8.argtypes = [P, P, P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
+        lib.rgg_grouped_gemm_fp8.restype = I
         lib.rgg_grouped_gemm_noalloc.argtypes = [P, P, P, P, I, I64, I, I, P, P]
         lib.rgg_grouped_gemm_noalloc.restype = I
         _lib = lib
@@ -128,9 +134,9 @@ def _handle(device: int) -> ctypes.c_void_p:
 
 
 def _options(bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0, tail64=0,
-             prefetch_kb=0):
+             prefetch_kb=0, op=0):
     opt = _Options(int(bm), int(bn), int(stages), int(max_ctas), int(timeout_ns), None, int(debug_flags),
-                   int(tail64), int(prefetch_kb))
+                   int(tail64), int(prefetch_kb), int(op))
     keep = None
     if host_counts is not None:
         import numpy as np
@@ -190,6 +196,86 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
     return Y
 
 
+def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
+                            host_counts=None, debug_flags=0, tail64=0, prefetch_kb=0, stream=None, check=False):
+    """H = silu(X_e . W13_e[:, :N]) * (X_e . W13_e[:, N:]) for every expert,
+    one kernel launch (the fused gate-up projection with SiLU activation).
+
+    X: bf16 CUDA [M_tot, K]; W13: bf16 CUDA [E, K, 2N] (gate columns first);
+    group_offsets: int32 CUDA [E+1]; H: optional bf16 CUDA [M_tot, N]."""
+    import torch
+    if not (X.is_cuda and W13.is_cuda and group_offsets.is_cuda):
+        raise ValueError("X, W13 and group_offsets must be CUDA tensors")
+    if X.dtype != torch.bfloat16 or W13.dtype != torch.bfloat16 or group_offsets.dtype != torch.int32:
+        raise TypeError("X and W13 must be bf16 and group_offsets int32")
+    if not (X.is_contiguous() and W13.is_contiguous() and group_offsets.is_contiguous()):
+        raise ValueError("X, W13 and group_offsets must be contiguous")
+    M_tot, K = X.shape
+    E, K2, N2 = W13.shape
+    if K2 != K or N2 % 2 != 0 or group_offsets.numel() != E + 1:
+        raise ValueError("shape mismatch: X %s, W13 %s, offsets %d" % (tuple(X.shape), tuple(W13.shape),
+                                                                      group_offsets.numel()))
+    N = N2 // 2
+    device = X.device.index if X.device.index is not None else torch.cuda.current_device()
+    if H is None:
+        H = torch.empty(M_tot, N, dtype=torch.bfloat16, device=X.device)
+    elif H.shape != (M_tot, N) or H.dtype != torch.bfloat16 or not H.is_contiguous() or not H.is_cuda:
+        raise ValueError("H must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
+    lib = load_library()
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, prefetch_kb)
+    st = _stream_ptr(stream, device)
+    s = lib.rgg_grouped_gemm_swiglu(_handle(device), X.data_ptr(), W13.data_ptr(), group_offsets.data_ptr(),
+                                    H.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
+    del keep
+    if s != RGG_OK:
+        _raise(s, "rgg_grouped_gemm_swiglu")
+    if check:
+        s = lib.rgg_query_status(_handle(device), st)
+        if s != RGG_OK:
+            _raise(s, "rgg_grouped_gemm_swiglu (device status)")
+    return H
+
+
+def rgg_grouped_gemm_fp8(X8, W8, sx, sw, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0,
+                         timeout_ns=0, host_counts=None, debug_flags=0, tail64=0, prefetch_kb=0, stream=None,
+                         check=False):
+    """Y[i, j] = sx[i] * sw[e, j] * (X8_e . W8_e)[i, j] with FP8 E4M3 operands.
+
+    X8: float8_e4m3fn CUDA [M_tot, K]; W8: float8_e4m3fn CUDA [E, K, N];
+    sx: float32 CUDA [M_tot]; sw: float32 CUDA [E, N]; group_offsets: int32
+    CUDA [E+1]; Y: optional bf16 CUDA [M_tot, N]."""
+    import torch
+    for t in (X8, W8, sx, sw, group_offsets):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("all operands must be contiguous CUDA tensors")
+    if X8.dtype != torch.float8_e4m3fn or W8.dtype != torch.float8_e4m3fn:
+        raise TypeError("X8 and W8 must be float8_e4m3fn")
+    if sx.dtype != torch.float32 or sw.dtype != torch.float32 or group_offsets.dtype != torch.int32:
+        raise TypeError("sx and sw must be float32 and group_offsets int32")
+    M_tot, K = X8.shape
+    E, K2, N = W8.shape
+    if K2 != K or group_offsets.numel() != E + 1 or sx.shape != (M_tot,) or sw.shape != (E, N):
+        raise ValueError("shape mismatch")
+    device = X8.device.index if X8.device.index is not None else torch.cuda.current_device()
+    if Y is None:
+        Y = torch.empty(M_tot, N, dtype=torch.bfloat16, device=X8.device)
+    elif Y.shape != (M_tot, N) or Y.dtype != torch.bfloat16 or not Y.is_contiguous() or not Y.is_cuda:
+        raise ValueError("Y must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
+    lib = load_library()
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, prefetch_kb)
+    st = _stream_ptr(stream, device)
+    s = lib.rgg_grouped_gemm_fp8(_handle(device), X8.data_ptr(), W8.data_ptr(), sx.data_ptr(), sw.data_ptr(),
+                                 group_offsets.data_ptr(), Y.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
+    del keep
+    if s != RGG_OK:
+        _raise(s, "rgg_grouped_gemm_fp8")
+    if check:
+        s = lib.rgg_query_status(_handle(device), st)
+        if s != RGG_OK:
+            _raise(s, "rgg_grouped_gemm_fp8 (device status)")
+    return Y
+
+
 def rgg_grouped_gemm_noalloc(X, W, group_offsets, Y=None, status_out=None, stream=None):
     """The same product through the entry point that allocates nothing (no
     handle; the kernel's status word lives in a fixed device array inside
@@ -245,10 +331,12 @@ def rgg_query_status(device: int | None = None, stream=None) -> int:
 
 
 def rgg_plan(E: int, M_tot: int, K: int, N: int, *, num_sms: int = 0, smem_optin: int = 0, bm=0, bn=0,
-             stages=0, max_ctas=0, host_counts=None, tail64=0, prefetch_kb=0) -> dict:
-    """The launch configuration rgg_grouped_gemm would use (host-only)."""
+             stages=0, max_ctas=0, host_counts=None, tail64=0, prefetch_kb=0, op: str = "gemm") -> dict:
+    """The launch configuration rgg_grouped_gemm (op="gemm") or
+    rgg_grouped_gemm_swiglu (op="swiglu", N = output width) would use (host-only)."""
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, 0, host_counts, 0, tail64, prefetch_kb)
+    opt, keep = _options(bm, bn, stages, max_ctas, 0, host_counts, 0, tail64, prefetch_kb,
+                         {"gemm": 0, "swiglu": 1, "fp8": 2}[op])
     info = _PlanInfo()
     s = lib.rgg_plan(int(num_sms), int(smem_optin), int(E), int(M_tot), int(K), int(N), ctypes.byref(opt),
                      ctypes.byref(info))

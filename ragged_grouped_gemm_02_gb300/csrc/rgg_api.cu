@@ -97,8 +97,10 @@ rgg_status check_sizes(int E, int64_t M_tot, int K, int N) {
     return RGG_OK;
 }
 
+// `fused`: the fused gate-up + SiLU op (N then counts the 2N weight columns)
+// or the FP8 op: tiles are 1-CTA (64 or 128 rows) and BN is 128 or 256.
 rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N, const rgg_options* opt,
-                     Plan* out) {
+                     Plan* out, bool fused = false) {
     rgg_status s = check_sizes(E, M_tot, K, N);
     if (s != RGG_OK) return s;
     if (num_sms <= 0) num_sms = kDefaultSms;
@@ -110,6 +112,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (want_bm != 0 && want_bm != 64 && want_bm != 128 && want_bm != 256) return RGG_ERR_INVALID_ARG;
     if (want_bn != 0 && want_bn != 128 && want_bn != 192 && want_bn != 256) return RGG_ERR_INVALID_ARG;
     if (want_bm == 256 && want_bn == 192) return RGG_ERR_INVALID_ARG;  // pair tiles split BN in whole panels
+    if (fused && (want_bm == 256 || want_bn == 192)) return RGG_ERR_INVALID_ARG;
     if (want_stages != 0 && (want_stages < 2 || want_stages > rgg::kMaxStages)) return RGG_ERR_INVALID_ARG;
     if (max_ctas < 0) return RGG_ERR_INVALID_ARG;
     const int want_tail = opt ? opt->tail64 : 0;
@@ -129,44 +132,57 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         return static_cast<int64_t>(E) * ceil_div(avg, bm);
     };
 
-    // BM: 64-row tiles when experts average 64 rows or fewer (counting only
-    // experts that have rows, when the counts are known).
-    int bm = want_bm;
-    if (bm == 0) {
-        double avg = static_cast<double>(M_tot) / E;
-        if (opt && opt->host_counts) {
-            int64_t rows = 0, busy = 0;
-            for (int e = 0; e < E; ++e)
-                if (opt->host_counts[e] > 0) {
-                    rows += opt->host_counts[e];
-                    ++busy;
-                }
-            avg = busy ? static_cast<double>(rows) / busy : 0.0;
-        }
-        bm = (avg <= 64.0) ? 64 : 128;
+    // Tile shape.  Experts that average 64 rows or fewer (counting only the
+    // experts that have rows, when the counts are known) take 64-row tiles:
+    // the weight-bound regime, where half-size X stages leave more of the
+    // ring to weights.  Otherwise every (BM, BN) candidate is costed as the
+    // number of waves of persistent work times a per-tile cost of (BN + 64)
+    // (MMA and weight bytes grow with BN, plus a fixed per-tile cost); a CTA
+    // pair's 256-row tile occupies two SMs and halves each CTA's weight
+    // stage, which measured as 0.87 of a 1-CTA tile of the same BN.  Ties go
+    // to the wider tile.  Without host counts the experts are assumed
+    // balanced, as in the worklog's eta estimate.
+    double avg = static_cast<double>(M_tot) / E;
+    if (opt && opt->host_counts) {
+        int64_t rows = 0, busy = 0;
+        for (int e = 0; e < E; ++e)
+            if (opt->host_counts[e] > 0) {
+                rows += opt->host_counts[e];
+                ++busy;
+            }
+        avg = busy ? static_cast<double>(rows) / busy : 0.0;
     }
-    const bool pair = (bm == 256);
-    // A CTA pair (256-row tile) counts as one unit of persistent work.
-    const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;
-
-    // BN: fewest waves of persistent work, a tile costing about (BN + 64)
-    // units (MMA and weight bytes scale with BN, plus a fixed per-tile cost);
-    // ties go to the wider tile.
+    int bm = want_bm;
     int bn = want_bn;
-    if (bn == 0) {
-        const int64_t mt = std::max<int64_t>(1, m_tiles(bm));
-        int64_t best = INT64_MAX;
-        for (int cand : {256, 192, 128}) {
-            if (pair && cand == 192) continue;
-            const int64_t tiles = mt * ceil_div(N, cand);
-            const int64_t waves = ceil_div(tiles, units);
-            const int64_t cost = waves * (cand + 64);
-            if (cost < best) {
-                best = cost;
-                bn = cand;
+    if (bm == 0 && avg <= 64.0) bm = 64;
+    {
+        double best = 1e300;
+        int best_bm = bm, best_bn = bn;
+        for (int cbm : {256, 128, 64}) {
+            if (bm != 0 && cbm != bm) continue;
+            if (fused && cbm == 256) continue;
+            if (bm == 0 && cbm == 64) continue;  // 64-row tiles only for small groups (above)
+            const bool cpair = (cbm == 256);
+            const int cunits = cpair ? std::max(1, grid_cap / 2) : grid_cap;
+            const int64_t mt = std::max<int64_t>(1, m_tiles(cbm));
+            for (int cbn : {256, 192, 128}) {
+                if (bn != 0 && cbn != bn) continue;
+                if ((cpair || fused) && cbn == 192) continue;
+                const int64_t waves = ceil_div(mt * ceil_div(N, cbn), cunits);
+                const double cost = static_cast<double>(waves) * (cbn + 64) * (cpair ? 0.87 : 1.0);
+                if (cost < best) {
+                    best = cost;
+                    best_bm = cbm;
+                    best_bn = cbn;
+                }
             }
         }
+        bm = best_bm;
+        bn = best_bn;
     }
+    const bool pair = (bm == 256);
+    const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;
+    (void)units;
 
     const int64_t max_tiles = tile_bound(E, M_tot, N, bm, bn);
     if (max_tiles >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
@@ -244,6 +260,42 @@ rgg_status encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K
             g_last_cuda_error = "cuTensorMapEncodeTiled(W) failed with CUresult " + std::to_string(static_cast<int>(r));
             return RGG_ERR_CUDA;
         }
+    }
+    return RGG_OK;
+}
+
+// FP8 operands: byte tensors with 128-byte boxes (one swizzle row = 128 K
+// elements of X, 128 N columns of W).
+rgg_status encode_maps_fp8(const void* X8, const void* W8, int E, int64_t M_tot, int K, int N, int bm,
+                           CUtensorMap* tx, CUtensorMap* tx64, CUtensorMap* tw) {
+    EncodeTiledFn encode = encode_tiled_fn();
+    if (!encode) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled is not available from the driver";
+        return RGG_ERR_CUDA;
+    }
+    const cuuint64_t xdims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M_tot)};
+    const cuuint64_t xstrides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t estr2[2] = {1, 1};
+    const cuuint32_t xbox[2] = {128, static_cast<cuuint32_t>(bm)};
+    const cuuint32_t xbox64[2] = {128, 64};
+    const cuuint64_t wdims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(E)};
+    const cuuint64_t wstrides[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(N) * K};
+    const cuuint32_t wbox[3] = {128, 128, 1};
+    const cuuint32_t estr3[3] = {1, 1, 1};
+    CUresult r = encode(tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(X8), xdims, xstrides, xbox, estr2,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS)
+        r = encode(tx64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(X8), xdims, xstrides, xbox64, estr2,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS)
+        r = encode(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(W8), wdims, wstrides, wbox, estr3,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled(FP8) failed with CUresult " + std::to_string(static_cast<int>(r));
+        return RGG_ERR_CUDA;
     }
     return RGG_OK;
 }
@@ -329,11 +381,15 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
                     rgg_plan_info* out) {
     if (!out) return RGG_ERR_INVALID_ARG;
     Plan p;
-    rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, N, opt, &p);
+    const int op = opt ? opt->op : 0;
+    if (op < 0 || op > 2) return RGG_ERR_INVALID_ARG;
+    if (op == 1 && (N < 8 || N % 8 != 0 || N > (1 << 30))) return RGG_ERR_INVALID_ARG;
+    if (op == 2 && (K % 16 != 0 || N % 16 != 0)) return RGG_ERR_INVALID_ARG;
+    rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, op == 1 ? 2 * N : N, opt, &p, op != 0);
     if (s != RGG_OK) return s;
     out->bm = p.bm;
     out->bn = p.bn;
-    out->bk = rgg::kBK;
+    out->bk = (op == 2) ? 128 : rgg::kBK;
     out->stages = p.stages;
     out->grid = p.grid;
     out->threads = rgg::kThreads;
@@ -391,6 +447,95 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
                       : (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
                                       : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm launch");
+}
+
+rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13, const int32_t* group_offsets,
+                                   void* H, int E, int64_t M_tot, int K, int N, void* stream,
+                                   const rgg_options* opt) {
+    if (!h || !group_offsets || !W13) return RGG_ERR_INVALID_ARG;
+    rgg_status s = check_sizes(E, M_tot, K, N);
+    if (s != RGG_OK) return s;
+    if (N > (1 << 30)) return RGG_ERR_INVALID_ARG;
+    if (M_tot > 0 && (!X || !H)) return RGG_ERR_INVALID_ARG;
+    if (!aligned(W13, 16) || !aligned(group_offsets, 4) || (M_tot > 0 && (!aligned(X, 16) || !aligned(H, 16))))
+        return RGG_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceScope scope(h->device);
+    if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
+    if (M_tot == 0) {
+        cudaError_t err = rgg::launch_validate_offsets(group_offsets, E, M_tot, h->d_status, st);
+        return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
+    }
+    Plan p;
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, /*fused=*/true);
+    if (s != RGG_OK) return s;
+    CUtensorMap tx, tx64, tw;
+    s = encode_maps(X, W13, E, M_tot, K, 2 * N, p.bm, &tx, &tx64, &tw);
+    if (s != RGG_OK) return s;
+    rgg::GemmArgs a;
+    a.offsets = group_offsets;
+    a.Y = static_cast<__nv_bfloat16*>(H);
+    a.status = h->d_status;
+    a.M_tot = M_tot;
+    a.E = E;
+    a.K = K;
+    a.N = N;  // output columns; the gate / up split of W13 is at column N
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(K, rgg::kBK));
+    a.n_tiles_n = static_cast<int32_t>(ceil_div(N, p.bn / 2));
+    a.stages = p.stages;
+    a.y_vec32 = ((N % 16) == 0 && aligned(H, 32)) ? 1 : 0;
+    a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+    a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
+    a.tail64 = p.tail64;
+    a.prefetch_kb = p.prefetch_kb;
+    cudaError_t err = rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_swiglu launch");
+}
+
+rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, const float* sx, const float* sw,
+                                const int32_t* group_offsets, void* Y, int E, int64_t M_tot, int K, int N,
+                                void* stream, const rgg_options* opt) {
+    if (!h || !group_offsets || !W8 || !sw) return RGG_ERR_INVALID_ARG;
+    rgg_status s = check_sizes(E, M_tot, K, N);
+    if (s != RGG_OK) return s;
+    if (K < 16 || N < 16 || K % 16 != 0 || N % 16 != 0) return RGG_ERR_INVALID_ARG;
+    if (M_tot > 0 && (!X8 || !Y || !sx)) return RGG_ERR_INVALID_ARG;
+    if (!aligned(W8, 16) || !aligned(sw, 16) || !aligned(group_offsets, 4) ||
+        (M_tot > 0 && (!aligned(X8, 16) || !aligned(Y, 16) || !aligned(sx, 4))))
+        return RGG_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceScope scope(h->device);
+    if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
+    if (M_tot == 0) {
+        cudaError_t err = rgg::launch_validate_offsets(group_offsets, E, M_tot, h->d_status, st);
+        return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
+    }
+    Plan p;
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p, /*fused=*/true);
+    if (s != RGG_OK) return s;
+    CUtensorMap tx, tx64, tw;
+    s = encode_maps_fp8(X8, W8, E, M_tot, K, N, p.bm, &tx, &tx64, &tw);
+    if (s != RGG_OK) return s;
+    rgg::GemmArgs a;
+    a.offsets = group_offsets;
+    a.Y = static_cast<__nv_bfloat16*>(Y);
+    a.status = h->d_status;
+    a.M_tot = M_tot;
+    a.E = E;
+    a.K = K;
+    a.N = N;
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(K, 128));
+    a.n_tiles_n = static_cast<int32_t>(ceil_div(N, p.bn));
+    a.stages = p.stages;
+    a.y_vec32 = ((N % 16) == 0 && aligned(Y, 32)) ? 1 : 0;
+    a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+    a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
+    a.tail64 = p.tail64;
+    a.prefetch_kb = p.prefetch_kb;
+    a.sx = sx;
+    a.sw = sw;
+    cudaError_t err = rgg::launch_gemm_fp8(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_fp8 launch");
 }
 
 rgg_status rgg_export_tiles(rgg_handle* h, const int32_t* group_offsets, int E, int64_t M_tot, int N, int bm,

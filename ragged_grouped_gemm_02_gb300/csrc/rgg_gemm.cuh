@@ -69,6 +69,8 @@ struct GemmArgs {
     int32_t tail64;          // 1: tiles holding <= 64 rows run as 64-row MMAs (128-row kernels)
     int32_t prefetch_kb;     // L2 prefetch lookahead in K blocks (0 = off)
     uint64_t timeout_ns;
+    const float* sx = nullptr;  // FP8 kernels: fp32 scale of each row of X [M_tot]
+    const float* sw = nullptr;  // FP8 kernels: fp32 scale of each (expert, column) of W [E, N]
 };
 
 // Shared-memory carve-up shared by the host planner and the kernel.  Offsets
@@ -117,16 +119,26 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
     return true;
 }
 
-template <int BM, int BN>
+// Element traits.  Every stage row is one 128-byte swizzle row, so a bf16
+// stage covers K = 64 and an FP8 (E4M3) stage K = 128, with the same bytes:
+// A is BM x 128 B, B is BN/kPanelN panels of kKStage K rows x 128 B.
+template <int BM, int BN, bool kFp8 = false>
 struct TileConfig {
     static_assert(BM == 64 || BM == 128, "tcgen05 cta_group::1 tiles are 64 or 128 rows");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN is a multiple of one 64-column panel, at most 256");
+    static_assert(!kFp8 || BN % 128 == 0, "FP8 weight panels are 128 columns wide");
+    static constexpr int kKStage = kFp8 ? 128 : 64;                        // K elements per stage
+    static constexpr int kPanelN = kFp8 ? 128 : 64;                        // W columns per panel
+    static constexpr uint32_t kPanelB = static_cast<uint32_t>(kKStage) * 128u;  // bytes per W panel
+    static constexpr uint32_t kBStep = kFp8 ? 4096u : 2048u;  // B start advance per MMA (32 or 16 K rows)
     static constexpr uint32_t kTmemCols = (2 * BN <= 256) ? 256u : 512u;  // two accumulator buffers
-    static constexpr uint32_t kStageTx = static_cast<uint32_t>((BM + BN) * kBK * 2);
-    static constexpr uint32_t kStageTx64 = static_cast<uint32_t>((64 + BN) * kBK * 2);  // 64-row tail tile
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, /*b_mn_major=*/true);
-    static constexpr uint32_t kIdesc64 = idesc_bf16_f32(64, BN, /*b_mn_major=*/true);
+    static constexpr uint32_t kStageTx = static_cast<uint32_t>((BM + BN) * 128);
+    static constexpr uint32_t kStageTx64 = static_cast<uint32_t>((64 + BN) * 128);  // 64-row tail tile
+    static constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(BM, BN, true) : idesc_bf16_f32(BM, BN, true);
+    static constexpr uint32_t kIdesc64 = kFp8 ? idesc_e4m3_f32(64, BN, true) : idesc_bf16_f32(64, BN, true);
 };
+
+constexpr int kMmasPerStage = 4;  // K = 16 (bf16) or 32 (FP8) per instruction
 
 // A 128-row tile whose rows are the last <= 64 of its expert runs as a
 // 64-row MMA (the "tail64" mode): the tile list is unchanged, only the MMA
@@ -136,11 +148,31 @@ __device__ __forceinline__ bool runs_as_64_rows(const GemmArgs& args, const Tile
     return BM == 64 || (args.tail64 != 0 && c.rows <= 64);
 }
 
-template <int BM, int BN>
+// Epilogue modes.  kEpiPlain stores the accumulator.  kEpiSwiGLU is the fused
+// gate-up projection: W holds 2N columns (gate [0, N), up [N, 2N)); a tile of
+// BN/2 output columns loads the matching BN/2 gate and BN/2 up columns into one
+// B stage, one MMA of width BN puts gate | up side by side in TMEM, and the
+// epilogue writes silu(gate) * up.
+constexpr int kEpiPlain = 0;
+constexpr int kEpiSwiGLU = 1;
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+
+template <int BM, int BN, int kEpi = kEpiPlain, bool kFp8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
                         const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
-    using Cfg = TileConfig<BM, BN>;
+    using Cfg = TileConfig<BM, BN, kFp8>;
+    static_assert(kEpi == kEpiPlain || (BN % 128) == 0, "fused gate-up tiles hold whole gate and up panels");
+    static_assert(!(kFp8 && kEpi == kEpiSwiGLU), "the fused gate-up epilogue is bf16 only");
+    constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;  // output columns per tile
+    constexpr int kPanels = BN / Cfg::kPanelN;
+    // Column of W read by B panel p of a tile whose first output column is col0.
+    auto w_col = [&](int32_t col0, int p) -> int32_t {
+        if (kEpi == kEpiSwiGLU)
+            return (p < kPanels / 2) ? col0 + Cfg::kPanelN * p : args.N + col0 + Cfg::kPanelN * (p - kPanels / 2);
+        return col0 + Cfg::kPanelN * p;
+    };
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
     const int warp = threadIdx.x >> 5;
@@ -216,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t t_ahead = -1;
             TileCoord c_ahead = {0, 0, 0, 0};
             for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
-                const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+                const TileCoord c = decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
                 const bool half = runs_as_64_rows<BM>(args, c);
                 const uint32_t tx_bytes = half ? Cfg::kStageTx64 : Cfg::kStageTx;
                 const CUtensorMap* xmap = (BM == 128 && half) ? &tmap_x64 : &tmap_x;
@@ -226,11 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full_bar(st), tx_bytes);
-                    tma_load_2d(a0 + st * sp.a_stage, xmap, full_bar(st), kb * kBK, c.row0);
+                    tma_load_2d(a0 + st * sp.a_stage, xmap, full_bar(st), kb * Cfg::kKStage, c.row0);
 #pragma unroll
-                    for (int p = 0; p < BN / 64; ++p)
-                        tma_load_3d(b0 + st * sp.b_stage + p * kPanelBytes, &tmap_w, full_bar(st), c.col0 + 64 * p,
-                                    kb * kBK, c.expert);
+                    for (int p = 0; p < kPanels; ++p)
+                        tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st), w_col(c.col0, p),
+                                    kb * Cfg::kKStage, c.expert);
                     ++issued;
                     if (++st == S) {
                         st = 0;
@@ -247,14 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (t_a < T) {
                             if (t_a != t_ahead) {
-                                c_ahead = decode_tile(s_off, s_pre, E, BM, BN, nN, t_a);
+                                c_ahead = decode_tile(s_off, s_pre, E, BM, kOutN, nN, t_a);
                                 t_ahead = t_a;
                             }
 #pragma unroll
-                            for (int p = 0; p < BN / 64; ++p)
-                                tma_prefetch_l2_3d(&tmap_w, c_ahead.col0 + 64 * p, kb_a * kBK, c_ahead.expert);
+                            for (int p = 0; p < kPanels; ++p)
+                                tma_prefetch_l2_3d(&tmap_w, w_col(c_ahead.col0, p), kb_a * Cfg::kKStage,
+                                                   c_ahead.expert);
                             tma_prefetch_l2_2d(runs_as_64_rows<BM>(args, c_ahead) ? &tmap_x64 : &tmap_x,
-                                               kb_a * kBK, c_ahead.row0);
+                                               kb_a * Cfg::kKStage, c_ahead.row0);
                         }
                     }
                 }
@@ -276,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_ph = 0;
             bool ok = true;
             for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
-                const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+                const TileCoord c = decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
                 const uint32_t idesc = runs_as_64_rows<BM>(args, c) ? Cfg::kIdesc64 : Cfg::kIdesc;
                 if (!wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, args.status, args.timeout_ns)) {
                     ok = false;
@@ -293,10 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_st = a0 + st * sp.a_stage;
                     const uint32_t b_st = b0 + st * sp.b_stage;
 #pragma unroll
-                    for (int j = 0; j < kBK / 16; ++j) {
+                    for (int j = 0; j < kMmasPerStage; ++j) {
                         const uint64_t ad = sw128_desc(a_st + 32u * j, 16u, 1024u);
-                        const uint64_t bd = sw128_desc(b_st + 2048u * j, kPanelBytes, 1024u);
-                        mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+                        const uint64_t bd = sw128_desc(b_st + Cfg::kBStep * j, Cfg::kPanelB, 1024u);
+                        if constexpr (kFp8)
+                            mma_f8_ss(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+                        else
+                            mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
                     }
                     mma_commit(empty_bar(st));  // frees the stage once these MMAs have read it
                     if (++st == S) {
@@ -324,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_ph = 0;
         for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
-            const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+            const TileCoord c = decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
             // M = 128: tile row 32q + lane sits in TMEM lane 32q + lane.  M = 64:
             // tile row 16q + i sits in TMEM lane 32q + i (i < 16).
             const bool half = runs_as_64_rows<BM>(args, c);
@@ -337,10 +373,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_ok = (!half || lane < 16) && (r_local < c.rows);
             __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0;
 #pragma unroll 1
-            for (int cc = 0; cc < BN; cc += 32) {
+            for (int cc = 0; cc < kOutN; cc += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
-                tmem_ld_wait();
+                if (kEpi == kEpiSwiGLU) {
+                    // gate in columns [cc, cc+32), up in [kOutN + cc, kOutN + cc + 32)
+                    uint32_t u[32];
+                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kOutN + cc), u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __float_as_uint(silu_f32(__uint_as_float(v[i])) * __uint_as_float(u[i]));
+                } else {
+                    tmem_ld_wait();
+                }
+                if constexpr (kFp8) {
+                    // dequantise: row scale of X times the expert's column scale of W
+                    if (row_ok) {
+                        const float rs = __ldg(args.sx + c.row0 + r_local);
+                        const float* swp = args.sw + static_cast<int64_t>(c.expert) * N + c.col0 + cc;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (c.col0 + cc + 16 * h < N) {
+#pragma unroll
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    const float4 s4 = __ldg(reinterpret_cast<const float4*>(swp + 16 * h) + q4);
+                                    const int i0 = 16 * h + 4 * q4;
+                                    v[i0 + 0] = __float_as_uint(__uint_as_float(v[i0 + 0]) * rs * s4.x);
+                                    v[i0 + 1] = __float_as_uint(__uint_as_float(v[i0 + 1]) * rs * s4.y);
+                                    v[i0 + 2] = __float_as_uint(__uint_as_float(v[i0 + 2]) * rs * s4.z);
+                                    v[i0 + 3] = __float_as_uint(__uint_as_float(v[i0 + 3]) * rs * s4.w);
+                                }
+                            }
+                        }
+                    }
+                }
                 if (row_ok) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {

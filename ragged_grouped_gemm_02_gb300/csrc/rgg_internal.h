@@ -20,6 +20,16 @@ cudaError_t launch_gemm_bm128(int bn, int grid, size_t smem, cudaStream_t stream
 cudaError_t launch_gemm_bm64(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                              const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 
+// Fused gate-up + SiLU (kEpiSwiGLU): `bm` is 64 or 128, `bn` (the MMA width,
+// twice the output columns per tile) is 128 or 256; tmap_w spans 2N columns.
+cudaError_t launch_gemm_swiglu(int bm, int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
+                               const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
+
+// FP8 (E4M3) operands with per-row / per-column scales: `bm` 64 or 128, `bn`
+// 128 or 256; the tensor maps are over bytes with 128-byte boxes.
+cudaError_t launch_gemm_fp8(int bm, int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
+                            const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
+
 // CTA-pair kernel (256-row tiles, clusters of two): `bn` is 128 or 256 and
 // `grid` is even.
 cudaError_t launch_gemm_pair(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,

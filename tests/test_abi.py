@@ -85,11 +85,27 @@ def test_plan_small_decode_uses_64_row_tiles(lib):
     assert p["smem_bytes"] <= 232448
 
 
-def test_plan_large_groups_use_128_row_tiles(lib):
+def test_plan_large_balanced_groups_use_cta_pairs(lib):
+    # 256 rows per expert, balanced: one 256-row pair tile per expert
     p = rgg.rgg_plan(64, 16384, 1024, 2688)
+    assert p["bm"] == 256 and p["bn"] == 256 and p["tmem_cols"] == 512 and p["grid"] % 2 == 0
+
+
+def test_plan_skewed_counts_prefer_128_row_tiles(lib):
+    # the same total under rank^-1.2 skew: 256-row tiles would be 40 % padding
+    from ragged_grouped_gemm_02_gb300 import workloads as wl
+    counts = wl.workload_counts("skew16k")
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=counts)
+    assert p["bm"] == 128 and p["bn"] == 256 and p["tail64"] == 1
+    # experts of 128 rows: a pair tile would be half empty
+    p = rgg.rgg_plan(32, 4096, 6144, 4096, host_counts=[128] * 32)
     assert p["bm"] == 128
-    assert p["bn"] in (128, 192, 256)
-    assert p["tmem_cols"] == (256 if p["bn"] == 128 else 512)
+
+
+def test_plan_wave_cost_prefers_exact_n_tiling(lib):
+    # N = 2688 = 14 x 192: with 1-CTA 128-row tiles forced, BN = 192 leaves no padded columns
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, bm=128)
+    assert p["bn"] == 192 and p["tmem_cols"] == 512
 
 
 def test_plan_stages_fill_shared_memory(lib):

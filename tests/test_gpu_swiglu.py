@@ -1,0 +1,107 @@
+"""Parity of the fused gate-up projection + SiLU (rgg_grouped_gemm_swiglu)
+with the fp64 oracle, on a GB300.
+
+Same bar as the plain GEMM: |gpu - oracle| <= 1e-2 * max(1, |oracle|)
+elementwise, rows of no expert untouched.  At full size the oracle value of a
+sampled output is silu(g) * u with g and u from the oracle's pinned grouped
+GEMM at the gate column j and the up column N + j.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ragged_grouped_gemm_02_gb300 as rgg
+from ragged_grouped_gemm_02_gb300 import _build
+from ragged_grouped_gemm_02_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+CANARY = 0x7FC1
+RTOL = 1e-2
+SHAPES = [(64, 128), (64, 256), (128, 128), (128, 256)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    _build.build()
+    oracle.build()
+
+
+def _run(inp, **opts):
+    X, W13 = inp.X.cuda(), inp.W.cuda()
+    off = torch.from_numpy(inp.offsets).cuda()
+    N = W13.shape[2] // 2
+    H = torch.full((X.shape[0], N), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    rgg.rgg_grouped_gemm_swiglu(X, W13, off, H, check=True, **opts)
+    torch.cuda.synchronize()
+    return H.cpu()
+
+
+def _check(inp, H):
+    ref = oracle.grouped_swiglu(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
+    M_used = int(inp.offsets[-1])
+    got = H[:M_used].double().numpy()
+    err = np.abs(got - ref[:M_used])
+    bound = RTOL * np.maximum(1.0, np.abs(ref[:M_used]))
+    bad = np.argwhere(~(err <= bound))
+    assert bad.size == 0, "%d outputs out of tolerance, first %s gpu %r oracle %r" % (
+        bad.shape[0], bad[0].tolist(), got[tuple(bad[0])], ref[:M_used][tuple(bad[0])])
+    assert bool((H.view(torch.int16)[M_used:] == CANARY).all())
+
+
+@pytest.mark.parametrize("bm,bn", SHAPES)
+def test_tiny_every_tile_shape(bm, bn):
+    inp = wl.make_custom([37, 0, 64, 155], K=256, N=2 * 256, seed=71, spare_rows=4)
+    _check(inp, _run(inp, bm=bm, bn=bn))
+
+
+@pytest.mark.parametrize("bm,bn", SHAPES)
+def test_ragged_k_and_n_tails(bm, bn):
+    # output N = 520: a half 16-column chunk at the end, and gate panels that
+    # run past column N into the up half (masked); K = 264
+    counts = [0, 1, 63, 64, 65, 127, 128, 129, 300, 17]
+    inp = wl.make_custom(counts, K=264, N=2 * 520, seed=72)
+    _check(inp, _run(inp, bm=bm, bn=bn))
+
+
+def test_auto_plan_and_tail_tiles():
+    counts = [500, 3, 0, 257, 1024, 77, 129, 2, 640, 64]
+    inp = wl.make_custom(counts, K=512, N=2 * 384, seed=73)
+    _check(inp, _run(inp))
+    _check(inp, _run(inp, tail64=-1))
+
+
+def test_bad_offsets_rejected():
+    inp = wl.make_custom([50, 10, 40], K=64, N=2 * 128, seed=74)
+    X, W13 = inp.X.cuda(), inp.W.cuda()
+    H = torch.full((100, 128), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_grouped_gemm_swiglu(X, W13, torch.tensor([0, 50, 40, 100], dtype=torch.int32, device="cuda"), H,
+                                    check=True)
+    assert ei.value.status == rgg.RGG_ERR_BAD_OFFSETS
+    assert bool((H.view(torch.int16) == CANARY).all())
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_full_size_sampled(name):
+    # the workload's weights read as W13 = [gate | up] with N/2 output columns
+    inp = wl.make_inputs(name)
+    X, W13 = inp.X.cuda(), inp.W.cuda()
+    off = torch.from_numpy(inp.offsets).cuda()
+    H = rgg.rgg_grouped_gemm_swiglu(X, W13, off, check=True, host_counts=inp.counts)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(H).all())
+    N = W13.shape[2] // 2
+    rng = np.random.default_rng(zlib.crc32(name.encode()) + 7)
+    rows = rng.integers(0, int(inp.offsets[-1]), 1500)
+    cols = rng.integers(0, N, 1500)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    g = oracle.grouped_gemm_points(xb, wb, inp.offsets, rows, cols)
+    u = oracle.grouped_gemm_points(xb, wb, inp.offsets, rows, cols + N)
+    ref = np.array([oracle.silu(a) for a in g]) * u
+    got = H[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
+    assert (np.abs(got - ref) <= RTOL * np.maximum(1.0, np.abs(ref))).all()
