@@ -64,7 +64,8 @@ def parse_args():
     p.add_argument("--bn", type=int, default=0)
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--tail64", type=int, default=0, help="0 auto, 1 on, -1 off")
-    p.add_argument("--prefetch-kb", type=int, default=0, help="L2 lookahead in K blocks: 0 auto, -1 off")
+    p.add_argument("--walk-order", type=int, default=0,
+                   help="0 list order, 1 front/back interleave, 2 scatter, 3 size-sorted interleave")
     p.add_argument("--op", default="gemm", choices=["gemm", "swiglu", "fp8"],
                    help="gemm: Y = X.W; swiglu: the workload's weights read as [gate | up], "
                         "H = silu(X.W_gate) * (X.W_up) with N/2 output columns; fp8: the same draws "
@@ -254,7 +255,8 @@ def run_profile(args):
     X, W = inp.X.to(dev), inp.W.to(dev)
     off = torch.from_numpy(inp.offsets).to(dev)
     Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device=dev)
-    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64, prefetch_kb=args.prefetch_kb,
+    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
+                walk_order=args.walk_order,
                 host_counts=inp.counts)
     for _ in range(args.warmup + 1):
         rgg.rgg_grouped_gemm(X, W, off, Y, **opts)
@@ -301,7 +303,8 @@ def run_ours(args):
     Y = torch.empty(M_tot, N_out, dtype=torch.bfloat16, device=dev)
     # The tile shape is planned from the routed counts, known on the host as in
     # the worklog's harness; the kernel itself reads the offsets on the device.
-    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64, prefetch_kb=args.prefetch_kb,
+    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
+                walk_order=args.walk_order,
                 host_counts=inp.counts)
     plan = rgg.rgg_plan(E, M_tot, K, N_out, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
                         op=args.op, **opts)
@@ -345,35 +348,98 @@ def run_ours(args):
     total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
-    # end to end through the public API: pinned host X and offsets in, Y out, every step
+    # End to end through the public API: every step copies its inputs (X, the
+    # offsets, and for FP8 the row scales) in from pinned host memory and its
+    # result out to pinned host memory, all inside the timed region.  As in a
+    # serving loop, two buffer sets let step i's copies overlap the GEMM of its
+    # neighbours: inputs go in on one stream, results come out on another,
+    # events keep each buffer from being overwritten while it is still in use.
     e2e = None
     if not args.no_e2e:
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         hX = inp.X.pin_memory()
         hoff = torch.from_numpy(inp.offsets).pin_memory()
-        hY = torch.empty(M_tot, N_out, dtype=torch.bfloat16).pin_memory()
-        dX = torch.empty_like(X)
-        doff = torch.empty_like(off)
-        for _ in range(3):
-            dX.copy_(hX, non_blocking=True)
-            doff.copy_(hoff, non_blocking=True)
-            gemm(dX, W, doff, Y, stream=stream, **opts)
-            hY.copy_(Y, non_blocking=True)
+        hY = [torch.empty(M_tot, N_out, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        dX = [torch.empty_like(X) for _ in range(2)]
+        doff = [torch.empty_like(off) for _ in range(2)]
+        dY = [Y, torch.empty_like(Y)]
+        fp8 = args.op == "fp8"
+        if fp8:
+            hsx = sx.pin_memory()
+            dsx = [torch.empty_like(sx_d) for _ in range(2)]
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        in_ready, gemm_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        for b in range(2):
+            gemm_done[b].record(stream)
+            out_done[b].record(stream)
+
+        def e2e_step(i):
+            b = i % 2
+            s_in.wait_event(gemm_done[b])          # the GEMM two steps back has read dX[b]
+            with torch.cuda.stream(s_in):
+                dX[b].copy_(hX, non_blocking=True)
+                doff[b].copy_(hoff, non_blocking=True)
+                if fp8:
+                    dsx[b].copy_(hsx, non_blocking=True)
+            in_ready[b].record(s_in)
+            stream.wait_event(in_ready[b])
+            stream.wait_event(out_done[b])         # dY[b] has been read out
+            if fp8:
+                rgg.rgg_grouped_gemm_fp8(dX[b], W, dsx[b], sw_d, doff[b], dY[b], stream=stream, **opts)
+            else:
+                gemm(dX[b], W, doff[b], dY[b], stream=stream, **opts)
+            gemm_done[b].record(stream)
+            s_out.wait_event(gemm_done[b])
+            with torch.cuda.stream(s_out):
+                hY[b].copy_(dY[b], non_blocking=True)
+            out_done[b].record(s_out)
+
+        for i in range(4):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
         e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize(dev)
         e_start.record(stream)
-        for _ in range(K_steps):
-            dX.copy_(hX, non_blocking=True)
-            doff.copy_(hoff, non_blocking=True)
-            gemm(dX, W, doff, Y, stream=stream, **opts)
-            hY.copy_(Y, non_blocking=True)
-        e_end.record(stream)
+        s_in.wait_event(e_start)
+        for i in range(K_steps):
+            e2e_step(i)
+        s_out.synchronize()
+        e_end.record(s_out)
         torch.cuda.synchronize(dev)
         barrier(world)
         e_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
+        # The same steps without overlap: copy in, GEMM, copy out, one after
+        # the other on one stream (what a caller that waits for each result sees).
+        def serial_step():
+            with torch.cuda.stream(stream):
+                dX[0].copy_(hX, non_blocking=True)
+                doff[0].copy_(hoff, non_blocking=True)
+                if fp8:
+                    dsx[0].copy_(hsx, non_blocking=True)
+                    rgg.rgg_grouped_gemm_fp8(dX[0], W, dsx[0], sw_d, doff[0], dY[0], stream=stream, **opts)
+                else:
+                    gemm(dX[0], W, doff[0], dY[0], stream=stream, **opts)
+                hY[0].copy_(dY[0], non_blocking=True)
+
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        s_start, s_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_start.record(stream)
+        for i in range(K_steps):
+            serial_step()
+        s_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        s_ms = max_over_ranks(s_start.elapsed_time(s_end), world, dev)
+        h2d = hX.numel() * hX.element_size() + hoff.numel() * 4 + (hsx.numel() * 4 if fp8 else 0)
         e2e = {"value": round(flops * K_steps * world / (e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(hX.numel() * hX.element_size() + hoff.numel() * 4),
-               "d2h_bytes_per_step": int(hY.numel() * 2), "ms_per_step": round(e_ms / K_steps, 4),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hY[0].numel() * 2),
+               "ms_per_step": round(e_ms / K_steps, 4),
+               "pipeline": "two buffer sets; step i's host copies overlap neighbouring GEMMs",
+               "serial": {"value": round(flops * K_steps * world / (s_ms / 1e3) / 1e12, 3),
+                          "ms_per_step": round(s_ms / K_steps, 4),
+                          "note": "copy in, GEMM, copy out in order on one stream"},
                "weights": "resident in HBM (model parameters); not copied per step"}
 
     peaks = load_peaks()

@@ -69,11 +69,15 @@ typedef struct rgg_options {
                                     bounded waits, which then report RGG_ERR_DEVICE_TIMEOUT */
     int tail64;                  /* 128-row tiles: 0 = auto (on), 1 = on, -1 = off.  A tile that holds the last
                                     <= 64 rows of its expert runs as a 64-row MMA with a 64-row X box */
-    int prefetch_kb;             /* L2 prefetch lookahead, in 64-wide K blocks of a CTA's walk: 0 = auto,
-                                    -1 = off, else 1..64 */
     int op;                      /* for rgg_plan only: 0 = plan rgg_grouped_gemm, 1 = plan
                                     rgg_grouped_gemm_swiglu (then N is the output width), 2 = plan
                                     rgg_grouped_gemm_fp8 */
+    int walk_order;              /* order of the persistent CTAs' walk over the tile list (any order gives the
+                                    same result): 0 = list order (the automatic choice unless host_counts
+                                    show a strong skew), 1 = front/back interleave, 2 = strided scatter,
+                                    3 = front/back interleave over the experts sorted by row count (E <= 256;
+                                    chosen automatically when the largest expert holds over four times the
+                                    mean).  1-CTA kernels only. */
 } rgg_options;
 
 #define RGG_DEBUG_PRODUCER_STALL 1
@@ -88,7 +92,7 @@ typedef struct rgg_plan_info {
     int tmem_cols;               /* TMEM columns allocated per CTA (two accumulator buffers) */
     int64_t max_tiles;           /* upper bound on the flat tile count for these sizes */
     int tail64;                  /* 1 when tail tiles of <= 64 rows run as 64-row MMAs */
-    int prefetch_kb;             /* L2 prefetch lookahead in K blocks (0 = off) */
+    int walk_order;              /* walk order (see rgg_options) */
 } rgg_plan_info;
 
 /*

@@ -52,15 +52,15 @@ class RggError(RuntimeError):
 class _Options(ctypes.Structure):
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("stages", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("timeout_ns", ctypes.c_uint64), ("host_counts", ctypes.c_void_p),
-                ("debug_flags", ctypes.c_int), ("tail64", ctypes.c_int), ("prefetch_kb", ctypes.c_int),
-                ("op", ctypes.c_int)]
+                ("debug_flags", ctypes.c_int), ("tail64", ctypes.c_int),
+                ("op", ctypes.c_int), ("walk_order", ctypes.c_int)]
 
 
 class _PlanInfo(ctypes.Structure):
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int), ("stages", ctypes.c_int),
                 ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("tmem_cols", ctypes.c_int), ("max_tiles", ctypes.c_int64), ("tail64", ctypes.c_int),
-                ("prefetch_kb", ctypes.c_int)]
+                ("walk_order", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -134,9 +134,9 @@ def _handle(device: int) -> ctypes.c_void_p:
 
 
 def _options(bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0, tail64=0,
-             prefetch_kb=0, op=0):
+             op=0, walk_order=0):
     opt = _Options(int(bm), int(bn), int(stages), int(max_ctas), int(timeout_ns), None, int(debug_flags),
-                   int(tail64), int(prefetch_kb), int(op))
+                   int(tail64), int(op), int(walk_order))
     keep = None
     if host_counts is not None:
         import numpy as np
@@ -153,7 +153,8 @@ def _stream_ptr(stream, device):
 
 
 def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
-                     host_counts=None, debug_flags=0, tail64=0, prefetch_kb=0, stream=None, check=False):
+                     host_counts=None, debug_flags=0, tail64=0, walk_order=0, stream=None,
+                     check=False):
     """Y_e = X_e . W_e for every expert (one kernel launch, asynchronous).
 
     X: bf16 CUDA [M_tot, K]; W: bf16 CUDA [E, K, N]; group_offsets: int32
@@ -182,7 +183,8 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
     elif Y.shape != (M_tot, N) or Y.dtype != torch.bfloat16 or not Y.is_contiguous() or not Y.is_cuda:
         raise ValueError("Y must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, prefetch_kb)
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0,
+                         walk_order)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm(_handle(device), X.data_ptr(), W.data_ptr(), group_offsets.data_ptr(), Y.data_ptr(),
                              E, M_tot, K, N, st, ctypes.byref(opt))
@@ -197,7 +199,8 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
 
 
 def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
-                            host_counts=None, debug_flags=0, tail64=0, prefetch_kb=0, stream=None, check=False):
+                            host_counts=None, debug_flags=0, tail64=0, walk_order=0, stream=None,
+                            check=False):
     """H = silu(X_e . W13_e[:, :N]) * (X_e . W13_e[:, N:]) for every expert,
     one kernel launch (the fused gate-up projection with SiLU activation).
 
@@ -222,7 +225,8 @@ def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages
     elif H.shape != (M_tot, N) or H.dtype != torch.bfloat16 or not H.is_contiguous() or not H.is_cuda:
         raise ValueError("H must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, prefetch_kb)
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64,
+                         0, walk_order)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm_swiglu(_handle(device), X.data_ptr(), W13.data_ptr(), group_offsets.data_ptr(),
                                     H.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
@@ -237,8 +241,8 @@ def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages
 
 
 def rgg_grouped_gemm_fp8(X8, W8, sx, sw, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0,
-                         timeout_ns=0, host_counts=None, debug_flags=0, tail64=0, prefetch_kb=0, stream=None,
-                         check=False):
+                         timeout_ns=0, host_counts=None, debug_flags=0, tail64=0, walk_order=0,
+                         stream=None, check=False):
     """Y[i, j] = sx[i] * sw[e, j] * (X8_e . W8_e)[i, j] with FP8 E4M3 operands.
 
     X8: float8_e4m3fn CUDA [M_tot, K]; W8: float8_e4m3fn CUDA [E, K, N];
@@ -262,7 +266,8 @@ def rgg_grouped_gemm_fp8(X8, W8, sx, sw, group_offsets, Y=None, *, bm=0, bn=0, s
     elif Y.shape != (M_tot, N) or Y.dtype != torch.bfloat16 or not Y.is_contiguous() or not Y.is_cuda:
         raise ValueError("Y must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, prefetch_kb)
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64,
+                         0, walk_order)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm_fp8(_handle(device), X8.data_ptr(), W8.data_ptr(), sx.data_ptr(), sw.data_ptr(),
                                  group_offsets.data_ptr(), Y.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
@@ -331,12 +336,13 @@ def rgg_query_status(device: int | None = None, stream=None) -> int:
 
 
 def rgg_plan(E: int, M_tot: int, K: int, N: int, *, num_sms: int = 0, smem_optin: int = 0, bm=0, bn=0,
-             stages=0, max_ctas=0, host_counts=None, tail64=0, prefetch_kb=0, op: str = "gemm") -> dict:
+             stages=0, max_ctas=0, host_counts=None, tail64=0, op: str = "gemm",
+             walk_order=0) -> dict:
     """The launch configuration rgg_grouped_gemm (op="gemm") or
     rgg_grouped_gemm_swiglu (op="swiglu", N = output width) would use (host-only)."""
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, 0, host_counts, 0, tail64, prefetch_kb,
-                         {"gemm": 0, "swiglu": 1, "fp8": 2}[op])
+    opt, keep = _options(bm, bn, stages, max_ctas, 0, host_counts, 0, tail64,
+                         {"gemm": 0, "swiglu": 1, "fp8": 2}[op], walk_order)
     info = _PlanInfo()
     s = lib.rgg_plan(int(num_sms), int(smem_optin), int(E), int(M_tot), int(K), int(N), ctypes.byref(opt),
                      ctypes.byref(info))

@@ -82,7 +82,7 @@ struct Plan {
     int smem_bytes;
     int64_t max_tiles;
     int tail64;       // 1: tail tiles of <= 64 rows run as 64-row MMAs (128-row tiles only)
-    int prefetch_kb;  // L2 lookahead in K blocks, 0 = off
+    int walk_order;   // 0 list order, 1 front/back interleave, 2 strided scatter
 };
 
 // Upper bound on the flat tile count: sum_e ceil(m_e/BM) <= floor(M_tot/BM) + E.
@@ -116,8 +116,10 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (want_stages != 0 && (want_stages < 2 || want_stages > rgg::kMaxStages)) return RGG_ERR_INVALID_ARG;
     if (max_ctas < 0) return RGG_ERR_INVALID_ARG;
     const int want_tail = opt ? opt->tail64 : 0;
-    const int want_pf = opt ? opt->prefetch_kb : 0;
-    if (want_tail < -1 || want_tail > 1 || want_pf < -1 || want_pf > 64) return RGG_ERR_INVALID_ARG;
+    if (want_tail < -1 || want_tail > 1) return RGG_ERR_INVALID_ARG;
+    const int want_walk = opt ? opt->walk_order : 0;
+    if (want_walk < 0 || want_walk > 3) return RGG_ERR_INVALID_ARG;
+    if (want_walk == 3 && E > rgg::kMaxSortedExperts) return RGG_ERR_UNSUPPORTED;
     int grid_cap = max_ctas > 0 ? std::min(max_ctas, num_sms) : num_sms;
 
     // Per-expert M tiles at each BM: exact with host counts, else the
@@ -181,6 +183,16 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         bn = best_bn;
     }
     const bool pair = (bm == 256);
+    if (pair && want_walk != 0) return RGG_ERR_INVALID_ARG;  // the pair kernel walks in list order
+    // Walk order: with the counts known and a strong skew (the largest expert
+    // holding over four times the mean of the busy experts), the size-sorted
+    // interleave runs tiles of big experts beside tiles of small ones.
+    int walk = want_walk;
+    if (walk == 0 && !pair && opt && opt->host_counts && E <= rgg::kMaxSortedExperts) {
+        int64_t mx = 0;
+        for (int e = 0; e < E; ++e) mx = std::max<int64_t>(mx, opt->host_counts[e]);
+        if (avg > 0.0 && static_cast<double>(mx) > 4.0 * avg) walk = 3;
+    }
     const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;
     (void)units;
 
@@ -190,14 +202,14 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     // Per-CTA tile extents: a pair CTA holds 128 rows of A and half of B.
     const int cta_m = pair ? 128 : bm;
     const int cta_n = pair ? bn / 2 : bn;
-    const rgg::SmemPlan probe = rgg::smem_plan(cta_m, cta_n, 0, E);
+    const rgg::SmemPlan probe = rgg::smem_plan(cta_m, cta_n, 0, E, walk == 3);
     const int64_t per_stage = static_cast<int64_t>(cta_m + cta_n) * 128 + 16;  // tiles + two barriers
     const int64_t room = static_cast<int64_t>(smem_optin) - 1024 - probe.total - 64;
     int fit = static_cast<int>(std::min<int64_t>(rgg::kMaxStages, room / per_stage));
     int stages = want_stages ? want_stages : fit;
     if (stages < 2 || stages > fit) return RGG_ERR_UNSUPPORTED;
 
-    const rgg::SmemPlan sp = rgg::smem_plan(cta_m, cta_n, stages, E);
+    const rgg::SmemPlan sp = rgg::smem_plan(cta_m, cta_n, stages, E, walk == 3);
     // Ask for more than half of the SM's shared memory so that exactly one CTA
     // (and one 2 x BN-column TMEM allocation) lives on each SM.
     const int smem = std::max<int>(static_cast<int>(sp.total) + 1024, smem_optin / 2 + 1024);
@@ -211,7 +223,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     out->smem_bytes = smem;
     out->max_tiles = max_tiles;
     out->tail64 = (bm == 128 && want_tail != -1) ? 1 : 0;
-    out->prefetch_kb = want_pf > 0 ? want_pf : 0;
+    out->walk_order = walk;
     return RGG_OK;
 }
 
@@ -397,7 +409,7 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->tmem_cols = (p.bm == 256 || 2 * p.bn > 256) ? 512 : 256;
     out->max_tiles = p.max_tiles;
     out->tail64 = p.tail64;
-    out->prefetch_kb = p.prefetch_kb;
+    out->walk_order = p.walk_order;
     return RGG_OK;
 }
 
@@ -441,7 +453,7 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
     a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
     a.tail64 = p.tail64;
-    a.prefetch_kb = p.prefetch_kb;
+    a.walk_order = p.walk_order;
 
     cudaError_t err = (p.bm == 256)   ? rgg::launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tw, a)
                       : (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
@@ -487,7 +499,7 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
     a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
     a.tail64 = p.tail64;
-    a.prefetch_kb = p.prefetch_kb;
+    a.walk_order = p.walk_order;
     cudaError_t err = rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_swiglu launch");
 }
@@ -531,7 +543,7 @@ rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, c
     a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
     a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
     a.tail64 = p.tail64;
-    a.prefetch_kb = p.prefetch_kb;
+    a.walk_order = p.walk_order;
     a.sx = sx;
     a.sw = sw;
     cudaError_t err = rgg::launch_gemm_fp8(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);

@@ -67,7 +67,7 @@ struct GemmArgs {
     int32_t y_vec32;         // 1: rows of Y are 32-byte aligned (256-bit stores)
     int32_t debug_flags;     // 0 in normal use; kDebugProducerStall for failure-detection tests
     int32_t tail64;          // 1: tiles holding <= 64 rows run as 64-row MMAs (128-row kernels)
-    int32_t prefetch_kb;     // L2 prefetch lookahead in K blocks (0 = off)
+    int32_t walk_order = 0;  // order of the persistent walk over the tile list (rgg_tiles.cuh)
     uint64_t timeout_ns;
     const float* sx = nullptr;  // FP8 kernels: fp32 scale of each row of X [M_tot]
     const float* sw = nullptr;  // FP8 kernels: fp32 scale of each (expert, column) of W [E, N]
@@ -77,10 +77,11 @@ struct GemmArgs {
 // are from a 1024-byte aligned base; the host adds 1024 bytes of slack for
 // aligning the dynamic shared-memory window.
 struct SmemPlan {
-    uint32_t a_stage, b_stage, a_off, b_off, bar_off, misc_off, off_off, pre_off, total;
+    uint32_t a_stage, b_stage, a_off, b_off, bar_off, misc_off, off_off, pre_off, ord_off, spre_off, total;
 };
 
-__host__ __device__ inline SmemPlan smem_plan(int BM, int BN, int stages, int E) {
+// `sorted`: room for the size-sorted walk (expert order and its tile prefix).
+__host__ __device__ inline SmemPlan smem_plan(int BM, int BN, int stages, int E, bool sorted = false) {
     SmemPlan p;
     p.a_stage = static_cast<uint32_t>(BM) * 128u;
     p.b_stage = static_cast<uint32_t>(BN) * 128u;
@@ -90,7 +91,9 @@ __host__ __device__ inline SmemPlan smem_plan(int BM, int BN, int stages, int E)
     p.misc_off = p.bar_off + 8u * (2u * stages + 5u);   // tmem base, abort flag (16 B reserved)
     p.off_off = p.misc_off + 16u;
     p.pre_off = p.off_off + 4u * static_cast<uint32_t>(E + 1);
-    p.total = p.pre_off + 4u * static_cast<uint32_t>(E + 1);
+    p.ord_off = p.pre_off + 4u * static_cast<uint32_t>(E + 1);
+    p.spre_off = p.ord_off + (sorted ? 4u * static_cast<uint32_t>(E + 1) : 0u);
+    p.total = p.spre_off + (sorted ? 4u * static_cast<uint32_t>(E + 1) : 0u);
     return p;
 }
 
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const SmemPlan sp = smem_plan(BM, BN, S, E);
+    const SmemPlan sp = smem_plan(BM, BN, S, E, args.walk_order == 3);
     const uint32_t a0 = base + sp.a_off;
     const uint32_t b0 = base + sp.b_off;
     const uint32_t bars = base + sp.bar_off;
@@ -195,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + sp.misc_off);
     int32_t* s_off = reinterpret_cast<int32_t*>(gbase + sp.off_off);
     int32_t* s_pre = reinterpret_cast<int32_t*>(gbase + sp.pre_off);
+    int32_t* s_order = reinterpret_cast<int32_t*>(gbase + sp.ord_off);  // walk order 3 only
+    int32_t* s_spre = reinterpret_cast<int32_t*>(gbase + sp.spre_off);
 
     // S1: group offsets -> validated per-expert tile prefix.
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
@@ -204,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
     __syncthreads();
     const int32_t T = s_pre[E];
+    if (args.walk_order == 3) build_size_order(s_off, s_order, s_spre, E, BM, args.n_tiles_n);
     if (static_cast<int32_t>(blockIdx.x) >= T) return;  // uniform over the CTA
 
     if (threadIdx.x == 32) {
@@ -236,6 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t* abort_flag = &misc[1];
     const int KB = args.num_k_blocks;
     const int nN = args.n_tiles_n;
+    const int WO = args.walk_order;  // walk position t visits tile walk_tile(t, ...)
+    const int32_t WS = walk_stride_for(T);
+    // The tile visited at walk position p.
+    auto tile_at = [&](int32_t p) -> TileCoord {
+        const int32_t t = walk_tile(p, T, WO, WS);
+        return WO == 3 ? decode_sorted_tile(s_off, s_order, s_spre, E, BM, kOutN, nN, t)
+                       : decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
+    };
 
     if (warp == 0) {
         // ---------------------------------------------------- S4: TMA producer
@@ -244,11 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = true;
-            const int PD = args.prefetch_kb;  // L2 lookahead, in K blocks of this CTA's walk
-            int32_t t_ahead = -1;
-            TileCoord c_ahead = {0, 0, 0, 0};
             for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
-                const TileCoord c = decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
+                const TileCoord c = tile_at(t);
                 const bool half = runs_as_64_rows<BM>(args, c);
                 const uint32_t tx_bytes = half ? Cfg::kStageTx64 : Cfg::kStageTx;
                 const CUtensorMap* xmap = (BM == 128 && half) ? &tmap_x64 : &tmap_x;
@@ -261,34 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(a0 + st * sp.a_stage, xmap, full_bar(st), kb * Cfg::kKStage, c.row0);
 #pragma unroll
                     for (int p = 0; p < kPanels; ++p)
-                        tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st), w_col(c.col0, p),
-                                    kb * Cfg::kKStage, c.expert);
+                        tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st),
+                                    w_col(c.col0, p), kb * Cfg::kKStage, c.expert);
                     ++issued;
                     if (++st == S) {
                         st = 0;
                         ph ^= 1u;
-                    }
-                    if (PD > 0) {
-                        // Warm L2 with the boxes this CTA will load PD K blocks from
-                        // now, so HBM latency overlaps more MMA work than the ring holds.
-                        int kb_a = kb + PD;
-                        int32_t t_a = t;
-                        while (kb_a >= KB) {
-                            kb_a -= KB;
-                            t_a += gridDim.x;
-                        }
-                        if (t_a < T) {
-                            if (t_a != t_ahead) {
-                                c_ahead = decode_tile(s_off, s_pre, E, BM, kOutN, nN, t_a);
-                                t_ahead = t_a;
-                            }
-#pragma unroll
-                            for (int p = 0; p < kPanels; ++p)
-                                tma_prefetch_l2_3d(&tmap_w, w_col(c_ahead.col0, p), kb_a * Cfg::kKStage,
-                                                   c_ahead.expert);
-                            tma_prefetch_l2_2d(runs_as_64_rows<BM>(args, c_ahead) ? &tmap_x64 : &tmap_x,
-                                               kb_a * Cfg::kKStage, c_ahead.row0);
-                        }
                     }
                 }
             }
@@ -309,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_ph = 0;
             bool ok = true;
             for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
-                const TileCoord c = decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
+                const TileCoord c = tile_at(t);
                 const uint32_t idesc = runs_as_64_rows<BM>(args, c) ? Cfg::kIdesc64 : Cfg::kIdesc;
                 if (!wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, args.status, args.timeout_ns)) {
                     ok = false;
@@ -360,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_ph = 0;
         for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
-            const TileCoord c = decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
+            const TileCoord c = tile_at(t);
             // M = 128: tile row 32q + lane sits in TMEM lane 32q + lane.  M = 64:
             // tile row 16q + i sits in TMEM lane 32q + i (i < 16).
             const bool half = runs_as_64_rows<BM>(args, c);

@@ -140,9 +140,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = true;
-            const int PD = args.prefetch_kb;
-            int32_t t_ahead = -1;
-            TileCoord c_ahead = {0, 0, 0, 0};
             for (int32_t t = pair; ok && t < T; t += npairs) {
                 const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
                 const int32_t a_row = c.row0 + 128 * static_cast<int32_t>(rank);
@@ -164,26 +161,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (++st == S) {
                         st = 0;
                         ph ^= 1u;
-                    }
-                    if (PD > 0) {
-                        // Warm L2 with this CTA's boxes PD K blocks ahead of the ring.
-                        int kb_a = kb + PD;
-                        int32_t t_a = t;
-                        while (kb_a >= KB) {
-                            kb_a -= KB;
-                            t_a += npairs;
-                        }
-                        if (t_a < T) {
-                            if (t_a != t_ahead) {
-                                c_ahead = decode_tile(s_off, s_pre, E, BM, BN, nN, t_a);
-                                t_ahead = t_a;
-                            }
-#pragma unroll
-                            for (int p = 0; p < Cfg::kPanels; ++p)
-                                tma_prefetch_l2_3d(&tmap_w, c_ahead.col0 + Cfg::kHalfN * static_cast<int32_t>(rank) + 64 * p,
-                                                   kb_a * kBK, c_ahead.expert);
-                            tma_prefetch_l2_2d(&tmap_x, kb_a * kBK, c_ahead.row0 + 128 * static_cast<int32_t>(rank));
-                        }
                     }
                 }
             }

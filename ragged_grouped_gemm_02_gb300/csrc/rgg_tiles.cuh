@@ -97,4 +97,93 @@ __device__ __forceinline__ TileCoord decode_tile(const int32_t* s_off, const int
     return c;
 }
 
+// The order in which a persistent CTA visits the flat list.  Every order is a
+// permutation of [0, T), so the result does not depend on it; it only changes
+// which tiles run side by side on the GPU.  0: list order (CTA c takes
+// c, c + grid, ...).  1: front/back interleave (even walk positions from the
+// front of the list, odd ones from the back), which pairs the big experts at
+// one end of an expert-sorted list with the small ones at the other.
+// 2: strided scatter p -> p * s mod T with a prime s that does not divide T.
+__device__ __forceinline__ int32_t walk_stride_for(int32_t T) {
+    const int32_t primes[4] = {7919, 6841, 5009, 1009};
+    for (int i = 0; i < 4; ++i)
+        if (T % primes[i] != 0) return primes[i];
+    return 1;
+}
+
+__device__ __forceinline__ int32_t walk_tile(int32_t p, int32_t T, int order, int32_t stride) {
+    if (order == 1 || order == 3) return (p & 1) ? T - 1 - (p >> 1) : (p >> 1);
+    if (order == 2) return static_cast<int32_t>((static_cast<int64_t>(p) * stride) % T);
+    return p;
+}
+
+// Walk order 3 walks the tiles of the experts sorted by row count (largest
+// first, ties by index) with the front/back interleave, so that tiles of big
+// experts (weights reused from L2, MMA-heavy) run beside tiles of small ones
+// (weights streamed from HBM).  Every thread of the block calls this; it
+// fills s_order (rank -> expert) and the tile prefix over ranks s_spre[0..E].
+constexpr int kMaxSortedExperts = 256;
+
+__device__ __forceinline__ void build_size_order(const int32_t* s_off, int32_t* s_order, int32_t* s_spre, int E,
+                                                 int BM, int n_tiles_n) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t m = s_off[e + 1] - s_off[e];
+        int rank = 0;
+        for (int f = 0; f < E; ++f) {
+            const int32_t mf = s_off[f + 1] - s_off[f];
+            rank += (mf > m || (mf == m && f < e)) ? 1 : 0;
+        }
+        s_order[rank] = e;
+    }
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) {
+        const int lane = threadIdx.x & 31;
+        const int per = (E + 31) / 32;
+        const int r0 = min(E, lane * per);
+        const int r1 = min(E, r0 + per);
+        int32_t local = 0;
+        for (int r = r0; r < r1; ++r) {
+            const int e = s_order[r];
+            local += ((s_off[e + 1] - s_off[e] + BM - 1) / BM) * n_tiles_n;
+        }
+        int32_t incl = local;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        int32_t run = incl - local;
+        for (int r = r0; r < r1; ++r) {
+            s_spre[r] = run;
+            const int e = s_order[r];
+            run += ((s_off[e + 1] - s_off[e] + BM - 1) / BM) * n_tiles_n;
+        }
+        if (lane == 31) s_spre[E] = incl;
+    }
+    __syncthreads();
+}
+
+// Decode position t of the size-sorted sequence (0 <= t < s_spre[E]).
+__device__ __forceinline__ TileCoord decode_sorted_tile(const int32_t* s_off, const int32_t* s_order,
+                                                        const int32_t* s_spre, int E, int BM, int BN, int n_tiles_n,
+                                                        int32_t t) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_spre[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    const int e = s_order[lo];
+    const int32_t local = t - s_spre[lo];
+    const int32_t mt = local / n_tiles_n;
+    const int32_t nt = local - mt * n_tiles_n;
+    const int32_t m_e = s_off[e + 1] - s_off[e];
+    TileCoord c;
+    c.expert = e;
+    c.row0 = s_off[e] + mt * BM;
+    c.rows = min(BM, m_e - mt * BM);
+    c.col0 = nt * BN;
+    return c;
+}
+
 }  // namespace rgg

@@ -108,13 +108,25 @@ def test_integer_inputs_bit_exact(bm, bn, N):
 
 
 @pytest.mark.parametrize("bm,bn", SHAPES + PAIR_SHAPES)
-@pytest.mark.parametrize("tail64,prefetch_kb", [(0, 0), (-1, 0), (1, 3)])
-def test_integer_inputs_bit_exact_modes(bm, bn, tail64, prefetch_kb):
-    # 64-row tail tiles on and off, and the L2 lookahead (with K = 64 the
-    # lookahead crosses tile boundaries every step)
+@pytest.mark.parametrize("tail64", [0, -1, 1])
+def test_integer_inputs_bit_exact_modes(bm, bn, tail64):
+    # 64-row tail tiles automatic, off and on
     counts = [3, 0, 130, 64, 1, 200, 65, 127, 129]
     inp = wl.make_custom(counts, K=64, N=384, seed=38, integer_valued=True, spare_rows=3)
-    Y = _run(inp, bm=bm, bn=bn, tail64=tail64, prefetch_kb=prefetch_kb)
+    Y = _run(inp, bm=bm, bn=bn, tail64=tail64)
+    ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
+    M_used = int(inp.offsets[-1])
+    assert np.array_equal(Y[:M_used].double().numpy(), ref[:M_used])
+    _assert_untouched(Y, slice(M_used, None))
+
+
+@pytest.mark.parametrize("bm,bn", SHAPES)
+@pytest.mark.parametrize("walk_order", [1, 2, 3])
+def test_integer_inputs_bit_exact_walk_orders(bm, bn, walk_order):
+    # any walk over the tile list visits every tile exactly once
+    counts = [3, 0, 130, 64, 1, 200, 65, 127, 129, 500]
+    inp = wl.make_custom(counts, K=64, N=384, seed=39, integer_valued=True, spare_rows=3)
+    Y = _run(inp, bm=bm, bn=bn, walk_order=walk_order)
     ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
     M_used = int(inp.offsets[-1])
     assert np.array_equal(Y[:M_used].double().numpy(), ref[:M_used])
@@ -129,11 +141,10 @@ def test_ragged_random_k_and_n_tails(bm, bn):
     _full_parity(inp, bm=bm, bn=bn)
 
 
-@pytest.mark.parametrize("prefetch_kb", [0, 8])
-def test_ragged_random_auto_plan_many_tiles(prefetch_kb):
+def test_ragged_random_auto_plan_many_tiles():
     counts = [500, 3, 0, 257, 1024, 77, 129, 2, 640, 64]
     inp = wl.make_custom(counts, K=512, N=1024, seed=33)
-    _full_parity(inp, prefetch_kb=prefetch_kb)
+    _full_parity(inp)
 
 
 def test_offsets_need_not_cover_all_rows():
