@@ -36,6 +36,7 @@ _lib = None
 ORACLE_OK = 0
 ORACLE_ERR_INVALID_ARG = 1
 ORACLE_ERR_BAD_OFFSETS = 4
+ORACLE_ERR_BAD_ROW_INDEX = 7
 
 
 def build(force: bool = False) -> str:
@@ -79,6 +80,8 @@ def _load():
         lib.rgg_oracle_grouped_gemm_fp8.argtypes = [P, P, P, P, P, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int,
                                                     P, ctypes.c_int]
         lib.rgg_oracle_grouped_gemm_fp8.restype = ctypes.c_int
+        lib.rgg_oracle_gather_rows.argtypes = [P, i64, ctypes.c_int, P, i64, i64, P]
+        lib.rgg_oracle_gather_rows.restype = ctypes.c_int
         lib.rgg_oracle_max_threads.argtypes = []
         lib.rgg_oracle_max_threads.restype = ctypes.c_int
         del i32
@@ -220,6 +223,53 @@ def grouped_gemm_fp8(X8: np.ndarray, W8: np.ndarray, sx: np.ndarray, sw: np.ndar
     if rc != ORACLE_OK:
         raise OracleError("oracle rejected the arguments (code %d)" % rc)
     return out
+
+
+def gather_rows(Xtok_bits: np.ndarray, row_index, begin: int = 0, end: int | None = None,
+                out: np.ndarray | None = None) -> np.ndarray:
+    """Xg[i] = X_tok[row_index[i]] for begin <= i < end (the token gather the
+    worklog's "Scope of these results" leaves out).  Xtok_bits: uint16 [T, K];
+    row_index: int [M_tot].  Rows outside [begin, end) keep their value in
+    ``out`` (zero when not given).  An index outside [0, T) raises."""
+    Xtok_bits = _as_bits(Xtok_bits)
+    if Xtok_bits.ndim != 2:
+        raise ValueError("X_tok must be [T, K]")
+    T, K = Xtok_bits.shape
+    idx = np.ascontiguousarray(np.asarray(row_index, dtype=np.int64))
+    if idx.ndim != 1:
+        raise ValueError("row_index must be 1-D")
+    if idx.size and (idx.min() < -(2 ** 31) or idx.max() >= 2 ** 31):
+        raise ValueError("row_index must fit int32")
+    idx = idx.astype(np.int32)
+    M_tot = idx.size
+    end = M_tot if end is None else int(end)
+    if out is None:
+        out = np.zeros((M_tot, K), dtype=np.uint16)
+    if out.shape != (M_tot, K) or out.dtype != np.uint16 or not out.flags.c_contiguous:
+        raise ValueError("out must be a C-contiguous uint16 [M_tot, K] array")
+    if not 0 <= begin <= end <= M_tot:
+        raise ValueError("need 0 <= begin <= end <= M_tot")
+    rc = _load().rgg_oracle_gather_rows(_ptr(Xtok_bits), T, K, _ptr(idx), int(begin), int(end), _ptr(out))
+    if rc != ORACLE_OK:
+        raise OracleError("oracle rejected the gather (code %d)" % rc)
+    return out
+
+
+def grouped_gemm_gather(Xtok_bits: np.ndarray, row_index, W_bits: np.ndarray, off, nthreads: int = 0,
+                        out: np.ndarray | None = None) -> np.ndarray:
+    """Y[i] = X_tok[row_index[i]] . W_e for every row i of every expert e:
+    the grouped product of the gathered rows, fp64."""
+    off = _as_offsets(off)
+    Xg = gather_rows(Xtok_bits, row_index, int(off[0]), int(off[-1]))
+    return grouped_gemm(Xg, W_bits, off, nthreads=nthreads, out=out)
+
+
+def grouped_swiglu_gather(Xtok_bits: np.ndarray, row_index, W13_bits: np.ndarray, off, nthreads: int = 0,
+                          out: np.ndarray | None = None) -> np.ndarray:
+    """The fused gate-up projection with SiLU of the gathered rows, fp64."""
+    off = _as_offsets(off)
+    Xg = gather_rows(Xtok_bits, row_index, int(off[0]), int(off[-1]))
+    return grouped_swiglu(Xg, W13_bits, off, nthreads=nthreads, out=out)
 
 
 def tile_list(off, N: int, BM: int, BN: int) -> np.ndarray:

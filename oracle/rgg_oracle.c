@@ -52,6 +52,7 @@
 #define ORACLE_OK 0
 #define ORACLE_ERR_INVALID_ARG 1
 #define ORACLE_ERR_BAD_OFFSETS 4
+#define ORACLE_ERR_BAD_ROW_INDEX 7
 
 /* A bf16 value is the upper 16 bits of an IEEE binary32; widening is exact. */
 static double bf16_bits_to_f64(uint16_t h) {
@@ -257,6 +258,36 @@ int rgg_oracle_grouped_gemm_fp8(const uint8_t* X8, const uint8_t* W8, const floa
             }
             free(acc);
         }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Token gather ahead of the grouped product.  The worklog starts after
+ * routing, with the rows already grouped by expert ("What I am measuring"),
+ * and names the permutation of rows and the scatter/gather of tokens among the
+ * MoE work its kernel leaves out ("Scope of these results"); the InferenceX
+ * glossary entry "Grouped GEMM" ("Engineering details") describes that token
+ * permutation, which turns each expert's ragged group of tokens into operand
+ * rows.  Reading: routed row i of the grouped operand is token row_index[i] of
+ * an ungrouped token matrix X_tok [T, K],
+ *
+ *     Xg[i, k] = X_tok[row_index[i], k]        for begin <= i < end,
+ *
+ * and the gathered grouped product is the grouped product of Xg.  Only the
+ * rows [begin, end) are gathered (the rows some expert owns); every index read
+ * must lie in [0, T), otherwise nothing is written and the call fails.  Rows
+ * of Xg outside [begin, end) are left as they were.
+ */
+int rgg_oracle_gather_rows(const uint16_t* Xtok, int64_t T, int K, const int32_t* row_index, int64_t begin,
+                           int64_t end, uint16_t* Xg) {
+    if (Xtok == NULL || row_index == NULL || Xg == NULL || T < 1 || K < 1 || begin < 0 || end < begin)
+        return ORACLE_ERR_INVALID_ARG;
+    for (int64_t i = begin; i < end; ++i)
+        if (row_index[i] < 0 || (int64_t)row_index[i] >= T) return ORACLE_ERR_BAD_ROW_INDEX;
+    for (int64_t i = begin; i < end; ++i) {
+        const int64_t r = row_index[i];
+        for (int k = 0; k < K; ++k) Xg[i * K + k] = Xtok[r * K + k];
     }
     return ORACLE_OK;
 }

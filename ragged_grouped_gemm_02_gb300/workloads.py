@@ -261,6 +261,59 @@ def fp8_codes(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.uint8).numpy()
 
 
+@dataclass
+class GatherInputs:
+    Xtok: torch.Tensor        # bf16 [T, K], CPU: the tokens in their own order
+    row_index: np.ndarray     # int32 [M_tot]: routed row i reads token row_index[i]
+    W: torch.Tensor           # bf16 [E, K, N], CPU
+    offsets: np.ndarray       # int32 [E+1]
+    counts: np.ndarray        # int64 [E]
+
+
+def routed_row_index(counts, T: int, gen: torch.Generator, spare_rows: int = 0) -> np.ndarray:
+    """Token index of every routed row: expert e's m_e rows are m_e distinct
+    tokens drawn without replacement from [0, T), in increasing token order
+    (the order a stable sort of the (token, expert) pairs by expert leaves
+    them in).  Rows after the last expert (``spare_rows``) get -1: they belong
+    to no expert and must never be read."""
+    counts = np.asarray(counts, dtype=np.int64)
+    if counts.size and counts.max() > T:
+        raise ValueError("an expert cannot receive more distinct tokens than there are (m_e <= T)")
+    parts = [torch.randperm(T, generator=gen)[:int(m)].sort().values.numpy() for m in counts]
+    parts.append(np.full(int(spare_rows), -1, dtype=np.int64))
+    return np.concatenate(parts).astype(np.int32)
+
+
+def make_gather_custom(counts, T: int, K: int, N: int, seed: int, integer_valued: bool = False,
+                       spare_rows: int = 0) -> GatherInputs:
+    """Token matrix, weights and routed token indices for explicit counts:
+    X_tok [T, K] first, then W, then the index draws, from one seeded
+    generator (integer_valued: entries uniform in {-2..2})."""
+    counts = np.asarray(counts, dtype=np.int64)
+    E = counts.size
+    gen = torch.Generator().manual_seed(seed)
+    if integer_valued:
+        Xtok = torch.randint(-2, 3, (T, K), generator=gen).to(torch.bfloat16)
+        W = torch.randint(-2, 3, (E, K, N), generator=gen).to(torch.bfloat16)
+    else:
+        Xtok, W = draw_matrices(T, E, K, N, gen)
+    idx = routed_row_index(counts, T, gen, spare_rows)
+    return GatherInputs(Xtok, idx, W, offsets_from_counts(counts), counts)
+
+
+def make_gather_inputs(w: Workload | str, T: int | None = None) -> GatherInputs:
+    """A workload's routed counts and matrices, with the activations held as
+    T tokens (default T = M_tot) that the routed rows index into."""
+    w = WORKLOADS[w] if isinstance(w, str) else w
+    counts = workload_counts(w)
+    M_tot = int(counts.sum())
+    T = M_tot if T is None else int(T)
+    gen = torch.Generator().manual_seed(w.seed + 1000)
+    Xtok, W = draw_matrices(T, w.E, w.K, w.N, gen)
+    idx = routed_row_index(counts, T, gen)
+    return GatherInputs(Xtok, idx, W, offsets_from_counts(counts), counts)
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """The uint16 bit patterns of a bf16 CPU tensor (what the oracle reads)."""
     if t.dtype != torch.bfloat16:

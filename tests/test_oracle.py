@@ -355,3 +355,91 @@ def test_swiglu_integer_inputs_against_exact_products(oracle_mod):
         u = (Xi[off[e]:off[e + 1]] @ Wi[e][:, N:]).astype(np.float64)
         ref = g / (1.0 + np.exp(-g)) * u
         np.testing.assert_allclose(H[off[e]:off[e + 1]], ref, rtol=1e-14, atol=1e-12)
+
+
+# ------------------------------------------------------------ token gather
+
+def test_gather_worked_by_hand(oracle_mod):
+    # three tokens with distinct rows; routed rows read tokens 2, 0, 2, 1
+    Xtok = np.array([[1, 2, 3], [4, 5, 6], [7, 8, 9]], dtype=np.uint16)
+    Xg = oracle_mod.gather_rows(Xtok, [2, 0, 2, 1])
+    assert Xg.tolist() == [[7, 8, 9], [1, 2, 3], [7, 8, 9], [4, 5, 6]]
+
+
+def test_gather_equals_library_indexing(oracle_mod):
+    gen = np.random.default_rng(71)
+    Xtok = gen.integers(0, 1 << 16, size=(50, 24), dtype=np.uint16)
+    idx = gen.integers(0, 50, size=300)
+    np.testing.assert_array_equal(oracle_mod.gather_rows(Xtok, idx), Xtok[idx])
+
+
+def test_gather_by_permutation_and_its_inverse_is_identity(oracle_mod):
+    gen = np.random.default_rng(72)
+    Xtok = gen.integers(0, 1 << 16, size=(40, 16), dtype=np.uint16)
+    p = gen.permutation(40)
+    back = oracle_mod.gather_rows(oracle_mod.gather_rows(Xtok, p), np.argsort(p))
+    np.testing.assert_array_equal(back, Xtok)
+
+
+def test_gather_only_the_given_range_and_rejects_bad_indices(oracle_mod):
+    Xtok = np.arange(12, dtype=np.uint16).reshape(4, 3)
+    # rows outside [begin, end) are neither read nor written: their index may be anything
+    Xg = oracle_mod.gather_rows(Xtok, [-5, 3, 0, 99], begin=1, end=3)
+    assert Xg.tolist() == [[0, 0, 0], [9, 10, 11], [0, 1, 2], [0, 0, 0]]
+    oracle_mod.gather_rows(Xtok, [3])                       # T - 1 is the last valid token
+    for bad in ([4], [-1], [0, 2**31 - 1]):
+        with pytest.raises(oracle_mod.OracleError):
+            oracle_mod.gather_rows(Xtok, bad)
+
+
+def test_gathered_single_expert_is_plain_gemm_of_indexed_rows(oracle_mod):
+    g = wl.make_gather_custom([37], T=50, K=48, N=24, seed=73)
+    Y = oracle_mod.grouped_gemm_gather(wl.bf16_bits(g.Xtok), g.row_index, wl.bf16_bits(g.W), g.offsets)
+    ref = g.Xtok.double().numpy()[g.row_index] @ g.W[0].double().numpy()
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gathered_integer_inputs_are_exact(oracle_mod):
+    # tokens shared between experts (T < M_tot), an empty expert and spare rows
+    counts = [5, 0, 7, 3]
+    g = wl.make_gather_custom(counts, T=9, K=32, N=16, seed=74, integer_valued=True, spare_rows=2)
+    Y = oracle_mod.grouped_gemm_gather(wl.bf16_bits(g.Xtok), g.row_index, wl.bf16_bits(g.W), g.offsets)
+    Xi, Wi, off = g.Xtok.to(torch.int64).numpy(), g.W.to(torch.int64).numpy(), g.offsets
+    for e in range(len(counts)):
+        rows = g.row_index[off[e]:off[e + 1]]
+        np.testing.assert_array_equal(Y[off[e]:off[e + 1]], (Xi[rows] @ Wi[e]).astype(np.float64))
+    assert np.isnan(Y[off[-1]:]).all()
+
+
+def test_gathered_identity_index_is_the_grouped_gemm(oracle_mod):
+    inp = wl.make_custom([6, 0, 11, 2], K=40, N=24, seed=75)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    idx = np.arange(inp.X.shape[0])
+    np.testing.assert_array_equal(oracle_mod.grouped_gemm_gather(xb, idx, wb, inp.offsets),
+                                  oracle_mod.grouped_gemm(xb, wb, inp.offsets))
+
+
+def test_gathered_swiglu_is_swiglu_of_gathered_rows(oracle_mod):
+    N = 16
+    g = wl.make_gather_custom([4, 9, 0, 3], T=12, K=32, N=2 * N, seed=76, integer_valued=True)
+    H = oracle_mod.grouped_swiglu_gather(wl.bf16_bits(g.Xtok), g.row_index, wl.bf16_bits(g.W), g.offsets)
+    Xi, Wi, off = g.Xtok.to(torch.int64).numpy(), g.W.to(torch.int64).numpy(), g.offsets
+    for e in range(4):
+        rows = g.row_index[off[e]:off[e + 1]]
+        gate = (Xi[rows] @ Wi[e][:, :N]).astype(np.float64)
+        up = (Xi[rows] @ Wi[e][:, N:]).astype(np.float64)
+        np.testing.assert_allclose(H[off[e]:off[e + 1]], gate / (1.0 + np.exp(-gate)) * up, rtol=1e-14,
+                                   atol=1e-12)
+
+
+def test_routed_row_index_recipe():
+    counts = [5, 0, 7, 3]
+    idx = wl.routed_row_index(counts, 9, torch.Generator().manual_seed(1), spare_rows=2)
+    off = wl.offsets_from_counts(counts)
+    assert idx.dtype == np.int32 and idx.size == 17
+    for e in range(4):
+        part = idx[off[e]:off[e + 1]]
+        assert np.all(np.diff(part) > 0) and part.min(initial=0) >= 0 and part.max(initial=0) < 9
+    assert idx[15:].tolist() == [-1, -1]
+    with pytest.raises(ValueError):
+        wl.routed_row_index([10], 9, torch.Generator().manual_seed(1))

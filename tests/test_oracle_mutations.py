@@ -48,6 +48,12 @@ MUTANTS = {
     "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     "e4m3_subnormal": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
     "fp8_scale_ignores_expert": ("const float* swe = sw + (int64_t)e * N;", "const float* swe = sw;"),
+    "gather_ignores_index": ("for (int k = 0; k < K; ++k) Xg[i * K + k] = Xtok[r * K + k];",
+                             "for (int k = 0; k < K; ++k) Xg[i * K + k] = Xtok[(i % T) * K + k];"),
+    "gather_next_rows_index": ("const int64_t r = row_index[i];",
+                               "const int64_t r = row_index[i + 1 < end ? i + 1 : i];"),
+    "gather_accepts_t": ("(int64_t)row_index[i] >= T) return ORACLE_ERR_BAD_ROW_INDEX;",
+                         "(int64_t)row_index[i] > T) return ORACLE_ERR_BAD_ROW_INDEX;"),
 }
 
 
@@ -208,9 +214,38 @@ def _fp8_checks_pass(lib):
     return True
 
 
+def _gather_checks_pass(lib):
+    P = ctypes.c_void_p
+    lib.rgg_oracle_gather_rows.argtypes = [P, ctypes.c_int64, ctypes.c_int, P, ctypes.c_int64, ctypes.c_int64, P]
+    lib.rgg_oracle_gather_rows.restype = ctypes.c_int
+
+    def gather(Xtok, idx, begin, end):
+        Xtok = np.ascontiguousarray(Xtok, dtype=np.uint16)
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        out = np.zeros((idx.size, Xtok.shape[1]), dtype=np.uint16)
+        rc = lib.rgg_oracle_gather_rows(Xtok.ctypes.data, Xtok.shape[0], Xtok.shape[1], idx.ctypes.data, begin,
+                                        end, out.ctypes.data)
+        return rc, out
+
+    # the hand-worked case, then the library's fancy indexing, then the range rule
+    rc, Xg = gather([[1, 2, 3], [4, 5, 6], [7, 8, 9]], [2, 0, 2, 1], 0, 4)
+    if rc != 0 or Xg.tolist() != [[7, 8, 9], [1, 2, 3], [7, 8, 9], [4, 5, 6]]:
+        return False
+    gen = np.random.default_rng(71)
+    Xtok = gen.integers(0, 1 << 16, size=(50, 24), dtype=np.uint16)
+    idx = gen.integers(0, 50, size=300)
+    rc, Xg = gather(Xtok, idx, 0, 300)
+    if rc != 0 or not np.array_equal(Xg, Xtok[idx]):
+        return False
+    for bad in ([4], [-1]):
+        if gather(np.zeros((4, 3)), bad, 0, 1)[0] == 0:
+            return False
+    return True
+
+
 def _all_pass(lib):
     return (_product_checks_pass(lib) and _tile_checks_pass(lib) and _eta_checks_pass(lib)
-            and _swiglu_checks_pass(lib) and _fp8_checks_pass(lib))
+            and _swiglu_checks_pass(lib) and _fp8_checks_pass(lib) and _gather_checks_pass(lib))
 
 
 def test_unmutated_copy_passes(tmp_path):
