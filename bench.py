@@ -64,12 +64,15 @@ def parse_args():
     p.add_argument("--bn", type=int, default=0)
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--tail64", type=int, default=0, help="0 auto, 1 on, -1 off")
+    p.add_argument("--gather-mode", type=int, default=0, help="gather ops: 0 auto, 1 TMA gather4, 2 cp.async rows")
     p.add_argument("--walk-order", type=int, default=0,
                    help="0 list order, 1 front/back interleave, 2 scatter, 3 size-sorted interleave")
-    p.add_argument("--op", default="gemm", choices=["gemm", "swiglu", "fp8"],
+    p.add_argument("--op", default="gemm", choices=["gemm", "swiglu", "fp8", "gather", "swiglu_gather"],
                    help="gemm: Y = X.W; swiglu: the workload's weights read as [gate | up], "
                         "H = silu(X.W_gate) * (X.W_up) with N/2 output columns; fp8: the same draws "
-                        "quantised to E4M3 with per-row / per-column scales")
+                        "quantised to E4M3 with per-row / per-column scales; gather / swiglu_gather: "
+                        "the activations held as M_tot tokens in token order, each routed row read "
+                        "through its token index inside the kernel")
     p.add_argument("--profile", action="store_true",
                    help="for ncu: --warmup launches then one more, no timing, no CPU work after")
     return p.parse_args()
@@ -199,7 +202,7 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def oracle_cpu_rate(inp, budget_s=12.0, op="gemm", scales=None):
+def oracle_cpu_rate(inp, budget_s=12.0, op="gemm", scales=None, row_index=None):
     """The fp64 oracle as it stands, on the host cores, over a bounded sample
     of the workload: the first experts' complete rows (all N columns), about
     `budget_s` of work.  Returns (TFLOP/s, sample description, threads)."""
@@ -214,6 +217,13 @@ def oracle_cpu_rate(inp, budget_s=12.0, op="gemm", scales=None):
 
         def fn(x, w, off, r0=0, e0=0):
             return oracle.grouped_gemm_fp8(x, w, sxn[r0:r0 + x.shape[0]], swn[e0:e0 + w.shape[0]], off)
+    elif row_index is not None:
+        # the gathered ops: the oracle's gather of the sample's rows, then its product
+        xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+        base = oracle.grouped_swiglu if op == "swiglu_gather" else oracle.grouped_gemm
+
+        def fn(x, w, off, r0=0, e0=0):
+            return base(oracle.gather_rows(xb, row_index[r0:r0 + x.shape[0]]), w, off)
     else:
         xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
         base = oracle.grouped_swiglu if op == "swiglu" else oracle.grouped_gemm
@@ -258,11 +268,24 @@ def run_profile(args):
     opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
                 walk_order=args.walk_order,
                 host_counts=inp.counts)
+    if args.op == "gather":
+        # the same recipe as the timed gather op: M_tot tokens, distinct tokens per expert
+        gen = torch.Generator().manual_seed(inp.workload.seed + 7)
+        idx = torch.from_numpy(wl.routed_row_index(inp.counts, X.shape[0], gen)).to(dev)
+        opts["gather_mode"] = args.gather_mode
+
+        def launch():
+            rgg.rgg_grouped_gemm_gather(X, idx, W, off, Y, **opts)
+    elif args.op == "gemm":
+        def launch():
+            rgg.rgg_grouped_gemm(X, W, off, Y, **opts)
+    else:
+        raise SystemExit("--profile covers --op gemm and --op gather")
     for _ in range(args.warmup + 1):
-        rgg.rgg_grouped_gemm(X, W, off, Y, **opts)
+        launch()
     torch.cuda.synchronize(dev)
     status = rgg.rgg_query_status(0)
-    plan = rgg.rgg_plan(inp.workload.E, X.shape[0], inp.workload.K, inp.workload.N, **opts)
+    plan = rgg.rgg_plan(inp.workload.E, X.shape[0], inp.workload.K, inp.workload.N, op=args.op, **opts)
     print(json.dumps({"profile": args.workload, "launches": args.warmup + 1, "status": status, "plan": plan}))
     if status != rgg.RGG_OK:
         raise SystemExit(1)
@@ -281,7 +304,8 @@ def run_ours(args):
     K, N, E = w.K, w.N, w.E
     M_tot = inp.X.shape[0]
     flops, bytes_ = work_of(inp.counts, K, N)
-    fused = args.op == "swiglu"
+    fused = args.op in ("swiglu", "swiglu_gather")
+    gather = args.op in ("gather", "swiglu_gather")
     N_out = N // 2 if fused else N
     if fused:  # the output is half as wide; the weight bytes and MMA work are the same
         bytes_ -= 2.0 * M_tot * (N - N_out)
@@ -298,6 +322,19 @@ def run_ours(args):
 
         def gemm(Xd, Wd, offd, Yd, **kw):
             return rgg.rgg_grouped_gemm_fp8(Xd, Wd, sx_d, sw_d, offd, Yd, **kw)
+    idx_h = None
+    if gather:
+        # The activations are M_tot tokens in token order; routed row i reads
+        # token row_index[i] (each expert's rows are distinct tokens in
+        # increasing order).  The index adds 4 bytes per routed row.
+        gen = torch.Generator().manual_seed(w.seed + 1000 * rank + 7)
+        idx_h = torch.from_numpy(wl.routed_row_index(inp.counts, M_tot, gen))
+        idx_d = idx_h.to(dev)
+        bytes_ += 4.0 * M_tot
+        gfn = rgg.rgg_grouped_gemm_swiglu_gather if fused else rgg.rgg_grouped_gemm_gather
+
+        def gemm(Xd, Wd, offd, Yd, idx=None, **kw):
+            return gfn(Xd, idx_d if idx is None else idx, Wd, offd, Yd, **kw)
     X, W = inp.X.to(dev), inp.W.to(dev)
     off = torch.from_numpy(inp.offsets).to(dev)
     Y = torch.empty(M_tot, N_out, dtype=torch.bfloat16, device=dev)
@@ -306,6 +343,8 @@ def run_ours(args):
     opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
                 walk_order=args.walk_order,
                 host_counts=inp.counts)
+    if gather:
+        opts["gather_mode"] = args.gather_mode
     plan = rgg.rgg_plan(E, M_tot, K, N_out, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
                         op=args.op, **opts)
     stream = torch.cuda.current_stream(dev)
@@ -367,6 +406,9 @@ def run_ours(args):
         if fp8:
             hsx = sx.pin_memory()
             dsx = [torch.empty_like(sx_d) for _ in range(2)]
+        if gather:
+            hidx = idx_h.pin_memory()
+            didx = [torch.empty_like(idx_d) for _ in range(2)]
         ev = lambda: torch.cuda.Event()  # noqa: E731
         in_ready, gemm_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         for b in range(2):
@@ -381,11 +423,15 @@ def run_ours(args):
                 doff[b].copy_(hoff, non_blocking=True)
                 if fp8:
                     dsx[b].copy_(hsx, non_blocking=True)
+                if gather:
+                    didx[b].copy_(hidx, non_blocking=True)
             in_ready[b].record(s_in)
             stream.wait_event(in_ready[b])
             stream.wait_event(out_done[b])         # dY[b] has been read out
             if fp8:
                 rgg.rgg_grouped_gemm_fp8(dX[b], W, dsx[b], sw_d, doff[b], dY[b], stream=stream, **opts)
+            elif gather:
+                gemm(dX[b], W, doff[b], dY[b], idx=didx[b], stream=stream, **opts)
             else:
                 gemm(dX[b], W, doff[b], dY[b], stream=stream, **opts)
             gemm_done[b].record(stream)
@@ -418,6 +464,9 @@ def run_ours(args):
                 if fp8:
                     dsx[0].copy_(hsx, non_blocking=True)
                     rgg.rgg_grouped_gemm_fp8(dX[0], W, dsx[0], sw_d, doff[0], dY[0], stream=stream, **opts)
+                elif gather:
+                    didx[0].copy_(hidx, non_blocking=True)
+                    gemm(dX[0], W, doff[0], dY[0], idx=didx[0], stream=stream, **opts)
                 else:
                     gemm(dX[0], W, doff[0], dY[0], stream=stream, **opts)
                 hY[0].copy_(dY[0], non_blocking=True)
@@ -432,7 +481,8 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         barrier(world)
         s_ms = max_over_ranks(s_start.elapsed_time(s_end), world, dev)
-        h2d = hX.numel() * hX.element_size() + hoff.numel() * 4 + (hsx.numel() * 4 if fp8 else 0)
+        h2d = (hX.numel() * hX.element_size() + hoff.numel() * 4 + (hsx.numel() * 4 if fp8 else 0)
+               + (hidx.numel() * 4 if gather else 0))
         e2e = {"value": round(flops * K_steps * world / (e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hY[0].numel() * 2),
                "ms_per_step": round(e_ms / K_steps, 4),
@@ -465,7 +515,8 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, threads = oracle_cpu_rate(inp, op=args.op, scales=(sx, sw) if args.op == "fp8" else None)
+        v, sample, threads = oracle_cpu_rate(inp, op=args.op, scales=(sx, sw) if args.op == "fp8" else None,
+                                             row_index=idx_h.numpy() if gather else None)
         cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
 
     value = flops * K_steps * world / (total_ms / 1e3) / 1e12
@@ -479,6 +530,8 @@ def run_ours(args):
         "config": {"workload": args.workload + ("" if args.op == "gemm" else "+" + args.op), "op": args.op,
                    "E": E, "K": K,
                    "N": N_out, "weight_columns": N, "M_tot": M_tot,
+                   **({"tokens": M_tot, "row_index": "each expert's rows are distinct tokens, in token order"}
+                      if gather else {}),
                    "routing": w.routing, "note": w.note, "accumulate": "fp32", "out": "bf16",
                    "l2": "inputs larger than L2 (%.0f MB > 129 MB), no flush" % (bytes_ / 1e6)
                    if bytes_ > L2_BYTES else "inputs smaller than L2: back-to-back launches",

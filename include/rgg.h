@@ -50,7 +50,9 @@ typedef enum rgg_status {
     RGG_ERR_CUDA = 3,            /* a CUDA runtime / driver call failed; see rgg_last_cuda_error() */
     RGG_ERR_BAD_OFFSETS = 4,     /* device-detected: group offsets not valid; nothing was written */
     RGG_ERR_DEVICE_TIMEOUT = 5,  /* device-detected: a pipeline wait exceeded the time limit; Y is incomplete */
-    RGG_ERR_CAPACITY = 6         /* rgg_export_tiles: more tiles than the output capacity (count still exact) */
+    RGG_ERR_CAPACITY = 6,        /* rgg_export_tiles: more tiles than the output capacity (count still exact) */
+    RGG_ERR_BAD_ROW_INDEX = 7    /* device-detected (gather calls): a token index read was outside [0, T); the
+                                    rows with such an index hold unspecified values, all other rows are right */
 } rgg_status;
 
 typedef struct rgg_handle rgg_handle;
@@ -71,13 +73,27 @@ typedef struct rgg_options {
                                     <= 64 rows of its expert runs as a 64-row MMA with a 64-row X box */
     int op;                      /* for rgg_plan only: 0 = plan rgg_grouped_gemm, 1 = plan
                                     rgg_grouped_gemm_swiglu (then N is the output width), 2 = plan
-                                    rgg_grouped_gemm_fp8 */
+                                    rgg_grouped_gemm_fp8, 3 = plan rgg_grouped_gemm_gather, 4 = plan
+                                    rgg_grouped_gemm_swiglu_gather (N is the output width) */
     int walk_order;              /* order of the persistent CTAs' walk over the tile list (any order gives the
                                     same result): 0 = list order (the automatic choice unless host_counts
                                     show a strong skew), 1 = front/back interleave, 2 = strided scatter,
                                     3 = front/back interleave over the experts sorted by row count (E <= 256;
                                     chosen automatically when the largest expert holds over four times the
                                     mean).  1-CTA kernels only. */
+    int gather_mode;             /* gather calls only: how the routed rows are fetched (same result either
+                                    way).  1 = fused: the GEMM's producer loads them with TMA
+                                    tile::gather4, four rows per copy, once per N tile; 2 = two-pass: a
+                                    row-gather kernel writes them once, in routed order, into a workspace
+                                    and the grouped GEMM reads that with whole-tile TMA boxes.  0 = auto:
+                                    fused when the tile plan takes 64-row tiles (small expert groups),
+                                    else two-pass. */
+    void* workspace;             /* two-pass gather only: caller-owned device memory of at least
+                                    workspace_bytes = M_tot * K * 2 bytes, 16-byte aligned (rgg_plan
+                                    reports the size).  NULL: the handle keeps its own workspace and
+                                    grows it with cudaMalloc when a call needs more (that call then
+                                    allocates, and waits for the device while freeing the old one). */
+    int64_t workspace_bytes;     /* size of `workspace` in bytes */
 } rgg_options;
 
 #define RGG_DEBUG_PRODUCER_STALL 1
@@ -93,6 +109,8 @@ typedef struct rgg_plan_info {
     int64_t max_tiles;           /* upper bound on the flat tile count for these sizes */
     int tail64;                  /* 1 when tail tiles of <= 64 rows run as 64-row MMAs */
     int walk_order;              /* walk order (see rgg_options) */
+    int gather_mode;             /* gather ops: 1 = fused tile::gather4, 2 = two-pass; else 0 */
+    int64_t workspace_bytes;     /* two-pass gather: workspace the call needs; else 0 */
 } rgg_plan_info;
 
 /*
@@ -245,6 +263,55 @@ const char* rgg_last_cuda_error(void);
  */
 rgg_status rgg_grouped_gemm_noalloc(const void* X, const void* W, const int32_t* group_offsets, void* Y,
                                     int E, int64_t M_tot, int K, int N, int32_t* status_out, void* stream);
+
+/*
+ * rgg_grouped_gemm_gather -- the grouped product with the token gather fused
+ * into the activation loads:
+ *
+ *     Y[i, :] = X_tok[row_index[i], :] . W[e]      for every row i of expert e
+ *
+ * The Worklog starts after routing with the rows already grouped ("What I am
+ * measuring") and names the permutation of rows and the scatter/gather of
+ * tokens among the work it leaves out ("Scope of these results"); the
+ * InferenceX glossary entry "Grouped GEMM" ("Engineering details") describes
+ * that permutation.  Two ways to fetch the rows (rgg_options.gather_mode):
+ * fused, where each tile reads its rows straight from the token matrix, four
+ * rows per TMA tile::gather4 copy, only the groups of four that hold rows of
+ * the tile's expert; or two-pass, where one kernel copies each routed row
+ * once into a workspace and the grouped GEMM (CTA pairs included) reads it.
+ * The automatic choice is fused for small expert groups, two-pass otherwise.
+ *
+ * X_tok      device bf16 [T, K], row-major: the tokens in their own order;
+ *            16-byte aligned.  1 <= T < 2^31 (T may be 0 only when M_tot is 0).
+ * row_index  device int32 [M_tot], 4-byte aligned: the token of each routed
+ *            row.  Only the entries of rows [off[0], off[E]) are read; each
+ *            must lie in [0, T), else the status word records
+ *            RGG_ERR_BAD_ROW_INDEX, that row is computed from token 0 and the
+ *            others are unaffected.  A token may appear in several experts.
+ * W, group_offsets, Y, E, M_tot, K, N: as for rgg_grouped_gemm; Y is in
+ *            routed (grouped) row order.
+ * Options as for rgg_grouped_gemm, plus gather_mode and workspace; fused
+ * tiles are 64 or 128 rows (no CTA pair).  Two-pass calls without a caller
+ * workspace use the handle's, so such calls on different streams race on it.
+ * Errors: as for rgg_grouped_gemm, plus RGG_ERR_BAD_ROW_INDEX (device-detected,
+ * read with rgg_query_status) and RGG_ERR_INVALID_ARG for a workspace that is
+ * too small or misaligned.  Asynchronous on `stream`.
+ */
+rgg_status rgg_grouped_gemm_gather(rgg_handle* h, const void* X_tok, int64_t T, const int32_t* row_index,
+                                   const void* W, const int32_t* group_offsets, void* Y, int E, int64_t M_tot,
+                                   int K, int N, void* stream, const rgg_options* opt);
+
+/*
+ * rgg_grouped_gemm_swiglu_gather -- rgg_grouped_gemm_swiglu on gathered rows:
+ * H[i, :] = silu(X_tok[row_index[i]] . W13[e][:, :N]) * (X_tok[row_index[i]] .
+ * W13[e][:, N:]).  W13 is bf16 [E, K, 2N] (gate columns first), H is bf16
+ * [M_tot, N]; everything else as for rgg_grouped_gemm_gather.  The gate-up
+ * projection is the MoE op that reads tokens, so this is where the gather
+ * belongs in a layer.
+ */
+rgg_status rgg_grouped_gemm_swiglu_gather(rgg_handle* h, const void* X_tok, int64_t T, const int32_t* row_index,
+                                          const void* W13, const int32_t* group_offsets, void* H, int E,
+                                          int64_t M_tot, int K, int N, void* stream, const rgg_options* opt);
 
 #ifdef __cplusplus
 }

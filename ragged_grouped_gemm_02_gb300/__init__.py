@@ -17,10 +17,11 @@ import os
 import threading
 
 __all__ = [
-    "RggError", "rgg_grouped_gemm", "rgg_grouped_gemm_swiglu", "rgg_grouped_gemm_noalloc", "rgg_export_tiles", "rgg_query_status", "rgg_plan",
-    "rgg_status_string", "library_path", "load_library", "EXPORTED_SYMBOLS",
+    "RggError", "rgg_grouped_gemm", "rgg_grouped_gemm_swiglu", "rgg_grouped_gemm_fp8", "rgg_grouped_gemm_gather",
+    "rgg_grouped_gemm_swiglu_gather", "rgg_grouped_gemm_noalloc", "rgg_export_tiles", "rgg_query_status",
+    "rgg_plan", "rgg_status_string", "library_path", "load_library", "EXPORTED_SYMBOLS",
     "RGG_OK", "RGG_ERR_INVALID_ARG", "RGG_ERR_UNSUPPORTED", "RGG_ERR_CUDA", "RGG_ERR_BAD_OFFSETS",
-    "RGG_ERR_DEVICE_TIMEOUT", "RGG_ERR_CAPACITY",
+    "RGG_ERR_DEVICE_TIMEOUT", "RGG_ERR_CAPACITY", "RGG_ERR_BAD_ROW_INDEX",
 ]
 
 RGG_OK = 0
@@ -30,6 +31,7 @@ RGG_ERR_CUDA = 3
 RGG_ERR_BAD_OFFSETS = 4
 RGG_ERR_DEVICE_TIMEOUT = 5
 RGG_ERR_CAPACITY = 6
+RGG_ERR_BAD_ROW_INDEX = 7
 RGG_DEBUG_PRODUCER_STALL = 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -39,7 +41,7 @@ _LIB_PATH = os.path.join(_PKG, "librgg.so")
 EXPORTED_SYMBOLS = (
     "rgg_create", "rgg_destroy", "rgg_grouped_gemm", "rgg_export_tiles", "rgg_query_status",
     "rgg_plan", "rgg_status_string", "rgg_last_cuda_error", "rgg_grouped_gemm_noalloc", "rgg_grouped_gemm_swiglu",
-    "rgg_grouped_gemm_fp8",
+    "rgg_grouped_gemm_fp8", "rgg_grouped_gemm_gather", "rgg_grouped_gemm_swiglu_gather",
 )
 
 
@@ -53,14 +55,15 @@ class _Options(ctypes.Structure):
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("stages", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("timeout_ns", ctypes.c_uint64), ("host_counts", ctypes.c_void_p),
                 ("debug_flags", ctypes.c_int), ("tail64", ctypes.c_int),
-                ("op", ctypes.c_int), ("walk_order", ctypes.c_int)]
+                ("op", ctypes.c_int), ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64)]
 
 
 class _PlanInfo(ctypes.Structure):
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int), ("stages", ctypes.c_int),
                 ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("tmem_cols", ctypes.c_int), ("max_tiles", ctypes.c_int64), ("tail64", ctypes.c_int),
-                ("walk_order", ctypes.c_int)]
+                ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int), ("workspace_bytes", ctypes.c_int64)]
 
 
 _lock = threading.Lock()
@@ -102,6 +105,10 @@ def load_library() -> ctypes.CDLL:
         lib.rgg_grouped_gemm_swiglu.restype = I
         lib.rgg_grouped_gemm_fp8.argtypes = [P, P, P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
         lib.rgg_grouped_gemm_fp8.restype = I
+        for name in ("rgg_grouped_gemm_gather", "rgg_grouped_gemm_swiglu_gather"):
+            fn = getattr(lib, name)
+            fn.argtypes = [P, P, I64, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
+            fn.restype = I
         lib.rgg_grouped_gemm_noalloc.argtypes = [P, P, P, P, I, I64, I, I, P, P]
         lib.rgg_grouped_gemm_noalloc.restype = I
         _lib = lib
@@ -134,9 +141,9 @@ def _handle(device: int) -> ctypes.c_void_p:
 
 
 def _options(bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0, tail64=0,
-             op=0, walk_order=0):
+             op=0, walk_order=0, gather_mode=0):
     opt = _Options(int(bm), int(bn), int(stages), int(max_ctas), int(timeout_ns), None, int(debug_flags),
-                   int(tail64), int(op), int(walk_order))
+                   int(tail64), int(op), int(walk_order), int(gather_mode))
     keep = None
     if host_counts is not None:
         import numpy as np
@@ -303,6 +310,78 @@ def rgg_grouped_gemm_noalloc(X, W, group_offsets, Y=None, status_out=None, strea
     return Y
 
 
+def _gather_call(name, X_tok, row_index, W, group_offsets, out, swiglu, bm, bn, stages, max_ctas, timeout_ns,
+                 host_counts, debug_flags, tail64, walk_order, gather_mode, workspace, stream, check):
+    import torch
+    if not (X_tok.is_cuda and row_index.is_cuda and W.is_cuda and group_offsets.is_cuda):
+        raise ValueError("X_tok, row_index, W and group_offsets must be CUDA tensors")
+    if (X_tok.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or row_index.dtype != torch.int32
+            or group_offsets.dtype != torch.int32):
+        raise TypeError("X_tok and W must be bf16, row_index and group_offsets int32")
+    if not all(t.is_contiguous() for t in (X_tok, row_index, W, group_offsets)):
+        raise ValueError("X_tok, row_index, W and group_offsets must be contiguous")
+    T, K = X_tok.shape
+    E, K2, NW = W.shape
+    M_tot = row_index.numel()
+    if K2 != K or group_offsets.numel() != E + 1 or row_index.dim() != 1 or (swiglu and NW % 2 != 0):
+        raise ValueError("shape mismatch: X_tok %s, row_index %s, W %s, offsets %d" % (
+            tuple(X_tok.shape), tuple(row_index.shape), tuple(W.shape), group_offsets.numel()))
+    N = NW // 2 if swiglu else NW
+    device = X_tok.device.index if X_tok.device.index is not None else torch.cuda.current_device()
+    if out is None:
+        out = torch.empty(M_tot, N, dtype=torch.bfloat16, device=X_tok.device)
+    elif out.shape != (M_tot, N) or out.dtype != torch.bfloat16 or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("the output must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
+    lib = load_library()
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order,
+                         gather_mode)
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        opt.workspace = workspace.data_ptr()
+        opt.workspace_bytes = workspace.numel() * workspace.element_size()
+    st = _stream_ptr(stream, device)
+    s = getattr(lib, name)(_handle(device), X_tok.data_ptr(), T, row_index.data_ptr(), W.data_ptr(),
+                           group_offsets.data_ptr(), out.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
+    del keep
+    if s != RGG_OK:
+        _raise(s, name)
+    if check:
+        s = lib.rgg_query_status(_handle(device), st)
+        if s != RGG_OK:
+            _raise(s, name + " (device status)")
+    return out
+
+
+def rgg_grouped_gemm_gather(X_tok, row_index, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0,
+                            timeout_ns=0, host_counts=None, debug_flags=0, tail64=0, walk_order=0, gather_mode=0,
+                            workspace=None, stream=None, check=False):
+    """Y[i] = X_tok[row_index[i]] . W_e for every routed row i of expert e,
+    the token gather fused into the kernel's activation loads.
+
+    X_tok: bf16 CUDA [T, K]; row_index: int32 CUDA [M_tot]; W: bf16 CUDA
+    [E, K, N]; group_offsets: int32 CUDA [E+1]; Y: optional bf16 CUDA
+    [M_tot, N] (routed row order).  gather_mode: 0 auto, 1 fused (TMA
+    tile::gather4 in the GEMM), 2 two-pass (row gather into a workspace, then
+    the grouped GEMM); workspace: optional CUDA tensor of at least M_tot*K*2
+    bytes for the two-pass mode (else the handle's own is used)."""
+    return _gather_call("rgg_grouped_gemm_gather", X_tok, row_index, W, group_offsets, Y, False, bm, bn, stages,
+                        max_ctas, timeout_ns, host_counts, debug_flags, tail64, walk_order, gather_mode, workspace,
+                        stream, check)
+
+
+def rgg_grouped_gemm_swiglu_gather(X_tok, row_index, W13, group_offsets, H=None, *, bm=0, bn=0, stages=0,
+                                   max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0, tail64=0,
+                                   walk_order=0, gather_mode=0, workspace=None, stream=None, check=False):
+    """H[i] = silu(x W13_e[:, :N]) * (x W13_e[:, N:]) with x = X_tok[row_index[i]]:
+    the fused gate-up projection reading its tokens through the gather.
+
+    W13: bf16 CUDA [E, K, 2N] (gate columns first); H: optional bf16 CUDA [M_tot, N]."""
+    return _gather_call("rgg_grouped_gemm_swiglu_gather", X_tok, row_index, W13, group_offsets, H, True, bm, bn,
+                        stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, walk_order, gather_mode,
+                        workspace, stream, check)
+
+
 def rgg_export_tiles(group_offsets, M_tot: int, N: int, bm: int, bn: int, cap: int | None = None, stream=None):
     """The flat tile list the kernel walks, built on the device by the same
     code: returns (int32 CPU tensor [min(T, cap), 4] of (expert, row0, rows,
@@ -337,12 +416,13 @@ def rgg_query_status(device: int | None = None, stream=None) -> int:
 
 def rgg_plan(E: int, M_tot: int, K: int, N: int, *, num_sms: int = 0, smem_optin: int = 0, bm=0, bn=0,
              stages=0, max_ctas=0, host_counts=None, tail64=0, op: str = "gemm",
-             walk_order=0) -> dict:
+             walk_order=0, gather_mode=0) -> dict:
     """The launch configuration rgg_grouped_gemm (op="gemm") or
     rgg_grouped_gemm_swiglu (op="swiglu", N = output width) would use (host-only)."""
     lib = load_library()
     opt, keep = _options(bm, bn, stages, max_ctas, 0, host_counts, 0, tail64,
-                         {"gemm": 0, "swiglu": 1, "fp8": 2}[op], walk_order)
+                         {"gemm": 0, "swiglu": 1, "fp8": 2, "gather": 3, "swiglu_gather": 4}[op], walk_order,
+                         gather_mode)
     info = _PlanInfo()
     s = lib.rgg_plan(int(num_sms), int(smem_optin), int(E), int(M_tot), int(K), int(N), ctypes.byref(opt),
                      ctypes.byref(info))

@@ -24,6 +24,8 @@ struct rgg_handle {
     int num_sms;
     int smem_optin;
     int32_t* d_status;
+    void* workspace = nullptr;     // two-pass gather: the gathered rows, grown on demand
+    size_t workspace_bytes = 0;
 };
 
 namespace {
@@ -97,10 +99,18 @@ rgg_status check_sizes(int E, int64_t M_tot, int K, int N) {
     return RGG_OK;
 }
 
-// `fused`: the fused gate-up + SiLU op (N then counts the 2N weight columns)
-// or the FP8 op: tiles are 1-CTA (64 or 128 rows) and BN is 128 or 256.
+// Restrictions of the kernel family a plan is for.  kPlanNoPair: 1-CTA
+// tiles only (64 or 128 rows); kPlanNoBn192: BN is 128 or 256.  The fused
+// gate-up + SiLU op (N then counts the 2N weight columns) and the FP8 op take
+// both; the token-gather GEMM takes kPlanNoPair.
+constexpr int kPlanNoPair = 1;
+constexpr int kPlanNoBn192 = 2;
+constexpr int kPlanFused = kPlanNoPair | kPlanNoBn192;
+
 rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N, const rgg_options* opt,
-                     Plan* out, bool fused = false) {
+                     Plan* out, int kind = 0) {
+    const bool no_pair = (kind & kPlanNoPair) != 0;
+    const bool no_192 = (kind & kPlanNoBn192) != 0;
     rgg_status s = check_sizes(E, M_tot, K, N);
     if (s != RGG_OK) return s;
     if (num_sms <= 0) num_sms = kDefaultSms;
@@ -112,7 +122,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (want_bm != 0 && want_bm != 64 && want_bm != 128 && want_bm != 256) return RGG_ERR_INVALID_ARG;
     if (want_bn != 0 && want_bn != 128 && want_bn != 192 && want_bn != 256) return RGG_ERR_INVALID_ARG;
     if (want_bm == 256 && want_bn == 192) return RGG_ERR_INVALID_ARG;  // pair tiles split BN in whole panels
-    if (fused && (want_bm == 256 || want_bn == 192)) return RGG_ERR_INVALID_ARG;
+    if ((no_pair && want_bm == 256) || (no_192 && want_bn == 192)) return RGG_ERR_INVALID_ARG;
     if (want_stages != 0 && (want_stages < 2 || want_stages > rgg::kMaxStages)) return RGG_ERR_INVALID_ARG;
     if (max_ctas < 0) return RGG_ERR_INVALID_ARG;
     const int want_tail = opt ? opt->tail64 : 0;
@@ -162,14 +172,14 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         int best_bm = bm, best_bn = bn;
         for (int cbm : {256, 128, 64}) {
             if (bm != 0 && cbm != bm) continue;
-            if (fused && cbm == 256) continue;
+            if (no_pair && cbm == 256) continue;
             if (bm == 0 && cbm == 64) continue;  // 64-row tiles only for small groups (above)
             const bool cpair = (cbm == 256);
             const int cunits = cpair ? std::max(1, grid_cap / 2) : grid_cap;
             const int64_t mt = std::max<int64_t>(1, m_tiles(cbm));
             for (int cbn : {256, 192, 128}) {
                 if (bn != 0 && cbn != bn) continue;
-                if ((cpair || fused) && cbn == 192) continue;
+                if ((cpair || no_192) && cbn == 192) continue;
                 const int64_t waves = ceil_div(mt * ceil_div(N, cbn), cunits);
                 const double cost = static_cast<double>(waves) * (cbn + 64) * (cpair ? 0.87 : 1.0);
                 if (cost < best) {
@@ -224,6 +234,53 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     out->max_tiles = max_tiles;
     out->tail64 = (bm == 128 && want_tail != -1) ? 1 : 0;
     out->walk_order = walk;
+    return RGG_OK;
+}
+
+// Gather modes of the gather calls (rgg_options.gather_mode).
+constexpr int kGatherFused = 1;    // TMA tile::gather4 inside the GEMM's producer
+constexpr int kGatherTwoPass = 2;  // a row-gather kernel into a workspace, then the grouped GEMM
+
+int64_t gather_workspace_bytes(int64_t M_tot, int K) { return M_tot * static_cast<int64_t>(K) * 2; }
+
+constexpr double kFusedGatherMaxRows = 32.0;
+
+// The caller's mode, else: fused when the experts that have rows average at
+// most kFusedGatherMaxRows of them (the few gathered rows per tile hide under
+// the weight stream), two-pass otherwise.  Each fused row fetch is a separate
+// 128-byte copy repeated for every N tile, and on a GB300 such fetches top
+// out near 1.8 TB/s per GPU, a third of what whole-tile boxes reach; gathering
+// each routed row once and multiplying with whole-tile boxes wins as soon as
+// tiles hold more than a few dozen rows (measured: 16 rows per expert, fused
+// 2% faster; 64 rows, two-pass 29% faster).
+rgg_status choose_gather_mode(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N,
+                              const rgg_options* opt, bool swiglu, int* mode) {
+    const int want = opt ? opt->gather_mode : 0;
+    if (want < 0 || want > 2) return RGG_ERR_INVALID_ARG;
+    if (want != 0) {
+        *mode = want;
+        return RGG_OK;
+    }
+    (void)num_sms;
+    (void)smem_optin;
+    (void)K;
+    (void)N;
+    (void)swiglu;
+    if (opt && opt->bm == 256) {
+        *mode = kGatherTwoPass;
+        return RGG_OK;
+    }
+    double avg = static_cast<double>(M_tot) / E;
+    if (opt && opt->host_counts) {
+        int64_t rows = 0, busy = 0;
+        for (int e = 0; e < E; ++e)
+            if (opt->host_counts[e] > 0) {
+                rows += opt->host_counts[e];
+                ++busy;
+            }
+        avg = busy ? static_cast<double>(rows) / busy : 0.0;
+    }
+    *mode = (avg <= kFusedGatherMaxRows) ? kGatherFused : kGatherTwoPass;
     return RGG_OK;
 }
 
@@ -312,6 +369,36 @@ rgg_status encode_maps_fp8(const void* X8, const void* W8, int E, int64_t M_tot,
     return RGG_OK;
 }
 
+// The token matrix [T, K] for tile::gather4 loads: box one row high and one
+// 128-byte swizzle row wide, so four gathered rows fill one 512-byte block of
+// a stage in the same layout a {64, rows} box would give.
+rgg_status encode_token_map(const void* Xtok, int64_t T, int K, CUtensorMap* tx) {
+    EncodeTiledFn encode = encode_tiled_fn();
+    if (!encode) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled is not available from the driver";
+        return RGG_ERR_CUDA;
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(Xtok), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled(X_tok) failed with CUresult " +
+                            std::to_string(static_cast<int>(r));
+        return RGG_ERR_CUDA;
+    }
+    return RGG_OK;
+}
+
+// The token-gather GEMM, plain (Y = X_tok[row_index] . W_e) or with the fused
+// gate-up + SiLU epilogue (W then holds 2N columns and Y is H [M_tot, N]).
+rgg_status gather_call(rgg_handle* h, const void* X_tok, int64_t T, const int32_t* row_index, const void* W,
+                       const int32_t* group_offsets, void* Y, int E, int64_t M_tot, int K, int N, void* stream,
+                       const rgg_options* opt, bool swiglu);
+
 }  // namespace
 
 namespace rgg {
@@ -339,6 +426,7 @@ const char* rgg_status_string(rgg_status s) {
         case RGG_ERR_BAD_OFFSETS: return "RGG_ERR_BAD_OFFSETS: group offsets are not valid; nothing was written";
         case RGG_ERR_DEVICE_TIMEOUT: return "RGG_ERR_DEVICE_TIMEOUT: a device pipeline wait exceeded its limit";
         case RGG_ERR_CAPACITY: return "RGG_ERR_CAPACITY: more tiles than the output capacity";
+        case RGG_ERR_BAD_ROW_INDEX: return "RGG_ERR_BAD_ROW_INDEX: a token index is outside [0, T)";
     }
     return "unknown rgg_status";
 }
@@ -385,6 +473,7 @@ void rgg_destroy(rgg_handle* h) {
     {
         DeviceScope scope(h->device);
         cudaFree(h->d_status);
+        if (h->workspace) cudaFree(h->workspace);
     }
     delete h;
 }
@@ -394,10 +483,19 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     if (!out) return RGG_ERR_INVALID_ARG;
     Plan p;
     const int op = opt ? opt->op : 0;
-    if (op < 0 || op > 2) return RGG_ERR_INVALID_ARG;
-    if (op == 1 && (N < 8 || N % 8 != 0 || N > (1 << 30))) return RGG_ERR_INVALID_ARG;
+    if (op < 0 || op > 4) return RGG_ERR_INVALID_ARG;
+    const bool swiglu = (op == 1 || op == 4);
+    if (swiglu && (N < 8 || N % 8 != 0 || N > (1 << 30))) return RGG_ERR_INVALID_ARG;
     if (op == 2 && (K % 16 != 0 || N % 16 != 0)) return RGG_ERR_INVALID_ARG;
-    rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, op == 1 ? 2 * N : N, opt, &p, op != 0);
+    const bool gather = (op == 3 || op == 4);
+    int mode = 0;
+    if (gather) {
+        rgg_status sm = choose_gather_mode(num_sms, smem_optin, E, M_tot, K, N, opt, swiglu, &mode);
+        if (sm != RGG_OK) return sm;
+    }
+    // the two-pass gather runs the plain (or fused gate-up) kernel on the gathered rows
+    const int kind = (op == 0 || (op == 3 && mode == kGatherTwoPass)) ? 0 : (op == 3) ? kPlanNoPair : kPlanFused;
+    rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, swiglu ? 2 * N : N, opt, &p, kind);
     if (s != RGG_OK) return s;
     out->bm = p.bm;
     out->bn = p.bn;
@@ -410,6 +508,8 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->max_tiles = p.max_tiles;
     out->tail64 = p.tail64;
     out->walk_order = p.walk_order;
+    out->gather_mode = mode;
+    out->workspace_bytes = (mode == kGatherTwoPass) ? gather_workspace_bytes(M_tot, K) : 0;
     return RGG_OK;
 }
 
@@ -479,7 +579,7 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
         return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
     }
     Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, /*fused=*/true);
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, kPlanFused);
     if (s != RGG_OK) return s;
     CUtensorMap tx, tx64, tw;
     s = encode_maps(X, W13, E, M_tot, K, 2 * N, p.bm, &tx, &tx64, &tw);
@@ -523,7 +623,7 @@ rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, c
         return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
     }
     Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p, /*fused=*/true);
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p, kPlanFused);
     if (s != RGG_OK) return s;
     CUtensorMap tx, tx64, tw;
     s = encode_maps_fp8(X8, W8, E, M_tot, K, N, p.bm, &tx, &tx64, &tw);
@@ -548,6 +648,18 @@ rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, c
     a.sw = sw;
     cudaError_t err = rgg::launch_gemm_fp8(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_fp8 launch");
+}
+
+rgg_status rgg_grouped_gemm_gather(rgg_handle* h, const void* X_tok, int64_t T, const int32_t* row_index,
+                                   const void* W, const int32_t* group_offsets, void* Y, int E, int64_t M_tot, int K,
+                                   int N, void* stream, const rgg_options* opt) {
+    return gather_call(h, X_tok, T, row_index, W, group_offsets, Y, E, M_tot, K, N, stream, opt, false);
+}
+
+rgg_status rgg_grouped_gemm_swiglu_gather(rgg_handle* h, const void* X_tok, int64_t T, const int32_t* row_index,
+                                          const void* W13, const int32_t* group_offsets, void* H, int E,
+                                          int64_t M_tot, int K, int N, void* stream, const rgg_options* opt) {
+    return gather_call(h, X_tok, T, row_index, W13, group_offsets, H, E, M_tot, K, N, stream, opt, true);
 }
 
 rgg_status rgg_export_tiles(rgg_handle* h, const int32_t* group_offsets, int E, int64_t M_tot, int N, int bm,
@@ -578,3 +690,89 @@ rgg_status rgg_query_status(rgg_handle* h, void* stream) {
 }
 
 }  // extern "C"
+
+namespace {
+
+rgg_status gather_call(rgg_handle* h, const void* X_tok, int64_t T, const int32_t* row_index, const void* W,
+                       const int32_t* group_offsets, void* Y, int E, int64_t M_tot, int K, int N, void* stream,
+                       const rgg_options* opt, bool swiglu) {
+    if (!h || !group_offsets || !W) return RGG_ERR_INVALID_ARG;
+    rgg_status s = check_sizes(E, M_tot, K, N);
+    if (s != RGG_OK) return s;
+    if (swiglu && N > (1 << 30)) return RGG_ERR_INVALID_ARG;
+    if (T < 0 || T >= (int64_t(1) << 31)) return RGG_ERR_INVALID_ARG;
+    if (M_tot > 0 && (!X_tok || !row_index || !Y || T < 1)) return RGG_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(group_offsets, 4) ||
+        (M_tot > 0 && (!aligned(X_tok, 16) || !aligned(Y, 16) || !aligned(row_index, 4))))
+        return RGG_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceScope scope(h->device);
+    if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
+    if (M_tot == 0) {
+        cudaError_t err = rgg::launch_validate_offsets(group_offsets, E, M_tot, h->d_status, st);
+        return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
+    }
+    const int NW = swiglu ? 2 * N : N;  // weight columns
+    int mode = 0;
+    s = choose_gather_mode(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, swiglu, &mode);
+    if (s != RGG_OK) return s;
+    if (mode == kGatherTwoPass) {
+        // Pass 1 writes the routed rows, in routed order, into the workspace;
+        // pass 2 is the grouped product of those rows.
+        const int64_t need = gather_workspace_bytes(M_tot, K);
+        void* ws = opt ? opt->workspace : nullptr;
+        if (ws) {
+            if (opt->workspace_bytes < need || !aligned(ws, 16)) return RGG_ERR_INVALID_ARG;
+        } else {
+            if (h->workspace_bytes < static_cast<size_t>(need)) {
+                // cudaFree waits for the device, so no earlier call still reads the old buffer
+                if (h->workspace) cudaFree(h->workspace);
+                h->workspace = nullptr;
+                h->workspace_bytes = 0;
+                const size_t grow = (static_cast<size_t>(need) + (size_t(2) << 20) - 1) & ~((size_t(2) << 20) - 1);
+                cudaError_t err = cudaMalloc(&h->workspace, grow);
+                if (err != cudaSuccess) {
+                    h->workspace = nullptr;
+                    return cuda_failure(err, "cudaMalloc(gather workspace)");
+                }
+                h->workspace_bytes = grow;
+            }
+            ws = h->workspace;
+        }
+        cudaError_t err = rgg::launch_gather_rows(X_tok, row_index, group_offsets, E, M_tot, T, K, ws, h->num_sms,
+                                                  h->d_status, st);
+        if (err != cudaSuccess) return cuda_failure(err, "gather_rows launch");
+        return swiglu ? rgg_grouped_gemm_swiglu(h, ws, W, group_offsets, Y, E, M_tot, K, N, stream, opt)
+                      : rgg_grouped_gemm(h, ws, W, group_offsets, Y, E, M_tot, K, N, stream, opt);
+    }
+    Plan p;
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, NW, opt, &p, swiglu ? kPlanFused : kPlanNoPair);
+    if (s != RGG_OK) return s;
+    CUtensorMap tx, tx64, tw;
+    s = encode_maps(X_tok, W, E, T, K, NW, p.bm, &tx, &tx64, &tw);  // W map (the X maps are replaced below)
+    if (s != RGG_OK) return s;
+    s = encode_token_map(X_tok, T, K, &tx);
+    if (s != RGG_OK) return s;
+    rgg::GemmArgs a;
+    a.offsets = group_offsets;
+    a.Y = static_cast<__nv_bfloat16*>(Y);
+    a.status = h->d_status;
+    a.M_tot = M_tot;
+    a.E = E;
+    a.K = K;
+    a.N = N;
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(K, rgg::kBK));
+    a.n_tiles_n = static_cast<int32_t>(ceil_div(N, swiglu ? p.bn / 2 : p.bn));
+    a.stages = p.stages;
+    a.y_vec32 = ((N % 16) == 0 && aligned(Y, 32)) ? 1 : 0;
+    a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+    a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
+    a.tail64 = p.tail64;
+    a.walk_order = p.walk_order;
+    a.row_index = row_index;
+    a.t_rows = static_cast<int32_t>(T);
+    cudaError_t err = rgg::launch_gemm_gather(swiglu, p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tw, a);
+    return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_gather launch");
+}
+
+}  // namespace

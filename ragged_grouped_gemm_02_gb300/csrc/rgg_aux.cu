@@ -59,6 +59,53 @@ cudaError_t launch_export_tiles(const int32_t* offsets, int E, int64_t M_tot, in
     return cudaGetLastError();
 }
 
+// Two-pass token gather, first pass: Xg[i, :] = X_tok[row_index[i], :] for
+// the routed rows i in [off[0], off[E]), so that the grouped product can then
+// read Xg with whole-tile TMA boxes.  One warp copies one row at a time in
+// 16-byte pieces, four loads in flight per lane before their stores.  An
+// index outside [0, T) is reported (RGG_ERR_BAD_ROW_INDEX) and token 0 is
+// copied in its place, as in the fused gather.  Offsets are only clamped to
+// [0, M_tot] here; the GEMM that follows validates them.
+__global__ void __launch_bounds__(kGatherRowsThreads) gather_rows_kernel(
+    const uint4* __restrict__ xtok, const int32_t* __restrict__ row_index, const int32_t* __restrict__ offsets,
+    int E, int64_t M_tot, int64_t T, int kchunks, uint4* __restrict__ xg, int32_t* status) {
+    int64_t begin = offsets[0], end = offsets[E];
+    begin = begin < 0 ? 0 : (begin > M_tot ? M_tot : begin);
+    end = end < begin ? begin : (end > M_tot ? M_tot : end);
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t i = begin + warp; i < end; i += nwarps) {
+        int32_t tok = __ldg(row_index + i);
+        if (tok < 0 || tok >= T) {
+            if (lane == 0) atomicCAS(status, 0, kStatusBadRowIndex);
+            tok = 0;
+        }
+        const uint4* src = xtok + static_cast<int64_t>(tok) * kchunks;
+        uint4* dst = xg + i * kchunks;
+        int c = lane;
+        for (; c + 96 < kchunks; c += 128) {
+            const uint4 v0 = __ldg(src + c), v1 = __ldg(src + c + 32), v2 = __ldg(src + c + 64),
+                        v3 = __ldg(src + c + 96);
+            dst[c] = v0;
+            dst[c + 32] = v1;
+            dst[c + 64] = v2;
+            dst[c + 96] = v3;
+        }
+        for (; c < kchunks; c += 32) dst[c] = __ldg(src + c);
+    }
+}
+
+cudaError_t launch_gather_rows(const void* xtok, const int32_t* row_index, const int32_t* offsets, int E,
+                               int64_t M_tot, int64_t T, int K, void* xg, int num_sms, int32_t* status,
+                               cudaStream_t stream) {
+    const int64_t want = (M_tot + kGatherRowsThreads / 32 - 1) / (kGatherRowsThreads / 32);
+    const int grid = static_cast<int>(want < 1 ? 1 : (want > 4LL * num_sms ? 4LL * num_sms : want));
+    gather_rows_kernel<<<grid, kGatherRowsThreads, 0, stream>>>(static_cast<const uint4*>(xtok), row_index, offsets,
+                                                                 E, M_tot, T, K / 8, static_cast<uint4*>(xg), status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_validate_offsets(const int32_t* offsets, int E, int64_t M_tot, int32_t* status,
                                     cudaStream_t stream) {
     const size_t smem = 4u * static_cast<size_t>(E + 1);

@@ -46,6 +46,7 @@ namespace rgg {
 
 constexpr int kStatusTimeout = 5;
 constexpr int kStatusBadOffsets = 4;
+constexpr int kStatusBadRowIndex = 7;
 constexpr int kStatusCapacity = 6;
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 192;
@@ -71,6 +72,8 @@ struct GemmArgs {
     uint64_t timeout_ns;
     const float* sx = nullptr;  // FP8 kernels: fp32 scale of each row of X [M_tot]
     const float* sw = nullptr;  // FP8 kernels: fp32 scale of each (expert, column) of W [E, N]
+    const int32_t* row_index = nullptr;  // gather kernels: token row of each routed row [M_tot]
+    int32_t t_rows = 0;                  // gather kernels: rows of the token matrix
 };
 
 // Shared-memory carve-up shared by the host planner and the kernel.  Offsets
@@ -161,13 +164,27 @@ constexpr int kEpiSwiGLU = 1;
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
 
-template <int BM, int BN, int kEpi = kEpiPlain, bool kFp8 = false>
+// Token gather fused into the A loads (kGatherTma): the A rows are gathered
+// from a token matrix X_tok [T, K] through args.row_index (routed row i
+// reads token row_index[i]); tmap_x is the token matrix with a one-row box
+// and tmap_x64 is unused.  The producer warp loads four rows per TMA
+// tile::gather4 copy, one lane per group of four tile rows, and copies only
+// the groups that hold rows of the tile's expert.  Each gathered row is a
+// separate 128-byte fetch, and an A tile is fetched again for every N tile,
+// so this suits tiles of few rows (small expert groups); large groups are
+// gathered once by gather_rows_kernel and multiplied by the plain kernel.
+constexpr int kGatherNone = 0;
+constexpr int kGatherTma = 1;
+
+template <int BM, int BN, int kEpi = kEpiPlain, bool kFp8 = false, int kGather = kGatherNone>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
                         const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
     using Cfg = TileConfig<BM, BN, kFp8>;
     static_assert(kEpi == kEpiPlain || (BN % 128) == 0, "fused gate-up tiles hold whole gate and up panels");
     static_assert(!(kFp8 && kEpi == kEpiSwiGLU), "the fused gate-up epilogue is bf16 only");
+    static_assert(!(kFp8 && kGather != kGatherNone), "the token gather is bf16 only");
+    static_assert(BM / 4 <= 32, "one producer lane per group of four tile rows");
     constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;  // output columns per tile
     constexpr int kPanels = BN / Cfg::kPanelN;
     // Column of W read by B panel p of a tile whose first output column is col0.
@@ -251,7 +268,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                        : decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
     };
 
-    if (warp == 0) {
+    if (kGather == kGatherTma && warp == 0) {
+        // ------------------------------------- S4 with the token gather (TMA)
+        // Lane l owns tile rows 4l..4l+3.  The token indices of the next
+        // tile are loaded while the current tile's stages are issued, so
+        // their latency stays off the ring.  A row past the tile's last row
+        // in a partly filled group repeats the group's first row (its product
+        // is never stored); an index outside [0, T) is reported and replaced
+        // by token 0, so every copy stays inside the token matrix.
+        if ((args.debug_flags & kDebugProducerStall) == 0) {
+            int st = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            int32_t nxt[4] = {0, 0, 0, 0};
+            TileCoord cn = {0, 0, 0, 0};
+            auto fetch = [&](int32_t p) {
+                cn = tile_at(p);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 4 * lane + i < cn.rows ? 4 * lane + i : 4 * lane;
+                    nxt[i] = (4 * lane < cn.rows) ? __ldg(args.row_index + cn.row0 + r) : 0;
+                }
+            };
+            if (static_cast<int32_t>(blockIdx.x) < T) fetch(blockIdx.x);
+            for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
+                const TileCoord c = cn;
+                int32_t tok[4];
+                bool bad = false;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    tok[i] = nxt[i];
+                    if (tok[i] < 0 || tok[i] >= args.t_rows) {
+                        bad = true;
+                        tok[i] = 0;
+                    }
+                }
+                const int groups = (c.rows + 3) >> 2;
+                if (bad && 4 * lane < c.rows) atomicCAS(args.status, 0, kStatusBadRowIndex);
+                if (t + static_cast<int32_t>(gridDim.x) < T) fetch(t + gridDim.x);
+                const uint32_t tx_bytes = static_cast<uint32_t>(groups) * 512u + static_cast<uint32_t>(BN) * 128u;
+                for (int kb = 0; kb < KB; ++kb) {
+                    int got = 1;
+                    if (lane == 0) got = wait_or_abort(empty_bar(st), ph ^ 1u, abort_flag, args.status, args.timeout_ns);
+                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(full_bar(st), tx_bytes);
+                    __syncwarp();
+                    if (lane < groups)
+                        tma_gather4(a0 + st * sp.a_stage + 512u * lane, &tmap_x, full_bar(st), kb * Cfg::kKStage,
+                                    tok[0], tok[1], tok[2], tok[3]);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int p = 0; p < kPanels; ++p)
+                            tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st),
+                                        w_col(c.col0, p), kb * Cfg::kKStage, c.expert);
+                    }
+                    ++issued;
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok && lane == 0) {
+                // Let the copies already issued land before the CTA can exit.
+                const uint32_t n = issued < static_cast<uint32_t>(S) ? issued : static_cast<uint32_t>(S);
+                for (uint32_t i = issued - n; i < issued; ++i)
+                    wait_bounded(full_bar(static_cast<int>(i % S)), (i / S) & 1u, kDrainLimitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 0) {
         // ---------------------------------------------------- S4: TMA producer
         if (lane == 0 && (args.debug_flags & kDebugProducerStall) == 0) {
             int st = 0;

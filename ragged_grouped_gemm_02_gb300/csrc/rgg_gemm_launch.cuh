@@ -6,10 +6,10 @@
 
 namespace rgg {
 
-template <int BM, int BN, int kEpi = kEpiPlain, bool kFp8 = false>
+template <int BM, int BN, int kEpi = kEpiPlain, bool kFp8 = false, int kGather = kGatherNone>
 cudaError_t launch_gemm_instance(int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                                  const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args) {
-    auto kernel = grouped_gemm_kernel<BM, BN, kEpi, kFp8>;
+    auto kernel = grouped_gemm_kernel<BM, BN, kEpi, kFp8, kGather>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;

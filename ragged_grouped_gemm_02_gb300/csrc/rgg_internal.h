@@ -30,6 +30,21 @@ cudaError_t launch_gemm_swiglu(int bm, int bn, int grid, size_t smem, cudaStream
 cudaError_t launch_gemm_fp8(int bm, int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                             const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 
+// Token gather fused into the A loads (TMA tile::gather4): tmap_tok is the
+// token matrix [T, K] with a one-row box.  `swiglu` selects the fused gate-up
+// epilogue (then `bn` is the MMA width, 128 or 256); otherwise `bn` is 128,
+// 192 or 256.  `bm` is 64 or 128.
+cudaError_t launch_gemm_gather(bool swiglu, int bm, int bn, int grid, size_t smem, cudaStream_t stream,
+                               const CUtensorMap& tmap_tok, const CUtensorMap& tmap_w, const GemmArgs& args);
+
+// First pass of the two-pass gather: Xg[i] = X_tok[row_index[i]] for the rows
+// [off[0], off[E]) (clamped to [0, M_tot]).  xtok and xg are 16-byte aligned
+// bf16 [T, K] and [M_tot, K]; K is a multiple of 8.
+constexpr int kGatherRowsThreads = 512;
+cudaError_t launch_gather_rows(const void* xtok, const int32_t* row_index, const int32_t* offsets, int E,
+                               int64_t M_tot, int64_t T, int K, void* xg, int num_sms, int32_t* status,
+                               cudaStream_t stream);
+
 // CTA-pair kernel (256-row tiles, clusters of two): `bn` is 128 or 256 and
 // `grid` is even.
 cudaError_t launch_gemm_pair(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,

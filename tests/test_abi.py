@@ -51,7 +51,7 @@ def test_library_has_no_runtime_cuda_dependency():
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = rgg.rgg_status_string(code)
         assert s.startswith("RGG_")
     assert rgg.rgg_status_string(99) == "unknown rgg_status"
@@ -176,3 +176,38 @@ def test_plan_cta_pair_mode(lib):
     with pytest.raises(rgg.RggError) as ei:
         rgg.rgg_plan(64, 16384, 1024, 2688, bm=256, bn=192)
     assert ei.value.status == rgg.RGG_ERR_INVALID_ARG
+
+
+def test_plan_gather_modes(lib):
+    # small expert groups (64-row tiles): the gather is fused into the GEMM
+    p = rgg.rgg_plan(32, 512, 6144, 4096, op="gather")
+    assert p["gather_mode"] == 1 and p["bm"] == 64 and p["workspace_bytes"] == 0
+    p = rgg.rgg_plan(32, 512, 6144, 2048, op="swiglu_gather")
+    assert p["gather_mode"] == 1 and p["bm"] == 64 and p["bn"] in (128, 256)
+    # large groups: two passes, the second being the plain plan (CTA pairs included)
+    plain = rgg.rgg_plan(64, 16384, 1024, 2688)
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="gather")
+    assert p["gather_mode"] == 2 and p["workspace_bytes"] == 16384 * 1024 * 2
+    assert (p["bm"], p["bn"], p["stages"]) == (plain["bm"], plain["bn"], plain["stages"]) == (256, 256, 7)
+    assert plain["gather_mode"] == 0 and plain["workspace_bytes"] == 0
+    # 64 rows per expert: 64-row tiles, but already two-pass; 32 or fewer: fused
+    assert rgg.rgg_plan(32, 2048, 6144, 4096, op="gather")["gather_mode"] == 2
+    assert rgg.rgg_plan(32, 1024, 6144, 4096, op="gather")["gather_mode"] == 1
+    assert rgg.rgg_plan(4, 1024, 256, 256, op="gather", host_counts=[1000, 8, 8, 8])["gather_mode"] == 2
+    assert rgg.rgg_plan(4, 1024, 256, 256, op="gather", host_counts=[30, 0, 0, 0])["gather_mode"] == 1
+    # the fused mode on request: 1-CTA tiles only
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="gather", gather_mode=1)
+    assert p["gather_mode"] == 1 and p["bm"] == 128 and p["workspace_bytes"] == 0
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, op="gather", bm=256)["gather_mode"] == 2
+    for kw in ({"op": "gather", "bm": 256, "gather_mode": 1}, {"op": "swiglu_gather", "bn": 192},
+               {"op": "gather", "gather_mode": 3}):
+        with pytest.raises(rgg.RggError) as ei:
+            rgg.rgg_plan(64, 16384, 1024, 2688, **kw)
+        assert ei.value.status == rgg.RGG_ERR_INVALID_ARG
+
+
+def test_gather_null_handle_is_rejected_without_touching_cuda(lib):
+    P = ctypes.c_void_p
+    for fn in (lib.rgg_grouped_gemm_gather, lib.rgg_grouped_gemm_swiglu_gather):
+        s = fn(None, P(16), 100, P(16), P(16), P(16), P(16), 4, 256, 256, 512, None, None)
+        assert s == rgg.RGG_ERR_INVALID_ARG
