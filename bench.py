@@ -505,7 +505,8 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": round(flops / (launch_ms / 1e3) / 1e12, 1),
                 "peak": tc_peak, "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = measured_traffic(args.workload)
+    # the capture of this exact launch: the workload, and the op when it is not the plain GEMM
+    roof["traffic"] = measured_traffic(args.workload if args.op == "gemm" else args.workload + "+" + args.op)
     roof["peak_source"] = peaks["source"] + (" bf16 x 2 (nominal fp8/bf16 ratio)" if args.op == "fp8" else "")
     roof["algorithmic_per_launch"] = {"flops": flops, "bytes": bytes_}
     roof["launch_ms"] = round(launch_ms, 5)

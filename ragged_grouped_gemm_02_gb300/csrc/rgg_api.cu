@@ -243,7 +243,7 @@ constexpr int kGatherTwoPass = 2;  // a row-gather kernel into a workspace, then
 
 int64_t gather_workspace_bytes(int64_t M_tot, int K) { return M_tot * static_cast<int64_t>(K) * 2; }
 
-constexpr double kFusedGatherMaxRows = 32.0;
+constexpr double kFusedGatherMaxRows = 24.0;
 
 // The caller's mode, else: fused when the experts that have rows average at
 // most kFusedGatherMaxRows of them (the few gathered rows per tile hide under
@@ -251,8 +251,9 @@ constexpr double kFusedGatherMaxRows = 32.0;
 // 128-byte copy repeated for every N tile, and on a GB300 such fetches top
 // out near 1.8 TB/s per GPU, a third of what whole-tile boxes reach; gathering
 // each routed row once and multiplying with whole-tile boxes wins as soon as
-// tiles hold more than a few dozen rows (measured: 16 rows per expert, fused
-// 2% faster; 64 rows, two-pass 29% faster).
+// tiles hold more than a couple of dozen rows (measured with 32 experts,
+// K = 6144, N = 4096: fused faster at 1 to 16 rows per expert, by 2% at 16;
+// two-pass faster at 32 rows, by 3%, and at 64, by 29%).
 rgg_status choose_gather_mode(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N,
                               const rgg_options* opt, bool swiglu, int* mode) {
     const int want = opt ? opt->gather_mode : 0;

@@ -190,11 +190,11 @@ def test_plan_gather_modes(lib):
     assert p["gather_mode"] == 2 and p["workspace_bytes"] == 16384 * 1024 * 2
     assert (p["bm"], p["bn"], p["stages"]) == (plain["bm"], plain["bn"], plain["stages"]) == (256, 256, 7)
     assert plain["gather_mode"] == 0 and plain["workspace_bytes"] == 0
-    # 64 rows per expert: 64-row tiles, but already two-pass; 32 or fewer: fused
-    assert rgg.rgg_plan(32, 2048, 6144, 4096, op="gather")["gather_mode"] == 2
-    assert rgg.rgg_plan(32, 1024, 6144, 4096, op="gather")["gather_mode"] == 1
+    # 32 rows per expert: 64-row tiles, but already two-pass; 16 or fewer: fused
+    assert rgg.rgg_plan(32, 1024, 6144, 4096, op="gather")["gather_mode"] == 2
+    assert rgg.rgg_plan(32, 512, 6144, 4096, op="gather")["gather_mode"] == 1
     assert rgg.rgg_plan(4, 1024, 256, 256, op="gather", host_counts=[1000, 8, 8, 8])["gather_mode"] == 2
-    assert rgg.rgg_plan(4, 1024, 256, 256, op="gather", host_counts=[30, 0, 0, 0])["gather_mode"] == 1
+    assert rgg.rgg_plan(4, 1024, 256, 256, op="gather", host_counts=[20, 0, 0, 0])["gather_mode"] == 1
     # the fused mode on request: 1-CTA tiles only
     p = rgg.rgg_plan(64, 16384, 1024, 2688, op="gather", gather_mode=1)
     assert p["gather_mode"] == 1 and p["bm"] == 128 and p["workspace_bytes"] == 0
