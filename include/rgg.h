@@ -69,8 +69,10 @@ typedef struct rgg_options {
     int debug_flags;             /* 0 in normal use.  RGG_DEBUG_PRODUCER_STALL makes the load pipeline issue
                                     nothing, so the first MMA wait can only end by its time limit: a test of the
                                     bounded waits, which then report RGG_ERR_DEVICE_TIMEOUT */
-    int tail64;                  /* 128-row tiles: 0 = auto (on), 1 = on, -1 = off.  A tile that holds the last
-                                    <= 64 rows of its expert runs as a 64-row MMA with a 64-row X box */
+    int tail64;                  /* tail tiles: 0 = auto (on), 1 = on, -1 = off.  With 128-row tiles a tile
+                                    that holds the last <= 64 rows of its expert runs as a 64-row MMA
+                                    with a 64-row X box; with CTA-pair (256-row) tiles one that holds
+                                    the last <= 128 rows runs as a 128-row pair MMA, 64 rows per CTA */
     int op;                      /* for rgg_plan only: 0 = plan rgg_grouped_gemm, 1 = plan
                                     rgg_grouped_gemm_swiglu (then N is the output width), 2 = plan
                                     rgg_grouped_gemm_fp8, 3 = plan rgg_grouped_gemm_gather, 4 = plan
@@ -80,7 +82,7 @@ typedef struct rgg_options {
                                     show a strong skew), 1 = front/back interleave, 2 = strided scatter,
                                     3 = front/back interleave over the experts sorted by row count (E <= 256;
                                     chosen automatically when the largest expert holds over four times the
-                                    mean).  1-CTA kernels only. */
+                                    mean). */
     int gather_mode;             /* gather calls only: how the routed rows are fetched (same result either
                                     way).  1 = fused: the GEMM's producer loads them with TMA
                                     tile::gather4, four rows per copy, once per N tile; 2 = two-pass: a
@@ -107,7 +109,7 @@ typedef struct rgg_plan_info {
     int smem_bytes;              /* dynamic shared memory per CTA */
     int tmem_cols;               /* TMEM columns allocated per CTA (two accumulator buffers) */
     int64_t max_tiles;           /* upper bound on the flat tile count for these sizes */
-    int tail64;                  /* 1 when tail tiles of <= 64 rows run as 64-row MMAs */
+    int tail64;                  /* 1 when tail tiles run as shorter MMAs (see rgg_options.tail64) */
     int walk_order;              /* walk order (see rgg_options) */
     int gather_mode;             /* gather ops: 1 = fused tile::gather4, 2 = two-pass; else 0 */
     int64_t workspace_bytes;     /* two-pass gather: workspace the call needs; else 0 */

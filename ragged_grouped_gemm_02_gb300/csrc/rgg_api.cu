@@ -193,12 +193,11 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         bn = best_bn;
     }
     const bool pair = (bm == 256);
-    if (pair && want_walk != 0) return RGG_ERR_INVALID_ARG;  // the pair kernel walks in list order
     // Walk order: with the counts known and a strong skew (the largest expert
     // holding over four times the mean of the busy experts), the size-sorted
     // interleave runs tiles of big experts beside tiles of small ones.
     int walk = want_walk;
-    if (walk == 0 && !pair && opt && opt->host_counts && E <= rgg::kMaxSortedExperts) {
+    if (walk == 0 && opt && opt->host_counts && E <= rgg::kMaxSortedExperts) {
         int64_t mx = 0;
         for (int e = 0; e < E; ++e) mx = std::max<int64_t>(mx, opt->host_counts[e]);
         if (avg > 0.0 && static_cast<double>(mx) > 4.0 * avg) walk = 3;
@@ -232,7 +231,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
                      : static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(grid_cap, max_tiles)));
     out->smem_bytes = smem;
     out->max_tiles = max_tiles;
-    out->tail64 = (bm == 128 && want_tail != -1) ? 1 : 0;
+    out->tail64 = ((bm == 128 || bm == 256) && want_tail != -1) ? 1 : 0;
     out->walk_order = walk;
     return RGG_OK;
 }
@@ -556,7 +555,7 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
     a.tail64 = p.tail64;
     a.walk_order = p.walk_order;
 
-    cudaError_t err = (p.bm == 256)   ? rgg::launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tw, a)
+    cudaError_t err = (p.bm == 256)   ? rgg::launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
                       : (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
                                       : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm launch");

@@ -35,8 +35,17 @@ struct PairConfig {
     static constexpr int kPanels = kHalfN / 64;
     static constexpr uint32_t kTmemCols = 512;      // two BN-column fp32 buffers (BN <= 256)
     static constexpr uint32_t kStageBytesPerCta = static_cast<uint32_t>((128 + kHalfN) * kBK * 2);
+    static constexpr uint32_t kStageBytesPerCta64 = static_cast<uint32_t>((64 + kHalfN) * kBK * 2);
     static constexpr uint32_t kIdesc = idesc_bf16_f32(256, BN, /*b_mn_major=*/true);
+    static constexpr uint32_t kIdesc128 = idesc_bf16_f32(128, BN, /*b_mn_major=*/true);  // 64 rows per CTA
 };
+
+// A pair tile whose rows are the last <= 128 of its expert runs as an M = 128
+// pair MMA (args.tail64): each CTA loads and computes 64 rows, which halves
+// the padded MMA work of small experts while the tile list stays the same.
+__device__ __forceinline__ bool pair_runs_as_128_rows(const GemmArgs& args, const TileCoord& c) {
+    return args.tail64 != 0 && c.rows <= 128;
+}
 
 __device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                    uint32_t peer_flag_cluster, int32_t* status, uint64_t timeout_ns) {
@@ -62,8 +71,8 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 
 template <int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                             const GemmArgs args) {
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
+                             const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
     using Cfg = PairConfig<BN>;
     constexpr int BM = 256;  // rows per pair tile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -79,7 +88,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const SmemPlan sp = smem_plan(128, Cfg::kHalfN, S, E);
+    const SmemPlan sp = smem_plan(128, Cfg::kHalfN, S, E, args.walk_order == 3);
     const uint32_t a0 = base + sp.a_off;
     const uint32_t b0 = base + sp.b_off;
     const uint32_t bars = base + sp.bar_off;
@@ -91,6 +100,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + sp.misc_off);
     int32_t* s_off = reinterpret_cast<int32_t*>(gbase + sp.off_off);
     int32_t* s_pre = reinterpret_cast<int32_t*>(gbase + sp.pre_off);
+    int32_t* s_order = reinterpret_cast<int32_t*>(gbase + sp.ord_off);  // walk order 3 only
+    int32_t* s_spre = reinterpret_cast<int32_t*>(gbase + sp.spre_off);
 
     // S1, identical in both CTAs, so every early exit below is pair-uniform.
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
@@ -100,6 +111,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
     __syncthreads();
     const int32_t T = s_pre[E];
+    if (args.walk_order == 3) build_size_order(s_off, s_order, s_spre, E, BM, args.n_tiles_n);
     if (static_cast<int32_t>(pair) >= T) return;
 
     if (threadIdx.x == 32) {
@@ -132,6 +144,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t peer_flag = map_to_rank(smem_addr(&misc[1]), rank ^ 1u);
     const int KB = args.num_k_blocks;
     const int nN = args.n_tiles_n;
+    const int WO = args.walk_order;  // walk position t visits tile walk_tile(t, ...), the same in both CTAs
+    const int32_t WS = walk_stride_for(T);
+    auto tile_at = [&](int32_t p) -> TileCoord {
+        const int32_t t = walk_tile(p, T, WO, WS);
+        return WO == 3 ? decode_sorted_tile(s_off, s_order, s_spre, E, BM, BN, nN, t)
+                       : decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+    };
 
     if (warp == 0) {
         // ---------------------------------------------------- S4: TMA producer
@@ -141,9 +160,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t issued = 0;
             bool ok = true;
             for (int32_t t = pair; ok && t < T; t += npairs) {
-                const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
-                const int32_t a_row = c.row0 + 128 * static_cast<int32_t>(rank);
+                const TileCoord c = tile_at(t);
+                const bool half = pair_runs_as_128_rows(args, c);
+                const int32_t a_row = c.row0 + (half ? 64 : 128) * static_cast<int32_t>(rank);
                 const int32_t b_col = c.col0 + Cfg::kHalfN * static_cast<int32_t>(rank);
+                const CUtensorMap* xmap = half ? &tmap_x64 : &tmap_x;
+                const uint32_t tx_bytes = 2u * (half ? Cfg::kStageBytesPerCta64 : Cfg::kStageBytesPerCta);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!pair_wait_or_abort(empty_bar(st), ph ^ 1u, abort_flag, peer_flag, args.status,
                                             args.timeout_ns)) {
@@ -151,8 +173,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t full_leader = map_to_rank(full_bar(st), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(st), 2u * Cfg::kStageBytesPerCta);
-                    tma_load_2d_pair(a0 + st * sp.a_stage, &tmap_x, full_leader, kb * kBK, a_row);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(st), tx_bytes);
+                    tma_load_2d_pair(a0 + st * sp.a_stage, xmap, full_leader, kb * kBK, a_row);
 #pragma unroll
                     for (int p = 0; p < Cfg::kPanels; ++p)
                         tma_load_3d_pair(b0 + st * sp.b_stage + p * kPanelBytes, &tmap_w, full_leader, b_col + 64 * p,
@@ -187,6 +209,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t acc_ph = 0;
             bool ok = true;
             for (int32_t t = pair; ok && t < T; t += npairs) {
+                const uint32_t idesc =
+                    pair_runs_as_128_rows(args, tile_at(t)) ? Cfg::kIdesc128
+                                                                                              : Cfg::kIdesc;
                 if (!pair_wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, peer_flag, args.status,
                                         args.timeout_ns)) {
                     ok = false;
@@ -206,7 +231,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < kBK / 16; ++j) {
                         const uint64_t ad = sw128_desc(a_st + 32u * j, 16u, 1024u);
                         const uint64_t bd = sw128_desc(b_st + 2048u * j, kPanelBytes, 1024u);
-                        mma_bf16_ss_pair(d_tmem, ad, bd, Cfg::kIdesc, (kb | j) != 0 ? 1u : 0u);
+                        mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
                     }
                     mma_commit_pair(empty_bar(st), 0x3);
                     if (++st == S) {
@@ -230,28 +255,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------- S6: epilogue
         const int q = warp & 3;
-        const int r_local = 128 * static_cast<int>(rank) + q * 32 + lane;
         const int N = args.N;
         int acc = 0;
         uint32_t acc_ph = 0;
         for (int32_t t = pair; t < T; t += npairs) {
-            const TileCoord c = decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+            const TileCoord c = tile_at(t);
             bool ok = pair_wait_or_abort(accf_bar(acc), acc_ph, abort_flag, peer_flag, args.status, args.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            // M = 256: this CTA's 128 rows, one per TMEM lane, all BN columns.
+            // M = 128: this CTA's 64 rows fill the 128 lanes twice over (GB300
+            // layout, probed with one-hot operands): lane L < 64 holds row L,
+            // columns [0, BN/2); lane 64 + L holds row L, columns [BN/2, BN);
+            // both in TMEM columns [0, BN/2).
+            const bool half = pair_runs_as_128_rows(args, c);
+            const int r_local = half ? 64 * static_cast<int>(rank) + 32 * (q & 1) + lane
+                                     : 128 * static_cast<int>(rank) + q * 32 + lane;
+            const int ncols = half ? BN / 2 : BN;
+            const int cbase = half ? (q >> 1) * (BN / 2) : 0;  // first tile column this warp holds
             const bool row_ok = r_local < c.rows;
-            __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0;
+            __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0 + cbase;
 #pragma unroll 1
-            for (int cc = 0; cc < BN; cc += 32) {
+            for (int cc = 0; cc < ncols; cc += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
                 tmem_ld_wait();
                 if (row_ok) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int col = c.col0 + cc + 16 * h;
+                        const int col = c.col0 + cbase + cc + 16 * h;
                         uint32_t w[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);

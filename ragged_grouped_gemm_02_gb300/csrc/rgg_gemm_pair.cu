@@ -6,21 +6,22 @@ namespace rgg {
 
 template <int BN>
 static cudaError_t launch_pair_instance(int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
-                                        const CUtensorMap& tmap_w, const GemmArgs& args) {
+                                        const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w,
+                                        const GemmArgs& args) {
     auto kernel = grouped_gemm_pair_kernel<BN>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kernel<<<grid, kThreads, smem, stream>>>(tmap_x, tmap_w, args);
+    kernel<<<grid, kThreads, smem, stream>>>(tmap_x, tmap_x64, tmap_w, args);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_pair(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
-                             const CUtensorMap& tmap_w, const GemmArgs& args) {
+                             const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args) {
     if (grid % 2 != 0) return cudaErrorInvalidValue;
     switch (bn) {
-        case 128: return launch_pair_instance<128>(grid, smem, stream, tmap_x, tmap_w, args);
-        case 256: return launch_pair_instance<256>(grid, smem, stream, tmap_x, tmap_w, args);
+        case 128: return launch_pair_instance<128>(grid, smem, stream, tmap_x, tmap_x64, tmap_w, args);
+        case 256: return launch_pair_instance<256>(grid, smem, stream, tmap_x, tmap_x64, tmap_w, args);
         default: return cudaErrorInvalidValue;
     }
 }

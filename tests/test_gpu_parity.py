@@ -120,7 +120,7 @@ def test_integer_inputs_bit_exact_modes(bm, bn, tail64):
     _assert_untouched(Y, slice(M_used, None))
 
 
-@pytest.mark.parametrize("bm,bn", SHAPES)
+@pytest.mark.parametrize("bm,bn", SHAPES + PAIR_SHAPES)
 @pytest.mark.parametrize("walk_order", [1, 2, 3])
 def test_integer_inputs_bit_exact_walk_orders(bm, bn, walk_order):
     # any walk over the tile list visits every tile exactly once
