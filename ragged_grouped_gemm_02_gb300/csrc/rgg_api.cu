@@ -106,6 +106,11 @@ rgg_status check_sizes(int E, int64_t M_tot, int K, int N) {
 constexpr int kPlanNoPair = 1;
 constexpr int kPlanNoBn192 = 2;
 constexpr int kPlanFused = kPlanNoPair | kPlanNoBn192;
+// The fused gate-up op on CTA pairs: measured faster only for large groups
+// (prefill, ~1 024 rows per expert: 1 400-1 500 vs 1 385 TFLOP/s) and slower at
+// 256 rows per expert (uniform: 856 vs 918), so pairs need >= 512 rows per busy expert.
+constexpr int kPlanPairsLargeGroupsOnly = 8;
+constexpr double kPairMinAvgRows = 512.0;
 
 rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N, const rgg_options* opt,
                      Plan* out, int kind = 0) {
@@ -173,6 +178,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         for (int cbm : {256, 128, 64}) {
             if (bm != 0 && cbm != bm) continue;
             if (no_pair && cbm == 256) continue;
+            if ((kind & kPlanPairsLargeGroupsOnly) && cbm == 256 && bm == 0 && avg < kPairMinAvgRows) continue;
             if (bm == 0 && cbm == 64) continue;  // 64-row tiles only for small groups (above)
             const bool cpair = (cbm == 256);
             const int cunits = cpair ? std::max(1, grid_cap / 2) : grid_cap;
@@ -493,8 +499,13 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
         rgg_status sm = choose_gather_mode(num_sms, smem_optin, E, M_tot, K, N, opt, swiglu, &mode);
         if (sm != RGG_OK) return sm;
     }
-    // the two-pass gather runs the plain (or fused gate-up) kernel on the gathered rows
-    const int kind = (op == 0 || (op == 3 && mode == kGatherTwoPass)) ? 0 : (op == 3) ? kPlanNoPair : kPlanFused;
+    // the two-pass gather runs the plain (or fused gate-up) kernel on the gathered rows; the fused
+    // gate-up op takes CTA pairs but not BN = 192; FP8 and the fused gather take 1-CTA tiles only
+    const bool fused_gather = gather && mode == kGatherFused;
+    const int kind = (op == 2 || (op == 4 && fused_gather)) ? kPlanFused
+                     : (op == 3 && fused_gather)           ? kPlanNoPair
+                     : swiglu                              ? (kPlanNoBn192 | kPlanPairsLargeGroupsOnly)
+                                                           : 0;
     rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, swiglu ? 2 * N : N, opt, &p, kind);
     if (s != RGG_OK) return s;
     out->bm = p.bm;
@@ -508,6 +519,7 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->max_tiles = p.max_tiles;
     out->tail64 = p.tail64;
     out->walk_order = p.walk_order;
+    if (swiglu && p.bm == 256) out->tail64 = 0;  // fused gate-up pairs keep 256-row tail tiles
     out->gather_mode = mode;
     out->workspace_bytes = (mode == kGatherTwoPass) ? gather_workspace_bytes(M_tot, K) : 0;
     return RGG_OK;
@@ -579,7 +591,7 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
         return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
     }
     Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, kPlanFused);
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, kPlanNoBn192 | kPlanPairsLargeGroupsOnly);
     if (s != RGG_OK) return s;
     CUtensorMap tx, tx64, tw;
     s = encode_maps(X, W13, E, M_tot, K, 2 * N, p.bm, &tx, &tx64, &tw);
@@ -600,7 +612,9 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
     a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
     a.tail64 = p.tail64;
     a.walk_order = p.walk_order;
-    cudaError_t err = rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    if (p.bm == 256) a.tail64 = 0;  // the pair's 128-row tail layout splits gate and up across warps
+    cudaError_t err = (p.bm == 256) ? rgg::launch_gemm_pair_swiglu(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+                                    : rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_swiglu launch");
 }
 

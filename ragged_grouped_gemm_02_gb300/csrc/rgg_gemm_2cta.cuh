@@ -69,12 +69,19 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
     }
 }
 
-template <int BN>
+// kEpi = kEpiSwiGLU: the fused gate-up projection on a pair.  A tile covers
+// BN/2 output columns; CTA 0 loads the BN/2 gate columns and CTA 1 the
+// matching BN/2 up columns as the two halves of B, so the M = 256 MMA leaves
+// [gate | up] side by side in each CTA's TMEM for that CTA's 128 rows, and the
+// epilogue writes silu(gate) * up.  Tail tiles run at M = 256 in this mode.
+template <int BN, int kEpi = kEpiPlain>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
                              const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
     using Cfg = PairConfig<BN>;
     constexpr int BM = 256;  // rows per pair tile
+    constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;  // output columns per tile
+    auto half_tile = [&](const TileCoord& c) { return kEpi == kEpiPlain && pair_runs_as_128_rows(args, c); };
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
     const int warp = threadIdx.x >> 5;
@@ -148,8 +155,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int32_t WS = walk_stride_for(T);
     auto tile_at = [&](int32_t p) -> TileCoord {
         const int32_t t = walk_tile(p, T, WO, WS);
-        return WO == 3 ? decode_sorted_tile(s_off, s_order, s_spre, E, BM, BN, nN, t)
-                       : decode_tile(s_off, s_pre, E, BM, BN, nN, t);
+        return WO == 3 ? decode_sorted_tile(s_off, s_order, s_spre, E, BM, kOutN, nN, t)
+                       : decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
     };
 
     if (warp == 0) {
@@ -161,9 +168,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int32_t t = pair; ok && t < T; t += npairs) {
                 const TileCoord c = tile_at(t);
-                const bool half = pair_runs_as_128_rows(args, c);
+                const bool half = half_tile(c);
                 const int32_t a_row = c.row0 + (half ? 64 : 128) * static_cast<int32_t>(rank);
-                const int32_t b_col = c.col0 + Cfg::kHalfN * static_cast<int32_t>(rank);
+                // plain: this CTA's half of the tile's columns; SwiGLU: the gate (CTA 0) or up (CTA 1) columns
+                const int32_t b_col = (kEpi == kEpiSwiGLU) ? c.col0 + (rank ? args.N : 0)
+                                                           : c.col0 + Cfg::kHalfN * static_cast<int32_t>(rank);
                 const CUtensorMap* xmap = half ? &tmap_x64 : &tmap_x;
                 const uint32_t tx_bytes = 2u * (half ? Cfg::kStageBytesPerCta64 : Cfg::kStageBytesPerCta);
                 for (int kb = 0; kb < KB; ++kb) {
@@ -210,7 +219,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int32_t t = pair; ok && t < T; t += npairs) {
                 const uint32_t idesc =
-                    pair_runs_as_128_rows(args, tile_at(t)) ? Cfg::kIdesc128
+                    half_tile(tile_at(t)) ? Cfg::kIdesc128
                                                                                               : Cfg::kIdesc;
                 if (!pair_wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, peer_flag, args.status,
                                         args.timeout_ns)) {
@@ -270,10 +279,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // layout, probed with one-hot operands): lane L < 64 holds row L,
             // columns [0, BN/2); lane 64 + L holds row L, columns [BN/2, BN);
             // both in TMEM columns [0, BN/2).
-            const bool half = pair_runs_as_128_rows(args, c);
+            const bool half = half_tile(c);
             const int r_local = half ? 64 * static_cast<int>(rank) + 32 * (q & 1) + lane
                                      : 128 * static_cast<int>(rank) + q * 32 + lane;
-            const int ncols = half ? BN / 2 : BN;
+            const int ncols = half ? BN / 2 : kOutN;
             const int cbase = half ? (q >> 1) * (BN / 2) : 0;  // first tile column this warp holds
             const bool row_ok = r_local < c.rows;
             __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0 + cbase;
@@ -281,7 +290,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < ncols; cc += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
-                tmem_ld_wait();
+                if constexpr (kEpi == kEpiSwiGLU) {
+                    // gate in columns [cc, cc+32), up in [kOutN + cc, kOutN + cc + 32)
+                    uint32_t u[32];
+                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kOutN + cc), u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __float_as_uint(silu_f32(__uint_as_float(v[i])) * __uint_as_float(u[i]));
+                } else {
+                    tmem_ld_wait();
+                }
                 if (row_ok) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {

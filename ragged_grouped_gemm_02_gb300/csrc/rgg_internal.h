@@ -49,6 +49,9 @@ cudaError_t launch_gather_rows(const void* xtok, const int32_t* row_index, const
 // `grid` is even.
 cudaError_t launch_gemm_pair(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                              const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
+// The same with the fused gate-up + SiLU epilogue (tmap_w spans 2N columns; tail tiles stay M = 256).
+cudaError_t launch_gemm_pair_swiglu(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
+                                    const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 
 // The flat tile list written out by the same device code the GEMM uses.
 cudaError_t launch_export_tiles(const int32_t* offsets, int E, int64_t M_tot, int N, int bm, int bn,

@@ -211,3 +211,19 @@ def test_gather_null_handle_is_rejected_without_touching_cuda(lib):
     for fn in (lib.rgg_grouped_gemm_gather, lib.rgg_grouped_gemm_swiglu_gather):
         s = fn(None, P(16), 100, P(16), P(16), P(16), P(16), 4, 256, 256, 512, None, None)
         assert s == rgg.RGG_ERR_INVALID_ARG
+
+
+def test_plan_fused_gate_up_takes_pairs_without_tails(lib):
+    # balanced large groups: CTA pairs, 256-row tail tiles (the 128-row pair
+    # tail layout would split gate and up across warps); BN = 192 is refused
+    p = rgg.rgg_plan(32, 32768, 6144, 2048, op="swiglu")
+    assert p["bm"] == 256 and p["bn"] in (128, 256) and p["tail64"] == 0
+    # ... but not below 512 rows per expert, where the 1-CTA tiles measured faster
+    assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu")["bm"] == 128
+    assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", bm=256)["bm"] == 256
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, op="gemm", bm=256)["tail64"] == 1
+    assert rgg.rgg_plan(32, 512, 6144, 2048, op="swiglu")["bm"] == 64
+    with pytest.raises(rgg.RggError):
+        rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", bn=192)
+    # FP8 stays on 1-CTA tiles
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8")["bm"] == 128

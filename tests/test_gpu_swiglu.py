@@ -21,7 +21,8 @@ pytestmark = pytest.mark.gpu
 
 CANARY = 0x7FC1
 RTOL = 1e-2
-SHAPES = [(64, 128), (64, 256), (128, 128), (128, 256)]
+SHAPES = [(64, 128), (64, 256), (128, 128), (128, 256),
+          pytest.param(256, 128, marks=pytest.mark.pair), pytest.param(256, 256, marks=pytest.mark.pair)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -86,7 +87,7 @@ def test_bad_offsets_rejected():
     assert bool((H.view(torch.int16) == CANARY).all())
 
 
-@pytest.mark.parametrize("name", ["decode", "prefill"])
+@pytest.mark.parametrize("name", ["decode", "uniform", "prefill"])
 def test_full_size_sampled(name):
     # the workload's weights read as W13 = [gate | up] with N/2 output columns
     inp = wl.make_inputs(name)
