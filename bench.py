@@ -279,13 +279,20 @@ def run_profile(args):
     elif args.op == "gemm":
         def launch():
             rgg.rgg_grouped_gemm(X, W, off, Y, **opts)
+    elif args.op == "fp8":
+        X8, W8, sx, sw = wl.quantize_fp8(inp.X, inp.W)
+        X8, W8, sx, sw = X8.to(dev), W8.to(dev), sx.to(dev), sw.to(dev)
+        del X, W
+
+        def launch():
+            rgg.rgg_grouped_gemm_fp8(X8, W8, sx, sw, off, Y, **opts)
     else:
-        raise SystemExit("--profile covers --op gemm and --op gather")
+        raise SystemExit("--profile covers --op gemm, gather and fp8")
     for _ in range(args.warmup + 1):
         launch()
     torch.cuda.synchronize(dev)
     status = rgg.rgg_query_status(0)
-    plan = rgg.rgg_plan(inp.workload.E, X.shape[0], inp.workload.K, inp.workload.N, op=args.op, **opts)
+    plan = rgg.rgg_plan(inp.workload.E, inp.X.shape[0], inp.workload.K, inp.workload.N, op=args.op, **opts)
     print(json.dumps({"profile": args.workload, "launches": args.warmup + 1, "status": status, "plan": plan}))
     if status != rgg.RGG_OK:
         raise SystemExit(1)

@@ -106,11 +106,6 @@ rgg_status check_sizes(int E, int64_t M_tot, int K, int N) {
 constexpr int kPlanNoPair = 1;
 constexpr int kPlanNoBn192 = 2;
 constexpr int kPlanFused = kPlanNoPair | kPlanNoBn192;
-// The fused gate-up op on CTA pairs: measured faster only for large groups
-// (prefill, ~1 024 rows per expert: 1 400-1 500 vs 1 385 TFLOP/s) and slower at
-// 256 rows per expert (uniform: 856 vs 918), so pairs need >= 512 rows per busy expert.
-constexpr int kPlanPairsLargeGroupsOnly = 8;
-constexpr double kPairMinAvgRows = 512.0;
 
 rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N, const rgg_options* opt,
                      Plan* out, int kind = 0) {
@@ -178,7 +173,6 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         for (int cbm : {256, 128, 64}) {
             if (bm != 0 && cbm != bm) continue;
             if (no_pair && cbm == 256) continue;
-            if ((kind & kPlanPairsLargeGroupsOnly) && cbm == 256 && bm == 0 && avg < kPairMinAvgRows) continue;
             if (bm == 0 && cbm == 64) continue;  // 64-row tiles only for small groups (above)
             const bool cpair = (cbm == 256);
             const int cunits = cpair ? std::max(1, grid_cap / 2) : grid_cap;
@@ -504,7 +498,7 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     const bool fused_gather = gather && mode == kGatherFused;
     const int kind = (op == 2 || (op == 4 && fused_gather)) ? kPlanFused
                      : (op == 3 && fused_gather)           ? kPlanNoPair
-                     : swiglu                              ? (kPlanNoBn192 | kPlanPairsLargeGroupsOnly)
+                     : swiglu                              ? kPlanNoBn192
                                                            : 0;
     rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, swiglu ? 2 * N : N, opt, &p, kind);
     if (s != RGG_OK) return s;
@@ -513,7 +507,8 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->bk = (op == 2) ? 128 : rgg::kBK;
     out->stages = p.stages;
     out->grid = p.grid;
-    out->threads = rgg::kThreads;
+    // FP8 and the fused gate-up op run eight epilogue warps (on CTA pairs: per CTA)
+    out->threads = (op == 2 || swiglu) ? rgg::cta_threads<rgg::kEpiSwiGLU, false>() : rgg::kThreads;
     out->smem_bytes = p.smem_bytes;
     out->tmem_cols = (p.bm == 256 || 2 * p.bn > 256) ? 512 : 256;
     out->max_tiles = p.max_tiles;
@@ -591,7 +586,7 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
         return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
     }
     Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, kPlanNoBn192 | kPlanPairsLargeGroupsOnly);
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, kPlanNoBn192);
     if (s != RGG_OK) return s;
     CUtensorMap tx, tx64, tw;
     s = encode_maps(X, W13, E, M_tot, K, 2 * N, p.bm, &tx, &tx64, &tw);

@@ -12,7 +12,7 @@ static cudaError_t launch_pair_instance(int grid, size_t smem, cudaStream_t stre
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kernel<<<grid, kThreads, smem, stream>>>(tmap_x, tmap_x64, tmap_w, args);
+    kernel<<<grid, 64 + 32 * pair_epilogue_warps<kEpi>(), smem, stream>>>(tmap_x, tmap_x64, tmap_w, args);
     return cudaGetLastError();
 }
 

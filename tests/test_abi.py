@@ -218,12 +218,18 @@ def test_plan_fused_gate_up_takes_pairs_without_tails(lib):
     # tail layout would split gate and up across warps); BN = 192 is refused
     p = rgg.rgg_plan(32, 32768, 6144, 2048, op="swiglu")
     assert p["bm"] == 256 and p["bn"] in (128, 256) and p["tail64"] == 0
-    # ... but not below 512 rows per expert, where the 1-CTA tiles measured faster
-    assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu")["bm"] == 128
-    assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", bm=256)["bm"] == 256
+    assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu")["bm"] == 256
     assert rgg.rgg_plan(64, 16384, 1024, 2688, op="gemm", bm=256)["tail64"] == 1
     assert rgg.rgg_plan(32, 512, 6144, 2048, op="swiglu")["bm"] == 64
     with pytest.raises(rgg.RggError):
         rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", bn=192)
     # FP8 stays on 1-CTA tiles
     assert rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8")["bm"] == 128
+
+
+def test_plan_reports_the_launch_block_size(lib):
+    # plain bf16 and CTA pairs: 6 warps; FP8 and the fused gate-up op on 1-CTA tiles: 10
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, bm=128)["threads"] == 192
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8")["threads"] == 320
+    assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", bm=128)["threads"] == 320
+    assert rgg.rgg_plan(32, 32768, 6144, 2048, op="swiglu")["threads"] == 320  # pairs, per CTA
