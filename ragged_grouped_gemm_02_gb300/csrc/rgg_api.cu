@@ -106,11 +106,17 @@ rgg_status check_sizes(int E, int64_t M_tot, int K, int N) {
 constexpr int kPlanNoPair = 1;
 constexpr int kPlanNoBn192 = 2;
 constexpr int kPlanFused = kPlanNoPair | kPlanNoBn192;
+constexpr int kPlanPairBn256 = 16;  // CTA pairs only with BN = 256 (FP8: 128-column weight panels)
+// CTA pairs only when asked for (bm = 256): FP8 pairs measured slower than 128 x 256 tiles on every
+// benchmark shape (uniform 1 191 vs 1 390 TFLOP/s, skew16k 1 069 vs 1 291, prefill 2 714 vs 2 775).
+constexpr int kPlanPairOnRequest = 32;
 
 rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N, const rgg_options* opt,
                      Plan* out, int kind = 0) {
     const bool no_pair = (kind & kPlanNoPair) != 0;
     const bool no_192 = (kind & kPlanNoBn192) != 0;
+    const bool pair_256 = (kind & kPlanPairBn256) != 0;
+    const bool pair_on_request = (kind & kPlanPairOnRequest) != 0;
     rgg_status s = check_sizes(E, M_tot, K, N);
     if (s != RGG_OK) return s;
     if (num_sms <= 0) num_sms = kDefaultSms;
@@ -123,6 +129,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (want_bn != 0 && want_bn != 128 && want_bn != 192 && want_bn != 256) return RGG_ERR_INVALID_ARG;
     if (want_bm == 256 && want_bn == 192) return RGG_ERR_INVALID_ARG;  // pair tiles split BN in whole panels
     if ((no_pair && want_bm == 256) || (no_192 && want_bn == 192)) return RGG_ERR_INVALID_ARG;
+    if (pair_256 && want_bm == 256 && want_bn != 0 && want_bn != 256) return RGG_ERR_INVALID_ARG;
     if (want_stages != 0 && (want_stages < 2 || want_stages > rgg::kMaxStages)) return RGG_ERR_INVALID_ARG;
     if (max_ctas < 0) return RGG_ERR_INVALID_ARG;
     const int want_tail = opt ? opt->tail64 : 0;
@@ -173,6 +180,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         for (int cbm : {256, 128, 64}) {
             if (bm != 0 && cbm != bm) continue;
             if (no_pair && cbm == 256) continue;
+            if (pair_on_request && cbm == 256 && want_bm != 256) continue;
             if (bm == 0 && cbm == 64) continue;  // 64-row tiles only for small groups (above)
             const bool cpair = (cbm == 256);
             const int cunits = cpair ? std::max(1, grid_cap / 2) : grid_cap;
@@ -180,6 +188,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
             for (int cbn : {256, 192, 128}) {
                 if (bn != 0 && cbn != bn) continue;
                 if ((cpair || no_192) && cbn == 192) continue;
+                if (cpair && pair_256 && cbn != 256) continue;
                 const int64_t waves = ceil_div(mt * ceil_div(N, cbn), cunits);
                 const double cost = static_cast<double>(waves) * (cbn + 64) * (cpair ? 0.87 : 1.0);
                 if (cost < best) {
@@ -345,7 +354,7 @@ rgg_status encode_maps_fp8(const void* X8, const void* W8, int E, int64_t M_tot,
     const cuuint64_t xdims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M_tot)};
     const cuuint64_t xstrides[1] = {static_cast<cuuint64_t>(K)};
     const cuuint32_t estr2[2] = {1, 1};
-    const cuuint32_t xbox[2] = {128, static_cast<cuuint32_t>(bm)};
+    const cuuint32_t xbox[2] = {128, static_cast<cuuint32_t>(bm > 128 ? 128 : bm)};  // a pair CTA holds 128 rows
     const cuuint32_t xbox64[2] = {128, 64};
     const cuuint64_t wdims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(E)};
     const cuuint64_t wstrides[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(N) * K};
@@ -496,7 +505,8 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     // the two-pass gather runs the plain (or fused gate-up) kernel on the gathered rows; the fused
     // gate-up op takes CTA pairs but not BN = 192; FP8 and the fused gather take 1-CTA tiles only
     const bool fused_gather = gather && mode == kGatherFused;
-    const int kind = (op == 2 || (op == 4 && fused_gather)) ? kPlanFused
+    const int kind = (op == 2)                             ? (kPlanNoBn192 | kPlanPairBn256 | kPlanPairOnRequest)
+                     : (op == 4 && fused_gather)           ? kPlanFused
                      : (op == 3 && fused_gather)           ? kPlanNoPair
                      : swiglu                              ? kPlanNoBn192
                                                            : 0;
@@ -508,7 +518,7 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->stages = p.stages;
     out->grid = p.grid;
     // FP8 and the fused gate-up op run eight epilogue warps (on CTA pairs: per CTA)
-    out->threads = (op == 2 || swiglu) ? rgg::cta_threads<rgg::kEpiSwiGLU, false>() : rgg::kThreads;
+    out->threads = (op == 2 || swiglu) ? rgg::cta_threads<rgg::kEpiSwiGLU, false>() : rgg::kThreads;  // 320 or 192
     out->smem_bytes = p.smem_bytes;
     out->tmem_cols = (p.bm == 256 || 2 * p.bn > 256) ? 512 : 256;
     out->max_tiles = p.max_tiles;
@@ -632,7 +642,8 @@ rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, c
         return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
     }
     Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p, kPlanFused);
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p,
+                  kPlanNoBn192 | kPlanPairBn256 | kPlanPairOnRequest);
     if (s != RGG_OK) return s;
     CUtensorMap tx, tx64, tw;
     s = encode_maps_fp8(X8, W8, E, M_tot, K, N, p.bm, &tx, &tx64, &tw);
@@ -655,7 +666,8 @@ rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, c
     a.walk_order = p.walk_order;
     a.sx = sx;
     a.sw = sw;
-    cudaError_t err = rgg::launch_gemm_fp8(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    cudaError_t err = (p.bm == 256) ? rgg::launch_gemm_pair_fp8(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+                                    : rgg::launch_gemm_fp8(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_fp8 launch");
 }
 

@@ -28,16 +28,25 @@
 
 namespace rgg {
 
-template <int BN>
+// Every stage row is one 128-byte swizzle row in both element types: bf16
+// stages cover K = 64 with 64-column weight panels, FP8 (E4M3) stages K = 128
+// with 128-column panels (so FP8 pairs take BN = 256, one panel per CTA).
+template <int BN, bool kFp8 = false>
 struct PairConfig {
     static_assert(BN == 128 || BN == 256, "pair tiles split BN into two whole 64-column panel sets");
+    static_assert(!kFp8 || BN == 256, "FP8 weight panels are 128 columns: each CTA of a pair holds one");
     static constexpr int kHalfN = BN / 2;           // B columns held by each CTA
-    static constexpr int kPanels = kHalfN / 64;
+    static constexpr int kKStage = kFp8 ? 128 : kBK;                     // K elements per stage
+    static constexpr int kPanelN = kFp8 ? 128 : 64;                      // W columns per panel
+    static constexpr int kPanels = kHalfN / kPanelN;
+    static constexpr uint32_t kPanelB = static_cast<uint32_t>(kKStage) * 128u;  // bytes per W panel
+    static constexpr uint32_t kBStep = kFp8 ? 4096u : 2048u;  // B start advance per MMA (32 or 16 K rows)
     static constexpr uint32_t kTmemCols = 512;      // two BN-column fp32 buffers (BN <= 256)
-    static constexpr uint32_t kStageBytesPerCta = static_cast<uint32_t>((128 + kHalfN) * kBK * 2);
-    static constexpr uint32_t kStageBytesPerCta64 = static_cast<uint32_t>((64 + kHalfN) * kBK * 2);
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(256, BN, /*b_mn_major=*/true);
-    static constexpr uint32_t kIdesc128 = idesc_bf16_f32(128, BN, /*b_mn_major=*/true);  // 64 rows per CTA
+    static constexpr uint32_t kStageBytesPerCta = static_cast<uint32_t>((128 + kHalfN) * 128);
+    static constexpr uint32_t kStageBytesPerCta64 = static_cast<uint32_t>((64 + kHalfN) * 128);
+    static constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(256, BN, true) : idesc_bf16_f32(256, BN, true);
+    static constexpr uint32_t kIdesc128 =  // 64 rows per CTA
+        kFp8 ? idesc_e4m3_f32(128, BN, true) : idesc_bf16_f32(128, BN, true);
 };
 
 // A pair tile whose rows are the last <= 128 of its expert runs as an M = 128
@@ -74,20 +83,22 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 // matching BN/2 up columns as the two halves of B, so the M = 256 MMA leaves
 // [gate | up] side by side in each CTA's TMEM for that CTA's 128 rows, and the
 // epilogue writes silu(gate) * up.  Tail tiles run at M = 256 in this mode.
-// Epilogue warps per CTA: four for plain outputs, eight (two per TMEM lane
-// quadrant, each on half of the columns) for the fused gate-up epilogue, whose
-// exponentials otherwise outlast the main loop (measured: uniform 845 -> 1 018
-// TFLOP/s, prefill 1 417 -> 1 526).
-template <int kEpi>
+// Epilogue warps per CTA: four for plain bf16 outputs, eight (two per TMEM
+// lane quadrant, each on half of the columns) for the fused gate-up epilogue,
+// whose exponentials otherwise outlast the main loop (measured: uniform 845 ->
+// 1 018 TFLOP/s, prefill 1 417 -> 1 526), and for FP8, whose epilogue applies
+// the row and column scales.
+template <int kEpi, bool kFp8 = false>
 __host__ __device__ constexpr int pair_epilogue_warps() {
-    return kEpi == kEpiSwiGLU ? 8 : 4;
+    return (kEpi == kEpiSwiGLU || kFp8) ? 8 : 4;
 }
 
-template <int BN, int kEpi = kEpiPlain>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilogue_warps<kEpi>(), 1)
+template <int BN, int kEpi = kEpiPlain, bool kFp8 = false>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilogue_warps<kEpi, kFp8>(), 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
                              const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
-    using Cfg = PairConfig<BN>;
+    using Cfg = PairConfig<BN, kFp8>;
+    static_assert(!(kFp8 && kEpi == kEpiSwiGLU), "the fused gate-up epilogue is bf16 only");
     constexpr int BM = 256;  // rows per pair tile
     constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;  // output columns per tile
     auto half_tile = [&](const TileCoord& c) { return kEpi == kEpiPlain && pair_runs_as_128_rows(args, c); };
@@ -137,7 +148,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
-            mbar_init(acce_bar(a), 2 * pair_epilogue_warps<kEpi>());
+            mbar_init(acce_bar(a), 2 * pair_epilogue_warps<kEpi, kFp8>());
         }
         mbar_init(drain_bar, 1);
         misc[1] = 0u;
@@ -192,11 +203,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                     }
                     const uint32_t full_leader = map_to_rank(full_bar(st), 0);
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(st), tx_bytes);
-                    tma_load_2d_pair(a0 + st * sp.a_stage, xmap, full_leader, kb * kBK, a_row);
+                    tma_load_2d_pair(a0 + st * sp.a_stage, xmap, full_leader, kb * Cfg::kKStage, a_row);
 #pragma unroll
                     for (int p = 0; p < Cfg::kPanels; ++p)
-                        tma_load_3d_pair(b0 + st * sp.b_stage + p * kPanelBytes, &tmap_w, full_leader, b_col + 64 * p,
-                                         kb * kBK, c.expert);
+                        tma_load_3d_pair(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_leader,
+                                         b_col + Cfg::kPanelN * p, kb * Cfg::kKStage, c.expert);
                     ++issued;
                     if (++st == S) {
                         st = 0;
@@ -246,10 +257,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                     const uint32_t a_st = a0 + st * sp.a_stage;
                     const uint32_t b_st = b0 + st * sp.b_stage;
 #pragma unroll
-                    for (int j = 0; j < kBK / 16; ++j) {
+                    for (int j = 0; j < kMmasPerStage; ++j) {
                         const uint64_t ad = sw128_desc(a_st + 32u * j, 16u, 1024u);
-                        const uint64_t bd = sw128_desc(b_st + 2048u * j, kPanelBytes, 1024u);
-                        mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+                        const uint64_t bd = sw128_desc(b_st + Cfg::kBStep * j, Cfg::kPanelB, 1024u);
+                        if constexpr (kFp8)
+                            mma_f8_ss_pair(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+                        else
+                            mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
                     }
                     mma_commit_pair(empty_bar(st), 0x3);
                     if (++st == S) {
@@ -295,10 +309,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             const int cbase = half ? (q >> 1) * (BN / 2) : 0;  // first tile column this warp holds
             const bool row_ok = r_local < c.rows;
             __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0 + cbase;
-#pragma unroll 1
-            constexpr int kParts = pair_epilogue_warps<kEpi>() / 4;  // warps per lane quadrant
-            const int pc = ncols / kParts;                          // columns each of them writes
+            constexpr int kParts = pair_epilogue_warps<kEpi, kFp8>() / 4;  // warps per lane quadrant
+            const int pc = ncols / kParts;                                // columns each of them writes
             const int c0 = ((warp - 2) >> 2) * pc;
+#pragma unroll 1
             for (int cc = c0; cc < c0 + pc; cc += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
@@ -312,6 +326,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                         v[i] = __float_as_uint(silu_f32(__uint_as_float(v[i])) * __uint_as_float(u[i]));
                 } else {
                     tmem_ld_wait();
+                }
+                if constexpr (kFp8) {
+                    // dequantise: row scale of X times the expert's column scale of W
+                    if (row_ok) {
+                        const float rs = __ldg(args.sx + c.row0 + r_local);
+                        const float* swp = args.sw + static_cast<int64_t>(c.expert) * N + c.col0 + cbase + cc;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (c.col0 + cbase + cc + 16 * h < N) {
+#pragma unroll
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    const float4 s4 = __ldg(reinterpret_cast<const float4*>(swp + 16 * h) + q4);
+                                    const int i0 = 16 * h + 4 * q4;
+                                    v[i0 + 0] = __float_as_uint(__uint_as_float(v[i0 + 0]) * rs * s4.x);
+                                    v[i0 + 1] = __float_as_uint(__uint_as_float(v[i0 + 1]) * rs * s4.y);
+                                    v[i0 + 2] = __float_as_uint(__uint_as_float(v[i0 + 2]) * rs * s4.z);
+                                    v[i0 + 3] = __float_as_uint(__uint_as_float(v[i0 + 3]) * rs * s4.w);
+                                }
+                            }
+                        }
+                    }
                 }
                 if (row_ok) {
 #pragma unroll

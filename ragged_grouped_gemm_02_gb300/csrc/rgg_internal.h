@@ -49,6 +49,9 @@ cudaError_t launch_gather_rows(const void* xtok, const int32_t* row_index, const
 // `grid` is even.
 cudaError_t launch_gemm_pair(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                              const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
+// FP8 operands and scales on CTA pairs (`bn` 256; byte tensor maps as for launch_gemm_fp8).
+cudaError_t launch_gemm_pair_fp8(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
+                                 const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 // The same with the fused gate-up + SiLU epilogue (tmap_w spans 2N columns; tail tiles stay M = 256).
 cudaError_t launch_gemm_pair_swiglu(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                                     const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);

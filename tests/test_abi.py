@@ -223,8 +223,13 @@ def test_plan_fused_gate_up_takes_pairs_without_tails(lib):
     assert rgg.rgg_plan(32, 512, 6144, 2048, op="swiglu")["bm"] == 64
     with pytest.raises(rgg.RggError):
         rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", bn=192)
-    # FP8 stays on 1-CTA tiles
+    # FP8 takes CTA pairs only when asked for, and only with BN = 256 (one
+    # 128-column weight panel per CTA)
     assert rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8")["bm"] == 128
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8", bm=256)
+    assert p["bm"] == 256 and p["bn"] == 256 and p["threads"] == 320
+    with pytest.raises(rgg.RggError):
+        rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8", bm=256, bn=128)
 
 
 def test_plan_reports_the_launch_block_size(lib):
