@@ -279,6 +279,11 @@ def run_profile(args):
     elif args.op == "gemm":
         def launch():
             rgg.rgg_grouped_gemm(X, W, off, Y, **opts)
+    elif args.op == "swiglu":
+        H = torch.empty(X.shape[0], W.shape[2] // 2, dtype=torch.bfloat16, device=dev)
+
+        def launch():
+            rgg.rgg_grouped_gemm_swiglu(X, W, off, H, **opts)
     elif args.op == "fp8":
         X8, W8, sx, sw = wl.quantize_fp8(inp.X, inp.W)
         X8, W8, sx, sw = X8.to(dev), W8.to(dev), sx.to(dev), sw.to(dev)
@@ -287,12 +292,13 @@ def run_profile(args):
         def launch():
             rgg.rgg_grouped_gemm_fp8(X8, W8, sx, sw, off, Y, **opts)
     else:
-        raise SystemExit("--profile covers --op gemm, gather and fp8")
+        raise SystemExit("--profile covers --op gemm, gather, swiglu and fp8")
     for _ in range(args.warmup + 1):
         launch()
     torch.cuda.synchronize(dev)
     status = rgg.rgg_query_status(0)
-    plan = rgg.rgg_plan(inp.workload.E, inp.X.shape[0], inp.workload.K, inp.workload.N, op=args.op, **opts)
+    n_plan = inp.workload.N // 2 if args.op == "swiglu" else inp.workload.N
+    plan = rgg.rgg_plan(inp.workload.E, inp.X.shape[0], inp.workload.K, n_plan, op=args.op, **opts)
     print(json.dumps({"profile": args.workload, "launches": args.warmup + 1, "status": status, "plan": plan}))
     if status != rgg.RGG_OK:
         raise SystemExit(1)
@@ -375,29 +381,30 @@ def run_ours(args):
         raise RuntimeError("device status after warm-up: %s" % rgg.rgg_status_string(status))
 
     K_steps = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    # Launches of this library's kernels in one step: the two-pass gather runs
+    # its row gather and then the grouped GEMM, every other op one kernel.
+    per_step = 2 if plan.get("gather_mode") == 2 else 1
+
+    # Eager: K steps launched one by one from the host.
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
     start.record(stream)
     for i in range(K_steps):
-        ev[i][0].record(stream)
         step()
-        ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    clocks = sampler.stop()
     status = rgg.rgg_query_status(local, stream)
     if status != rgg.RGG_OK:
-        raise RuntimeError("device status after the timed region: %s" % rgg.rgg_status_string(status))
-    total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
-    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        raise RuntimeError("device status after the eager steps: %s" % rgg.rgg_status_string(status))
+    eager_ms = max_over_ranks(start.elapsed_time(end), world, dev)
 
-    # The same step captured once in a CUDA graph and replayed K times (the
-    # pages time their kernels inside CUDA graphs): same launch, no host work
-    # per step.
-    graph = None
+    # Timed region: one step captured in a CUDA graph and replayed K times on
+    # the same stream, so the device time has no host launch work in it (the
+    # pages time their kernels inside CUDA graphs too).
+    timing = "cuda_graph"
+    total_ms = None
     try:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -405,23 +412,30 @@ def run_ours(args):
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize(dev)
-        barrier(world)
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
         g0.record(stream)
         for _ in range(K_steps):
             g.replay()
         g1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
-        g_ms = max_over_ranks(g0.elapsed_time(g1), world, dev)
-        status = rgg.rgg_query_status(local, stream)
-        if status != rgg.RGG_OK:
-            raise RuntimeError("device status after graph replay: %s" % rgg.rgg_status_string(status))
-        graph = {"value": round(flops * K_steps * world / (g_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
-                 "ms_per_step": round(g_ms / K_steps, 5), "note": "one step captured in a CUDA graph, replayed K times"}
+        total_ms = max_over_ranks(g0.elapsed_time(g1), world, dev)
         del g
     except RuntimeError as e:
-        graph = {"unavailable": str(e)[:200]}
+        timing = "eager (graph capture failed: %s)" % str(e)[:160]
+        total_ms = eager_ms
+    clocks = sampler.stop()
+    status = rgg.rgg_query_status(local, stream)
+    if status != rgg.RGG_OK:
+        raise RuntimeError("device status after the timed region: %s" % rgg.rgg_status_string(status))
+    # average duration of one step in the timed region (for the one-kernel ops,
+    # one launch of the GEMM kernel plus the gap to the next)
+    launch_ms = total_ms / K_steps
+    eager = {"value": round(flops * K_steps * world / (eager_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+             "ms_per_step": round(eager_ms / K_steps, 5),
+             "note": "the same K steps launched one by one from the host"}
 
     # End to end through the public API: every step copies its inputs (X, the
     # offsets, and for FP8 the row scales) in from pinned host memory and its
@@ -546,6 +560,8 @@ def run_ours(args):
     roof["peak_source"] = peaks["source"] + (" bf16 x 2 (nominal fp8/bf16 ratio)" if args.op == "fp8" else "")
     roof["algorithmic_per_launch"] = {"flops": flops, "bytes": bytes_}
     roof["launch_ms"] = round(launch_ms, 5)
+    roof["launch_scope"] = ("one step of the CUDA-graph timed region: the row gather and the GEMM"
+                            if per_step == 2 else "one GEMM launch in the CUDA-graph timed region")
     roof["hbm_gbs"] = round(bytes_ / (launch_ms / 1e3) / 1e9, 1)
     roof["hbm_frac"] = round(bytes_ / (launch_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
     roof["tensor_frac"] = round(flops / (launch_ms / 1e3) / 1e12 / tc_peak, 4)
@@ -579,8 +595,8 @@ def run_ours(args):
                    if bytes_ > L2_BYTES else "inputs smaller than L2: back-to-back launches",
                    "plan": plan, "plan_from": "host-side routed counts (tile shape only)",
                    "parallelism": "expert replicas x%d" % world},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "graph": graph, "clocks": clocks,
-        "gpu_launches": K_steps, "impl": "ours",
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "timing": timing, "eager": eager,
+        "clocks": clocks, "gpu_launches": K_steps * per_step, "impl": "ours",
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
