@@ -64,7 +64,9 @@ def parse_args():
     p.add_argument("--bn", type=int, default=0)
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--tail64", type=int, default=0, help="0 auto, 1 on, -1 off")
-    p.add_argument("--gather-mode", type=int, default=0, help="gather ops: 0 auto, 1 TMA gather4, 2 cp.async rows")
+    p.add_argument("--gather-mode", type=int, default=0, help="gather ops: 0 auto, 1 TMA gather4, 2 two-pass")
+    p.add_argument("--multicast", type=int, default=0,
+                   help="0 auto, 1 128-row tiles on clusters of two CTAs sharing operands by TMA multicast, -1 off")
     p.add_argument("--walk-order", type=int, default=0,
                    help="0 list order, 1 front/back interleave, 2 scatter, 3 size-sorted interleave")
     p.add_argument("--op", default="gemm", choices=["gemm", "swiglu", "fp8", "gather", "swiglu_gather"],
@@ -266,7 +268,7 @@ def run_profile(args):
     off = torch.from_numpy(inp.offsets).to(dev)
     Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device=dev)
     opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
-                walk_order=args.walk_order,
+                walk_order=args.walk_order, multicast=args.multicast,
                 host_counts=inp.counts)
     if args.op == "gather":
         # the same recipe as the timed gather op: M_tot tokens, distinct tokens per expert
@@ -354,7 +356,7 @@ def run_ours(args):
     # The tile shape is planned from the routed counts, known on the host as in
     # the worklog's harness; the kernel itself reads the offsets on the device.
     opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
-                walk_order=args.walk_order,
+                walk_order=args.walk_order, multicast=args.multicast,
                 host_counts=inp.counts)
     if gather:
         opts["gather_mode"] = args.gather_mode

@@ -96,6 +96,14 @@ typedef struct rgg_options {
                                     grows it with cudaMalloc when a call needs more (that call then
                                     allocates, and waits for the device while freeing the old one). */
     int64_t workspace_bytes;     /* size of `workspace` in bytes */
+    int multicast;               /* 128-row tiles on clusters of two CTAs that share one operand of each pair of
+                                    tiles through TMA multicast (consecutive M tiles of an expert share the
+                                    weight panel, neighbouring N tiles share the X rows); same result.
+                                    0 = auto (currently off), 1 = on, -1 = off.  On: BN is 128 or 256
+                                    (256 for the fused gate-up and FP8 ops), bm must be 0 or 128, walk
+                                    orders 0-2 (an automatic size-sorted walk becomes 1; asking for 3 is
+                                    RGG_ERR_INVALID_ARG), and the gather calls take the two-pass mode;
+                                    the fused-gather GEMM has no multicast form (RGG_ERR_UNSUPPORTED). */
 } rgg_options;
 
 #define RGG_DEBUG_PRODUCER_STALL 1
@@ -113,6 +121,7 @@ typedef struct rgg_plan_info {
     int walk_order;              /* walk order (see rgg_options) */
     int gather_mode;             /* gather ops: 1 = fused tile::gather4, 2 = two-pass; else 0 */
     int64_t workspace_bytes;     /* two-pass gather: workspace the call needs; else 0 */
+    int multicast;               /* 1 when the plan runs the cluster-multicast kernel (see rgg_options) */
 } rgg_plan_info;
 
 /*

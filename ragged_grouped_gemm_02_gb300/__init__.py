@@ -56,14 +56,15 @@ class _Options(ctypes.Structure):
                 ("max_ctas", ctypes.c_int), ("timeout_ns", ctypes.c_uint64), ("host_counts", ctypes.c_void_p),
                 ("debug_flags", ctypes.c_int), ("tail64", ctypes.c_int),
                 ("op", ctypes.c_int), ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64), ("multicast", ctypes.c_int)]
 
 
 class _PlanInfo(ctypes.Structure):
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int), ("stages", ctypes.c_int),
                 ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("tmem_cols", ctypes.c_int), ("max_tiles", ctypes.c_int64), ("tail64", ctypes.c_int),
-                ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int), ("workspace_bytes", ctypes.c_int64)]
+                ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int), ("workspace_bytes", ctypes.c_int64),
+                ("multicast", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -141,9 +142,10 @@ def _handle(device: int) -> ctypes.c_void_p:
 
 
 def _options(bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0, tail64=0,
-             op=0, walk_order=0, gather_mode=0):
+             op=0, walk_order=0, gather_mode=0, multicast=0):
     opt = _Options(int(bm), int(bn), int(stages), int(max_ctas), int(timeout_ns), None, int(debug_flags),
                    int(tail64), int(op), int(walk_order), int(gather_mode))
+    opt.multicast = int(multicast)
     keep = None
     if host_counts is not None:
         import numpy as np
@@ -160,7 +162,7 @@ def _stream_ptr(stream, device):
 
 
 def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
-                     host_counts=None, debug_flags=0, tail64=0, walk_order=0, stream=None,
+                     host_counts=None, debug_flags=0, tail64=0, walk_order=0, multicast=0, stream=None,
                      check=False):
     """Y_e = X_e . W_e for every expert (one kernel launch, asynchronous).
 
@@ -191,7 +193,7 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
         raise ValueError("Y must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
     opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0,
-                         walk_order)
+                         walk_order, multicast=multicast)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm(_handle(device), X.data_ptr(), W.data_ptr(), group_offsets.data_ptr(), Y.data_ptr(),
                              E, M_tot, K, N, st, ctypes.byref(opt))
@@ -206,7 +208,7 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
 
 
 def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
-                            host_counts=None, debug_flags=0, tail64=0, walk_order=0, stream=None,
+                            host_counts=None, debug_flags=0, tail64=0, walk_order=0, multicast=0, stream=None,
                             check=False):
     """H = silu(X_e . W13_e[:, :N]) * (X_e . W13_e[:, N:]) for every expert,
     one kernel launch (the fused gate-up projection with SiLU activation).
@@ -233,7 +235,7 @@ def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages
         raise ValueError("H must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
     opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64,
-                         0, walk_order)
+                         0, walk_order, multicast=multicast)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm_swiglu(_handle(device), X.data_ptr(), W13.data_ptr(), group_offsets.data_ptr(),
                                     H.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
@@ -249,7 +251,7 @@ def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages
 
 def rgg_grouped_gemm_fp8(X8, W8, sx, sw, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0,
                          timeout_ns=0, host_counts=None, debug_flags=0, tail64=0, walk_order=0,
-                         stream=None, check=False):
+                         multicast=0, stream=None, check=False):
     """Y[i, j] = sx[i] * sw[e, j] * (X8_e . W8_e)[i, j] with FP8 E4M3 operands.
 
     X8: float8_e4m3fn CUDA [M_tot, K]; W8: float8_e4m3fn CUDA [E, K, N];
@@ -274,7 +276,7 @@ def rgg_grouped_gemm_fp8(X8, W8, sx, sw, group_offsets, Y=None, *, bm=0, bn=0, s
         raise ValueError("Y must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
     opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64,
-                         0, walk_order)
+                         0, walk_order, multicast=multicast)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm_fp8(_handle(device), X8.data_ptr(), W8.data_ptr(), sx.data_ptr(), sw.data_ptr(),
                                  group_offsets.data_ptr(), Y.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
@@ -311,7 +313,8 @@ def rgg_grouped_gemm_noalloc(X, W, group_offsets, Y=None, status_out=None, strea
 
 
 def _gather_call(name, X_tok, row_index, W, group_offsets, out, swiglu, bm, bn, stages, max_ctas, timeout_ns,
-                 host_counts, debug_flags, tail64, walk_order, gather_mode, workspace, stream, check):
+                 host_counts, debug_flags, tail64, walk_order, gather_mode, workspace, stream, check,
+                 multicast=0):
     import torch
     if not (X_tok.is_cuda and row_index.is_cuda and W.is_cuda and group_offsets.is_cuda):
         raise ValueError("X_tok, row_index, W and group_offsets must be CUDA tensors")
@@ -334,7 +337,7 @@ def _gather_call(name, X_tok, row_index, W, group_offsets, out, swiglu, bm, bn, 
         raise ValueError("the output must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
     opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order,
-                         gather_mode)
+                         gather_mode, multicast)
     if workspace is not None:
         if not (workspace.is_cuda and workspace.is_contiguous()):
             raise ValueError("workspace must be a contiguous CUDA tensor")
@@ -355,7 +358,7 @@ def _gather_call(name, X_tok, row_index, W, group_offsets, out, swiglu, bm, bn, 
 
 def rgg_grouped_gemm_gather(X_tok, row_index, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0,
                             timeout_ns=0, host_counts=None, debug_flags=0, tail64=0, walk_order=0, gather_mode=0,
-                            workspace=None, stream=None, check=False):
+                            workspace=None, multicast=0, stream=None, check=False):
     """Y[i] = X_tok[row_index[i]] . W_e for every routed row i of expert e,
     the token gather fused into the kernel's activation loads.
 
@@ -367,19 +370,20 @@ def rgg_grouped_gemm_gather(X_tok, row_index, W, group_offsets, Y=None, *, bm=0,
     bytes for the two-pass mode (else the handle's own is used)."""
     return _gather_call("rgg_grouped_gemm_gather", X_tok, row_index, W, group_offsets, Y, False, bm, bn, stages,
                         max_ctas, timeout_ns, host_counts, debug_flags, tail64, walk_order, gather_mode, workspace,
-                        stream, check)
+                        stream, check, multicast)
 
 
 def rgg_grouped_gemm_swiglu_gather(X_tok, row_index, W13, group_offsets, H=None, *, bm=0, bn=0, stages=0,
                                    max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0, tail64=0,
-                                   walk_order=0, gather_mode=0, workspace=None, stream=None, check=False):
+                                   walk_order=0, gather_mode=0, workspace=None, multicast=0, stream=None,
+                                   check=False):
     """H[i] = silu(x W13_e[:, :N]) * (x W13_e[:, N:]) with x = X_tok[row_index[i]]:
     the fused gate-up projection reading its tokens through the gather.
 
     W13: bf16 CUDA [E, K, 2N] (gate columns first); H: optional bf16 CUDA [M_tot, N]."""
     return _gather_call("rgg_grouped_gemm_swiglu_gather", X_tok, row_index, W13, group_offsets, H, True, bm, bn,
                         stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, walk_order, gather_mode,
-                        workspace, stream, check)
+                        workspace, stream, check, multicast)
 
 
 def rgg_export_tiles(group_offsets, M_tot: int, N: int, bm: int, bn: int, cap: int | None = None, stream=None):
@@ -416,13 +420,13 @@ def rgg_query_status(device: int | None = None, stream=None) -> int:
 
 def rgg_plan(E: int, M_tot: int, K: int, N: int, *, num_sms: int = 0, smem_optin: int = 0, bm=0, bn=0,
              stages=0, max_ctas=0, host_counts=None, tail64=0, op: str = "gemm",
-             walk_order=0, gather_mode=0) -> dict:
+             walk_order=0, gather_mode=0, multicast=0) -> dict:
     """The launch configuration rgg_grouped_gemm (op="gemm") or
     rgg_grouped_gemm_swiglu (op="swiglu", N = output width) would use (host-only)."""
     lib = load_library()
     opt, keep = _options(bm, bn, stages, max_ctas, 0, host_counts, 0, tail64,
                          {"gemm": 0, "swiglu": 1, "fp8": 2, "gather": 3, "swiglu_gather": 4}[op], walk_order,
-                         gather_mode)
+                         gather_mode, multicast)
     info = _PlanInfo()
     s = lib.rgg_plan(int(num_sms), int(smem_optin), int(E), int(M_tot), int(K), int(N), ctypes.byref(opt),
                      ctypes.byref(info))

@@ -85,6 +85,7 @@ struct Plan {
     int64_t max_tiles;
     int tail64;       // 1: tail tiles of <= 64 rows run as 64-row MMAs (128-row tiles only)
     int walk_order;   // 0 list order, 1 front/back interleave, 2 strided scatter
+    int mc;           // 1: 128-row tiles on clusters of two CTAs sharing operands by TMA multicast
 };
 
 // Upper bound on the flat tile count: sum_e ceil(m_e/BM) <= floor(M_tot/BM) + E.
@@ -110,6 +111,9 @@ constexpr int kPlanPairBn256 = 16;  // CTA pairs only with BN = 256 (FP8: 128-co
 // CTA pairs only when asked for (bm = 256): FP8 pairs measured slower than 128 x 256 tiles on every
 // benchmark shape (uniform 1 191 vs 1 390 TFLOP/s, skew16k 1 069 vs 1 291, prefill 2 714 vs 2 775).
 constexpr int kPlanPairOnRequest = 32;
+// The cluster-multicast kernel (rgg_gemm_mc.cuh) exists for this op.  With
+// kPlanNoBn192 (fused gate-up, FP8) it takes BN = 256 only.
+constexpr int kPlanMcOk = 64;
 
 rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N, const rgg_options* opt,
                      Plan* out, int kind = 0) {
@@ -117,6 +121,9 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     const bool no_192 = (kind & kPlanNoBn192) != 0;
     const bool pair_256 = (kind & kPlanPairBn256) != 0;
     const bool pair_on_request = (kind & kPlanPairOnRequest) != 0;
+    const int want_mc = opt ? opt->multicast : 0;
+    if (want_mc < -1 || want_mc > 1) return RGG_ERR_INVALID_ARG;
+    const bool mc = (want_mc == 1);
     rgg_status s = check_sizes(E, M_tot, K, N);
     if (s != RGG_OK) return s;
     if (num_sms <= 0) num_sms = kDefaultSms;
@@ -137,6 +144,13 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     const int want_walk = opt ? opt->walk_order : 0;
     if (want_walk < 0 || want_walk > 3) return RGG_ERR_INVALID_ARG;
     if (want_walk == 3 && E > rgg::kMaxSortedExperts) return RGG_ERR_UNSUPPORTED;
+    if (mc) {
+        // cluster multicast: 128-row tiles, BN 128 or 256 (256 for the fused gate-up and FP8 ops),
+        // walk orders 0-2
+        if ((kind & kPlanMcOk) == 0) return RGG_ERR_UNSUPPORTED;
+        if ((want_bm != 0 && want_bm != 128) || want_bn == 192 || want_walk == 3) return RGG_ERR_INVALID_ARG;
+        if (no_192 && want_bn != 0 && want_bn != 256) return RGG_ERR_INVALID_ARG;
+    }
     int grid_cap = max_ctas > 0 ? std::min(max_ctas, num_sms) : num_sms;
 
     // Per-expert M tiles at each BM: exact with host counts, else the
@@ -171,8 +185,8 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
             }
         avg = busy ? static_cast<double>(rows) / busy : 0.0;
     }
-    int bm = want_bm;
-    int bn = want_bn;
+    int bm = mc ? 128 : want_bm;
+    int bn = (mc && no_192) ? 256 : want_bn;
     if (bm == 0 && avg <= 64.0) bm = 64;
     {
         double best = 1e300;
@@ -187,7 +201,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
             const int64_t mt = std::max<int64_t>(1, m_tiles(cbm));
             for (int cbn : {256, 192, 128}) {
                 if (bn != 0 && cbn != bn) continue;
-                if ((cpair || no_192) && cbn == 192) continue;
+                if ((cpair || no_192 || mc) && cbn == 192) continue;
                 if (cpair && pair_256 && cbn != 256) continue;
                 const int64_t waves = ceil_div(mt * ceil_div(N, cbn), cunits);
                 const double cost = static_cast<double>(waves) * (cbn + 64) * (cpair ? 0.87 : 1.0);
@@ -209,7 +223,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (walk == 0 && opt && opt->host_counts && E <= rgg::kMaxSortedExperts) {
         int64_t mx = 0;
         for (int e = 0; e < E; ++e) mx = std::max<int64_t>(mx, opt->host_counts[e]);
-        if (avg > 0.0 && static_cast<double>(mx) > 4.0 * avg) walk = 3;
+        if (avg > 0.0 && static_cast<double>(mx) > 4.0 * avg) walk = mc ? 1 : 3;
     }
     const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;
     (void)units;
@@ -220,14 +234,16 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     // Per-CTA tile extents: a pair CTA holds 128 rows of A and half of B.
     const int cta_m = pair ? 128 : bm;
     const int cta_n = pair ? bn / 2 : bn;
-    const rgg::SmemPlan probe = rgg::smem_plan(cta_m, cta_n, 0, E, walk == 3);
+    // walk order 3 and the multicast kernel's unit list each keep two more prefixes in shared memory
+    const bool extra_prefix = (walk == 3 || mc);
+    const rgg::SmemPlan probe = rgg::smem_plan(cta_m, cta_n, 0, E, extra_prefix);
     const int64_t per_stage = static_cast<int64_t>(cta_m + cta_n) * 128 + 16;  // tiles + two barriers
     const int64_t room = static_cast<int64_t>(smem_optin) - 1024 - probe.total - 64;
     int fit = static_cast<int>(std::min<int64_t>(rgg::kMaxStages, room / per_stage));
     int stages = want_stages ? want_stages : fit;
     if (stages < 2 || stages > fit) return RGG_ERR_UNSUPPORTED;
 
-    const rgg::SmemPlan sp = rgg::smem_plan(cta_m, cta_n, stages, E, walk == 3);
+    const rgg::SmemPlan sp = rgg::smem_plan(cta_m, cta_n, stages, E, extra_prefix);
     // Ask for more than half of the SM's shared memory so that exactly one CTA
     // (and one 2 x BN-column TMEM allocation) lives on each SM.
     const int smem = std::max<int>(static_cast<int>(sp.total) + 1024, smem_optin / 2 + 1024);
@@ -236,12 +252,15 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     out->bm = bm;
     out->bn = bn;
     out->stages = stages;
+    // a multicast cluster walks units of two tiles
     out->grid = pair ? static_cast<int>(2 * std::max<int64_t>(1, std::min<int64_t>(units, max_tiles)))
+                : mc ? static_cast<int>(2 * std::max<int64_t>(1, std::min<int64_t>(grid_cap / 2, (max_tiles + 1) / 2)))
                      : static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(grid_cap, max_tiles)));
     out->smem_bytes = smem;
     out->max_tiles = max_tiles;
     out->tail64 = ((bm == 128 || bm == 256) && want_tail != -1) ? 1 : 0;
     out->walk_order = walk;
+    out->mc = mc ? 1 : 0;
     return RGG_OK;
 }
 
@@ -275,7 +294,7 @@ rgg_status choose_gather_mode(int num_sms, int smem_optin, int E, int64_t M_tot,
     (void)K;
     (void)N;
     (void)swiglu;
-    if (opt && opt->bm == 256) {
+    if (opt && (opt->bm == 256 || opt->multicast == 1)) {  // CTA pairs and multicast clusters read whole boxes
         *mode = kGatherTwoPass;
         return RGG_OK;
     }
@@ -505,11 +524,11 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     // the two-pass gather runs the plain (or fused gate-up) kernel on the gathered rows; the fused
     // gate-up op takes CTA pairs but not BN = 192; FP8 and the fused gather take 1-CTA tiles only
     const bool fused_gather = gather && mode == kGatherFused;
-    const int kind = (op == 2)                             ? (kPlanNoBn192 | kPlanPairBn256 | kPlanPairOnRequest)
-                     : (op == 4 && fused_gather)           ? kPlanFused
-                     : (op == 3 && fused_gather)           ? kPlanNoPair
-                     : swiglu                              ? kPlanNoBn192
-                                                           : 0;
+    const int kind = (op == 2)                   ? (kPlanNoBn192 | kPlanPairBn256 | kPlanPairOnRequest | kPlanMcOk)
+                     : (op == 4 && fused_gather) ? kPlanFused
+                     : (op == 3 && fused_gather) ? kPlanNoPair
+                     : swiglu                    ? (kPlanNoBn192 | kPlanMcOk)
+                                                 : kPlanMcOk;
     rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, swiglu ? 2 * N : N, opt, &p, kind);
     if (s != RGG_OK) return s;
     out->bm = p.bm;
@@ -527,6 +546,7 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     if (swiglu && p.bm == 256) out->tail64 = 0;  // fused gate-up pairs keep 256-row tail tiles
     out->gather_mode = mode;
     out->workspace_bytes = (mode == kGatherTwoPass) ? gather_workspace_bytes(M_tot, K) : 0;
+    out->multicast = p.mc;
     return RGG_OK;
 }
 
@@ -548,7 +568,7 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
     }
 
     Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p);
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p, kPlanMcOk);
     if (s != RGG_OK) return s;
 
     CUtensorMap tx, tx64, tw;
@@ -572,9 +592,11 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
     a.tail64 = p.tail64;
     a.walk_order = p.walk_order;
 
-    cudaError_t err = (p.bm == 256)   ? rgg::launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-                      : (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-                                      : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    cudaError_t err =
+        p.mc            ? rgg::launch_gemm_mc(rgg::kMcPlain, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+        : (p.bm == 256) ? rgg::launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+        : (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+                        : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm launch");
 }
 
@@ -596,7 +618,7 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
         return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
     }
     Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, kPlanNoBn192);
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, kPlanNoBn192 | kPlanMcOk);
     if (s != RGG_OK) return s;
     CUtensorMap tx, tx64, tw;
     s = encode_maps(X, W13, E, M_tot, K, 2 * N, p.bm, &tx, &tx64, &tw);
@@ -618,8 +640,10 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
     a.tail64 = p.tail64;
     a.walk_order = p.walk_order;
     if (p.bm == 256) a.tail64 = 0;  // the pair's 128-row tail layout splits gate and up across warps
-    cudaError_t err = (p.bm == 256) ? rgg::launch_gemm_pair_swiglu(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-                                    : rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    cudaError_t err =
+        p.mc            ? rgg::launch_gemm_mc(rgg::kMcSwiGLU, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+        : (p.bm == 256) ? rgg::launch_gemm_pair_swiglu(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+                        : rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_swiglu launch");
 }
 
@@ -643,7 +667,7 @@ rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, c
     }
     Plan p;
     s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p,
-                  kPlanNoBn192 | kPlanPairBn256 | kPlanPairOnRequest);
+                  kPlanNoBn192 | kPlanPairBn256 | kPlanPairOnRequest | kPlanMcOk);
     if (s != RGG_OK) return s;
     CUtensorMap tx, tx64, tw;
     s = encode_maps_fp8(X8, W8, E, M_tot, K, N, p.bm, &tx, &tx64, &tw);
@@ -666,8 +690,10 @@ rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, c
     a.walk_order = p.walk_order;
     a.sx = sx;
     a.sw = sw;
-    cudaError_t err = (p.bm == 256) ? rgg::launch_gemm_pair_fp8(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-                                    : rgg::launch_gemm_fp8(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    cudaError_t err =
+        p.mc            ? rgg::launch_gemm_mc(rgg::kMcFp8, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+        : (p.bm == 256) ? rgg::launch_gemm_pair_fp8(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+                        : rgg::launch_gemm_fp8(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_fp8 launch");
 }
 

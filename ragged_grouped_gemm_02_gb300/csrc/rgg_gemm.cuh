@@ -125,6 +125,31 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
     return true;
 }
 
+// Kernels on clusters of two CTAs: as wait_or_abort, and a timeout also raises
+// the other CTA's abort flag (its shared::cluster address), so both leave
+// their loops instead of waiting on arrivals that will not come.
+__device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                   uint32_t peer_flag_cluster, int32_t* status, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1u;
+            st_shared_cluster_u32(peer_flag_cluster, 1u);
+            atomicCAS(status, 0, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) {
+    }
+}
+
 // Element traits.  Every stage row is one 128-byte swizzle row, so a bf16
 // stage covers K = 64 and an FP8 (E4M3) stage K = 128, with the same bytes:
 // A is BM x 128 B, B is BN/kPanelN panels of kKStage K rows x 128 B.
@@ -181,6 +206,80 @@ __host__ __device__ constexpr int cta_threads() {
 }
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+
+// Epilogue of one finished accumulator buffer of a 1-CTA tile, for one
+// epilogue warp: lane `lane` of the warp holds tile row r_local (TMEM row
+// address t_row: the warp's lane quadrant and the buffer's first column) and
+// writes columns [cc0, cc0 + kOutN / parts) of it, 32 at a time, through
+// registers to Y with 256-bit stores ("Pearl's grouped GEMM kernel for MoE
+// models, explained").  Rows past the tile's valid rows, and every row when
+// `store` is false, are read from TMEM but not written.
+template <int BN, int kEpi, bool kFp8>
+__device__ __forceinline__ void epilogue_store_tile(const GemmArgs& args, const TileCoord& c, bool half, int r_local,
+                                                    uint32_t t_row, int lane, int cc0, bool store) {
+    constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;
+    constexpr int kPartCols = kOutN / (epilogue_warps<kEpi, kFp8>() / 4);
+    const int N = args.N;
+    const bool row_ok = store && (!half || lane < 16) && (r_local < c.rows);
+    __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0;
+#pragma unroll 1
+    for (int cc = cc0; cc < cc0 + kPartCols; cc += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
+        if (kEpi == kEpiSwiGLU) {
+            // gate in columns [cc, cc+32), up in [kOutN + cc, kOutN + cc + 32)
+            uint32_t u[32];
+            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kOutN + cc), u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                v[i] = __float_as_uint(silu_f32(__uint_as_float(v[i])) * __uint_as_float(u[i]));
+        } else {
+            tmem_ld_wait();
+        }
+        if constexpr (kFp8) {
+            // dequantise: row scale of X times the expert's column scale of W
+            if (row_ok) {
+                const float rs = __ldg(args.sx + c.row0 + r_local);
+                const float* swp = args.sw + static_cast<int64_t>(c.expert) * N + c.col0 + cc;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (c.col0 + cc + 16 * h < N) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float4 s4 = __ldg(reinterpret_cast<const float4*>(swp + 16 * h) + q4);
+                            const int i0 = 16 * h + 4 * q4;
+                            v[i0 + 0] = __float_as_uint(__uint_as_float(v[i0 + 0]) * rs * s4.x);
+                            v[i0 + 1] = __float_as_uint(__uint_as_float(v[i0 + 1]) * rs * s4.y);
+                            v[i0 + 2] = __float_as_uint(__uint_as_float(v[i0 + 2]) * rs * s4.z);
+                            v[i0 + 3] = __float_as_uint(__uint_as_float(v[i0 + 3]) * rs * s4.w);
+                        }
+                    }
+                }
+            }
+        }
+        if (row_ok) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int col = c.col0 + cc + 16 * h;
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
+                __nv_bfloat16* dst = yrow + cc + 16 * h;
+                if (col + 16 <= N) {
+                    if (args.y_vec32) {
+                        st_global_v8(dst, w);
+                    } else {
+                        st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                        st_global_v4(dst + 8, w[4], w[5], w[6], w[7]);
+                    }
+                } else if (col + 8 <= N) {
+                    st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+    }
+}
 
 // Token gather fused into the A loads (kGatherTma): the A rows are gathered
 // from a token matrix X_tok [T, K] through args.row_index (routed row i
@@ -457,7 +556,6 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
         constexpr int kPartCols = kOutN / kParts;                  // tile columns each of them writes
         static_assert(kPartCols % 32 == 0, "each epilogue warp handles whole 32-column chunks");
         const int cc0 = ((warp - 2) >> 2) * kPartCols;
-        const int N = args.N;
         int acc = 0;
         uint32_t acc_ph = 0;
         for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
@@ -471,65 +569,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            const bool row_ok = (!half || lane < 16) && (r_local < c.rows);
-            __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0;
-#pragma unroll 1
-            for (int cc = cc0; cc < cc0 + kPartCols; cc += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
-                if (kEpi == kEpiSwiGLU) {
-                    // gate in columns [cc, cc+32), up in [kOutN + cc, kOutN + cc + 32)
-                    uint32_t u[32];
-                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kOutN + cc), u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = __float_as_uint(silu_f32(__uint_as_float(v[i])) * __uint_as_float(u[i]));
-                } else {
-                    tmem_ld_wait();
-                }
-                if constexpr (kFp8) {
-                    // dequantise: row scale of X times the expert's column scale of W
-                    if (row_ok) {
-                        const float rs = __ldg(args.sx + c.row0 + r_local);
-                        const float* swp = args.sw + static_cast<int64_t>(c.expert) * N + c.col0 + cc;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            if (c.col0 + cc + 16 * h < N) {
-#pragma unroll
-                                for (int q4 = 0; q4 < 4; ++q4) {
-                                    const float4 s4 = __ldg(reinterpret_cast<const float4*>(swp + 16 * h) + q4);
-                                    const int i0 = 16 * h + 4 * q4;
-                                    v[i0 + 0] = __float_as_uint(__uint_as_float(v[i0 + 0]) * rs * s4.x);
-                                    v[i0 + 1] = __float_as_uint(__uint_as_float(v[i0 + 1]) * rs * s4.y);
-                                    v[i0 + 2] = __float_as_uint(__uint_as_float(v[i0 + 2]) * rs * s4.z);
-                                    v[i0 + 3] = __float_as_uint(__uint_as_float(v[i0 + 3]) * rs * s4.w);
-                                }
-                            }
-                        }
-                    }
-                }
-                if (row_ok) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int col = c.col0 + cc + 16 * h;
-                        uint32_t w[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
-                        __nv_bfloat16* dst = yrow + cc + 16 * h;
-                        if (col + 16 <= N) {
-                            if (args.y_vec32) {
-                                st_global_v8(dst, w);
-                            } else {
-                                st_global_v4(dst, w[0], w[1], w[2], w[3]);
-                                st_global_v4(dst + 8, w[4], w[5], w[6], w[7]);
-                            }
-                        } else if (col + 8 <= N) {
-                            st_global_v4(dst, w[0], w[1], w[2], w[3]);
-                        }
-                    }
-                }
-            }
+            epilogue_store_tile<BN, kEpi, kFp8>(args, c, half, r_local, t_row, lane, cc0, true);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));

@@ -56,28 +56,6 @@ __device__ __forceinline__ bool pair_runs_as_128_rows(const GemmArgs& args, cons
     return args.tail64 != 0 && c.rows <= 128;
 }
 
-__device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                                   uint32_t peer_flag_cluster, int32_t* status, uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > timeout_ns) {
-            *abort_flag = 1u;
-            st_shared_cluster_u32(peer_flag_cluster, 1u);
-            atomicCAS(status, 0, kStatusTimeout);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void spin_ns(uint64_t ns) {
-    const uint64_t t0 = global_timer_ns();
-    while (global_timer_ns() - t0 < ns) {
-    }
-}
-
 // kEpi = kEpiSwiGLU: the fused gate-up projection on a pair.  A tile covers
 // BN/2 output columns; CTA 0 loads the BN/2 gate columns and CTA 1 the
 // matching BN/2 up columns as the two halves of B, so the M = 256 MMA leaves

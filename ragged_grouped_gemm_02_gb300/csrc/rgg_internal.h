@@ -56,6 +56,17 @@ cudaError_t launch_gemm_pair_fp8(int bn, int grid, size_t smem, cudaStream_t str
 cudaError_t launch_gemm_pair_swiglu(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                                     const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 
+// 128-row 1-CTA tiles on clusters of two CTAs that share the weight panel
+// (consecutive M tiles) or the X rows (neighbouring N tiles) of each pair of
+// tiles through TMA multicast.  `kind` selects the operation; `bn` is the MMA
+// width: plain 128 or 256, fused gate-up 256 (128 output columns), FP8 256.
+// `grid` is even.
+constexpr int kMcPlain = 0;
+constexpr int kMcSwiGLU = 1;
+constexpr int kMcFp8 = 2;
+cudaError_t launch_gemm_mc(int kind, int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
+                           const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
+
 // The flat tile list written out by the same device code the GEMM uses.
 cudaError_t launch_export_tiles(const int32_t* offsets, int E, int64_t M_tot, int N, int bm, int bn,
                                 int32_t* desc, int64_t cap, int32_t* n_tiles, int32_t* status,

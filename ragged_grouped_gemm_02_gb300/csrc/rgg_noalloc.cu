@@ -134,7 +134,9 @@ extern "C" rgg_status rgg_grouped_gemm_noalloc(const void* X, const void* W, con
         a.tail64 = plan.tail64;
         a.walk_order = plan.walk_order;
         a.timeout_ns = 2000000000ull;
-        err = (plan.bm == 256)   ? rgg::launch_gemm_pair(plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a)
+        err = plan.multicast
+                  ? rgg::launch_gemm_mc(rgg::kMcPlain, plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a)
+              : (plan.bm == 256) ? rgg::launch_gemm_pair(plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a)
               : (plan.bm == 128) ? rgg::launch_gemm_bm128(plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a)
                                  : rgg::launch_gemm_bm64(plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a);
     }

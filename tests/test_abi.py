@@ -135,6 +135,42 @@ def test_plan_grid_never_exceeds_tiles_or_sms(lib):
     assert rgg.rgg_plan(64, 16384, 1024, 2688, num_sms=148)["grid"] == 148
 
 
+def test_plan_multicast_clusters(lib):
+    # 128-row tiles on clusters of two CTAs sharing operands by TMA multicast: on request only
+    from ragged_grouped_gemm_02_gb300 import workloads as wl
+    counts = wl.workload_counts("skew16k")
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=counts)["multicast"] == 0
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=counts, multicast=1)
+    assert p["multicast"] == 1 and p["bm"] == 128 and p["bn"] in (128, 256) and p["tail64"] == 1
+    assert p["grid"] % 2 == 0 and p["grid"] <= 152 and p["threads"] == 192
+    # the automatic size-sorted walk becomes the front/back interleave
+    assert p["walk_order"] == 1
+    # BN 192 is not offered; the fused gate-up and FP8 ops take BN = 256
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, multicast=1, bn=128)["bn"] == 128
+    assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", multicast=1)["bn"] == 256
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8", multicast=1)
+    assert p["bn"] == 256 and p["bk"] == 128 and p["multicast"] == 1 and p["threads"] == 320
+    # one cluster at least, even when fewer CTAs are allowed
+    assert rgg.rgg_plan(4, 256, 256, 512, multicast=1, max_ctas=1)["grid"] == 2
+    assert rgg.rgg_plan(4, 256, 256, 512, multicast=1, max_ctas=7)["grid"] == 6
+    # the gather calls read whole boxes in the two-pass mode
+    p = rgg.rgg_plan(32, 512, 6144, 4096, host_counts=[16] * 32, op="gather", multicast=1)
+    assert p["gather_mode"] == 2 and p["multicast"] == 1
+
+
+@pytest.mark.parametrize("kw,status", [(dict(bm=64), "INVALID_ARG"), (dict(bm=256), "INVALID_ARG"),
+                                       (dict(bn=192), "INVALID_ARG"), (dict(walk_order=3), "INVALID_ARG"),
+                                       (dict(op="swiglu", bn=128), "INVALID_ARG"),
+                                       (dict(op="gather", gather_mode=1), "UNSUPPORTED"),
+                                       (dict(multicast=2), "INVALID_ARG"), (dict(multicast=-2), "INVALID_ARG")])
+def test_plan_multicast_rejects(lib, kw, status):
+    args = dict(multicast=1)
+    args.update(kw)
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_plan(4, 256, 256, 512, **args)
+    assert ei.value.status == getattr(rgg, "RGG_ERR_" + status)
+
+
 @pytest.mark.parametrize("kw", [dict(E=0), dict(K=12), dict(N=100), dict(K=4), dict(M_tot=-1),
                                 dict(M_tot=2 ** 31)])
 def test_plan_rejects_bad_sizes(lib, kw):
