@@ -68,7 +68,8 @@ def parse_args():
     p.add_argument("--multicast", type=int, default=0,
                    help="0 auto, 1 128-row tiles on clusters of two CTAs sharing operands by TMA multicast, -1 off")
     p.add_argument("--walk-order", type=int, default=0,
-                   help="0 list order, 1 front/back interleave, 2 scatter, 3 size-sorted interleave")
+                   help="0 auto, -1 list order, 1 front/back interleave, 2 scatter, 3 size-sorted interleave, "
+                        "4 N-major within each expert")
     p.add_argument("--op", default="gemm", choices=["gemm", "swiglu", "fp8", "gather", "swiglu_gather"],
                    help="gemm: Y = X.W; swiglu: the workload's weights read as [gate | up], "
                         "H = silu(X.W_gate) * (X.W_up) with N/2 output columns; fp8: the same draws "

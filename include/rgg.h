@@ -78,11 +78,14 @@ typedef struct rgg_options {
                                     rgg_grouped_gemm_fp8, 3 = plan rgg_grouped_gemm_gather, 4 = plan
                                     rgg_grouped_gemm_swiglu_gather (N is the output width) */
     int walk_order;              /* order of the persistent CTAs' walk over the tile list (any order gives the
-                                    same result): 0 = list order (the automatic choice unless host_counts
-                                    show a strong skew), 1 = front/back interleave, 2 = strided scatter,
+                                    same result): 0 = automatic (list order, or 3 when host_counts show a
+                                    strong skew, or 4 when experts average three M tiles or more),
+                                    1 = front/back interleave, 2 = strided scatter,
                                     3 = front/back interleave over the experts sorted by row count (E <= 256;
                                     chosen automatically when the largest expert holds over four times the
-                                    mean). */
+                                    mean), 4 = list order with each expert's tiles taken N tile by N tile
+                                    (the M tiles that read one weight panel run side by side), -1 = list
+                                    order, never replaced. */
     int gather_mode;             /* gather calls only: how the routed rows are fetched (same result either
                                     way).  1 = fused: the GEMM's producer loads them with TMA
                                     tile::gather4, four rows per copy, once per N tile; 2 = two-pass: a
@@ -101,8 +104,8 @@ typedef struct rgg_options {
                                     weight panel, neighbouring N tiles share the X rows); same result.
                                     0 = auto (currently off), 1 = on, -1 = off.  On: BN is 128 or 256
                                     (256 for the fused gate-up and FP8 ops), bm must be 0 or 128, walk
-                                    orders 0-2 (an automatic size-sorted walk becomes 1; asking for 3 is
-                                    RGG_ERR_INVALID_ARG), and the gather calls take the two-pass mode;
+                                    orders 0-2 (an automatic size-sorted walk becomes 1; asking for 3 or 4
+                                    is RGG_ERR_INVALID_ARG), and the gather calls take the two-pass mode;
                                     the fused-gather GEMM has no multicast form (RGG_ERR_UNSUPPORTED). */
 } rgg_options;
 

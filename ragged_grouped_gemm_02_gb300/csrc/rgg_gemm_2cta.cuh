@@ -154,7 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     auto tile_at = [&](int32_t p) -> TileCoord {
         const int32_t t = walk_tile(p, T, WO, WS);
         return WO == 3 ? decode_sorted_tile(s_off, s_order, s_spre, E, BM, kOutN, nN, t)
-                       : decode_tile(s_off, s_pre, E, BM, kOutN, nN, t);
+                       : decode_tile(s_off, s_pre, E, BM, kOutN, nN, t, WO == 4);
     };
 
     if (warp == 0) {

@@ -77,8 +77,11 @@ __device__ __forceinline__ void build_tile_prefix_warp(const int32_t* s_off, int
 
 // Decode flat tile t (0 <= t < s_pre[E]).  The expert is the last e with
 // s_pre[e] <= t, which skips empty experts because they add no tiles.
+// `n_major` (walk order 4) visits an expert's tiles N tile by N tile (all M
+// tiles of one weight panel, then the next panel) instead of M tile by M tile;
+// the set of tiles is the same.
 __device__ __forceinline__ TileCoord decode_tile(const int32_t* s_off, const int32_t* s_pre, int E, int BM,
-                                                 int BN, int n_tiles_n, int32_t t) {
+                                                 int BN, int n_tiles_n, int32_t t, bool n_major = false) {
     int lo = 0, hi = E;  // s_pre[lo] <= t < s_pre[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -86,9 +89,16 @@ __device__ __forceinline__ TileCoord decode_tile(const int32_t* s_off, const int
         else hi = mid;
     }
     const int32_t local = t - s_pre[lo];
-    const int32_t mt = local / n_tiles_n;
-    const int32_t nt = local - mt * n_tiles_n;
     const int32_t m_e = s_off[lo + 1] - s_off[lo];
+    int32_t mt, nt;
+    if (n_major) {
+        const int32_t nm = (m_e + BM - 1) / BM;
+        nt = local / nm;
+        mt = local - nt * nm;
+    } else {
+        mt = local / n_tiles_n;
+        nt = local - mt * n_tiles_n;
+    }
     TileCoord c;
     c.expert = lo;
     c.row0 = s_off[lo] + mt * BM;
@@ -104,6 +114,8 @@ __device__ __forceinline__ TileCoord decode_tile(const int32_t* s_off, const int
 // front of the list, odd ones from the back), which pairs the big experts at
 // one end of an expert-sorted list with the small ones at the other.
 // 2: strided scatter p -> p * s mod T with a prime s that does not divide T.
+// (3 is the size-sorted walk below; 4 is list order with each expert's tiles
+// taken N-major, see decode_tile.)
 __device__ __forceinline__ int32_t walk_stride_for(int32_t T) {
     const int32_t primes[4] = {7919, 6841, 5009, 1009};
     for (int i = 0; i < 4; ++i)

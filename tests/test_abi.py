@@ -135,6 +135,26 @@ def test_plan_grid_never_exceeds_tiles_or_sms(lib):
     assert rgg.rgg_plan(64, 16384, 1024, 2688, num_sms=148)["grid"] == 148
 
 
+def test_plan_walk_order_choice(lib):
+    from ragged_grouped_gemm_02_gb300 import workloads as wl
+    # experts of three M tiles or more: each expert's tiles walked N-major
+    p = rgg.rgg_plan(32, 32768, 6144, 4096, host_counts=wl.workload_counts("prefill"))
+    assert p["walk_order"] == 4
+    assert rgg.rgg_plan(32, 32768, 6144, 4096, host_counts=wl.workload_counts("prefill"), op="fp8")["walk_order"] == 4
+    assert rgg.rgg_plan(32, 32768, 6144, 4096)["walk_order"] == 4  # balanced estimate without counts
+    # one or two M tiles per expert: list order
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("uniform"))["walk_order"] == 0
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("uniform"), op="fp8")["walk_order"] == 0
+    assert rgg.rgg_plan(32, 512, 6144, 4096, host_counts=wl.workload_counts("decode"))["walk_order"] == 0
+    # strong skew: the size-sorted interleave
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("skew16k"))["walk_order"] == 3
+    # an explicit order is kept; -1 asks for list order
+    assert rgg.rgg_plan(32, 32768, 6144, 4096, walk_order=1)["walk_order"] == 1
+    assert rgg.rgg_plan(32, 32768, 6144, 4096, walk_order=-1)["walk_order"] == 0
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("skew16k"),
+                        walk_order=-1)["walk_order"] == 0
+
+
 def test_plan_multicast_clusters(lib):
     # 128-row tiles on clusters of two CTAs sharing operands by TMA multicast: on request only
     from ragged_grouped_gemm_02_gb300 import workloads as wl
@@ -160,6 +180,7 @@ def test_plan_multicast_clusters(lib):
 
 @pytest.mark.parametrize("kw,status", [(dict(bm=64), "INVALID_ARG"), (dict(bm=256), "INVALID_ARG"),
                                        (dict(bn=192), "INVALID_ARG"), (dict(walk_order=3), "INVALID_ARG"),
+                                       (dict(walk_order=4), "INVALID_ARG"),
                                        (dict(op="swiglu", bn=128), "INVALID_ARG"),
                                        (dict(op="gather", gather_mode=1), "UNSUPPORTED"),
                                        (dict(multicast=2), "INVALID_ARG"), (dict(multicast=-2), "INVALID_ARG")])
@@ -181,7 +202,8 @@ def test_plan_rejects_bad_sizes(lib, kw):
     assert ei.value.status == rgg.RGG_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("kw", [dict(bm=32), dict(bn=64), dict(stages=1), dict(stages=17), dict(max_ctas=-1)])
+@pytest.mark.parametrize("kw", [dict(bm=32), dict(bn=64), dict(stages=1), dict(stages=17), dict(max_ctas=-1),
+                                dict(walk_order=5), dict(walk_order=-2)])
 def test_plan_rejects_bad_options(lib, kw):
     with pytest.raises(rgg.RggError) as ei:
         rgg.rgg_plan(4, 256, 256, 512, **kw)

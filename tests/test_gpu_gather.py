@@ -101,7 +101,7 @@ def test_ragged_random_k_and_n_tails(bm, bn, mode):
 def test_auto_plan_many_tiles_and_walk_orders(mode):
     counts = [500, 3, 0, 257, 1024, 77, 129, 2, 640, 64]
     g = wl.make_gather_custom(counts, T=1100, K=512, N=1024, seed=93)
-    for walk in (0, 1, 3):
+    for walk in (0, 1, 3, 4):
         _check_close(g, _run(g, walk_order=walk, gather_mode=mode))
 
 

@@ -121,7 +121,7 @@ def test_integer_inputs_bit_exact_modes(bm, bn, tail64):
 
 
 @pytest.mark.parametrize("bm,bn", SHAPES + PAIR_SHAPES)
-@pytest.mark.parametrize("walk_order", [1, 2, 3])
+@pytest.mark.parametrize("walk_order", [1, 2, 3, 4])
 def test_integer_inputs_bit_exact_walk_orders(bm, bn, walk_order):
     # any walk over the tile list visits every tile exactly once
     counts = [3, 0, 130, 64, 1, 200, 65, 127, 129, 500]
