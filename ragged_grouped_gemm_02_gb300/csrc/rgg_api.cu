@@ -237,8 +237,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         if (skewed) walk = mc ? 1 : 3;
     }
     if (walk == 0 && !keep_list && !skewed && !mc && avg >= 3.0 * bm) walk = 4;
-    const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;
-    (void)units;
+    const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;  // persistent CTAs or CTA pairs
 
     const int64_t max_tiles = tile_bound(E, M_tot, N, bm, bn);
     if (max_tiles >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
@@ -293,19 +292,13 @@ constexpr double kFusedGatherMaxRows = 24.0;
 // tiles hold more than a couple of dozen rows (measured with 32 experts,
 // K = 6144, N = 4096: fused faster at 1 to 16 rows per expert, by 2% at 16;
 // two-pass faster at 32 rows, by 3%, and at 64, by 29%).
-rgg_status choose_gather_mode(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N,
-                              const rgg_options* opt, bool swiglu, int* mode) {
+rgg_status choose_gather_mode(int E, int64_t M_tot, const rgg_options* opt, int* mode) {
     const int want = opt ? opt->gather_mode : 0;
     if (want < 0 || want > 2) return RGG_ERR_INVALID_ARG;
     if (want != 0) {
         *mode = want;
         return RGG_OK;
     }
-    (void)num_sms;
-    (void)smem_optin;
-    (void)K;
-    (void)N;
-    (void)swiglu;
     if (opt && (opt->bm == 256 || opt->multicast == 1)) {  // CTA pairs and multicast clusters read whole boxes
         *mode = kGatherTwoPass;
         return RGG_OK;
@@ -530,7 +523,7 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     const bool gather = (op == 3 || op == 4);
     int mode = 0;
     if (gather) {
-        rgg_status sm = choose_gather_mode(num_sms, smem_optin, E, M_tot, K, N, opt, swiglu, &mode);
+        rgg_status sm = choose_gather_mode(E, M_tot, opt, &mode);
         if (sm != RGG_OK) return sm;
     }
     // the two-pass gather runs the plain (or fused gate-up) kernel on the gathered rows; the fused
@@ -773,7 +766,7 @@ rgg_status gather_call(rgg_handle* h, const void* X_tok, int64_t T, const int32_
     }
     const int NW = swiglu ? 2 * N : N;  // weight columns
     int mode = 0;
-    s = choose_gather_mode(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, swiglu, &mode);
+    s = choose_gather_mode(E, M_tot, opt, &mode);
     if (s != RGG_OK) return s;
     if (mode == kGatherTwoPass) {
         // Pass 1 writes the routed rows, in routed order, into the workspace;

@@ -15,10 +15,12 @@
 //    accumulator's two halves are synchronised separately so one tile's
 //    epilogue overlaps the next tile's main loop.
 //
-// CTA = 192 threads, one CTA per SM, persistent over tiles t = cta, cta+grid..
+// CTA = 192 threads (320 for the fused gate-up and FP8 epilogues), one CTA per
+// SM, persistent over tiles t = cta, cta+grid.. (or another walk order)
 //   warp 0   : TMA producer (one lane)          smem ring  <- X tile, W tile
 //   warp 1   : TMEM owner + MMA issuer (one lane) TMEM acc <- tcgen05.mma
-//   warps 2-5: epilogue                          Y        <- TMEM via registers
+//   warps 2-5: epilogue (2-9: two warps per      Y        <- TMEM via registers
+//              TMEM lane quadrant, see epilogue_warps)
 // The TMEM accumulator holds two BN-column buffers; acc_full/acc_empty
 // barriers per buffer let the epilogue of tile i run under the MMAs of i+1.
 //
@@ -50,9 +52,7 @@ constexpr int kStatusBadRowIndex = 7;
 constexpr int kStatusCapacity = 6;
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 192;
-constexpr int kEpilogueWarps = 4;
 constexpr int kBK = 64;                  // K elements per stage = one 128-byte swizzle row
-constexpr uint32_t kPanelBytes = 64 * 128;  // one 64-column W panel of 64 K rows
 constexpr uint64_t kDrainLimitNs = 2000000000ull;  // teardown waits for copies/MMAs already issued
 constexpr int32_t kDebugProducerStall = 1;  // test hook: the producer issues nothing
 

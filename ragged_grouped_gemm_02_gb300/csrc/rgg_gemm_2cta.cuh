@@ -18,8 +18,10 @@
 //   warp 1        : allocates the pair's TMEM in both CTAs; lane 0 of the
 //                   leader issues every MMA and commits to the empty /
 //                   acc_full barriers of both CTAs at once (multicast).
-//   warps 2-5     : epilogue of the CTA's own 128 rows; they arrive on the
-//                   leader's acc_empty (8 arrivals: 4 warps x 2 CTAs).
+//   warps 2-5     : epilogue of the CTA's own 128 rows (warps 2-9, two per
+//   (or 2-9)        TMEM lane quadrant, for the fused gate-up and FP8 epilogues);
+//                   they arrive on the leader's acc_empty (one arrival per
+//                   epilogue warp of both CTAs).
 // All waits are bounded; an abort raised in either CTA is mirrored into the
 // other CTA's flag so the pair leaves its loops together.
 #pragma once
