@@ -219,6 +219,21 @@ rgg_status rgg_export_tiles(rgg_handle* h, const int32_t* group_offsets, int E, 
                             void* stream);
 
 /*
+ * The same tile list in the order the persistent walk visits it: entry p is
+ * the tile at walk position p, which persistent CTA (or CTA pair) c of a grid
+ * of G visits in its (p / G)-th step when p % G == c.  walk_order as in
+ * rgg_options (0..4; 3 needs E <= 256, else RGG_ERR_UNSUPPORTED): 0 is the
+ * list order of rgg_export_tiles, 1 the front/back interleave, 2 the strided
+ * scatter, 3 the interleave over the experts sorted by row count, 4 each
+ * expert's tiles N tile by N tile.  Every order lists each tile exactly once.
+ * Decoded on the device by the code the GEMM kernels use; arguments, capacity
+ * and status as for rgg_export_tiles.
+ */
+rgg_status rgg_export_walk(rgg_handle* h, const int32_t* group_offsets, int E, int64_t M_tot, int N, int bm,
+                           int bn, int walk_order, int32_t* desc_out, int64_t cap, int32_t* n_tiles_out,
+                           void* stream);
+
+/*
  * Synchronize `stream`, read the device status word, reset it to RGG_OK and
  * return what it held (RGG_OK when no launch reported a problem).  Host-side
  * CUDA failures return RGG_ERR_CUDA.

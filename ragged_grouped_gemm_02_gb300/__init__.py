@@ -18,7 +18,8 @@ import threading
 
 __all__ = [
     "RggError", "rgg_grouped_gemm", "rgg_grouped_gemm_swiglu", "rgg_grouped_gemm_fp8", "rgg_grouped_gemm_gather",
-    "rgg_grouped_gemm_swiglu_gather", "rgg_grouped_gemm_noalloc", "rgg_export_tiles", "rgg_query_status",
+    "rgg_grouped_gemm_swiglu_gather", "rgg_grouped_gemm_noalloc", "rgg_export_tiles", "rgg_export_walk",
+    "rgg_query_status",
     "rgg_plan", "rgg_status_string", "library_path", "load_library", "EXPORTED_SYMBOLS",
     "RGG_OK", "RGG_ERR_INVALID_ARG", "RGG_ERR_UNSUPPORTED", "RGG_ERR_CUDA", "RGG_ERR_BAD_OFFSETS",
     "RGG_ERR_DEVICE_TIMEOUT", "RGG_ERR_CAPACITY", "RGG_ERR_BAD_ROW_INDEX",
@@ -41,7 +42,7 @@ _LIB_PATH = os.path.join(_PKG, "librgg.so")
 EXPORTED_SYMBOLS = (
     "rgg_create", "rgg_destroy", "rgg_grouped_gemm", "rgg_export_tiles", "rgg_query_status",
     "rgg_plan", "rgg_status_string", "rgg_last_cuda_error", "rgg_grouped_gemm_noalloc", "rgg_grouped_gemm_swiglu",
-    "rgg_grouped_gemm_fp8", "rgg_grouped_gemm_gather", "rgg_grouped_gemm_swiglu_gather",
+    "rgg_grouped_gemm_fp8", "rgg_grouped_gemm_gather", "rgg_grouped_gemm_swiglu_gather", "rgg_export_walk",
 )
 
 
@@ -94,6 +95,8 @@ def load_library() -> ctypes.CDLL:
         lib.rgg_grouped_gemm.restype = I
         lib.rgg_export_tiles.argtypes = [P, P, I, I64, I, I, I, P, I64, P, P]
         lib.rgg_export_tiles.restype = I
+        lib.rgg_export_walk.argtypes = [P, P, I, I64, I, I, I, I, P, I64, P, P]
+        lib.rgg_export_walk.restype = I
         lib.rgg_query_status.argtypes = [P, P]
         lib.rgg_query_status.restype = I
         lib.rgg_plan.argtypes = [I, I, I, I64, I, I, ctypes.POINTER(_Options), ctypes.POINTER(_PlanInfo)]
@@ -390,6 +393,18 @@ def rgg_export_tiles(group_offsets, M_tot: int, N: int, bm: int, bn: int, cap: i
     """The flat tile list the kernel walks, built on the device by the same
     code: returns (int32 CPU tensor [min(T, cap), 4] of (expert, row0, rows,
     col0), T).  Raises if the device rejects the offsets."""
+    return _export("rgg_export_tiles", group_offsets, M_tot, N, bm, bn, None, cap, stream)
+
+
+def rgg_export_walk(group_offsets, M_tot: int, N: int, bm: int, bn: int, walk_order: int, cap: int | None = None,
+                    stream=None):
+    """The same tile list in the order walk order ``walk_order`` (0..4)
+    visits it: row p is the tile at walk position p.  Returns (descriptors, T)
+    as rgg_export_tiles."""
+    return _export("rgg_export_walk", group_offsets, M_tot, N, bm, bn, int(walk_order), cap, stream)
+
+
+def _export(name, group_offsets, M_tot, N, bm, bn, walk_order, cap, stream):
     import torch
     E = group_offsets.numel() - 1
     device = group_offsets.device.index if group_offsets.device.index is not None else torch.cuda.current_device()
@@ -399,14 +414,16 @@ def rgg_export_tiles(group_offsets, M_tot: int, N: int, bm: int, bn: int, cap: i
     n = torch.empty(1, dtype=torch.int32, device=group_offsets.device)
     lib = load_library()
     st = _stream_ptr(stream, device)
-    s = lib.rgg_export_tiles(_handle(device), group_offsets.data_ptr(), E, int(M_tot), int(N), int(bm), int(bn),
-                             desc.data_ptr(), int(cap), n.data_ptr(), st)
+    args = [_handle(device), group_offsets.data_ptr(), E, int(M_tot), int(N), int(bm), int(bn)]
+    if walk_order is not None:
+        args.append(walk_order)
+    s = getattr(lib, name)(*args, desc.data_ptr(), int(cap), n.data_ptr(), st)
     if s != RGG_OK:
-        _raise(s, "rgg_export_tiles")
+        _raise(s, name)
     s = lib.rgg_query_status(_handle(device), st)
     T = int(n.item())
     if s not in (RGG_OK, RGG_ERR_CAPACITY):
-        _raise(s, "rgg_export_tiles (device status)")
+        _raise(s, name + " (device status)")
     return desc[: 4 * min(T, cap)].view(-1, 4).cpu(), T
 
 

@@ -723,9 +723,26 @@ rgg_status rgg_export_tiles(rgg_handle* h, const int32_t* group_offsets, int E, 
     if (tile_bound(E, M_tot, N, bm, bn) >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
     DeviceScope scope(h->device);
     if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
-    cudaError_t err = rgg::launch_export_tiles(group_offsets, E, M_tot, N, bm, bn, desc_out, cap, n_tiles_out,
+    cudaError_t err = rgg::launch_export_tiles(group_offsets, E, M_tot, N, bm, bn, 0, desc_out, cap, n_tiles_out,
                                                h->d_status, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "export_tiles launch");
+}
+
+rgg_status rgg_export_walk(rgg_handle* h, const int32_t* group_offsets, int E, int64_t M_tot, int N, int bm,
+                           int bn, int walk_order, int32_t* desc_out, int64_t cap, int32_t* n_tiles_out,
+                           void* stream) {
+    if (!h || !group_offsets || !n_tiles_out || cap < 0 || (cap > 0 && !desc_out)) return RGG_ERR_INVALID_ARG;
+    if (E < 1 || E > rgg::kMaxExperts || M_tot < 0 || M_tot >= (int64_t(1) << 31) || N < 1)
+        return RGG_ERR_INVALID_ARG;
+    if ((bm != 64 && bm != 128 && bm != 256) || (bn != 128 && bn != 192 && bn != 256)) return RGG_ERR_INVALID_ARG;
+    if (walk_order < 0 || walk_order > 4) return RGG_ERR_INVALID_ARG;
+    if (walk_order == 3 && E > rgg::kMaxSortedExperts) return RGG_ERR_UNSUPPORTED;
+    if (tile_bound(E, M_tot, N, bm, bn) >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
+    DeviceScope scope(h->device);
+    if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
+    cudaError_t err = rgg::launch_export_tiles(group_offsets, E, M_tot, N, bm, bn, walk_order, desc_out, cap,
+                                               n_tiles_out, h->d_status, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? RGG_OK : cuda_failure(err, "export_walk launch");
 }
 
 rgg_status rgg_query_status(rgg_handle* h, void* stream) {

@@ -380,9 +380,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     const int32_t WS = walk_stride_for(T);
     // The tile visited at walk position p.
     auto tile_at = [&](int32_t p) -> TileCoord {
-        const int32_t t = walk_tile(p, T, WO, WS);
-        return WO == 3 ? decode_sorted_tile(s_off, s_order, s_spre, E, BM, kOutN, nN, t)
-                       : decode_tile(s_off, s_pre, E, BM, kOutN, nN, t, WO == 4);
+        return walk_decode(s_off, s_pre, s_order, s_spre, E, BM, kOutN, nN, T, WO, WS, p);
     };
 
     if (kGather == kGatherTma && warp == 0) {

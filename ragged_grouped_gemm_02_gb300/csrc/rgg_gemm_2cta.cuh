@@ -154,9 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     const int WO = args.walk_order;  // walk position t visits tile walk_tile(t, ...), the same in both CTAs
     const int32_t WS = walk_stride_for(T);
     auto tile_at = [&](int32_t p) -> TileCoord {
-        const int32_t t = walk_tile(p, T, WO, WS);
-        return WO == 3 ? decode_sorted_tile(s_off, s_order, s_spre, E, BM, kOutN, nN, t)
-                       : decode_tile(s_off, s_pre, E, BM, kOutN, nN, t, WO == 4);
+        return walk_decode(s_off, s_pre, s_order, s_spre, E, BM, kOutN, nN, T, WO, WS, p);
     };
 
     if (warp == 0) {

@@ -67,9 +67,10 @@ constexpr int kMcFp8 = 2;
 cudaError_t launch_gemm_mc(int kind, int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                            const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 
-// The flat tile list written out by the same device code the GEMM uses.
+// The flat tile list written out by the same device code the GEMM uses, in
+// list order (walk_order 0) or in the order walk_order visits it.
 cudaError_t launch_export_tiles(const int32_t* offsets, int E, int64_t M_tot, int N, int bm, int bn,
-                                int32_t* desc, int64_t cap, int32_t* n_tiles, int32_t* status,
+                                int walk_order, int32_t* desc, int64_t cap, int32_t* n_tiles, int32_t* status,
                                 cudaStream_t stream);
 
 // Host helpers defined in rgg_api.cu: the X / W tensor maps for a tile of

@@ -198,6 +198,17 @@ __device__ __forceinline__ TileCoord decode_sorted_tile(const int32_t* s_off, co
     return c;
 }
 
+// The tile visited at walk position p (0 <= p < T) under walk order WO (WS =
+// walk_stride_for(T)): the decode every GEMM kernel and the walk export use.
+// s_order / s_spre are read only for the size-sorted walk (3).
+__device__ __forceinline__ TileCoord walk_decode(const int32_t* s_off, const int32_t* s_pre, const int32_t* s_order,
+                                                 const int32_t* s_spre, int E, int BM, int BN, int n_tiles_n,
+                                                 int32_t T, int WO, int32_t WS, int32_t p) {
+    const int32_t t = walk_tile(p, T, WO, WS);
+    if (WO == 3) return decode_sorted_tile(s_off, s_order, s_spre, E, BM, BN, n_tiles_n, t);
+    return decode_tile(s_off, s_pre, E, BM, BN, n_tiles_n, t, WO == 4);
+}
+
 // ---------------------------------------------------------------------------
 // Two-tile units for clusters of two CTAs that share one operand through TMA
 // multicast.  A unit holds one tile for each CTA of the cluster, of the same

@@ -256,6 +256,54 @@ def test_tile_list_capacity():
     assert np.array_equal(desc.numpy(), ref[:5])
 
 
+def _walk_reference(off, N, bm, bn, walk_order):
+    """The visit order of each walk, restated from its definition on top of
+    the oracle's list-order enumeration."""
+    ref = oracle.tile_list(off, N, bm, bn)
+    T = ref.shape[0]
+    if walk_order == 0:
+        return ref
+    if walk_order == 1:
+        return ref[[(T - 1 - (p >> 1)) if (p & 1) else (p >> 1) for p in range(T)]]
+    if walk_order == 2:
+        stride = next((q for q in (7919, 6841, 5009, 1009) if T % q), 1)
+        return ref[[(p * stride) % T for p in range(T)]]
+    counts = np.diff(np.asarray(off, dtype=np.int64))
+    first = {}
+    for i, e in enumerate(ref[:, 0]):
+        first.setdefault(int(e), i)
+    if walk_order == 4:  # each expert's tiles by (N tile, M tile)
+        out = []
+        for e in sorted(first):
+            block = ref[ref[:, 0] == e]
+            out.append(block[np.lexsort((block[:, 1], block[:, 3]))])
+        return np.concatenate(out) if out else ref
+    # 3: experts by decreasing row count (ties by index), their tiles in list order, then front/back
+    order = sorted(range(counts.size), key=lambda e: (-counts[e], e))
+    seq = np.concatenate([ref[ref[:, 0] == e] for e in order if e in first])
+    return seq[[(T - 1 - (p >> 1)) if (p & 1) else (p >> 1) for p in range(T)]]
+
+
+@pytest.mark.parametrize("bm,bn", [(64, 128), (128, 256), pytest.param(256, 256, marks=pytest.mark.pair)])
+@pytest.mark.parametrize("name", ["tiny", "decode", "uniform", "skew16k", "skew2k", "prefill", "worklog_skew16k"])
+@pytest.mark.parametrize("walk_order", [0, 1, 2, 3, 4])
+def test_walk_export_bit_exact(name, bm, bn, walk_order):
+    # the order in which the persistent CTAs visit the tiles, written out by the kernels' own decode
+    w = wl.WORKLOADS[name]
+    counts = wl.workload_counts(w)
+    off = wl.offsets_from_counts(counts)
+    M = int(counts.sum())
+    d_off = torch.from_numpy(np.asarray(off, dtype=np.int32)).cuda()
+    desc, T = rgg.rgg_export_walk(d_off, M, w.N, bm, bn, walk_order)
+    canon = oracle.tile_list(off, w.N, bm, bn)
+    assert T == canon.shape[0]
+    got = desc.numpy()
+    # a permutation of the list: every tile exactly once
+    key = lambda a: a[np.lexsort(a.T[::-1])]  # noqa: E731
+    assert np.array_equal(key(got), key(canon))
+    assert np.array_equal(got, _walk_reference(off, w.N, bm, bn, walk_order))
+
+
 # --------------------------------------------------------- full-size configs
 
 FULL = ["decode", "uniform", "skew16k", "skew2k", "prefill"] + [
