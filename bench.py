@@ -5,7 +5,9 @@ A step is one launch of the whole hot path: Y_e = X_e . W_e for every expert
 of one batch of synthetic input (offsets -> tile list -> TMA -> tcgen05 ->
 epilogue, all inside the kernel).  The metric is useful TFLOP/s,
 2 * M_tot * K * N / t ("Grouped GEMM for Imbalanced Experts on Blackwell: A WIP
-Worklog", section 1), with t measured on the device with CUDA events.
+Worklog", section 1), with t measured on the device with CUDA events around K
+replays of one step captured in a CUDA graph (the same K steps launched one by
+one from the host are reported beside it as "eager").
 
 Default workload: the small-decode, weight-bound configuration -- 32 experts
 x 16 rows, K = 6144, N = 4096 (the decode example of "Pearl's grouped GEMM
