@@ -137,3 +137,35 @@ def test_four_million_rows_sampled():
     ref = oracle.grouped_gemm_points(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets, rows, cols)
     got = Y[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
     _close(got, ref)
+
+
+@pytest.mark.parametrize("opts", [dict(bm=64, bn=256), dict(bm=128, bn=256), dict(bm=256, bn=256),
+                                  dict(bm=128, bn=192, walk_order=3), dict(bm=256, bn=256, walk_order=4)],
+                         ids=["64x256", "128x256", "pair", "128x192-sorted", "pair-nmajor"])
+@pytest.mark.parametrize("max_ctas", [1, 2, 3, 37])
+def test_few_persistent_ctas_walk_every_tile(opts, max_ctas):
+    # a grid far smaller than the tile count: each CTA (or pair) walks many tiles, rings wrap many times
+    counts = [3, 0, 130, 64, 1, 200, 65, 127, 129, 500]
+    inp = wl.make_custom(counts, K=128, N=392, seed=153, integer_valued=True, spare_rows=2)
+    K64 = wl.make_custom(counts, K=64, N=392, seed=153, integer_valued=True, spare_rows=2)
+    for case in (inp, K64):
+        Y = _run(case, max_ctas=max_ctas, **opts)
+        ref = oracle.grouped_gemm(wl.bf16_bits(case.X), wl.bf16_bits(case.W), case.offsets)
+        M = int(case.offsets[-1])
+        if case is K64:
+            assert np.array_equal(Y[:M].double().numpy(), ref[:M])
+        else:
+            _close(Y[:M].double().numpy(), ref[:M])
+        assert bool((Y.view(torch.int16)[M:] == CANARY).all())
+
+
+def test_host_counts_that_disagree_with_the_device_offsets():
+    # host counts only steer the plan; the kernels read the offsets on the device
+    counts = np.array([700, 0, 3, 260, 1, 90])
+    inp = wl.make_custom(counts, K=64, N=264, seed=154, integer_valued=True, spare_rows=3)
+    ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
+    M = int(inp.offsets[-1])
+    for wrong in ([16] * 6, [1000, 1000, 1000, 1000, 1000, 1000], [0, 0, 0, 0, 0, 1054], counts[::-1]):
+        Y = _run(inp, host_counts=np.asarray(wrong))
+        assert np.array_equal(Y[:M].double().numpy(), ref[:M]), wrong
+        assert bool((Y.view(torch.int16)[M:] == CANARY).all())
