@@ -130,9 +130,16 @@ typedef struct rgg_plan_info {
 /*
  * Create a handle bound to CUDA device `device`: queries the SM count and the
  * shared-memory limit, checks for compute capability 10.3 (sm_103), and
- * allocates the device status word (the only device allocation the library
- * makes, once per handle).  On success *out owns the handle; release it with
- * rgg_destroy.  Returns RGG_ERR_UNSUPPORTED on any other GPU.
+ * allocates the device status word (once per handle; the only other device
+ * allocation is the two-pass gather's workspace, made by a gather call only
+ * when the caller passes none).  On success *out owns the handle; release it
+ * with rgg_destroy.  Returns RGG_ERR_UNSUPPORTED on any other GPU.
+ *
+ * Concurrency: calls on one handle may run on any streams, but they share the
+ * handle's status word (rgg_query_status returns the first error any of them
+ * recorded) and its gather workspace (two-pass gather calls that use it must
+ * be ordered on one stream, or pass their own rgg_options.workspace).  Use a
+ * handle from several host threads only under the caller's own lock.
  */
 rgg_status rgg_create(rgg_handle** out, int device);
 
