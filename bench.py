@@ -67,8 +67,6 @@ def parse_args():
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--tail64", type=int, default=0, help="0 auto, 1 on, -1 off")
     p.add_argument("--gather-mode", type=int, default=0, help="gather ops: 0 auto, 1 TMA gather4, 2 two-pass")
-    p.add_argument("--multicast", type=int, default=0,
-                   help="0 auto, 1 128-row tiles on clusters of two CTAs sharing operands by TMA multicast, -1 off")
     p.add_argument("--walk-order", type=int, default=0,
                    help="0 auto, -1 list order, 1 front/back interleave, 2 scatter, 3 size-sorted interleave, "
                         "4 N-major within each expert")
@@ -271,13 +269,13 @@ def run_profile(args):
     off = torch.from_numpy(inp.offsets).to(dev)
     Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device=dev)
     opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
-                walk_order=args.walk_order, multicast=args.multicast,
-                host_counts=inp.counts)
+                walk_order=args.walk_order, host_counts=inp.counts)
     if args.op == "gather":
         # the same recipe as the timed gather op: M_tot tokens, distinct tokens per expert
         gen = torch.Generator().manual_seed(inp.workload.seed + 7)
         idx = torch.from_numpy(wl.routed_row_index(inp.counts, X.shape[0], gen)).to(dev)
         opts["gather_mode"] = args.gather_mode
+        opts["workspace"] = torch.empty_like(X)  # the two-pass mode's gathered rows
 
         def launch():
             rgg.rgg_grouped_gemm_gather(X, idx, W, off, Y, **opts)
@@ -359,10 +357,10 @@ def run_ours(args):
     # The tile shape is planned from the routed counts, known on the host as in
     # the worklog's harness; the kernel itself reads the offsets on the device.
     opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
-                walk_order=args.walk_order, multicast=args.multicast,
-                host_counts=inp.counts)
+                walk_order=args.walk_order, host_counts=inp.counts)
     if gather:
         opts["gather_mode"] = args.gather_mode
+        opts["workspace"] = torch.empty_like(X)  # the two-pass mode's gathered rows, allocated once
     plan = rgg.rgg_plan(E, M_tot, K, N_out, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
                         op=args.op, **opts)
     stream = torch.cuda.current_stream(dev)

@@ -91,22 +91,15 @@ typedef struct rgg_options {
                                     tile::gather4, four rows per copy, once per N tile; 2 = two-pass: a
                                     row-gather kernel writes them once, in routed order, into a workspace
                                     and the grouped GEMM reads that with whole-tile TMA boxes.  0 = auto:
-                                    fused when the tile plan takes 64-row tiles (small expert groups),
-                                    else two-pass. */
+                                    two-pass when the experts that have rows average more than 24 rows and
+                                    the caller passes a workspace, else fused. */
     void* workspace;             /* two-pass gather only: caller-owned device memory of at least
-                                    workspace_bytes = M_tot * K * 2 bytes, 16-byte aligned (rgg_plan
-                                    reports the size).  NULL: the handle keeps its own workspace and
-                                    grows it with cudaMalloc when a call needs more (that call then
-                                    allocates, and waits for the device while freeing the old one). */
+                                    M_tot * K * 2 bytes, 16-byte aligned (rgg_plan reports the size in
+                                    rgg_plan_info.workspace_bytes).  The library never allocates inside a
+                                    call: without a workspace the automatic mode runs the fused gather,
+                                    and gather_mode = 2 (or bm = 256, which only the two-pass mode can
+                                    run) is RGG_ERR_INVALID_ARG. */
     int64_t workspace_bytes;     /* size of `workspace` in bytes */
-    int multicast;               /* 128-row tiles on clusters of two CTAs that share one operand of each pair of
-                                    tiles through TMA multicast (consecutive M tiles of an expert share the
-                                    weight panel, neighbouring N tiles share the X rows); same result.
-                                    0 = auto (currently off), 1 = on, -1 = off.  On: BN is 128 or 256
-                                    (256 for the fused gate-up and FP8 ops), bm must be 0 or 128, walk
-                                    orders 0-2 (an automatic size-sorted walk becomes 1; asking for 3 or 4
-                                    is RGG_ERR_INVALID_ARG), and the gather calls take the two-pass mode;
-                                    the fused-gather GEMM has no multicast form (RGG_ERR_UNSUPPORTED). */
 } rgg_options;
 
 #define RGG_DEBUG_PRODUCER_STALL 1
@@ -122,24 +115,24 @@ typedef struct rgg_plan_info {
     int64_t max_tiles;           /* upper bound on the flat tile count for these sizes */
     int tail64;                  /* 1 when tail tiles run as shorter MMAs (see rgg_options.tail64) */
     int walk_order;              /* walk order (see rgg_options) */
-    int gather_mode;             /* gather ops: 1 = fused tile::gather4, 2 = two-pass; else 0 */
-    int64_t workspace_bytes;     /* two-pass gather: workspace the call needs; else 0 */
-    int multicast;               /* 1 when the plan runs the cluster-multicast kernel (see rgg_options) */
+    int gather_mode;             /* gather ops: the mode the call runs with these options (1 = fused
+                                    tile::gather4, 2 = two-pass); else 0 */
+    int64_t workspace_bytes;     /* gather ops: the workspace the two-pass mode needs when it is asked
+                                    for, or when the automatic choice prefers it (it runs only with a
+                                    caller workspace); else 0 */
 } rgg_plan_info;
 
 /*
  * Create a handle bound to CUDA device `device`: queries the SM count and the
  * shared-memory limit, checks for compute capability 10.3 (sm_103), and
- * allocates the device status word (once per handle; the only other device
- * allocation is the two-pass gather's workspace, made by a gather call only
- * when the caller passes none).  On success *out owns the handle; release it
- * with rgg_destroy.  Returns RGG_ERR_UNSUPPORTED on any other GPU.
+ * allocates the device status word (once per handle; no call allocates device
+ * memory after this).  On success *out owns the handle; release it with
+ * rgg_destroy.  Returns RGG_ERR_UNSUPPORTED on any other GPU.
  *
  * Concurrency: calls on one handle may run on any streams, but they share the
  * handle's status word (rgg_query_status returns the first error any of them
- * recorded) and its gather workspace (two-pass gather calls that use it must
- * be ordered on one stream, or pass their own rgg_options.workspace).  Use a
- * handle from several host threads only under the caller's own lock.
+ * recorded).  Use a handle from several host threads only under the caller's
+ * own lock.
  */
 rgg_status rgg_create(rgg_handle** out, int device);
 
@@ -178,8 +171,9 @@ rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const i
  * W13: bf16 [E, K, 2N] (gate columns [0, N), up columns [N, 2N)); H: bf16
  * [M_tot, N].  Each tile loads BN/2 gate and the matching BN/2 up columns,
  * one MMA of width BN puts both in TMEM, and the epilogue forms silu(g) * u in
- * fp32 before rounding once to bf16.  Tiles are 1-CTA (rgg_options.bm 0, 64
- * or 128; bn 0, 128 or 256, the MMA width).  Other arguments, requirements
+ * fp32 before rounding once to bf16.  Tiles are 64 or 128 rows on one CTA
+ * or 256 rows on a CTA pair (rgg_options.bm 0, 64, 128 or 256; bn 0, 128 or
+ * 256, the MMA width).  Other arguments, requirements
  * (N % 8 == 0 here is the output width) and errors as for rgg_grouped_gemm.
  */
 rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13, const int32_t* group_offsets,
@@ -266,16 +260,16 @@ const char* rgg_last_cuda_error(void);
 
 /*
  * rgg_grouped_gemm_noalloc -- the same product as rgg_grouped_gemm (default
- * options, same kernel and tile plan) for callers that cannot allocate device
- * memory.  The pages have no counterpart to this entry point.
+ * options, same plan, kernels and launch code) for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry point.
  *
  * Who needs it: code that must not call cudaMalloc where it runs the GEMM --
- * an inference-engine plugin whose execute step may not allocate, code running
- * while a stream is captured into a CUDA graph in global capture mode (where
- * cudaMalloc is refused), a process whose device memory all belongs to a pool
- * allocator.  rgg_grouped_gemm needs a handle, and rgg_create allocates the
- * handle's status word.  This call takes no handle and allocates nothing: no
- * cudaMalloc, no cudaFree, no allocating library routine.
+ * an inference-engine plugin whose execute step runs inside the engine's
+ * memory budget and may not allocate, or a process whose device memory all
+ * belongs to a pool allocator that other code may not go around.
+ * rgg_grouped_gemm needs a handle, and rgg_create allocates the handle's status
+ * word.  This call takes no handle and allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
  *
  * Scratch: the kernel's only scratch (its 4-byte status word) lives in a
  * file-scope device array of 256 bytes that every GPU which loads librgg.so
@@ -287,7 +281,9 @@ const char* rgg_last_cuda_error(void);
  * The call runs on the current CUDA device.  Its first call on a device sets
  * up that device (it looks up the array's device address with
  * cudaGetSymbolAddress and reads the SM count); make that first call before
- * any stream capture.  Each call clears the status word, launches the kernel
+ * any stream capture.  The address is kept for the life of the process: do not
+ * use this entry point on a device after cudaDeviceReset() on that device.
+ * Each call clears the status word, launches the kernel
  * and, when status_out is not NULL, copies the final status word into
  * *status_out (device memory or pinned host memory, int32): RGG_OK,
  * RGG_ERR_BAD_OFFSETS or RGG_ERR_DEVICE_TIMEOUT, valid once the stream has
@@ -327,11 +323,13 @@ rgg_status rgg_grouped_gemm_noalloc(const void* X, const void* W, const int32_t*
  * W, group_offsets, Y, E, M_tot, K, N: as for rgg_grouped_gemm; Y is in
  *            routed (grouped) row order.
  * Options as for rgg_grouped_gemm, plus gather_mode and workspace; fused
- * tiles are 64 or 128 rows (no CTA pair).  Two-pass calls without a caller
- * workspace use the handle's, so such calls on different streams race on it.
+ * tiles are 64 or 128 rows (no CTA pair).  The two-pass mode runs only with a
+ * caller workspace (rgg_options.workspace; the call allocates nothing): calls
+ * that share one workspace must be ordered on one stream.
  * Errors: as for rgg_grouped_gemm, plus RGG_ERR_BAD_ROW_INDEX (device-detected,
  * read with rgg_query_status) and RGG_ERR_INVALID_ARG for a workspace that is
- * too small or misaligned.  Asynchronous on `stream`.
+ * missing (gather_mode = 2 or bm = 256), too small or misaligned.
+ * Asynchronous on `stream`.
  */
 rgg_status rgg_grouped_gemm_gather(rgg_handle* h, const void* X_tok, int64_t T, const int32_t* row_index,
                                    const void* W, const int32_t* group_offsets, void* Y, int E, int64_t M_tot,

@@ -57,15 +57,14 @@ class _Options(ctypes.Structure):
                 ("max_ctas", ctypes.c_int), ("timeout_ns", ctypes.c_uint64), ("host_counts", ctypes.c_void_p),
                 ("debug_flags", ctypes.c_int), ("tail64", ctypes.c_int),
                 ("op", ctypes.c_int), ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64), ("multicast", ctypes.c_int)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64)]
 
 
 class _PlanInfo(ctypes.Structure):
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int), ("stages", ctypes.c_int),
                 ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("tmem_cols", ctypes.c_int), ("max_tiles", ctypes.c_int64), ("tail64", ctypes.c_int),
-                ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int), ("workspace_bytes", ctypes.c_int64),
-                ("multicast", ctypes.c_int)]
+                ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int), ("workspace_bytes", ctypes.c_int64)]
 
 
 _lock = threading.Lock()
@@ -145,16 +144,23 @@ def _handle(device: int) -> ctypes.c_void_p:
 
 
 def _options(bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0, tail64=0,
-             op=0, walk_order=0, gather_mode=0, multicast=0):
+             op=0, walk_order=0, gather_mode=0):
     opt = _Options(int(bm), int(bn), int(stages), int(max_ctas), int(timeout_ns), None, int(debug_flags),
                    int(tail64), int(op), int(walk_order), int(gather_mode))
-    opt.multicast = int(multicast)
     keep = None
     if host_counts is not None:
         import numpy as np
         keep = np.ascontiguousarray(np.asarray(host_counts, dtype=np.int32))
         opt.host_counts = keep.ctypes.data
     return opt, keep
+
+
+def _set_workspace(opt, workspace):
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        opt.workspace = workspace.data_ptr()
+        opt.workspace_bytes = workspace.numel() * workspace.element_size()
 
 
 def _stream_ptr(stream, device):
@@ -165,8 +171,7 @@ def _stream_ptr(stream, device):
 
 
 def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
-                     host_counts=None, debug_flags=0, tail64=0, walk_order=0, multicast=0, stream=None,
-                     check=False):
+                     host_counts=None, debug_flags=0, tail64=0, walk_order=0, stream=None, check=False):
     """Y_e = X_e . W_e for every expert (one kernel launch, asynchronous).
 
     X: bf16 CUDA [M_tot, K]; W: bf16 CUDA [E, K, N]; group_offsets: int32
@@ -195,8 +200,7 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
     elif Y.shape != (M_tot, N) or Y.dtype != torch.bfloat16 or not Y.is_contiguous() or not Y.is_cuda:
         raise ValueError("Y must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0,
-                         walk_order, multicast=multicast)
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm(_handle(device), X.data_ptr(), W.data_ptr(), group_offsets.data_ptr(), Y.data_ptr(),
                              E, M_tot, K, N, st, ctypes.byref(opt))
@@ -211,8 +215,7 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
 
 
 def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
-                            host_counts=None, debug_flags=0, tail64=0, walk_order=0, multicast=0, stream=None,
-                            check=False):
+                            host_counts=None, debug_flags=0, tail64=0, walk_order=0, stream=None, check=False):
     """H = silu(X_e . W13_e[:, :N]) * (X_e . W13_e[:, N:]) for every expert,
     one kernel launch (the fused gate-up projection with SiLU activation).
 
@@ -237,8 +240,7 @@ def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages
     elif H.shape != (M_tot, N) or H.dtype != torch.bfloat16 or not H.is_contiguous() or not H.is_cuda:
         raise ValueError("H must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64,
-                         0, walk_order, multicast=multicast)
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm_swiglu(_handle(device), X.data_ptr(), W13.data_ptr(), group_offsets.data_ptr(),
                                     H.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
@@ -253,8 +255,8 @@ def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages
 
 
 def rgg_grouped_gemm_fp8(X8, W8, sx, sw, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0,
-                         timeout_ns=0, host_counts=None, debug_flags=0, tail64=0, walk_order=0,
-                         multicast=0, stream=None, check=False):
+                         timeout_ns=0, host_counts=None, debug_flags=0, tail64=0, walk_order=0, stream=None,
+                         check=False):
     """Y[i, j] = sx[i] * sw[e, j] * (X8_e . W8_e)[i, j] with FP8 E4M3 operands.
 
     X8: float8_e4m3fn CUDA [M_tot, K]; W8: float8_e4m3fn CUDA [E, K, N];
@@ -278,8 +280,7 @@ def rgg_grouped_gemm_fp8(X8, W8, sx, sw, group_offsets, Y=None, *, bm=0, bn=0, s
     elif Y.shape != (M_tot, N) or Y.dtype != torch.bfloat16 or not Y.is_contiguous() or not Y.is_cuda:
         raise ValueError("Y must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64,
-                         0, walk_order, multicast=multicast)
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm_fp8(_handle(device), X8.data_ptr(), W8.data_ptr(), sx.data_ptr(), sw.data_ptr(),
                                  group_offsets.data_ptr(), Y.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
@@ -316,8 +317,7 @@ def rgg_grouped_gemm_noalloc(X, W, group_offsets, Y=None, status_out=None, strea
 
 
 def _gather_call(name, X_tok, row_index, W, group_offsets, out, swiglu, bm, bn, stages, max_ctas, timeout_ns,
-                 host_counts, debug_flags, tail64, walk_order, gather_mode, workspace, stream, check,
-                 multicast=0):
+                 host_counts, debug_flags, tail64, walk_order, gather_mode, workspace, stream, check):
     import torch
     if not (X_tok.is_cuda and row_index.is_cuda and W.is_cuda and group_offsets.is_cuda):
         raise ValueError("X_tok, row_index, W and group_offsets must be CUDA tensors")
@@ -340,12 +340,8 @@ def _gather_call(name, X_tok, row_index, W, group_offsets, out, swiglu, bm, bn, 
         raise ValueError("the output must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
     opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order,
-                         gather_mode, multicast)
-    if workspace is not None:
-        if not (workspace.is_cuda and workspace.is_contiguous()):
-            raise ValueError("workspace must be a contiguous CUDA tensor")
-        opt.workspace = workspace.data_ptr()
-        opt.workspace_bytes = workspace.numel() * workspace.element_size()
+                         gather_mode)
+    _set_workspace(opt, workspace)
     st = _stream_ptr(stream, device)
     s = getattr(lib, name)(_handle(device), X_tok.data_ptr(), T, row_index.data_ptr(), W.data_ptr(),
                            group_offsets.data_ptr(), out.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))
@@ -361,7 +357,7 @@ def _gather_call(name, X_tok, row_index, W, group_offsets, out, swiglu, bm, bn, 
 
 def rgg_grouped_gemm_gather(X_tok, row_index, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0,
                             timeout_ns=0, host_counts=None, debug_flags=0, tail64=0, walk_order=0, gather_mode=0,
-                            workspace=None, multicast=0, stream=None, check=False):
+                            workspace=None, stream=None, check=False):
     """Y[i] = X_tok[row_index[i]] . W_e for every routed row i of expert e,
     the token gather fused into the kernel's activation loads.
 
@@ -369,24 +365,24 @@ def rgg_grouped_gemm_gather(X_tok, row_index, W, group_offsets, Y=None, *, bm=0,
     [E, K, N]; group_offsets: int32 CUDA [E+1]; Y: optional bf16 CUDA
     [M_tot, N] (routed row order).  gather_mode: 0 auto, 1 fused (TMA
     tile::gather4 in the GEMM), 2 two-pass (row gather into a workspace, then
-    the grouped GEMM); workspace: optional CUDA tensor of at least M_tot*K*2
-    bytes for the two-pass mode (else the handle's own is used)."""
+    the grouped GEMM); workspace: CUDA tensor of at least M_tot*K*2 bytes,
+    needed by the two-pass mode (the library allocates nothing: without one
+    the automatic mode runs the fused gather)."""
     return _gather_call("rgg_grouped_gemm_gather", X_tok, row_index, W, group_offsets, Y, False, bm, bn, stages,
                         max_ctas, timeout_ns, host_counts, debug_flags, tail64, walk_order, gather_mode, workspace,
-                        stream, check, multicast)
+                        stream, check)
 
 
 def rgg_grouped_gemm_swiglu_gather(X_tok, row_index, W13, group_offsets, H=None, *, bm=0, bn=0, stages=0,
                                    max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0, tail64=0,
-                                   walk_order=0, gather_mode=0, workspace=None, multicast=0, stream=None,
-                                   check=False):
+                                   walk_order=0, gather_mode=0, workspace=None, stream=None, check=False):
     """H[i] = silu(x W13_e[:, :N]) * (x W13_e[:, N:]) with x = X_tok[row_index[i]]:
     the fused gate-up projection reading its tokens through the gather.
 
     W13: bf16 CUDA [E, K, 2N] (gate columns first); H: optional bf16 CUDA [M_tot, N]."""
     return _gather_call("rgg_grouped_gemm_swiglu_gather", X_tok, row_index, W13, group_offsets, H, True, bm, bn,
                         stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, walk_order, gather_mode,
-                        workspace, stream, check, multicast)
+                        workspace, stream, check)
 
 
 def rgg_export_tiles(group_offsets, M_tot: int, N: int, bm: int, bn: int, cap: int | None = None, stream=None):
@@ -437,13 +433,21 @@ def rgg_query_status(device: int | None = None, stream=None) -> int:
 
 def rgg_plan(E: int, M_tot: int, K: int, N: int, *, num_sms: int = 0, smem_optin: int = 0, bm=0, bn=0,
              stages=0, max_ctas=0, host_counts=None, tail64=0, op: str = "gemm",
-             walk_order=0, gather_mode=0, multicast=0) -> dict:
+             walk_order=0, gather_mode=0, workspace=None) -> dict:
     """The launch configuration rgg_grouped_gemm (op="gemm") or
-    rgg_grouped_gemm_swiglu (op="swiglu", N = output width) would use (host-only)."""
+    rgg_grouped_gemm_swiglu (op="swiglu", N = output width) would use (host-only).
+    For the gather ops, ``workspace`` (the tensor the call would get, True
+    for "a workspace will be given", or None) decides whether the two-pass
+    mode can run; the planner only looks at whether there is one."""
     lib = load_library()
     opt, keep = _options(bm, bn, stages, max_ctas, 0, host_counts, 0, tail64,
                          {"gemm": 0, "swiglu": 1, "fp8": 2, "gather": 3, "swiglu_gather": 4}[op], walk_order,
-                         gather_mode, multicast)
+                         gather_mode)
+    if workspace is True:
+        opt.workspace = 16  # never dereferenced: rgg_plan reads only whether a workspace is given
+        opt.workspace_bytes = 1 << 62
+    else:
+        _set_workspace(opt, workspace)
     info = _PlanInfo()
     s = lib.rgg_plan(int(num_sms), int(smem_optin), int(E), int(M_tot), int(K), int(N), ctypes.byref(opt),
                      ctypes.byref(info))

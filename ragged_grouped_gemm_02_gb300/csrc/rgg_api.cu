@@ -24,8 +24,6 @@ struct rgg_handle {
     int num_sms;
     int smem_optin;
     int32_t* d_status;
-    void* workspace = nullptr;     // two-pass gather: the gathered rows, grown on demand
-    size_t workspace_bytes = 0;
 };
 
 namespace {
@@ -85,7 +83,6 @@ struct Plan {
     int64_t max_tiles;
     int tail64;       // 1: tail tiles of <= 64 rows run as 64-row MMAs (128-row tiles only)
     int walk_order;   // 0 list order, 1 front/back interleave, 2 strided scatter, 3 size-sorted, 4 N-major
-    int mc;           // 1: 128-row tiles on clusters of two CTAs sharing operands by TMA multicast
 };
 
 // Upper bound on the flat tile count: sum_e ceil(m_e/BM) <= floor(M_tot/BM) + E.
@@ -101,29 +98,20 @@ rgg_status check_sizes(int E, int64_t M_tot, int K, int N) {
 }
 
 // Restrictions of the kernel family a plan is for.  kPlanNoPair: 1-CTA
-// tiles only (64 or 128 rows); kPlanNoBn192: BN is 128 or 256.  The fused
-// gate-up + SiLU op (N then counts the 2N weight columns) and the FP8 op take
-// both; the token-gather GEMM takes kPlanNoPair.
+// tiles only (64 or 128 rows); kPlanNoBn192: BN is 128 or 256.  The FP8 op
+// (1-CTA tiles only: on CTA pairs it measured slower than 128 x 256 tiles on
+// every benchmark shape -- uniform 1 191 vs 1 390 TFLOP/s, skew16k 1 069 vs
+// 1 291, prefill 2 714 vs 2 775 -- so it has no pair form) and the fused
+// token gather take both; the fused gate-up + SiLU op (N then counts the 2N
+// weight columns) takes kPlanNoBn192; the plain token-gather GEMM kPlanNoPair.
 constexpr int kPlanNoPair = 1;
 constexpr int kPlanNoBn192 = 2;
 constexpr int kPlanFused = kPlanNoPair | kPlanNoBn192;
-constexpr int kPlanPairBn256 = 16;  // CTA pairs only with BN = 256 (FP8: 128-column weight panels)
-// CTA pairs only when asked for (bm = 256): FP8 pairs measured slower than 128 x 256 tiles on every
-// benchmark shape (uniform 1 191 vs 1 390 TFLOP/s, skew16k 1 069 vs 1 291, prefill 2 714 vs 2 775).
-constexpr int kPlanPairOnRequest = 32;
-// The cluster-multicast kernel (rgg_gemm_mc.cuh) exists for this op.  With
-// kPlanNoBn192 (fused gate-up, FP8) it takes BN = 256 only.
-constexpr int kPlanMcOk = 64;
 
 rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, int N, const rgg_options* opt,
                      Plan* out, int kind = 0) {
     const bool no_pair = (kind & kPlanNoPair) != 0;
     const bool no_192 = (kind & kPlanNoBn192) != 0;
-    const bool pair_256 = (kind & kPlanPairBn256) != 0;
-    const bool pair_on_request = (kind & kPlanPairOnRequest) != 0;
-    const int want_mc = opt ? opt->multicast : 0;
-    if (want_mc < -1 || want_mc > 1) return RGG_ERR_INVALID_ARG;
-    const bool mc = (want_mc == 1);
     rgg_status s = check_sizes(E, M_tot, K, N);
     if (s != RGG_OK) return s;
     if (num_sms <= 0) num_sms = kDefaultSms;
@@ -136,7 +124,6 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (want_bn != 0 && want_bn != 128 && want_bn != 192 && want_bn != 256) return RGG_ERR_INVALID_ARG;
     if (want_bm == 256 && want_bn == 192) return RGG_ERR_INVALID_ARG;  // pair tiles split BN in whole panels
     if ((no_pair && want_bm == 256) || (no_192 && want_bn == 192)) return RGG_ERR_INVALID_ARG;
-    if (pair_256 && want_bm == 256 && want_bn != 0 && want_bn != 256) return RGG_ERR_INVALID_ARG;
     if (want_stages != 0 && (want_stages < 2 || want_stages > rgg::kMaxStages)) return RGG_ERR_INVALID_ARG;
     if (max_ctas < 0) return RGG_ERR_INVALID_ARG;
     const int want_tail = opt ? opt->tail64 : 0;
@@ -144,13 +131,6 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     const int want_walk = opt ? opt->walk_order : 0;
     if (want_walk < -1 || want_walk > 4) return RGG_ERR_INVALID_ARG;  // -1: list order, never replaced
     if (want_walk == 3 && E > rgg::kMaxSortedExperts) return RGG_ERR_UNSUPPORTED;
-    if (mc) {
-        // cluster multicast: 128-row tiles, BN 128 or 256 (256 for the fused gate-up and FP8 ops),
-        // walk orders 0-2
-        if ((kind & kPlanMcOk) == 0) return RGG_ERR_UNSUPPORTED;
-        if ((want_bm != 0 && want_bm != 128) || want_bn == 192 || want_walk >= 3) return RGG_ERR_INVALID_ARG;
-        if (no_192 && want_bn != 0 && want_bn != 256) return RGG_ERR_INVALID_ARG;
-    }
     int grid_cap = max_ctas > 0 ? std::min(max_ctas, num_sms) : num_sms;
 
     // Per-expert M tiles at each BM: exact with host counts, else the
@@ -185,8 +165,8 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
             }
         avg = busy ? static_cast<double>(rows) / busy : 0.0;
     }
-    int bm = mc ? 128 : want_bm;
-    int bn = (mc && no_192) ? 256 : want_bn;
+    int bm = want_bm;
+    int bn = want_bn;
     if (bm == 0 && avg <= 64.0) bm = 64;
     {
         double best = 1e300;
@@ -194,15 +174,13 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         for (int cbm : {256, 128, 64}) {
             if (bm != 0 && cbm != bm) continue;
             if (no_pair && cbm == 256) continue;
-            if (pair_on_request && cbm == 256 && want_bm != 256) continue;
             if (bm == 0 && cbm == 64) continue;  // 64-row tiles only for small groups (above)
             const bool cpair = (cbm == 256);
             const int cunits = cpair ? std::max(1, grid_cap / 2) : grid_cap;
             const int64_t mt = std::max<int64_t>(1, m_tiles(cbm));
             for (int cbn : {256, 192, 128}) {
                 if (bn != 0 && cbn != bn) continue;
-                if ((cpair || no_192 || mc) && cbn == 192) continue;
-                if (cpair && pair_256 && cbn != 256) continue;
+                if ((cpair || no_192) && cbn == 192) continue;
                 const int64_t waves = ceil_div(mt * ceil_div(N, cbn), cunits);
                 const double cost = static_cast<double>(waves) * (cbn + 64) * (cpair ? 0.87 : 1.0);
                 if (cost < best) {
@@ -234,9 +212,9 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         int64_t mx = 0;
         for (int e = 0; e < E; ++e) mx = std::max<int64_t>(mx, opt->host_counts[e]);
         skewed = (avg > 0.0 && static_cast<double>(mx) > 4.0 * avg);
-        if (skewed) walk = mc ? 1 : 3;
+        if (skewed) walk = 3;
     }
-    if (walk == 0 && !keep_list && !skewed && !mc && avg >= 3.0 * bm) walk = 4;
+    if (walk == 0 && !keep_list && !skewed && avg >= 3.0 * bm) walk = 4;
     const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;  // persistent CTAs or CTA pairs
 
     const int64_t max_tiles = tile_bound(E, M_tot, N, bm, bn);
@@ -245,8 +223,8 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     // Per-CTA tile extents: a pair CTA holds 128 rows of A and half of B.
     const int cta_m = pair ? 128 : bm;
     const int cta_n = pair ? bn / 2 : bn;
-    // walk order 3 and the multicast kernel's unit list each keep two more prefixes in shared memory
-    const bool extra_prefix = (walk == 3 || mc);
+    // walk order 3 keeps the size order and its tile prefix in shared memory as well
+    const bool extra_prefix = (walk == 3);
     const rgg::SmemPlan probe = rgg::smem_plan(cta_m, cta_n, 0, E, extra_prefix);
     const int64_t per_stage = static_cast<int64_t>(cta_m + cta_n) * 128 + 16;  // tiles + two barriers
     const int64_t room = static_cast<int64_t>(smem_optin) - 1024 - probe.total - 64;
@@ -263,15 +241,12 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     out->bm = bm;
     out->bn = bn;
     out->stages = stages;
-    // a multicast cluster walks units of two tiles
     out->grid = pair ? static_cast<int>(2 * std::max<int64_t>(1, std::min<int64_t>(units, max_tiles)))
-                : mc ? static_cast<int>(2 * std::max<int64_t>(1, std::min<int64_t>(grid_cap / 2, (max_tiles + 1) / 2)))
                      : static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(grid_cap, max_tiles)));
     out->smem_bytes = smem;
     out->max_tiles = max_tiles;
     out->tail64 = ((bm == 128 || bm == 256) && want_tail != -1) ? 1 : 0;
     out->walk_order = walk;
-    out->mc = mc ? 1 : 0;
     return RGG_OK;
 }
 
@@ -292,28 +267,39 @@ constexpr double kFusedGatherMaxRows = 24.0;
 // tiles hold more than a couple of dozen rows (measured with 32 experts,
 // K = 6144, N = 4096: fused faster at 1 to 16 rows per expert, by 2% at 16;
 // two-pass faster at 32 rows, by 3%, and at 64, by 29%).
-rgg_status choose_gather_mode(int E, int64_t M_tot, const rgg_options* opt, int* mode) {
+//
+// The two-pass mode needs the caller's workspace: the library never allocates
+// inside a call.  *prefers_two_pass says whether the automatic choice would
+// take two passes given a workspace; without one it runs the fused mode
+// (CTA pairs, which only the two-pass mode reaches, then cannot be asked for).
+rgg_status choose_gather_mode(int E, int64_t M_tot, const rgg_options* opt, int* mode, bool* prefers_two_pass) {
     const int want = opt ? opt->gather_mode : 0;
     if (want < 0 || want > 2) return RGG_ERR_INVALID_ARG;
+    *prefers_two_pass = (want == kGatherTwoPass);
     if (want != 0) {
         *mode = want;
         return RGG_OK;
     }
-    if (opt && (opt->bm == 256 || opt->multicast == 1)) {  // CTA pairs and multicast clusters read whole boxes
-        *mode = kGatherTwoPass;
-        return RGG_OK;
+    bool two = false;
+    if (opt && opt->bm == 256) {  // CTA pairs read whole boxes
+        two = true;
+    } else {
+        double avg = static_cast<double>(M_tot) / E;
+        if (opt && opt->host_counts) {
+            int64_t rows = 0, busy = 0;
+            for (int e = 0; e < E; ++e)
+                if (opt->host_counts[e] > 0) {
+                    rows += opt->host_counts[e];
+                    ++busy;
+                }
+            avg = busy ? static_cast<double>(rows) / busy : 0.0;
+        }
+        two = avg > kFusedGatherMaxRows;
     }
-    double avg = static_cast<double>(M_tot) / E;
-    if (opt && opt->host_counts) {
-        int64_t rows = 0, busy = 0;
-        for (int e = 0; e < E; ++e)
-            if (opt->host_counts[e] > 0) {
-                rows += opt->host_counts[e];
-                ++busy;
-            }
-        avg = busy ? static_cast<double>(rows) / busy : 0.0;
-    }
-    *mode = (avg <= kFusedGatherMaxRows) ? kGatherFused : kGatherTwoPass;
+    *prefers_two_pass = two;
+    const bool have_ws = opt && opt->workspace;
+    if (two && !have_ws && opt && opt->bm == 256) return RGG_ERR_INVALID_ARG;
+    *mode = (two && have_ws) ? kGatherTwoPass : kGatherFused;
     return RGG_OK;
 }
 
@@ -437,14 +423,55 @@ rgg_status gather_call(rgg_handle* h, const void* X_tok, int64_t T, const int32_
 namespace rgg {
 
 // Host helpers shared with the other C-ABI translation unit (rgg_noalloc.cu).
-rgg_status host_encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K, int N, int bm,
-                            CUtensorMap* tx, CUtensorMap* tx64, CUtensorMap* tw) {
-    return encode_maps(X, W, E, M_tot, K, N, bm, tx, tx64, tw);
-}
-
 rgg_status host_cuda_failure(cudaError_t err, const char* what) { return cuda_failure(err, what); }
 
 void host_set_last_error(const char* what) { g_last_cuda_error = what; }
+
+rgg_status host_check_gemm_args(const void* X, const void* W, const int32_t* group_offsets, const void* Y, int E,
+                                int64_t M_tot, int K, int N) {
+    if (!group_offsets || !W) return RGG_ERR_INVALID_ARG;
+    rgg_status s = check_sizes(E, M_tot, K, N);
+    if (s != RGG_OK) return s;
+    if (M_tot > 0 && (!X || !Y)) return RGG_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(group_offsets, 4) || (M_tot > 0 && (!aligned(X, 16) || !aligned(Y, 16))))
+        return RGG_ERR_INVALID_ARG;
+    return RGG_OK;
+}
+
+rgg_status host_grouped_gemm(int num_sms, int smem_optin, int32_t* status, const void* X, const void* W,
+                             const int32_t* group_offsets, void* Y, int E, int64_t M_tot, int K, int N,
+                             cudaStream_t st, const rgg_options* opt) {
+    if (M_tot == 0) {
+        cudaError_t err = launch_validate_offsets(group_offsets, E, M_tot, status, st);
+        return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
+    }
+    Plan p;
+    rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, N, opt, &p, 0);
+    if (s != RGG_OK) return s;
+    CUtensorMap tx, tx64, tw;
+    s = encode_maps(X, W, E, M_tot, K, N, p.bm, &tx, &tx64, &tw);
+    if (s != RGG_OK) return s;
+    GemmArgs a;
+    a.offsets = group_offsets;
+    a.Y = static_cast<__nv_bfloat16*>(Y);
+    a.status = status;
+    a.M_tot = M_tot;
+    a.E = E;
+    a.K = K;
+    a.N = N;
+    a.num_k_blocks = static_cast<int32_t>(ceil_div(K, kBK));
+    a.n_tiles_n = static_cast<int32_t>(ceil_div(N, p.bn));
+    a.stages = p.stages;
+    a.y_vec32 = ((N % 16) == 0 && aligned(Y, 32)) ? 1 : 0;
+    a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+    a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
+    a.tail64 = p.tail64;
+    a.walk_order = p.walk_order;
+    cudaError_t err = (p.bm == 256)   ? launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+                      : (p.bm == 128) ? launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+                                      : launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm launch");
+}
 
 }  // namespace rgg
 
@@ -506,7 +533,6 @@ void rgg_destroy(rgg_handle* h) {
     {
         DeviceScope scope(h->device);
         cudaFree(h->d_status);
-        if (h->workspace) cudaFree(h->workspace);
     }
     delete h;
 }
@@ -522,18 +548,19 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     if (op == 2 && (K % 16 != 0 || N % 16 != 0)) return RGG_ERR_INVALID_ARG;
     const bool gather = (op == 3 || op == 4);
     int mode = 0;
+    bool prefers_two_pass = false;
     if (gather) {
-        rgg_status sm = choose_gather_mode(E, M_tot, opt, &mode);
+        rgg_status sm = choose_gather_mode(E, M_tot, opt, &mode, &prefers_two_pass);
         if (sm != RGG_OK) return sm;
     }
     // the two-pass gather runs the plain (or fused gate-up) kernel on the gathered rows; the fused
     // gate-up op takes CTA pairs but not BN = 192; FP8 and the fused gather take 1-CTA tiles only
     const bool fused_gather = gather && mode == kGatherFused;
-    const int kind = (op == 2)                   ? (kPlanNoBn192 | kPlanPairBn256 | kPlanPairOnRequest | kPlanMcOk)
+    const int kind = (op == 2)                   ? kPlanFused
                      : (op == 4 && fused_gather) ? kPlanFused
                      : (op == 3 && fused_gather) ? kPlanNoPair
-                     : swiglu                    ? (kPlanNoBn192 | kPlanMcOk)
-                                                 : kPlanMcOk;
+                     : swiglu                    ? kPlanNoBn192
+                                                 : 0;
     rgg_status s = make_plan(num_sms, smem_optin, E, M_tot, K, swiglu ? 2 * N : N, opt, &p, kind);
     if (s != RGG_OK) return s;
     out->bm = p.bm;
@@ -550,59 +577,19 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->walk_order = p.walk_order;
     if (swiglu && p.bm == 256) out->tail64 = 0;  // fused gate-up pairs keep 256-row tail tiles
     out->gather_mode = mode;
-    out->workspace_bytes = (mode == kGatherTwoPass) ? gather_workspace_bytes(M_tot, K) : 0;
-    out->multicast = p.mc;
+    out->workspace_bytes = prefers_two_pass ? gather_workspace_bytes(M_tot, K) : 0;
     return RGG_OK;
 }
 
 rgg_status rgg_grouped_gemm(rgg_handle* h, const void* X, const void* W, const int32_t* group_offsets, void* Y,
                             int E, int64_t M_tot, int K, int N, void* stream, const rgg_options* opt) {
-    if (!h || !group_offsets || !W) return RGG_ERR_INVALID_ARG;
-    rgg_status s = check_sizes(E, M_tot, K, N);
+    if (!h) return RGG_ERR_INVALID_ARG;
+    rgg_status s = rgg::host_check_gemm_args(X, W, group_offsets, Y, E, M_tot, K, N);
     if (s != RGG_OK) return s;
-    if (M_tot > 0 && (!X || !Y)) return RGG_ERR_INVALID_ARG;
-    if (!aligned(W, 16) || !aligned(group_offsets, 4) || (M_tot > 0 && (!aligned(X, 16) || !aligned(Y, 16))))
-        return RGG_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     DeviceScope scope(h->device);
     if (scope.error() != cudaSuccess) return cuda_failure(scope.error(), "cudaSetDevice");
-
-    if (M_tot == 0) {
-        cudaError_t err = rgg::launch_validate_offsets(group_offsets, E, M_tot, h->d_status, st);
-        return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
-    }
-
-    Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p, kPlanMcOk);
-    if (s != RGG_OK) return s;
-
-    CUtensorMap tx, tx64, tw;
-    s = encode_maps(X, W, E, M_tot, K, N, p.bm, &tx, &tx64, &tw);
-    if (s != RGG_OK) return s;
-
-    rgg::GemmArgs a;
-    a.offsets = group_offsets;
-    a.Y = static_cast<__nv_bfloat16*>(Y);
-    a.status = h->d_status;
-    a.M_tot = M_tot;
-    a.E = E;
-    a.K = K;
-    a.N = N;
-    a.num_k_blocks = static_cast<int32_t>(ceil_div(K, rgg::kBK));
-    a.n_tiles_n = static_cast<int32_t>(ceil_div(N, p.bn));
-    a.stages = p.stages;
-    a.y_vec32 = ((N % 16) == 0 && aligned(Y, 32)) ? 1 : 0;
-    a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
-    a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
-    a.tail64 = p.tail64;
-    a.walk_order = p.walk_order;
-
-    cudaError_t err =
-        p.mc            ? rgg::launch_gemm_mc(rgg::kMcPlain, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-        : (p.bm == 256) ? rgg::launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-        : (p.bm == 128) ? rgg::launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-                        : rgg::launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
-    return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm launch");
+    return rgg::host_grouped_gemm(h->num_sms, h->smem_optin, h->d_status, X, W, group_offsets, Y, E, M_tot, K, N,
+                                  static_cast<cudaStream_t>(stream), opt);
 }
 
 rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13, const int32_t* group_offsets,
@@ -623,7 +610,7 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
         return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
     }
     Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, kPlanNoBn192 | kPlanMcOk);
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, 2 * N, opt, &p, kPlanNoBn192);
     if (s != RGG_OK) return s;
     CUtensorMap tx, tx64, tw;
     s = encode_maps(X, W13, E, M_tot, K, 2 * N, p.bm, &tx, &tx64, &tw);
@@ -645,10 +632,8 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
     a.tail64 = p.tail64;
     a.walk_order = p.walk_order;
     if (p.bm == 256) a.tail64 = 0;  // the pair's 128-row tail layout splits gate and up across warps
-    cudaError_t err =
-        p.mc            ? rgg::launch_gemm_mc(rgg::kMcSwiGLU, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-        : (p.bm == 256) ? rgg::launch_gemm_pair_swiglu(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-                        : rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    cudaError_t err = (p.bm == 256) ? rgg::launch_gemm_pair_swiglu(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
+                                    : rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_swiglu launch");
 }
 
@@ -671,8 +656,7 @@ rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, c
         return err == cudaSuccess ? RGG_OK : cuda_failure(err, "validate_offsets launch");
     }
     Plan p;
-    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p,
-                  kPlanNoBn192 | kPlanPairBn256 | kPlanPairOnRequest | kPlanMcOk);
+    s = make_plan(h->num_sms, h->smem_optin, E, M_tot, K, N, opt, &p, kPlanFused);
     if (s != RGG_OK) return s;
     CUtensorMap tx, tx64, tw;
     s = encode_maps_fp8(X8, W8, E, M_tot, K, N, p.bm, &tx, &tx64, &tw);
@@ -695,10 +679,7 @@ rgg_status rgg_grouped_gemm_fp8(rgg_handle* h, const void* X8, const void* W8, c
     a.walk_order = p.walk_order;
     a.sx = sx;
     a.sw = sw;
-    cudaError_t err =
-        p.mc            ? rgg::launch_gemm_mc(rgg::kMcFp8, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-        : (p.bm == 256) ? rgg::launch_gemm_pair_fp8(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
-                        : rgg::launch_gemm_fp8(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
+    cudaError_t err = rgg::launch_gemm_fp8(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_fp8 launch");
 }
 
@@ -783,31 +764,15 @@ rgg_status gather_call(rgg_handle* h, const void* X_tok, int64_t T, const int32_
     }
     const int NW = swiglu ? 2 * N : N;  // weight columns
     int mode = 0;
-    s = choose_gather_mode(E, M_tot, opt, &mode);
+    bool prefers_two_pass = false;
+    s = choose_gather_mode(E, M_tot, opt, &mode, &prefers_two_pass);
     if (s != RGG_OK) return s;
     if (mode == kGatherTwoPass) {
-        // Pass 1 writes the routed rows, in routed order, into the workspace;
-        // pass 2 is the grouped product of those rows.
+        // Pass 1 writes the routed rows, in routed order, into the caller's
+        // workspace; pass 2 is the grouped product of those rows.
         const int64_t need = gather_workspace_bytes(M_tot, K);
         void* ws = opt ? opt->workspace : nullptr;
-        if (ws) {
-            if (opt->workspace_bytes < need || !aligned(ws, 16)) return RGG_ERR_INVALID_ARG;
-        } else {
-            if (h->workspace_bytes < static_cast<size_t>(need)) {
-                // cudaFree waits for the device, so no earlier call still reads the old buffer
-                if (h->workspace) cudaFree(h->workspace);
-                h->workspace = nullptr;
-                h->workspace_bytes = 0;
-                const size_t grow = (static_cast<size_t>(need) + (size_t(2) << 20) - 1) & ~((size_t(2) << 20) - 1);
-                cudaError_t err = cudaMalloc(&h->workspace, grow);
-                if (err != cudaSuccess) {
-                    h->workspace = nullptr;
-                    return cuda_failure(err, "cudaMalloc(gather workspace)");
-                }
-                h->workspace_bytes = grow;
-            }
-            ws = h->workspace;
-        }
+        if (!ws || opt->workspace_bytes < need || !aligned(ws, 16)) return RGG_ERR_INVALID_ARG;
         cudaError_t err = rgg::launch_gather_rows(X_tok, row_index, group_offsets, E, M_tot, T, K, ws, h->num_sms,
                                                   h->d_status, st);
         if (err != cudaSuccess) return cuda_failure(err, "gather_rows launch");

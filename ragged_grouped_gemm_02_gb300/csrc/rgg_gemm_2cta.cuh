@@ -9,7 +9,7 @@
 // writes each CTA's 128 accumulator rows into that CTA's TMEM.  Each CTA
 // therefore loads only half of the weight tile per stage, which halves the
 // shared-memory fill per FLOP compared with one CTA holding the whole
-// 128 x BN tile.  No TMA multicast is used: every CTA loads its own boxes.
+// 128 x BN tile.  Every CTA loads its own boxes into its own shared memory.
 //
 // Roles (both CTAs run the same code, rank = %cluster_ctarank):
 //   warp 0 lane 0 : producer.  Waits its own empty[s]; the leader (rank 0)
@@ -17,9 +17,9 @@
 //                   loads complete on the leader's full[s].
 //   warp 1        : allocates the pair's TMEM in both CTAs; lane 0 of the
 //                   leader issues every MMA and commits to the empty /
-//                   acc_full barriers of both CTAs at once (multicast).
+//                   acc_full barriers of both CTAs with one commit.
 //   warps 2-5     : epilogue of the CTA's own 128 rows (warps 2-9, two per
-//   (or 2-9)        TMEM lane quadrant, for the fused gate-up and FP8 epilogues);
+//   (or 2-9)        TMEM lane quadrant, for the fused gate-up epilogue);
 //                   they arrive on the leader's acc_empty (one arrival per
 //                   epilogue warp of both CTAs).
 // All waits are bounded; an abort raised in either CTA is mirrored into the
@@ -30,25 +30,21 @@
 
 namespace rgg {
 
-// Every stage row is one 128-byte swizzle row in both element types: bf16
-// stages cover K = 64 with 64-column weight panels, FP8 (E4M3) stages K = 128
-// with 128-column panels (so FP8 pairs take BN = 256, one panel per CTA).
-template <int BN, bool kFp8 = false>
+// bf16 stages: K = 64 (one 128-byte swizzle row) with 64-column weight panels.
+template <int BN>
 struct PairConfig {
     static_assert(BN == 128 || BN == 256, "pair tiles split BN into two whole 64-column panel sets");
-    static_assert(!kFp8 || BN == 256, "FP8 weight panels are 128 columns: each CTA of a pair holds one");
     static constexpr int kHalfN = BN / 2;           // B columns held by each CTA
-    static constexpr int kKStage = kFp8 ? 128 : kBK;                     // K elements per stage
-    static constexpr int kPanelN = kFp8 ? 128 : 64;                      // W columns per panel
+    static constexpr int kKStage = kBK;              // K elements per stage
+    static constexpr int kPanelN = 64;               // W columns per panel
     static constexpr int kPanels = kHalfN / kPanelN;
     static constexpr uint32_t kPanelB = static_cast<uint32_t>(kKStage) * 128u;  // bytes per W panel
-    static constexpr uint32_t kBStep = kFp8 ? 4096u : 2048u;  // B start advance per MMA (32 or 16 K rows)
+    static constexpr uint32_t kBStep = 2048u;       // B start advance per MMA (16 K rows)
     static constexpr uint32_t kTmemCols = 512;      // two BN-column fp32 buffers (BN <= 256)
     static constexpr uint32_t kStageBytesPerCta = static_cast<uint32_t>((128 + kHalfN) * 128);
     static constexpr uint32_t kStageBytesPerCta64 = static_cast<uint32_t>((64 + kHalfN) * 128);
-    static constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(256, BN, true) : idesc_bf16_f32(256, BN, true);
-    static constexpr uint32_t kIdesc128 =  // 64 rows per CTA
-        kFp8 ? idesc_e4m3_f32(128, BN, true) : idesc_bf16_f32(128, BN, true);
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(256, BN, true);
+    static constexpr uint32_t kIdesc128 = idesc_bf16_f32(128, BN, true);  // 64 rows per CTA
 };
 
 // A pair tile whose rows are the last <= 128 of its expert runs as an M = 128
@@ -66,19 +62,17 @@ __device__ __forceinline__ bool pair_runs_as_128_rows(const GemmArgs& args, cons
 // Epilogue warps per CTA: four for plain bf16 outputs, eight (two per TMEM
 // lane quadrant, each on half of the columns) for the fused gate-up epilogue,
 // whose exponentials otherwise outlast the main loop (measured: uniform 845 ->
-// 1 018 TFLOP/s, prefill 1 417 -> 1 526), and for FP8, whose epilogue applies
-// the row and column scales.
-template <int kEpi, bool kFp8 = false>
+// 1 018 TFLOP/s, prefill 1 417 -> 1 526).
+template <int kEpi>
 __host__ __device__ constexpr int pair_epilogue_warps() {
-    return (kEpi == kEpiSwiGLU || kFp8) ? 8 : 4;
+    return kEpi == kEpiSwiGLU ? 8 : 4;
 }
 
-template <int BN, int kEpi = kEpiPlain, bool kFp8 = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilogue_warps<kEpi, kFp8>(), 1)
+template <int BN, int kEpi = kEpiPlain>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilogue_warps<kEpi>(), 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
                              const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
-    using Cfg = PairConfig<BN, kFp8>;
-    static_assert(!(kFp8 && kEpi == kEpiSwiGLU), "the fused gate-up epilogue is bf16 only");
+    using Cfg = PairConfig<BN>;
     constexpr int BM = 256;  // rows per pair tile
     constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;  // output columns per tile
     auto half_tile = [&](const TileCoord& c) { return kEpi == kEpiPlain && pair_runs_as_128_rows(args, c); };
@@ -128,7 +122,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
-            mbar_init(acce_bar(a), 2 * pair_epilogue_warps<kEpi, kFp8>());
+            mbar_init(acce_bar(a), 2 * pair_epilogue_warps<kEpi>());
         }
         mbar_init(drain_bar, 1);
         misc[1] = 0u;
@@ -238,10 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                     for (int j = 0; j < kMmasPerStage; ++j) {
                         const uint64_t ad = sw128_desc(a_st + 32u * j, 16u, 1024u);
                         const uint64_t bd = sw128_desc(b_st + Cfg::kBStep * j, Cfg::kPanelB, 1024u);
-                        if constexpr (kFp8)
-                            mma_f8_ss_pair(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
-                        else
-                            mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+                        mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
                     }
                     mma_commit_pair(empty_bar(st), 0x3);
                     if (++st == S) {
@@ -287,7 +278,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             const int cbase = half ? (q >> 1) * (BN / 2) : 0;  // first tile column this warp holds
             const bool row_ok = r_local < c.rows;
             __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0 + cbase;
-            constexpr int kParts = pair_epilogue_warps<kEpi, kFp8>() / 4;  // warps per lane quadrant
+            constexpr int kParts = pair_epilogue_warps<kEpi>() / 4;  // warps per lane quadrant
             const int pc = ncols / kParts;                                // columns each of them writes
             const int c0 = ((warp - 2) >> 2) * pc;
 #pragma unroll 1
@@ -304,27 +295,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                         v[i] = __float_as_uint(silu_f32(__uint_as_float(v[i])) * __uint_as_float(u[i]));
                 } else {
                     tmem_ld_wait();
-                }
-                if constexpr (kFp8) {
-                    // dequantise: row scale of X times the expert's column scale of W
-                    if (row_ok) {
-                        const float rs = __ldg(args.sx + c.row0 + r_local);
-                        const float* swp = args.sw + static_cast<int64_t>(c.expert) * N + c.col0 + cbase + cc;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            if (c.col0 + cbase + cc + 16 * h < N) {
-#pragma unroll
-                                for (int q4 = 0; q4 < 4; ++q4) {
-                                    const float4 s4 = __ldg(reinterpret_cast<const float4*>(swp + 16 * h) + q4);
-                                    const int i0 = 16 * h + 4 * q4;
-                                    v[i0 + 0] = __float_as_uint(__uint_as_float(v[i0 + 0]) * rs * s4.x);
-                                    v[i0 + 1] = __float_as_uint(__uint_as_float(v[i0 + 1]) * rs * s4.y);
-                                    v[i0 + 2] = __float_as_uint(__uint_as_float(v[i0 + 2]) * rs * s4.z);
-                                    v[i0 + 3] = __float_as_uint(__uint_as_float(v[i0 + 3]) * rs * s4.w);
-                                }
-                            }
-                        }
-                    }
                 }
                 if (row_ok) {
 #pragma unroll

@@ -49,23 +49,9 @@ cudaError_t launch_gather_rows(const void* xtok, const int32_t* row_index, const
 // `grid` is even.
 cudaError_t launch_gemm_pair(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                              const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
-// FP8 operands and scales on CTA pairs (`bn` 256; byte tensor maps as for launch_gemm_fp8).
-cudaError_t launch_gemm_pair_fp8(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
-                                 const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 // The same with the fused gate-up + SiLU epilogue (tmap_w spans 2N columns; tail tiles stay M = 256).
 cudaError_t launch_gemm_pair_swiglu(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                                     const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
-
-// 128-row 1-CTA tiles on clusters of two CTAs that share the weight panel
-// (consecutive M tiles) or the X rows (neighbouring N tiles) of each pair of
-// tiles through TMA multicast.  `kind` selects the operation; `bn` is the MMA
-// width: plain 128 or 256, fused gate-up 256 (128 output columns), FP8 256.
-// `grid` is even.
-constexpr int kMcPlain = 0;
-constexpr int kMcSwiGLU = 1;
-constexpr int kMcFp8 = 2;
-cudaError_t launch_gemm_mc(int kind, int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
-                           const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 
 // The flat tile list written out by the same device code the GEMM uses, in
 // list order (walk_order 0) or in the order walk_order visits it.
@@ -73,13 +59,21 @@ cudaError_t launch_export_tiles(const int32_t* offsets, int E, int64_t M_tot, in
                                 int walk_order, int32_t* desc, int64_t cap, int32_t* n_tiles, int32_t* status,
                                 cudaStream_t stream);
 
-// Host helpers defined in rgg_api.cu: the X / W tensor maps for a tile of
-// `bm` rows (256 = a CTA pair, 128 rows per CTA) plus X with a 64-row box,
-// and the thread-local text behind rgg_last_cuda_error().
-rgg_status host_encode_maps(const void* X, const void* W, int E, int64_t M_tot, int K, int N, int bm,
-                            CUtensorMap* tx, CUtensorMap* tx64, CUtensorMap* tw);
+// Host helpers defined in rgg_api.cu: the thread-local text behind
+// rgg_last_cuda_error().
 rgg_status host_cuda_failure(cudaError_t err, const char* what);
 void host_set_last_error(const char* what);
+
+// The argument checks of rgg_grouped_gemm (null pointers, sizes, alignment).
+rgg_status host_check_gemm_args(const void* X, const void* W, const int32_t* group_offsets, const void* Y, int E,
+                                int64_t M_tot, int K, int N);
+// Plan, encode and launch rgg_grouped_gemm on the current device for a GPU of
+// `num_sms` SMs and `smem_optin` bytes of shared memory per block, recording
+// device-detected errors in the device word `status`.  Arguments already
+// checked by host_check_gemm_args.
+rgg_status host_grouped_gemm(int num_sms, int smem_optin, int32_t* status, const void* X, const void* W,
+                             const int32_t* group_offsets, void* Y, int E, int64_t M_tot, int K, int N,
+                             cudaStream_t stream, const rgg_options* opt);
 
 // Offsets check alone (used when there are no rows to multiply).
 cudaError_t launch_validate_offsets(const int32_t* offsets, int E, int64_t M_tot, int32_t* status,

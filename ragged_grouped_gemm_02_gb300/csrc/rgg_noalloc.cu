@@ -3,14 +3,13 @@
 //
 // Some callers are not allowed to call cudaMalloc at the point where they run
 // the GEMM: an inference-engine plugin whose execute step runs inside the
-// engine's own memory budget and must not allocate, code running while a
-// stream is being captured into a CUDA graph in global capture mode (where
-// cudaMalloc is refused), or a process whose device memory is entirely owned
-// by a pool allocator.  rgg_grouped_gemm needs a handle, and rgg_create
-// allocates the handle's device status word with cudaMalloc.  This entry
-// point needs no handle: the only scratch the kernel uses beyond its inputs
-// and outputs -- the status word that records bad offsets or a timed-out
-// wait -- lives in a file-scope device array instead.
+// engine's own memory budget and must not allocate, or a process whose device
+// memory is entirely owned by a pool allocator that other code may not go
+// around.  rgg_grouped_gemm needs a handle, and rgg_create allocates the
+// handle's device status word with cudaMalloc.  This entry point needs no
+// handle: the only scratch the kernel uses beyond its inputs and outputs --
+// the status word that records bad offsets or a timed-out wait -- lives in a
+// file-scope device array instead.
 //
 // The array is small and fixed: every GPU that loads librgg.so holds it until
 // the process exits.  All calls share it, so calls that run at the same time
@@ -20,7 +19,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <cstring>
 #include <mutex>
 
 #include "rgg.h"
@@ -50,7 +48,9 @@ DeviceSetup g_setup[kMaxDevices];
 
 // Once per device, with that device current: find the device address of the
 // scratch array (host code cannot use the array's name as a device pointer),
-// and read the SM count and shared-memory limit the planner needs.
+// and read the SM count and shared-memory limit the planner needs.  The
+// address is kept for the life of the process, so the entry point must not be
+// used on a device after cudaDeviceReset() on it.
 rgg_status setup_device(int device, DeviceSetup* out) {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     DeviceSetup& s = g_setup[device];
@@ -82,14 +82,12 @@ rgg_status setup_device(int device, DeviceSetup* out) {
 extern "C" rgg_status rgg_grouped_gemm_noalloc(const void* X, const void* W, const int32_t* group_offsets, void* Y,
                                                int E, int64_t M_tot, int K, int N, int32_t* status_out,
                                                void* stream) {
-    if (!group_offsets || !W || (M_tot > 0 && (!X || !Y))) return RGG_ERR_INVALID_ARG;
-    auto aligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
-    if (!aligned(W, 16) || !aligned(group_offsets, 4) || (M_tot > 0 && (!aligned(X, 16) || !aligned(Y, 16))) ||
-        (status_out && !aligned(status_out, 4)))
-        return RGG_ERR_INVALID_ARG;
+    rgg_status s = rgg::host_check_gemm_args(X, W, group_offsets, Y, E, M_tot, K, N);
+    if (s != RGG_OK) return s;
+    if (status_out && (reinterpret_cast<uintptr_t>(status_out) % 4) != 0) return RGG_ERR_INVALID_ARG;
     // The kernel's scratch need does not grow with the problem: one status
     // word.  Sizes the kernel itself cannot take (E > 4096, M_tot >= 2^31,
-    // K or N not a multiple of 8, ...) are rejected by the planner below.
+    // K or N not a multiple of 8) were rejected above.
     if (kStatusWordBytes > sizeof(g_noalloc_scratch)) {
         rgg::host_set_last_error("rgg_grouped_gemm_noalloc: request needs more than the 256-byte scratch");
         return RGG_ERR_UNSUPPORTED;
@@ -100,47 +98,17 @@ extern "C" rgg_status rgg_grouped_gemm_noalloc(const void* X, const void* W, con
     if (err != cudaSuccess) return rgg::host_cuda_failure(err, "rgg_grouped_gemm_noalloc: cudaGetDevice");
     if (device < 0 || device >= kMaxDevices) return RGG_ERR_UNSUPPORTED;
     DeviceSetup dev;
-    rgg_status s = setup_device(device, &dev);
-    if (s != RGG_OK) return s;
-
-    rgg_plan_info plan;
-    s = rgg_plan(dev.num_sms, dev.smem_optin, E, M_tot, K, N, nullptr, &plan);
+    s = setup_device(device, &dev);
     if (s != RGG_OK) return s;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The status word must start at zero: the kernel only records the first error.
     err = cudaMemsetAsync(dev.scratch, 0, kStatusWordBytes, st);
     if (err != cudaSuccess) return rgg::host_cuda_failure(err, "rgg_grouped_gemm_noalloc: cudaMemsetAsync");
-
-    if (M_tot == 0) {
-        err = rgg::launch_validate_offsets(group_offsets, E, M_tot, dev.scratch, st);
-    } else {
-        CUtensorMap tx, tx64, tw;
-        s = rgg::host_encode_maps(X, W, E, M_tot, K, N, plan.bm, &tx, &tx64, &tw);
-        if (s != RGG_OK) return s;
-        rgg::GemmArgs a;
-        a.offsets = group_offsets;
-        a.Y = static_cast<__nv_bfloat16*>(Y);
-        a.status = dev.scratch;
-        a.M_tot = M_tot;
-        a.E = E;
-        a.K = K;
-        a.N = N;
-        a.num_k_blocks = (K + rgg::kBK - 1) / rgg::kBK;
-        a.n_tiles_n = (N + plan.bn - 1) / plan.bn;
-        a.stages = plan.stages;
-        a.y_vec32 = ((N % 16) == 0 && aligned(Y, 32)) ? 1 : 0;
-        a.debug_flags = 0;
-        a.tail64 = plan.tail64;
-        a.walk_order = plan.walk_order;
-        a.timeout_ns = 2000000000ull;
-        err = plan.multicast
-                  ? rgg::launch_gemm_mc(rgg::kMcPlain, plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a)
-              : (plan.bm == 256) ? rgg::launch_gemm_pair(plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a)
-              : (plan.bm == 128) ? rgg::launch_gemm_bm128(plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a)
-                                 : rgg::launch_gemm_bm64(plan.bn, plan.grid, plan.smem_bytes, st, tx, tx64, tw, a);
-    }
-    if (err != cudaSuccess) return rgg::host_cuda_failure(err, "rgg_grouped_gemm_noalloc: launch");
+    // The same plan, kernels and launch as rgg_grouped_gemm with default options.
+    s = rgg::host_grouped_gemm(dev.num_sms, dev.smem_optin, dev.scratch, X, W, group_offsets, Y, E, M_tot, K, N, st,
+                               nullptr);
+    if (s != RGG_OK) return s;
     if (status_out) {
         err = cudaMemcpyAsync(status_out, dev.scratch, kStatusWordBytes, cudaMemcpyDefault, st);
         if (err != cudaSuccess) return rgg::host_cuda_failure(err, "rgg_grouped_gemm_noalloc: status copy");

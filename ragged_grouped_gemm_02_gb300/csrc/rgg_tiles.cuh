@@ -209,138 +209,4 @@ __device__ __forceinline__ TileCoord walk_decode(const int32_t* s_off, const int
     return decode_tile(s_off, s_pre, E, BM, BN, n_tiles_n, t, WO == 4);
 }
 
-// ---------------------------------------------------------------------------
-// Two-tile units for clusters of two CTAs that share one operand through TMA
-// multicast.  A unit holds one tile for each CTA of the cluster, of the same
-// expert wherever possible:
-//   kShareB: M tiles 2i and 2i + 1 of an expert at the same N tile (the two
-//            CTAs read the same weight panel; each loads half of it for both);
-//   kShareA: the last, unpaired M tile of an expert at N tiles 2j and 2j + 1
-//            (the same X rows; each CTA loads half of the box for both);
-//   kShareNone: the leftover tile (last M tile, last N tile) of two experts
-//            whose M and N tile counts are both odd; with an odd number of
-//            such leftovers the last unit gives its second CTA a repeat of the
-//            first CTA's tile, computed but not stored.
-// Per expert with nm = ceil(m_e / BM) M tiles and nN N tiles: the expert adds
-// (nm / 2) * nN kShareB units, (nm % 2) * (nN / 2) kShareA units and
-// (nm % 2) * (nN % 2) leftover tiles.  All units of all experts come first,
-// in expert order, then the leftover pairs.  Every tile of the flat list
-// appears exactly once (plus the one repeat), so the result is that of the
-// flat list.
-constexpr int kShareNone = 0;
-constexpr int kShareA = 1;
-constexpr int kShareB = 2;
-
-struct UnitTile {
-    TileCoord c;
-    int share;   // kShareNone, kShareA or kShareB
-    bool store;  // false only for the repeated tile of an odd leftover count
-};
-
-__device__ __forceinline__ int32_t units_of_expert(int32_t m, int BM, int n_tiles_n) {
-    const int32_t nm = (m + BM - 1) / BM;
-    return (nm >> 1) * n_tiles_n + (nm & 1) * (n_tiles_n >> 1);
-}
-
-__device__ __forceinline__ int32_t leftovers_of_expert(int32_t m, int BM, int n_tiles_n) {
-    const int32_t nm = (m + BM - 1) / BM;
-    return (nm & 1) * (n_tiles_n & 1);
-}
-
-// Exclusive prefixes over the experts, one warp: s_upre[0..E] of units and
-// s_lpre[0..E] of leftover tiles.  The caller synchronises the block.
-__device__ __forceinline__ void build_unit_prefix_warp(const int32_t* s_off, int32_t* s_upre, int32_t* s_lpre,
-                                                       int E, int BM, int n_tiles_n) {
-    const int lane = threadIdx.x & 31;
-    const int per = (E + 31) / 32;
-    const int e0 = min(E, lane * per);
-    const int e1 = min(E, e0 + per);
-    int32_t lu = 0, ll = 0;
-    for (int e = e0; e < e1; ++e) {
-        const int32_t m = s_off[e + 1] - s_off[e];
-        lu += units_of_expert(m, BM, n_tiles_n);
-        ll += leftovers_of_expert(m, BM, n_tiles_n);
-    }
-    int32_t iu = lu, il = ll;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int32_t vu = __shfl_up_sync(0xffffffffu, iu, d);
-        const int32_t vl = __shfl_up_sync(0xffffffffu, il, d);
-        if (lane >= d) {
-            iu += vu;
-            il += vl;
-        }
-    }
-    int32_t ru = iu - lu, rl = il - ll;
-    for (int e = e0; e < e1; ++e) {
-        s_upre[e] = ru;
-        s_lpre[e] = rl;
-        const int32_t m = s_off[e + 1] - s_off[e];
-        ru += units_of_expert(m, BM, n_tiles_n);
-        rl += leftovers_of_expert(m, BM, n_tiles_n);
-    }
-    if (lane == 31) {
-        s_upre[E] = iu;
-        s_lpre[E] = il;
-    }
-}
-
-// Number of units: the per-expert ones plus the leftover tiles in pairs.
-__device__ __forceinline__ int32_t unit_count(const int32_t* s_upre, const int32_t* s_lpre, int E) {
-    return s_upre[E] + ((s_lpre[E] + 1) >> 1);
-}
-
-// The last e in [0, E) with pre[e] <= v (pre non-decreasing, pre[0] = 0).
-__device__ __forceinline__ int last_at_or_below(const int32_t* pre, int E, int32_t v) {
-    int lo = 0, hi = E;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (pre[mid] <= v) lo = mid;
-        else hi = mid;
-    }
-    return lo;
-}
-
-// The tile that CTA `rank` (0 or 1) of a cluster takes in unit u.
-__device__ __forceinline__ UnitTile decode_unit(const int32_t* s_off, const int32_t* s_upre, const int32_t* s_lpre,
-                                                int E, int BM, int BN, int n_tiles_n, int32_t u, int rank) {
-    UnitTile r;
-    r.store = true;
-    int e;
-    int32_t mt, nt;
-    const int32_t U0 = s_upre[E];
-    if (u < U0) {
-        e = last_at_or_below(s_upre, E, u);
-        const int32_t local = u - s_upre[e];
-        const int32_t nm = (s_off[e + 1] - s_off[e] + BM - 1) / BM;
-        const int32_t ub = (nm >> 1) * n_tiles_n;
-        if (local < ub) {
-            const int32_t i = local / n_tiles_n;
-            mt = 2 * i + rank;
-            nt = local - i * n_tiles_n;
-            r.share = kShareB;
-        } else {
-            mt = nm - 1;
-            nt = 2 * (local - ub) + rank;
-            r.share = kShareA;
-        }
-    } else {
-        int32_t k = 2 * (u - U0) + rank;
-        if (k >= s_lpre[E]) {  // odd leftover count: repeat the first CTA's tile
-            k -= 1;
-            r.store = false;
-        }
-        e = last_at_or_below(s_lpre, E, k);
-        mt = (s_off[e + 1] - s_off[e] + BM - 1) / BM - 1;
-        nt = n_tiles_n - 1;
-        r.share = kShareNone;
-    }
-    const int32_t m_e = s_off[e + 1] - s_off[e];
-    r.c.expert = e;
-    r.c.row0 = s_off[e] + mt * BM;
-    r.c.rows = min(BM, m_e - mt * BM);
-    r.c.col0 = nt * BN;
-    return r;
-}
-
 }  // namespace rgg

@@ -155,43 +155,6 @@ def test_plan_walk_order_choice(lib):
                         walk_order=-1)["walk_order"] == 0
 
 
-def test_plan_multicast_clusters(lib):
-    # 128-row tiles on clusters of two CTAs sharing operands by TMA multicast: on request only
-    from ragged_grouped_gemm_02_gb300 import workloads as wl
-    counts = wl.workload_counts("skew16k")
-    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=counts)["multicast"] == 0
-    p = rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=counts, multicast=1)
-    assert p["multicast"] == 1 and p["bm"] == 128 and p["bn"] in (128, 256) and p["tail64"] == 1
-    assert p["grid"] % 2 == 0 and p["grid"] <= 152 and p["threads"] == 192
-    # the automatic size-sorted walk becomes the front/back interleave
-    assert p["walk_order"] == 1
-    # BN 192 is not offered; the fused gate-up and FP8 ops take BN = 256
-    assert rgg.rgg_plan(64, 16384, 1024, 2688, multicast=1, bn=128)["bn"] == 128
-    assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", multicast=1)["bn"] == 256
-    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8", multicast=1)
-    assert p["bn"] == 256 and p["bk"] == 128 and p["multicast"] == 1 and p["threads"] == 320
-    # one cluster at least, even when fewer CTAs are allowed
-    assert rgg.rgg_plan(4, 256, 256, 512, multicast=1, max_ctas=1)["grid"] == 2
-    assert rgg.rgg_plan(4, 256, 256, 512, multicast=1, max_ctas=7)["grid"] == 6
-    # the gather calls read whole boxes in the two-pass mode
-    p = rgg.rgg_plan(32, 512, 6144, 4096, host_counts=[16] * 32, op="gather", multicast=1)
-    assert p["gather_mode"] == 2 and p["multicast"] == 1
-
-
-@pytest.mark.parametrize("kw,status", [(dict(bm=64), "INVALID_ARG"), (dict(bm=256), "INVALID_ARG"),
-                                       (dict(bn=192), "INVALID_ARG"), (dict(walk_order=3), "INVALID_ARG"),
-                                       (dict(walk_order=4), "INVALID_ARG"),
-                                       (dict(op="swiglu", bn=128), "INVALID_ARG"),
-                                       (dict(op="gather", gather_mode=1), "UNSUPPORTED"),
-                                       (dict(multicast=2), "INVALID_ARG"), (dict(multicast=-2), "INVALID_ARG")])
-def test_plan_multicast_rejects(lib, kw, status):
-    args = dict(multicast=1)
-    args.update(kw)
-    with pytest.raises(rgg.RggError) as ei:
-        rgg.rgg_plan(4, 256, 256, 512, **args)
-    assert ei.value.status == getattr(rgg, "RGG_ERR_" + status)
-
-
 @pytest.mark.parametrize("kw", [dict(E=0), dict(K=12), dict(N=100), dict(K=4), dict(M_tot=-1),
                                 dict(M_tot=2 ** 31)])
 def test_plan_rejects_bad_sizes(lib, kw):
@@ -238,27 +201,36 @@ def test_plan_cta_pair_mode(lib):
 
 def test_plan_gather_modes(lib):
     # small expert groups (64-row tiles): the gather is fused into the GEMM
-    p = rgg.rgg_plan(32, 512, 6144, 4096, op="gather")
+    p = rgg.rgg_plan(32, 512, 6144, 4096, op="gather", workspace=True)
     assert p["gather_mode"] == 1 and p["bm"] == 64 and p["workspace_bytes"] == 0
     p = rgg.rgg_plan(32, 512, 6144, 2048, op="swiglu_gather")
     assert p["gather_mode"] == 1 and p["bm"] == 64 and p["bn"] in (128, 256)
-    # large groups: two passes, the second being the plain plan (CTA pairs included)
+    # large groups with a caller workspace: two passes, the second being the plain plan (CTA pairs included)
     plain = rgg.rgg_plan(64, 16384, 1024, 2688)
-    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="gather")
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="gather", workspace=True)
     assert p["gather_mode"] == 2 and p["workspace_bytes"] == 16384 * 1024 * 2
-    assert (p["bm"], p["bn"], p["stages"]) == (plain["bm"], plain["bn"], plain["stages"]) == (256, 256, 7)
+    assert (p["bm"], p["bn"], p["stages"]) == (plain["bm"], plain["bn"], plain["stages"])
     assert plain["gather_mode"] == 0 and plain["workspace_bytes"] == 0
+    # without one the call allocates nothing and runs the fused gather; the plan still
+    # reports the workspace the preferred two-pass mode would need
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="gather")
+    assert p["gather_mode"] == 1 and p["bm"] in (64, 128) and p["workspace_bytes"] == 16384 * 1024 * 2
     # 32 rows per expert: 64-row tiles, but already two-pass; 16 or fewer: fused
-    assert rgg.rgg_plan(32, 1024, 6144, 4096, op="gather")["gather_mode"] == 2
-    assert rgg.rgg_plan(32, 512, 6144, 4096, op="gather")["gather_mode"] == 1
-    assert rgg.rgg_plan(4, 1024, 256, 256, op="gather", host_counts=[1000, 8, 8, 8])["gather_mode"] == 2
-    assert rgg.rgg_plan(4, 1024, 256, 256, op="gather", host_counts=[20, 0, 0, 0])["gather_mode"] == 1
+    assert rgg.rgg_plan(32, 1024, 6144, 4096, op="gather", workspace=True)["gather_mode"] == 2
+    assert rgg.rgg_plan(32, 512, 6144, 4096, op="gather", workspace=True)["gather_mode"] == 1
+    assert rgg.rgg_plan(4, 1024, 256, 256, op="gather", host_counts=[1000, 8, 8, 8],
+                        workspace=True)["gather_mode"] == 2
+    assert rgg.rgg_plan(4, 1024, 256, 256, op="gather", host_counts=[20, 0, 0, 0],
+                        workspace=True)["gather_mode"] == 1
     # the fused mode on request: 1-CTA tiles only
-    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="gather", gather_mode=1)
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="gather", gather_mode=1, workspace=True)
     assert p["gather_mode"] == 1 and p["bm"] == 128 and p["workspace_bytes"] == 0
-    assert rgg.rgg_plan(64, 16384, 1024, 2688, op="gather", bm=256)["gather_mode"] == 2
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, op="gather", bm=256, workspace=True)["gather_mode"] == 2
+    # the two-pass mode on request reports its workspace (the call itself needs one)
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="gather", gather_mode=2)
+    assert p["gather_mode"] == 2 and p["workspace_bytes"] == 16384 * 1024 * 2
     for kw in ({"op": "gather", "bm": 256, "gather_mode": 1}, {"op": "swiglu_gather", "bn": 192},
-               {"op": "gather", "gather_mode": 3}):
+               {"op": "gather", "gather_mode": 3}, {"op": "gather", "bm": 256}):
         with pytest.raises(rgg.RggError) as ei:
             rgg.rgg_plan(64, 16384, 1024, 2688, **kw)
         assert ei.value.status == rgg.RGG_ERR_INVALID_ARG
@@ -281,13 +253,12 @@ def test_plan_fused_gate_up_takes_pairs_without_tails(lib):
     assert rgg.rgg_plan(32, 512, 6144, 2048, op="swiglu")["bm"] == 64
     with pytest.raises(rgg.RggError):
         rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", bn=192)
-    # FP8 takes CTA pairs only when asked for, and only with BN = 256 (one
-    # 128-column weight panel per CTA)
+    # FP8 runs on 1-CTA tiles only (64 or 128 rows; BN 128 or 256)
     assert rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8")["bm"] == 128
-    p = rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8", bm=256)
-    assert p["bm"] == 256 and p["bn"] == 256 and p["threads"] == 320
-    with pytest.raises(rgg.RggError):
-        rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8", bm=256, bn=128)
+    for kw in (dict(bm=256), dict(bn=192)):
+        with pytest.raises(rgg.RggError) as ei:
+            rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8", **kw)
+        assert ei.value.status == rgg.RGG_ERR_INVALID_ARG
 
 
 def test_plan_reports_the_launch_block_size(lib):

@@ -42,6 +42,8 @@ def _run(g, swiglu=False, **opts):
     off = torch.from_numpy(g.offsets).cuda()
     N = W.shape[2] // 2 if swiglu else W.shape[2]
     Y = _canary(idx.numel(), N)
+    if opts.get("gather_mode") == 2 and "workspace" not in opts:  # the two-pass mode runs on a caller workspace
+        opts["workspace"] = torch.empty(idx.numel(), Xtok.shape[1], dtype=torch.bfloat16, device="cuda")
     fn = rgg.rgg_grouped_gemm_swiglu_gather if swiglu else rgg.rgg_grouped_gemm_gather
     fn(Xtok, idx, W, off, Y, check=True, **opts)
     torch.cuda.synchronize()
@@ -178,12 +180,21 @@ def test_caller_workspace_and_its_size_check():
         assert ei.value.status == rgg.RGG_ERR_INVALID_ARG
 
 
-def test_handle_workspace_grows_between_calls():
-    # a small call, then one whose rows (19 000 x 64 bf16 = 2.4 MB) need a larger handle
-    # workspace than the first 2 MB granule, then the small one again
-    for counts, T, seed in (([5, 9], 20, 101), ([3000, 7000, 9000], 9500, 102), ([5, 9], 20, 103)):
-        g = wl.make_gather_custom(counts, T=T, K=64, N=256, seed=seed, integer_valued=True)
-        assert np.array_equal(_run(g, gather_mode=2).double().numpy(), _ref(g))
+def test_no_workspace_means_no_two_pass_call():
+    # the library allocates nothing: two passes need the caller's workspace, and without one
+    # the automatic choice runs the fused gather even where two passes would be faster
+    g = wl.make_gather_custom([3000, 7000, 9000], T=9500, K=64, N=256, seed=102, integer_valued=True)
+    Xtok, W = g.Xtok.cuda(), g.W.cuda()
+    idx, off = torch.from_numpy(g.row_index).cuda(), torch.from_numpy(g.offsets).cuda()
+    for kw in (dict(gather_mode=2), dict(bm=256)):
+        with pytest.raises(rgg.RggError) as ei:
+            rgg.rgg_grouped_gemm_gather(Xtok, idx, W, off, **kw)
+        assert ei.value.status == rgg.RGG_ERR_INVALID_ARG
+    assert rgg.rgg_plan(3, idx.numel(), 64, 256, op="gather", host_counts=g.counts)["gather_mode"] == 1
+    assert np.array_equal(_run(g, host_counts=g.counts).double().numpy(), _ref(g))
+    ws = torch.empty(idx.numel(), 64, dtype=torch.bfloat16, device="cuda")
+    assert rgg.rgg_plan(3, idx.numel(), 64, 256, op="gather", host_counts=g.counts, workspace=ws)["gather_mode"] == 2
+    assert np.array_equal(_run(g, host_counts=g.counts, workspace=ws).double().numpy(), _ref(g))
 
 
 def test_no_routed_rows():
@@ -221,8 +232,9 @@ def test_full_size_sampled(name, swiglu):
     Xtok, W = g.Xtok.cuda(), g.W.cuda()
     idx, off = torch.from_numpy(g.row_index).cuda(), torch.from_numpy(g.offsets).cuda()
     fn = rgg.rgg_grouped_gemm_swiglu_gather if swiglu else rgg.rgg_grouped_gemm_gather
-    # the launch configuration the benchmark times (tile shape planned from the counts)
-    Y = fn(Xtok, idx, W, off, check=True, host_counts=g.counts)
+    # the launch configuration the benchmark times (tile shape planned from the counts, a caller workspace)
+    ws = torch.empty(idx.numel(), Xtok.shape[1], dtype=torch.bfloat16, device="cuda")
+    Y = fn(Xtok, idx, W, off, check=True, host_counts=g.counts, workspace=ws)
     torch.cuda.synchronize()
     assert bool(torch.isfinite(Y).all())
     N = W.shape[2] // 2 if swiglu else W.shape[2]

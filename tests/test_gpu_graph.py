@@ -1,9 +1,9 @@
 """The library's launches can be captured in a CUDA graph and replayed (GB300).
 
-Each call reads the routed counts on the device and allocates nothing per call
-(the handle's status word and, for the two-pass gather, its workspace exist
-once a first call has run), so a captured launch replays on new data in the
-same buffers.  Checked against the fp64 oracle with the usual tolerance.
+Each call reads the routed counts on the device and allocates nothing (the
+handle's status word exists from rgg_create; the two-pass gather's workspace
+is the caller's), so a captured launch replays on new data in the same
+buffers.  Checked against the fp64 oracle with the usual tolerance.
 """
 import numpy as np
 import pytest
@@ -61,10 +61,11 @@ def test_two_pass_gather_replays_on_new_indices():
     Xtok, W = a.Xtok.cuda(), a.W.cuda()
     idx, off = torch.from_numpy(a.row_index).cuda(), torch.from_numpy(a.offsets).cuda()
     Y = torch.empty(idx.numel(), 256, dtype=torch.bfloat16, device="cuda")
-    rgg.rgg_grouped_gemm_gather(Xtok, idx, W, off, Y, gather_mode=2, check=True)  # sizes the handle's workspace
+    ws = torch.empty(idx.numel(), 128, dtype=torch.bfloat16, device="cuda")
+    rgg.rgg_grouped_gemm_gather(Xtok, idx, W, off, Y, gather_mode=2, workspace=ws, check=True)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        rgg.rgg_grouped_gemm_gather(Xtok, idx, W, off, Y, gather_mode=2)
+        rgg.rgg_grouped_gemm_gather(Xtok, idx, W, off, Y, gather_mode=2, workspace=ws)
     for inp in (b, a):
         Xtok.copy_(inp.Xtok.cuda())
         W.copy_(inp.W.cuda())

@@ -8,7 +8,7 @@ oracle, on a GB300.
   result must equal the oracle bit for bit.
 * Seeded random configurations over expert counts, row counts (with empty
   and single-row experts), K and N tails, tile shapes, walk orders, tail-tile
-  modes and the multicast kernel, against the tolerance
+  modes, against the tolerance
   |gpu - oracle| <= 1e-2 * max(1, |oracle|), rows of no expert untouched.
 * Four million routed rows, checked at sampled outputs.
 """
@@ -56,9 +56,8 @@ def _close(got, ref):
         bad.shape[0], bad[0].tolist(), got[tuple(bad[0])], ref[tuple(bad[0])])
 
 
-@pytest.mark.parametrize("opts", [dict(), dict(bm=64, bn=128), dict(bm=128, bn=256), dict(bm=256, bn=256),
-                                  dict(multicast=1)],
-                         ids=["auto", "64x128", "128x256", "pair", "multicast"])
+@pytest.mark.parametrize("opts", [dict(), dict(bm=64, bn=128), dict(bm=128, bn=256), dict(bm=256, bn=256)],
+                         ids=["auto", "64x128", "128x256", "pair"])
 def test_max_experts_bit_exact(opts):
     rng = np.random.default_rng(4096)
     counts = rng.integers(0, 6, 4096) * (rng.random(4096) < 0.6)
@@ -91,11 +90,9 @@ def _random_case(seed):
     K = int(rng.choice([64, 128, 200, 264, 512]))
     N = 8 * int(rng.integers(2, 96))
     choices = [dict(), dict(bm=64), dict(bm=128), dict(bm=256), dict(bm=128, bn=192), dict(bm=64, bn=128),
-               dict(multicast=1), dict(bm=128, tail64=-1), dict(bm=256, tail64=-1)]
+               dict(bm=256, bn=128), dict(bm=128, tail64=-1), dict(bm=256, tail64=-1)]
     opts = dict(choices[int(rng.integers(len(choices)))])
-    walks = [0, 1, 2, 4] if opts.get("multicast") else ([0, 1, 2, 3, 4] if E <= 256 else [0, 1, 2, 4])
-    if opts.get("multicast"):
-        walks = [0, 1, 2]
+    walks = [0, 1, 2, 3, 4] if E <= 256 else [0, 1, 2, 4]
     opts["walk_order"] = int(rng.choice(walks))
     if rng.random() < 0.5:
         opts["host_counts"] = counts
