@@ -9,11 +9,16 @@ Worklog", section 1), with t measured on the device with CUDA events around K
 replays of one step captured in a CUDA graph (the same K steps launched one by
 one from the host are reported beside it as "eager").
 
-Default workload: the small-decode, weight-bound configuration -- 32 experts
-x 16 rows, K = 6144, N = 4096 (the decode example of "Pearl's grouped GEMM
-kernel for MoE models, explained", "Why MoE needs a grouped GEMM").  Its
-inputs (1.6 GB of weights) are larger than the 129 MB L2, so no flush is
-needed between steps.
+Headline workload (the default): prefill-scale routing, the largest of the
+workloads -- 32 experts, K = 6144, N = 4096, 32 768 tokens each routed to one
+uniformly random expert.  Beside it, in the same JSON line ("configs"), the
+other workloads are timed in the same way: the worklog's uniform and skewed
+16k-row routings (section 1, "Some Results First") and the skewed one at 2k
+rows, the small-decode shape (32 experts x 16 rows, the decode example of
+"Pearl's grouped GEMM kernel for MoE models, explained", "Why MoE needs a
+grouped GEMM"), and the skewed routings once more with the tile shape planned
+from the device offsets alone.  Every workload's inputs are larger than the
+129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -58,10 +63,12 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
-    p.add_argument("--workload", default="decode", choices=sorted(wl.WORKLOADS))
+    p.add_argument("--workload", default="prefill", choices=sorted(wl.WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="time only the headline workload (no uniform / skew / decode side configurations)")
     p.add_argument("--bm", type=int, default=0)
     p.add_argument("--bn", type=int, default=0)
     p.add_argument("--stages", type=int, default=0)
@@ -307,98 +314,113 @@ def run_profile(args):
         raise SystemExit(1)
 
 
-def run_ours(args):
-    import ragged_grouped_gemm_02_gb300 as rgg
-    from ragged_grouped_gemm_02_gb300 import _build
+class Step:
+    """One workload and op on the device: inputs resident in HBM, the launch
+    of one step, its algorithmic work and what the end-to-end run copies."""
 
-    world, rank, local = dist_setup("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    _build.build()
-    w = wl.WORKLOADS[args.workload]
-    inp = wl.make_inputs(wl.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank}))
-    K, N, E = w.K, w.N, w.E
-    M_tot = inp.X.shape[0]
-    flops, bytes_ = work_of(inp.counts, K, N)
-    fused = args.op in ("swiglu", "swiglu_gather")
-    gather = args.op in ("gather", "swiglu_gather")
-    N_out = N // 2 if fused else N
-    if fused:  # the output is half as wide; the weight bytes and MMA work are the same
-        bytes_ -= 2.0 * M_tot * (N - N_out)
-    gemm = rgg.rgg_grouped_gemm_swiglu if fused else rgg.rgg_grouped_gemm
-    if args.op == "fp8":
-        # the same draws quantised to E4M3 with per-row / per-column scales:
-        # X and W stream at one byte per element, scales are fp32
-        X8, W8, sx, sw = wl.quantize_fp8(inp.X, inp.W)
-        active = int(np.count_nonzero(inp.counts))
-        bytes_ = (1.0 * (active * K * N + M_tot * K) + 2.0 * M_tot * N + 4.0 * (M_tot + E * N)
-                  + 4.0 * (E + 1))
-        sx_d, sw_d = sx.to(dev), sw.to(dev)
-        inp.X, inp.W = X8, W8
+    def __init__(self, rgg, args, workload, op, rank, dev, host_counts=True):
+        w = wl.WORKLOADS[workload]
+        self.rgg, self.op, self.workload, self.dev = rgg, op, workload, dev
+        inp = wl.make_inputs(wl.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank}))
+        self.w, self.inp = w, inp
+        K, N, E = w.K, w.N, w.E
+        self.K, self.N, self.E = K, N, E
+        M_tot = inp.X.shape[0]
+        self.M_tot = M_tot
+        flops, bytes_ = work_of(inp.counts, K, N)
+        self.fused = op in ("swiglu", "swiglu_gather")
+        self.gather = op in ("gather", "swiglu_gather")
+        self.N_out = N // 2 if self.fused else N
+        if self.fused:  # the output is half as wide; the weight bytes and MMA work are the same
+            bytes_ -= 2.0 * M_tot * (N - self.N_out)
+        self.sx = self.sw = self.idx_h = None
+        gemm = rgg.rgg_grouped_gemm_swiglu if self.fused else rgg.rgg_grouped_gemm
+        if op == "fp8":
+            # the same draws quantised to E4M3 with per-row / per-column scales:
+            # X and W stream at one byte per element, scales are fp32
+            X8, W8, sx, sw = wl.quantize_fp8(inp.X, inp.W)
+            active = int(np.count_nonzero(inp.counts))
+            bytes_ = (1.0 * (active * K * N + M_tot * K) + 2.0 * M_tot * N + 4.0 * (M_tot + E * N)
+                      + 4.0 * (E + 1))
+            self.sx, self.sw = sx, sw
+            self.sx_d, self.sw_d = sx.to(dev), sw.to(dev)
+            inp.X, inp.W = X8, W8
 
-        def gemm(Xd, Wd, offd, Yd, **kw):
-            return rgg.rgg_grouped_gemm_fp8(Xd, Wd, sx_d, sw_d, offd, Yd, **kw)
-    idx_h = None
-    if gather:
-        # The activations are M_tot tokens in token order; routed row i reads
-        # token row_index[i] (each expert's rows are distinct tokens in
-        # increasing order).  The index adds 4 bytes per routed row.
-        gen = torch.Generator().manual_seed(w.seed + 1000 * rank + 7)
-        idx_h = torch.from_numpy(wl.routed_row_index(inp.counts, M_tot, gen))
-        idx_d = idx_h.to(dev)
-        bytes_ += 4.0 * M_tot
-        gfn = rgg.rgg_grouped_gemm_swiglu_gather if fused else rgg.rgg_grouped_gemm_gather
+            def gemm(Xd, Wd, offd, Yd, sxd=None, **kw):
+                return rgg.rgg_grouped_gemm_fp8(Xd, Wd, self.sx_d if sxd is None else sxd, self.sw_d, offd, Yd, **kw)
+        if self.gather:
+            # The activations are M_tot tokens in token order; routed row i reads
+            # token row_index[i] (each expert's rows are distinct tokens in
+            # increasing order).  The index adds 4 bytes per routed row.
+            gen = torch.Generator().manual_seed(w.seed + 1000 * rank + 7)
+            self.idx_h = torch.from_numpy(wl.routed_row_index(inp.counts, M_tot, gen))
+            self.idx_d = self.idx_h.to(dev)
+            bytes_ += 4.0 * M_tot
+            gfn = rgg.rgg_grouped_gemm_swiglu_gather if self.fused else rgg.rgg_grouped_gemm_gather
 
-        def gemm(Xd, Wd, offd, Yd, idx=None, **kw):
-            return gfn(Xd, idx_d if idx is None else idx, Wd, offd, Yd, **kw)
-    X, W = inp.X.to(dev), inp.W.to(dev)
-    off = torch.from_numpy(inp.offsets).to(dev)
-    Y = torch.empty(M_tot, N_out, dtype=torch.bfloat16, device=dev)
-    # The tile shape is planned from the routed counts, known on the host as in
-    # the worklog's harness; the kernel itself reads the offsets on the device.
-    opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
-                walk_order=args.walk_order, host_counts=inp.counts)
-    if gather:
-        opts["gather_mode"] = args.gather_mode
-        opts["workspace"] = torch.empty_like(X)  # the two-pass mode's gathered rows, allocated once
-    plan = rgg.rgg_plan(E, M_tot, K, N_out, num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
-                        op=args.op, **opts)
+            def gemm(Xd, Wd, offd, Yd, idx=None, **kw):
+                return gfn(Xd, self.idx_d if idx is None else idx, Wd, offd, Yd, **kw)
+        self.gemm = gemm
+        self.flops, self.bytes = flops, bytes_
+        self.X, self.W = inp.X.to(dev), inp.W.to(dev)
+        self.off = torch.from_numpy(inp.offsets).to(dev)
+        self.Y = torch.empty(M_tot, self.N_out, dtype=torch.bfloat16, device=dev)
+        # The tile shape is planned from the routed counts, known on the host as
+        # in the worklog's harness (host_counts=False: from the device offsets
+        # alone); the kernel itself reads the offsets on the device.
+        self.opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
+                         walk_order=args.walk_order, host_counts=inp.counts if host_counts else None)
+        self.plan_from = ("host-side routed counts (tile shape only)" if host_counts
+                          else "device offsets only (no host counts)")
+        if self.gather:
+            self.opts["gather_mode"] = args.gather_mode
+            # the two-pass mode's gathered rows, allocated once outside the timed region
+            self.opts["workspace"] = torch.empty_like(self.X)
+        self.plan = rgg.rgg_plan(E, M_tot, K, self.N_out,
+                                 num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
+                                 op=op, **self.opts)
+        # launches of this library's kernels in one step: the two-pass gather runs
+        # its row gather and then the grouped GEMM, every other op one kernel
+        self.per_step = 2 if self.plan.get("gather_mode") == 2 else 1
+
+    def launch(self, stream):
+        self.gemm(self.X, self.W, self.off, self.Y, stream=stream, **self.opts)
+
+
+def time_step(step, args, world, dev, ramp_s):
+    """W warm-up steps (after an untimed ramp of about `ramp_s` seconds that
+    brings the GPU to its clocks under load), then K steps launched one by one
+    (eager) and K replays of one step captured in a CUDA graph (the timed
+    region), on the launching stream, bracketed by a barrier and a device
+    synchronisation.  Returns the timings and the clock record."""
+    rgg = step.rgg
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        gemm(X, W, off, Y, stream=stream, **opts)
-
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(dev.index)
     sampler.start()
-    # warm-up: at least W steps and about a second of GPU work, so the clock
-    # record covers the GPU under load
     t_begin = time.time()
-    n_warm = 0
-    while n_warm < max(3, args.warmup) or time.time() - t_begin < 1.0:
-        step()
-        n_warm += 1
-        if n_warm % 64 == 0:
+    ramp = 0
+    while time.time() - t_begin < ramp_s:
+        step.launch(stream)
+        ramp += 1
+        if ramp % 64 == 0:
             torch.cuda.synchronize(dev)
-    status = rgg.rgg_query_status(local, stream)
+    for _ in range(max(3, args.warmup)):
+        step.launch(stream)
+    status = rgg.rgg_query_status(dev.index, stream)
     if status != rgg.RGG_OK:
         raise RuntimeError("device status after warm-up: %s" % rgg.rgg_status_string(status))
-
     K_steps = args.steps
-    # Launches of this library's kernels in one step: the two-pass gather runs
-    # its row gather and then the grouped GEMM, every other op one kernel.
-    per_step = 2 if plan.get("gather_mode") == 2 else 1
 
-    # Eager: K steps launched one by one from the host.
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
     start.record(stream)
-    for i in range(K_steps):
-        step()
+    for _ in range(K_steps):
+        step.launch(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    status = rgg.rgg_query_status(local, stream)
+    status = rgg.rgg_query_status(dev.index, stream)
     if status != rgg.RGG_OK:
         raise RuntimeError("device status after the eager steps: %s" % rgg.rgg_status_string(status))
     eager_ms = max_over_ranks(start.elapsed_time(end), world, dev)
@@ -407,11 +429,10 @@ def run_ours(args):
     # the same stream, so the device time has no host launch work in it (the
     # pages time their kernels inside CUDA graphs too).
     timing = "cuda_graph"
-    total_ms = None
     try:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            gemm(X, W, off, Y, stream=torch.cuda.current_stream(dev), **opts)
+            step.launch(torch.cuda.current_stream(dev))
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize(dev)
@@ -430,176 +451,245 @@ def run_ours(args):
         timing = "eager (graph capture failed: %s)" % str(e)[:160]
         total_ms = eager_ms
     clocks = sampler.stop()
-    status = rgg.rgg_query_status(local, stream)
+    status = rgg.rgg_query_status(dev.index, stream)
     if status != rgg.RGG_OK:
         raise RuntimeError("device status after the timed region: %s" % rgg.rgg_status_string(status))
-    # average duration of one step in the timed region (for the one-kernel ops,
-    # one launch of the GEMM kernel plus the gap to the next)
-    launch_ms = total_ms / K_steps
-    eager = {"value": round(flops * K_steps * world / (eager_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
-             "ms_per_step": round(eager_ms / K_steps, 5),
-             "note": "the same K steps launched one by one from the host"}
+    return {"total_ms": total_ms, "eager_ms": eager_ms, "timing": timing, "clocks": clocks,
+            "ramp": {"steps": ramp, "seconds": round(ramp_s, 2),
+                     "note": "untimed launches before the warm-up, so the clocks are those under load"}}
 
-    # End to end through the public API: every step copies its inputs (X, the
-    # offsets, and for FP8 the row scales) in from pinned host memory and its
-    # result out to pinned host memory, all inside the timed region.  As in a
-    # serving loop, two buffer sets let step i's copies overlap the GEMM of its
-    # neighbours: inputs go in on one stream, results come out on another,
-    # events keep each buffer from being overwritten while it is still in use.
-    e2e = None
-    if not args.no_e2e:
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        hX = inp.X.pin_memory()
-        hoff = torch.from_numpy(inp.offsets).pin_memory()
-        hY = [torch.empty(M_tot, N_out, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-        dX = [torch.empty_like(X) for _ in range(2)]
-        doff = [torch.empty_like(off) for _ in range(2)]
-        dY = [Y, torch.empty_like(Y)]
-        fp8 = args.op == "fp8"
-        if fp8:
-            hsx = sx.pin_memory()
-            dsx = [torch.empty_like(sx_d) for _ in range(2)]
-        if gather:
-            hidx = idx_h.pin_memory()
-            didx = [torch.empty_like(idx_d) for _ in range(2)]
-        ev = lambda: torch.cuda.Event()  # noqa: E731
-        in_ready, gemm_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-        for b in range(2):
-            gemm_done[b].record(stream)
-            out_done[b].record(stream)
 
-        def e2e_step(i):
-            b = i % 2
-            s_in.wait_event(gemm_done[b])          # the GEMM two steps back has read dX[b]
-            with torch.cuda.stream(s_in):
-                dX[b].copy_(hX, non_blocking=True)
-                doff[b].copy_(hoff, non_blocking=True)
-                if fp8:
-                    dsx[b].copy_(hsx, non_blocking=True)
-                if gather:
-                    didx[b].copy_(hidx, non_blocking=True)
-            in_ready[b].record(s_in)
-            stream.wait_event(in_ready[b])
-            stream.wait_event(out_done[b])         # dY[b] has been read out
-            if fp8:
-                rgg.rgg_grouped_gemm_fp8(dX[b], W, dsx[b], sw_d, doff[b], dY[b], stream=stream, **opts)
-            elif gather:
-                gemm(dX[b], W, doff[b], dY[b], idx=didx[b], stream=stream, **opts)
-            else:
-                gemm(dX[b], W, doff[b], dY[b], stream=stream, **opts)
-            gemm_done[b].record(stream)
-            s_out.wait_event(gemm_done[b])
-            with torch.cuda.stream(s_out):
-                hY[b].copy_(dY[b], non_blocking=True)
-            out_done[b].record(s_out)
-
-        for i in range(4):
-            e2e_step(i)
-        torch.cuda.synchronize(dev)
-        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        e_start.record(stream)
-        s_in.wait_event(e_start)
-        for i in range(K_steps):
-            e2e_step(i)
-        s_out.synchronize()
-        e_end.record(s_out)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        e_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
-        # The same steps without overlap: copy in, GEMM, copy out, one after
-        # the other on one stream (what a caller that waits for each result sees).
-        def serial_step():
-            with torch.cuda.stream(stream):
-                dX[0].copy_(hX, non_blocking=True)
-                doff[0].copy_(hoff, non_blocking=True)
-                if fp8:
-                    dsx[0].copy_(hsx, non_blocking=True)
-                    rgg.rgg_grouped_gemm_fp8(dX[0], W, dsx[0], sw_d, doff[0], dY[0], stream=stream, **opts)
-                elif gather:
-                    didx[0].copy_(hidx, non_blocking=True)
-                    gemm(dX[0], W, doff[0], dY[0], idx=didx[0], stream=stream, **opts)
-                else:
-                    gemm(dX[0], W, doff[0], dY[0], stream=stream, **opts)
-                hY[0].copy_(dY[0], non_blocking=True)
-
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        s_start, s_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s_start.record(stream)
-        for i in range(K_steps):
-            serial_step()
-        s_end.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        s_ms = max_over_ranks(s_start.elapsed_time(s_end), world, dev)
-        h2d = (hX.numel() * hX.element_size() + hoff.numel() * 4 + (hsx.numel() * 4 if fp8 else 0)
-               + (hidx.numel() * 4 if gather else 0))
-        e2e = {"value": round(flops * K_steps * world / (e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hY[0].numel() * 2),
-               "ms_per_step": round(e_ms / K_steps, 4),
-               "pipeline": "two buffer sets; step i's host copies overlap neighbouring GEMMs",
-               "serial": {"value": round(flops * K_steps * world / (s_ms / 1e3) / 1e12, 3),
-                          "ms_per_step": round(s_ms / K_steps, 4),
-                          "note": "copy in, GEMM, copy out in order on one stream"},
-               "weights": "resident in HBM (model parameters); not copied per step"}
-
-    peaks = load_peaks()
-    t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
+def roofline_of(step, launch_ms, peaks):
+    """Achieved algorithmic bytes (or FLOPs) per launch over the launch time,
+    against the measured peak of the bound that is larger."""
+    op = step.op
+    t_hbm = step.bytes / (peaks["hbm_gbs"] * 1e9)
     # a contraction is measured against the peak of its own operand type: FP8
     # takes the measured bf16 peak times the nominal fp8/bf16 ratio (2)
-    tc_peak = peaks["bf16_tflops"] * (2.0 if args.op == "fp8" else 1.0)
-    t_tc = flops / (tc_peak * 1e12)
+    tc_peak = peaks["bf16_tflops"] * (2.0 if op == "fp8" else 1.0)
+    t_tc = step.flops / (tc_peak * 1e12)
     if t_hbm >= t_tc:
-        roof = {"bound": "hbm", "achieved": round(bytes_ / (launch_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+        roof = {"bound": "hbm", "achieved": round(step.bytes / (launch_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     else:
-        roof = {"bound": "tensor", "achieved": round(flops / (launch_ms / 1e3) / 1e12, 1),
+        roof = {"bound": "tensor", "achieved": round(step.flops / (launch_ms / 1e3) / 1e12, 1),
                 "peak": tc_peak, "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     # the capture of this exact launch: the workload, and the op when it is not the plain GEMM
-    roof["traffic"] = measured_traffic(args.workload if args.op == "gemm" else args.workload + "+" + args.op)
-    roof["peak_source"] = peaks["source"] + (" bf16 x 2 (nominal fp8/bf16 ratio)" if args.op == "fp8" else "")
-    roof["algorithmic_per_launch"] = {"flops": flops, "bytes": bytes_}
+    roof["traffic"] = measured_traffic(step.workload if op == "gemm" else step.workload + "+" + op)
+    roof["peak_source"] = peaks["source"] + (" bf16 x 2 (nominal fp8/bf16 ratio)" if op == "fp8" else "")
+    roof["algorithmic_per_launch"] = {"flops": step.flops, "bytes": step.bytes}
     roof["launch_ms"] = round(launch_ms, 5)
     roof["launch_scope"] = ("one step of the CUDA-graph timed region: the row gather and the GEMM"
-                            if per_step == 2 else "one GEMM launch in the CUDA-graph timed region")
-    roof["hbm_gbs"] = round(bytes_ / (launch_ms / 1e3) / 1e9, 1)
-    roof["hbm_frac"] = round(bytes_ / (launch_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
-    roof["tensor_frac"] = round(flops / (launch_ms / 1e3) / 1e12 / tc_peak, 4)
+                            if step.per_step == 2 else "one GEMM launch in the CUDA-graph timed region")
+    roof["hbm_gbs"] = round(step.bytes / (launch_ms / 1e3) / 1e9, 1)
+    roof["hbm_frac"] = round(step.bytes / (launch_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
+    roof["tensor_frac"] = round(step.flops / (launch_ms / 1e3) / 1e12 / tc_peak, 4)
     # The measured sustained bf16 rate (a seconds-long GEMM loop under the power cap) is the
-    # fairer yardstick for shapes that draw the cap during this long back-to-back loop; the
+    # fairer yardstick for shapes that draw the cap during a long back-to-back loop; the
     # burst figure above stays the roofline's denominator.
-    tc_sust = peaks["bf16_tflops_sustained"] * (2.0 if args.op == "fp8" else 1.0)
-    roof["tensor_frac_of_sustained"] = round(flops / (launch_ms / 1e3) / 1e12 / tc_sust, 4)
+    tc_sust = peaks["bf16_tflops_sustained"] * (2.0 if op == "fp8" else 1.0)
+    roof["tensor_frac_of_sustained"] = round(step.flops / (launch_ms / 1e3) / 1e12 / tc_sust, 4)
+    return roof
 
+
+def e2e_of(step, args, world, dev):
+    """The same metric end to end through the public API: every step copies
+    its inputs (X, the offsets, and for FP8 the row scales, for the gather ops
+    the token indices) in from pinned host memory and its result out to pinned
+    host memory, all inside the timed region.  As in a serving loop, two
+    buffer sets let step i's copies overlap the GEMM of its neighbours: inputs
+    go in on one stream, results come out on another, events keep each buffer
+    from being overwritten while it is still in use."""
+    rgg = step.rgg
+    K_steps = args.steps
+    stream = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    inp = step.inp
+    hX = inp.X.pin_memory()
+    hoff = torch.from_numpy(inp.offsets).pin_memory()
+    hY = [torch.empty(step.M_tot, step.N_out, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dX = [torch.empty_like(step.X) for _ in range(2)]
+    doff = [torch.empty_like(step.off) for _ in range(2)]
+    dY = [step.Y, torch.empty_like(step.Y)]
+    fp8, gather = step.op == "fp8", step.gather
+    if fp8:
+        hsx = step.sx.pin_memory()
+        dsx = [torch.empty_like(step.sx_d) for _ in range(2)]
+    if gather:
+        hidx = step.idx_h.pin_memory()
+        didx = [torch.empty_like(step.idx_d) for _ in range(2)]
+    opts = step.opts
+
+    def run(b, st):
+        if fp8:
+            step.gemm(dX[b], step.W, doff[b], dY[b], sxd=dsx[b], stream=st, **opts)
+        elif gather:
+            step.gemm(dX[b], step.W, doff[b], dY[b], idx=didx[b], stream=st, **opts)
+        else:
+            step.gemm(dX[b], step.W, doff[b], dY[b], stream=st, **opts)
+
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, gemm_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for b in range(2):
+        gemm_done[b].record(stream)
+        out_done[b].record(stream)
+
+    def e2e_step(i):
+        b = i % 2
+        s_in.wait_event(gemm_done[b])          # the GEMM two steps back has read dX[b]
+        with torch.cuda.stream(s_in):
+            dX[b].copy_(hX, non_blocking=True)
+            doff[b].copy_(hoff, non_blocking=True)
+            if fp8:
+                dsx[b].copy_(hsx, non_blocking=True)
+            if gather:
+                didx[b].copy_(hidx, non_blocking=True)
+        in_ready[b].record(s_in)
+        stream.wait_event(in_ready[b])
+        stream.wait_event(out_done[b])         # dY[b] has been read out
+        run(b, stream)
+        gemm_done[b].record(stream)
+        s_out.wait_event(gemm_done[b])
+        with torch.cuda.stream(s_out):
+            hY[b].copy_(dY[b], non_blocking=True)
+        out_done[b].record(s_out)
+
+    for i in range(4):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e_start.record(stream)
+    s_in.wait_event(e_start)
+    for i in range(K_steps):
+        e2e_step(i)
+    s_out.synchronize()
+    e_end.record(s_out)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
+
+    # The same steps without overlap: copy in, GEMM, copy out, one after the
+    # other on one stream (what a caller that waits for each result sees).
+    def serial_step():
+        with torch.cuda.stream(stream):
+            dX[0].copy_(hX, non_blocking=True)
+            doff[0].copy_(hoff, non_blocking=True)
+            if fp8:
+                dsx[0].copy_(hsx, non_blocking=True)
+            if gather:
+                didx[0].copy_(hidx, non_blocking=True)
+            run(0, stream)
+            hY[0].copy_(dY[0], non_blocking=True)
+
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    s_start, s_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_start.record(stream)
+    for _ in range(K_steps):
+        serial_step()
+    s_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    s_ms = max_over_ranks(s_start.elapsed_time(s_end), world, dev)
+    status = rgg.rgg_query_status(dev.index, stream)
+    if status != rgg.RGG_OK:
+        raise RuntimeError("device status after the end-to-end steps: %s" % rgg.rgg_status_string(status))
+    h2d = (hX.numel() * hX.element_size() + hoff.numel() * 4 + (hsx.numel() * 4 if fp8 else 0)
+           + (hidx.numel() * 4 if gather else 0))
+    return {"value": round(step.flops * K_steps * world / (e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hY[0].numel() * 2),
+            "ms_per_step": round(e_ms / K_steps, 4),
+            "pipeline": "two buffer sets; step i's host copies overlap neighbouring GEMMs",
+            "serial": {"value": round(step.flops * K_steps * world / (s_ms / 1e3) / 1e12, 3),
+                       "ms_per_step": round(s_ms / K_steps, 4),
+                       "note": "copy in, GEMM, copy out in order on one stream"},
+            "weights": "resident in HBM (model parameters); not copied per step"}
+
+
+def config_of(step, world):
+    w = step.w
+    cfg = {"workload": step.workload + ("" if step.op == "gemm" else "+" + step.op), "op": step.op,
+           "E": step.E, "K": step.K, "N": step.N_out, "weight_columns": step.N, "M_tot": step.M_tot,
+           "routing": w.routing, "note": w.note, "accumulate": "fp32", "out": "bf16",
+           "l2": "inputs larger than L2 (%.0f MB > 129 MB), no flush" % (step.bytes / 1e6)
+           if step.bytes > L2_BYTES else "inputs smaller than L2: back-to-back launches",
+           "plan": step.plan, "plan_from": step.plan_from, "parallelism": "expert replicas x%d" % world}
+    if step.gather:
+        cfg.update({"tokens": step.M_tot, "row_index": "each expert's rows are distinct tokens, in token order"})
+    return cfg
+
+
+# The other workloads timed beside the headline, in the same way: the large
+# uniform and skewed routings and the small-decode shape, and the skewed
+# routings once more with the tile shape planned from the device offsets alone.
+SIDE_CONFIGS = [("uniform", True), ("skew16k", True), ("skew2k", True), ("decode", True),
+                ("skew16k", False), ("skew2k", False)]
+
+
+def run_ours(args):
+    import ragged_grouped_gemm_02_gb300 as rgg
+    from ragged_grouped_gemm_02_gb300 import _build
+
+    world, rank, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    peaks = load_peaks()
+
+    step = Step(rgg, args, args.workload, args.op, rank, dev)
+    t = time_step(step, args, world, dev, ramp_s=1.0)
+    K_steps = args.steps
+    launch_ms = t["total_ms"] / K_steps
+    value = step.flops * K_steps * world / (t["total_ms"] / 1e3) / 1e12
+    eager = {"value": round(step.flops * K_steps * world / (t["eager_ms"] / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+             "ms_per_step": round(t["eager_ms"] / K_steps, 5),
+             "note": "the same K steps launched one by one from the host"}
+    roof = roofline_of(step, launch_ms, peaks)
+    e2e = None if args.no_e2e else e2e_of(step, args, world, dev)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, threads = oracle_cpu_rate(inp, op=args.op, scales=(sx, sw) if args.op == "fp8" else None,
-                                             row_index=idx_h.numpy() if gather else None)
+        v, sample, threads = oracle_cpu_rate(step.inp, op=args.op,
+                                             scales=(step.sx, step.sw) if args.op == "fp8" else None,
+                                             row_index=step.idx_h.numpy() if step.gather else None)
         cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
+    launches = K_steps * step.per_step
+    headline_cfg = config_of(step, world)
+    del step
+    torch.cuda.empty_cache()
 
-    value = flops * K_steps * world / (total_ms / 1e3) / 1e12
+    configs = {}
+    if not args.no_configs:
+        for name, from_counts in SIDE_CONFIGS:
+            if name == args.workload and from_counts:
+                continue
+            s = Step(rgg, args, name, args.op, rank, dev, host_counts=from_counts)
+            ts = time_step(s, args, world, dev, ramp_s=0.5)
+            lm = ts["total_ms"] / K_steps
+            key = name if from_counts else name + " (plan from device offsets)"
+            configs[key] = {
+                "value": round(s.flops * K_steps * world / (ts["total_ms"] / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(lm, 5), "roofline": roofline_of(s, lm, peaks), "timing": ts["timing"],
+                "clocks": ts["clocks"], "config": config_of(s, world)}
+            launches += K_steps * s.per_step
+            del s
+            torch.cuda.empty_cache()
+
     page = PAGE_NUMBERS.get(args.workload)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K_steps,
-        "warmup": n_warm, "ms_per_step": round(total_ms / K_steps, 5), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(t["total_ms"] / K_steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": round(value / page, 4) if page and args.op == "gemm" else None,
         "dtype": "e4m3" if args.op == "fp8" else "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,1/K) weights)",
-        "config": {"workload": args.workload + ("" if args.op == "gemm" else "+" + args.op), "op": args.op,
-                   "E": E, "K": K,
-                   "N": N_out, "weight_columns": N, "M_tot": M_tot,
-                   **({"tokens": M_tot, "row_index": "each expert's rows are distinct tokens, in token order"}
-                      if gather else {}),
-                   "routing": w.routing, "note": w.note, "accumulate": "fp32", "out": "bf16",
-                   "l2": "inputs larger than L2 (%.0f MB > 129 MB), no flush" % (bytes_ / 1e6)
-                   if bytes_ > L2_BYTES else "inputs smaller than L2: back-to-back launches",
-                   "plan": plan, "plan_from": "host-side routed counts (tile shape only)",
-                   "parallelism": "expert replicas x%d" % world},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "timing": timing, "eager": eager,
-        "clocks": clocks, "gpu_launches": K_steps * per_step, "impl": "ours",
+        "config": headline_cfg,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "timing": t["timing"], "eager": eager,
+        "ramp": t["ramp"], "clocks": t["clocks"], "configs": configs,
+        "gpu_launches": launches,
+        "gpu_launches_note": "kernels of this library launched in the timed regions: the headline's K steps "
+                             "plus each side configuration's K steps", "impl": "ours",
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

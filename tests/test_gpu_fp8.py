@@ -7,7 +7,6 @@ applies: |gpu - oracle| <= 1e-2 * max(1, |oracle|).  Integer codes with unit
 scales are exact in fp32 and bf16 (bit-exact comparison), which pins the FP8
 operand layouts, the K = 32 MMA steps and the 128-column weight panels.
 """
-import zlib
 
 import numpy as np
 import pytest
@@ -96,27 +95,17 @@ def test_bad_offsets_rejected():
     assert bool((Y.view(torch.int16) == CANARY).all())
 
 
-@pytest.mark.parametrize("name", ["decode", "uniform", "prefill"])
-def test_full_size_sampled(name):
+@pytest.mark.parametrize("name", ["decode", "uniform", "skew16k", "prefill"])
+def test_full_size(name):
+    # every routed output against the whole fp64 oracle product, in the benchmark's launch configuration
     f = wl.make_fp8_inputs(name)
     X8, W8, sx, sw = f.X8.cuda(), f.W8.cuda(), f.sx.cuda(), f.sw.cuda()
     off = torch.from_numpy(f.offsets).cuda()
     Y = rgg.rgg_grouped_gemm_fp8(X8, W8, sx, sw, off, check=True, host_counts=f.counts)
     torch.cuda.synchronize()
-    assert bool(torch.isfinite(Y).all())
-    rng = np.random.default_rng(zlib.crc32(name.encode()) + 11)
-    M_used = int(f.offsets[-1])
-    rows = rng.integers(0, M_used, 1500)
-    cols = rng.integers(0, W8.shape[2], 1500)
-    X8c, W8c = wl.fp8_codes(f.X8), wl.fp8_codes(f.W8)
-    # the oracle on just the sampled rows (each row with its own expert's weights)
-    e_of_row = np.searchsorted(f.offsets, rows, side="right") - 1
-    ref = np.empty(rows.size)
-    for p in range(rows.size):
-        e = int(e_of_row[p])
-        sub = oracle.grouped_gemm_fp8(X8c[rows[p]:rows[p] + 1], np.ascontiguousarray(W8c[e:e + 1, :, cols[p]:cols[p] + 16]),
-                                      f.sx.numpy()[rows[p]:rows[p] + 1],
-                                      np.ascontiguousarray(f.sw.numpy()[e:e + 1, cols[p]:cols[p] + 16]), [0, 1])
-        ref[p] = sub[0, 0]
-    got = Y[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
-    assert (np.abs(got - ref) <= RTOL * np.maximum(1.0, np.abs(ref))).all()
+    ref = oracle.grouped_gemm_fp8(wl.fp8_codes(f.X8), wl.fp8_codes(f.W8), f.sx.numpy(), f.sw.numpy(), f.offsets)
+    lo, hi = int(f.offsets[0]), int(f.offsets[-1])
+    got = Y[lo:hi].double().cpu().numpy()
+    err = np.abs(got - ref[lo:hi])
+    bad = ~(err <= RTOL * np.maximum(1.0, np.abs(ref[lo:hi])))
+    assert not bad.any(), "%s: %d outputs out of tolerance, max err %.4g" % (name, int(bad.sum()), err.max())

@@ -10,9 +10,8 @@ oracle, on a GB300.
   and single-row experts), K and N tails, tile shapes, walk orders, tail-tile
   modes, against the tolerance
   |gpu - oracle| <= 1e-2 * max(1, |oracle|), rows of no expert untouched.
-* Four million routed rows, checked at sampled outputs.
+* Four million routed rows, every output checked.
 """
-import zlib
 
 import numpy as np
 import pytest
@@ -120,20 +119,21 @@ def test_random_configurations(seed):
     assert bool((Y.view(torch.int16)[M:] == CANARY).all())
 
 
-def test_four_million_rows_sampled():
+def test_four_million_rows():
+    # 4 194 304 routed rows over 16 experts, every output checked: the oracle runs expert by
+    # expert (each expert's product is independent) so that its fp64 result stays ~0.5 GB
     rng = np.random.default_rng(77)
     counts = rng.multinomial(1 << 22, np.full(16, 1.0 / 16))
     inp = wl.make_custom(counts, K=64, N=256, seed=152)
     X, W = inp.X.cuda(), inp.W.cuda()
     Y = rgg.rgg_grouped_gemm(X, W, torch.from_numpy(inp.offsets).cuda(), check=True, host_counts=counts)
     torch.cuda.synchronize()
-    assert bool(torch.isfinite(Y).all())
-    rows = np.concatenate([inp.offsets[1:-1] - 1, inp.offsets[1:-1], rng.integers(0, 1 << 22, 4000),
-                           [0, (1 << 22) - 1]]).astype(np.int64)
-    cols = rng.integers(0, 256, rows.size).astype(np.int64)
-    ref = oracle.grouped_gemm_points(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets, rows, cols)
-    got = Y[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
-    _close(got, ref)
+    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
+    off = inp.offsets
+    for e in range(counts.size):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        ref = oracle.grouped_gemm(np.ascontiguousarray(xb[r0:r1]), np.ascontiguousarray(wb[e:e + 1]), [0, r1 - r0])
+        _close(Y[r0:r1].double().cpu().numpy(), ref)
 
 
 @pytest.mark.parametrize("opts", [dict(bm=64, bn=256), dict(bm=128, bn=256), dict(bm=256, bn=256),

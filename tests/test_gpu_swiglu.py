@@ -6,7 +6,6 @@ elementwise, rows of no expert untouched.  At full size the oracle value of a
 sampled output is silu(g) * u with g and u from the oracle's pinned grouped
 GEMM at the gate column j and the up column N + j.
 """
-import zlib
 
 import numpy as np
 import pytest
@@ -87,22 +86,18 @@ def test_bad_offsets_rejected():
     assert bool((H.view(torch.int16) == CANARY).all())
 
 
-@pytest.mark.parametrize("name", ["decode", "uniform", "prefill"])
-def test_full_size_sampled(name):
-    # the workload's weights read as W13 = [gate | up] with N/2 output columns
+@pytest.mark.parametrize("name", ["decode", "uniform", "skew16k", "prefill"])
+def test_full_size(name):
+    # the workload's weights read as W13 = [gate | up] with N/2 output columns; every routed
+    # output against the whole fp64 oracle product, in the benchmark's launch configuration
     inp = wl.make_inputs(name)
     X, W13 = inp.X.cuda(), inp.W.cuda()
     off = torch.from_numpy(inp.offsets).cuda()
     H = rgg.rgg_grouped_gemm_swiglu(X, W13, off, check=True, host_counts=inp.counts)
     torch.cuda.synchronize()
-    assert bool(torch.isfinite(H).all())
-    N = W13.shape[2] // 2
-    rng = np.random.default_rng(zlib.crc32(name.encode()) + 7)
-    rows = rng.integers(0, int(inp.offsets[-1]), 1500)
-    cols = rng.integers(0, N, 1500)
-    xb, wb = wl.bf16_bits(inp.X), wl.bf16_bits(inp.W)
-    g = oracle.grouped_gemm_points(xb, wb, inp.offsets, rows, cols)
-    u = oracle.grouped_gemm_points(xb, wb, inp.offsets, rows, cols + N)
-    ref = np.array([oracle.silu(a) for a in g]) * u
-    got = H[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
-    assert (np.abs(got - ref) <= RTOL * np.maximum(1.0, np.abs(ref))).all()
+    ref = oracle.grouped_swiglu(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
+    lo, hi = int(inp.offsets[0]), int(inp.offsets[-1])
+    got = H[lo:hi].double().cpu().numpy()
+    err = np.abs(got - ref[lo:hi])
+    bad = ~(err <= RTOL * np.maximum(1.0, np.abs(ref[lo:hi])))
+    assert not bad.any(), "%s: %d outputs out of tolerance, max err %.4g" % (name, int(bad.sum()), err.max())
