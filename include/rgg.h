@@ -100,6 +100,19 @@ typedef struct rgg_options {
                                     and gather_mode = 2 (or bm = 256, which only the two-pass mode can
                                     run) is RGG_ERR_INVALID_ARG. */
     int64_t workspace_bytes;     /* size of `workspace` in bytes */
+    int mixed;                   /* rgg_grouped_gemm only: the mixed launch.  1 = on: experts of at least
+                                    pair_min_rows rows run 256 x 256 tiles on CTA pairs (tcgen05
+                                    cta_group::2; an expert's last tile of <= 128 rows as a 128-row pair
+                                    MMA) and the other experts 128 x 256 tiles on single CTAs (<= 64-row
+                                    tails as 64-row MMAs), as two kernels on disjoint SMs that claim tiles
+                                    from two device counters and take each other's tiles when their own
+                                    class runs out.  The classes are formed on the device from the offsets.
+                                    0 = auto (the planner's choice), -1 = off.  On: bm and bn must be 0 or
+                                    256, tail64 must not be -1, walk_order is not used. */
+    int mixed_pair_sms;          /* mixed launch: SMs given to the pair kernel (even; the 1-CTA kernel gets
+                                    the rest).  0 = split by the estimated work of each class (from
+                                    host_counts, else balanced experts), -1 = no pair kernel. */
+    int pair_min_rows;           /* mixed launch: smallest expert (rows) that runs on CTA pairs; 0 = 256 */
 } rgg_options;
 
 #define RGG_DEBUG_PRODUCER_STALL 1
@@ -120,6 +133,12 @@ typedef struct rgg_plan_info {
     int64_t workspace_bytes;     /* gather ops: the workspace the two-pass mode needs when it is asked
                                     for, or when the automatic choice prefers it (it runs only with a
                                     caller workspace); else 0 */
+    int mixed;                   /* 1 for the mixed launch: then bm, bn, stages, grid, smem_bytes describe
+                                    its pair kernel (grid 0: none) and the next three its 1-CTA kernel */
+    int single_grid;             /* mixed launch: CTAs of the 1-CTA kernel (0: none) */
+    int single_stages;           /* mixed launch: ring depth of the 1-CTA kernel */
+    int single_smem_bytes;       /* mixed launch: dynamic shared memory per CTA of the 1-CTA kernel */
+    int pair_min_rows;           /* mixed launch: smallest expert on CTA pairs */
 } rgg_plan_info;
 
 /*

@@ -57,14 +57,17 @@ class _Options(ctypes.Structure):
                 ("max_ctas", ctypes.c_int), ("timeout_ns", ctypes.c_uint64), ("host_counts", ctypes.c_void_p),
                 ("debug_flags", ctypes.c_int), ("tail64", ctypes.c_int),
                 ("op", ctypes.c_int), ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64), ("mixed", ctypes.c_int),
+                ("mixed_pair_sms", ctypes.c_int), ("pair_min_rows", ctypes.c_int)]
 
 
 class _PlanInfo(ctypes.Structure):
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int), ("stages", ctypes.c_int),
                 ("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("tmem_cols", ctypes.c_int), ("max_tiles", ctypes.c_int64), ("tail64", ctypes.c_int),
-                ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int), ("workspace_bytes", ctypes.c_int64)]
+                ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int), ("workspace_bytes", ctypes.c_int64),
+                ("mixed", ctypes.c_int), ("single_grid", ctypes.c_int), ("single_stages", ctypes.c_int),
+                ("single_smem_bytes", ctypes.c_int), ("pair_min_rows", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -144,9 +147,12 @@ def _handle(device: int) -> ctypes.c_void_p:
 
 
 def _options(bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0, host_counts=None, debug_flags=0, tail64=0,
-             op=0, walk_order=0, gather_mode=0):
+             op=0, walk_order=0, gather_mode=0, mixed=0, mixed_pair_sms=0, pair_min_rows=0):
     opt = _Options(int(bm), int(bn), int(stages), int(max_ctas), int(timeout_ns), None, int(debug_flags),
                    int(tail64), int(op), int(walk_order), int(gather_mode))
+    opt.mixed = int(mixed)
+    opt.mixed_pair_sms = int(mixed_pair_sms)
+    opt.pair_min_rows = int(pair_min_rows)
     keep = None
     if host_counts is not None:
         import numpy as np
@@ -171,8 +177,11 @@ def _stream_ptr(stream, device):
 
 
 def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
-                     host_counts=None, debug_flags=0, tail64=0, walk_order=0, stream=None, check=False):
-    """Y_e = X_e . W_e for every expert (one kernel launch, asynchronous).
+                     host_counts=None, debug_flags=0, tail64=0, walk_order=0, mixed=0, mixed_pair_sms=0,
+                     pair_min_rows=0, stream=None, check=False):
+    """Y_e = X_e . W_e for every expert (one kernel launch, asynchronous; the
+    mixed launch, ``mixed=1``, runs a CTA-pair kernel and a 1-CTA kernel side
+    by side).
 
     X: bf16 CUDA [M_tot, K]; W: bf16 CUDA [E, K, N]; group_offsets: int32
     CUDA [E+1]; Y: optional bf16 CUDA [M_tot, N] (allocated uninitialised when
@@ -200,7 +209,8 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
     elif Y.shape != (M_tot, N) or Y.dtype != torch.bfloat16 or not Y.is_contiguous() or not Y.is_cuda:
         raise ValueError("Y must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order)
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order,
+                         mixed=mixed, mixed_pair_sms=mixed_pair_sms, pair_min_rows=pair_min_rows)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm(_handle(device), X.data_ptr(), W.data_ptr(), group_offsets.data_ptr(), Y.data_ptr(),
                              E, M_tot, K, N, st, ctypes.byref(opt))
@@ -433,7 +443,7 @@ def rgg_query_status(device: int | None = None, stream=None) -> int:
 
 def rgg_plan(E: int, M_tot: int, K: int, N: int, *, num_sms: int = 0, smem_optin: int = 0, bm=0, bn=0,
              stages=0, max_ctas=0, host_counts=None, tail64=0, op: str = "gemm",
-             walk_order=0, gather_mode=0, workspace=None) -> dict:
+             walk_order=0, gather_mode=0, workspace=None, mixed=0, mixed_pair_sms=0, pair_min_rows=0) -> dict:
     """The launch configuration rgg_grouped_gemm (op="gemm") or
     rgg_grouped_gemm_swiglu (op="swiglu", N = output width) would use (host-only).
     For the gather ops, ``workspace`` (the tensor the call would get, True
@@ -442,7 +452,7 @@ def rgg_plan(E: int, M_tot: int, K: int, N: int, *, num_sms: int = 0, smem_optin
     lib = load_library()
     opt, keep = _options(bm, bn, stages, max_ctas, 0, host_counts, 0, tail64,
                          {"gemm": 0, "swiglu": 1, "fp8": 2, "gather": 3, "swiglu_gather": 4}[op], walk_order,
-                         gather_mode)
+                         gather_mode, mixed=mixed, mixed_pair_sms=mixed_pair_sms, pair_min_rows=pair_min_rows)
     if workspace is True:
         opt.workspace = 16  # never dereferenced: rgg_plan reads only whether a workspace is given
         opt.workspace_bytes = 1 << 62

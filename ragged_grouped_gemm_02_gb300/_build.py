@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "librgg.so")
 
 SOURCES = ["rgg_api.cu", "rgg_aux.cu", "rgg_gemm_bm128.cu", "rgg_gemm_bm64.cu", "rgg_gemm_pair.cu",
-           "rgg_noalloc.cu", "rgg_gemm_swiglu.cu", "rgg_gemm_fp8.cu", "rgg_gemm_gather.cu"]
+           "rgg_noalloc.cu", "rgg_gemm_swiglu.cu", "rgg_gemm_fp8.cu", "rgg_gemm_gather.cu",
+           "rgg_gemm_mixed.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -83,7 +83,14 @@ struct Plan {
     int64_t max_tiles;
     int tail64;       // 1: tail tiles of <= 64 rows run as 64-row MMAs (128-row tiles only)
     int walk_order;   // 0 list order, 1 front/back interleave, 2 strided scatter, 3 size-sorted, 4 N-major
+    // the mixed launch: `grid` / `stages` / `smem_bytes` are the pair kernel's
+    // (grid 0: no pair kernel), these the 1-CTA kernel's (grid 0: none)
+    int mixed = 0;
+    int single_grid = 0, single_stages = 0, single_smem = 0;
+    int pair_min_rows = 0;
 };
+
+
 
 // Upper bound on the flat tile count: sum_e ceil(m_e/BM) <= floor(M_tot/BM) + E.
 int64_t tile_bound(int E, int64_t M_tot, int N, int bm, int bn) {
@@ -94,6 +101,105 @@ rgg_status check_sizes(int E, int64_t M_tot, int K, int N) {
     if (E < 1 || E > rgg::kMaxExperts) return E < 1 ? RGG_ERR_INVALID_ARG : RGG_ERR_UNSUPPORTED;
     if (M_tot < 0 || M_tot >= (int64_t(1) << 31)) return RGG_ERR_INVALID_ARG;
     if (K < 8 || N < 8 || (K % 8) != 0 || (N % 8) != 0) return RGG_ERR_INVALID_ARG;
+    return RGG_OK;
+}
+
+// Stages that fit beside a shared-memory carve-up whose fixed part is
+// `fixed` bytes, for stages of `per_stage` bytes (tiles + two barriers).
+int stages_that_fit(int smem_optin, uint32_t fixed, int64_t per_stage) {
+    const int64_t room = static_cast<int64_t>(smem_optin) - 1024 - fixed - 64;
+    return static_cast<int>(std::min<int64_t>(rgg::kMaxStages, room / per_stage));
+}
+
+// The mixed launch (csrc/rgg_sched.cuh): experts of at least pair_min_rows
+// rows on CTA pairs in 256 x 256 tiles, the rest on single CTAs in 128 x 256
+// tiles, two kernels on disjoint SMs.  The split of the SMs follows the
+// estimated work of each class in SM-time, taken as the bytes each SM pulls
+// into shared memory per tile (the quantity that set the pace of both tile
+// shapes on a GB300): (128 + cols/2) per CTA of a pair tile (64 + cols/2 for
+// a tile of <= 128 rows), 128 + cols per 1-CTA tile (64 + cols for <= 64
+// rows).  The kernels steal each other's tiles when their own class runs out,
+// so an inexact split costs only the less efficient shape on the stolen
+// tiles.  Without host counts the experts are taken as balanced.
+rgg_status plan_mixed(int grid_cap, int smem_optin, int E, int64_t M_tot, int N, const rgg_options* opt, Plan* out) {
+    const int want_bm = opt ? opt->bm : 0;
+    const int want_bn = opt ? opt->bn : 0;
+    const int want_tail = opt ? opt->tail64 : 0;
+    const int want_stages = opt ? opt->stages : 0;
+    const int want_psms = opt ? opt->mixed_pair_sms : 0;
+    const int pmin = (opt && opt->pair_min_rows > 0) ? opt->pair_min_rows : rgg::kPairMinRowsDefault;
+    if ((want_bm != 0 && want_bm != 256) || (want_bn != 0 && want_bn != 256) || want_tail == -1)
+        return RGG_ERR_INVALID_ARG;
+    if (want_psms < -1 || want_psms > grid_cap || (want_psms > 0 && want_psms % 2 != 0)) return RGG_ERR_INVALID_ARG;
+    if (tile_bound(E, M_tot, N, 128, rgg::kMixedBN) >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
+    int pair_sms = 0;
+    if (want_psms == -1) {
+        pair_sms = 0;
+    } else if (want_psms > 0) {
+        pair_sms = want_psms;
+    } else {
+        double cost_p = 0.0, cost_s = 0.0;
+        auto add_expert = [&](int64_t m, double weight) {
+            for (int64_t c0 = 0; c0 < N; c0 += rgg::kMixedBN) {
+                const int64_t cols = std::min<int64_t>(rgg::kMixedBN, N - c0);
+                if (m >= pmin) {
+                    const double pc = static_cast<double>(ceil_div(cols, 128) * 128);
+                    const int64_t rem = m % 256;
+                    cost_p += weight * ((m / 256) * 2.0 * (128 + pc / 2) +
+                                        (rem > 128 ? 2.0 * (128 + pc / 2) : rem > 0 ? 2.0 * (64 + pc / 2) : 0.0));
+                } else {
+                    const double sc = static_cast<double>(ceil_div(cols, 64) * 64);
+                    const int64_t rem = m % 128;
+                    cost_s += weight *
+                              ((m / 128) * (128 + sc) + (rem > 64 ? 128 + sc : rem > 0 ? 64 + sc : 0.0));
+                }
+            }
+        };
+        if (opt && opt->host_counts) {
+            for (int e = 0; e < E; ++e) add_expert(std::max<int64_t>(0, opt->host_counts[e]), 1.0);
+        } else {
+            add_expert(M_tot / E, static_cast<double>(E));
+        }
+        if (cost_p <= 0.0) {
+            pair_sms = 0;
+        } else if (cost_s <= 0.0) {
+            pair_sms = grid_cap & ~1;
+        } else {
+            pair_sms = static_cast<int>(grid_cap * cost_p / (cost_p + cost_s) + 1.0) & ~1;
+            pair_sms = std::max(2, std::min(pair_sms, (grid_cap - 1) & ~1));
+        }
+    }
+    pair_sms = std::min(pair_sms, grid_cap & ~1);
+    const int single = grid_cap - pair_sms;
+    if (pair_sms == 0 && single == 0) return RGG_ERR_INVALID_ARG;
+
+    // shared memory: each kernel keeps the offsets, both class prefixes and the tile queue
+    const rgg::SmemPlan pp = rgg::smem_plan(128, 128, 0, E, false, true);
+    const rgg::SmemPlan ps = rgg::smem_plan(128, rgg::kMixedBN, 0, E, false, true);
+    const int fit_p = stages_that_fit(smem_optin, pp.total, (128 + 128) * 128 + 16);
+    const int fit_s = stages_that_fit(smem_optin, ps.total, (128 + rgg::kMixedBN) * 128 + 16);
+    const int st_p = want_stages ? want_stages : fit_p;
+    const int st_s = want_stages ? want_stages : fit_s;
+    if (st_p < 2 || st_p > fit_p || st_s < 2 || st_s > fit_s) return RGG_ERR_UNSUPPORTED;
+    const int smem_p = std::max<int>(static_cast<int>(rgg::smem_plan(128, 128, st_p, E, false, true).total) + 1024,
+                                     smem_optin / 2 + 1024);
+    const int smem_s = std::max<int>(
+        static_cast<int>(rgg::smem_plan(128, rgg::kMixedBN, st_s, E, false, true).total) + 1024,
+        smem_optin / 2 + 1024);
+    if (smem_p > smem_optin || smem_s > smem_optin) return RGG_ERR_UNSUPPORTED;
+    out->bm = 256;
+    out->bn = rgg::kMixedBN;
+    out->stages = st_p;
+    out->grid = pair_sms;
+    out->smem_bytes = smem_p;
+    out->max_tiles = tile_bound(E, M_tot, N, 128, rgg::kMixedBN);
+    out->tail64 = 1;
+    out->walk_order = 0;
+    out->mixed = 1;
+    out->single_grid = single;
+    out->single_stages = st_s;
+    out->single_smem = smem_s;
+    out->pair_min_rows = pmin;
     return RGG_OK;
 }
 
@@ -132,6 +238,12 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (want_walk < -1 || want_walk > 4) return RGG_ERR_INVALID_ARG;  // -1: list order, never replaced
     if (want_walk == 3 && E > rgg::kMaxSortedExperts) return RGG_ERR_UNSUPPORTED;
     int grid_cap = max_ctas > 0 ? std::min(max_ctas, num_sms) : num_sms;
+    const int want_mixed = opt ? opt->mixed : 0;
+    if (want_mixed < -1 || want_mixed > 1 || (opt && opt->pair_min_rows < 0)) return RGG_ERR_INVALID_ARG;
+    if (want_mixed == 1) {
+        if (kind != 0) return RGG_ERR_UNSUPPORTED;  // the plain bf16 GEMM only
+        return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out);
+    }
 
     // Per-expert M tiles at each BM: exact with host counts, else the
     // balanced estimate E * ceil(avg / BM).
@@ -467,6 +579,17 @@ rgg_status host_grouped_gemm(int num_sms, int smem_optin, int32_t* status, const
     a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
     a.tail64 = p.tail64;
     a.walk_order = p.walk_order;
+    if (p.mixed) {
+        // two claim counters after the status word (the device word's first 64 bytes), zeroed per call
+        a.sched = status + 16;
+        a.pair_min_rows = p.pair_min_rows;
+        cudaError_t err = cudaMemsetAsync(a.sched, 0, 2 * sizeof(int32_t), st);
+        if (err != cudaSuccess) return cuda_failure(err, "cudaMemsetAsync(tile counters)");
+        GemmArgs as = a;
+        as.stages = p.single_stages;
+        err = launch_gemm_mixed(p.grid, p.smem_bytes, a, p.single_grid, p.single_smem, as, st, tx, tx64, tw);
+        return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm (mixed) launch");
+    }
     cudaError_t err = (p.bm == 256)   ? launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
                       : (p.bm == 128) ? launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
                                       : launch_gemm_bm64(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
@@ -578,6 +701,12 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     if (swiglu && p.bm == 256) out->tail64 = 0;  // fused gate-up pairs keep 256-row tail tiles
     out->gather_mode = mode;
     out->workspace_bytes = prefers_two_pass ? gather_workspace_bytes(M_tot, K) : 0;
+    out->mixed = p.mixed;
+    out->single_grid = p.single_grid;
+    out->single_stages = p.single_stages;
+    out->single_smem_bytes = p.single_smem;
+    out->pair_min_rows = p.pair_min_rows;
+    if (p.mixed) out->tmem_cols = 512;
     return RGG_OK;
 }
 

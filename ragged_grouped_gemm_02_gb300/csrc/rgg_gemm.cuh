@@ -42,6 +42,7 @@
 #include <cstdint>
 
 #include "rgg_ptx.cuh"
+#include "rgg_sched.cuh"
 #include "rgg_tiles.cuh"
 
 namespace rgg {
@@ -74,18 +75,27 @@ struct GemmArgs {
     const float* sw = nullptr;  // FP8 kernels: fp32 scale of each (expert, column) of W [E, N]
     const int32_t* row_index = nullptr;  // gather kernels: token row of each routed row [M_tot]
     int32_t t_rows = 0;                  // gather kernels: rows of the token matrix
+    // Mixed launch (rgg_sched.cuh): tiles claimed from two device counters
+    // sched[0] (class P) and sched[1] (class S), zeroed before the launch.
+    int32_t* sched = nullptr;
+    int32_t pair_min_rows = kPairMinRowsDefault;
 };
 
 // Shared-memory carve-up shared by the host planner and the kernel.  Offsets
 // are from a 1024-byte aligned base; the host adds 1024 bytes of slack for
 // aligning the dynamic shared-memory window.
 struct SmemPlan {
-    uint32_t a_stage, b_stage, a_off, b_off, bar_off, misc_off, off_off, pre_off, ord_off, spre_off, total;
+    uint32_t a_stage, b_stage, a_off, b_off, bar_off, misc_off, off_off, pre_off, ord_off, spre_off, q_off,
+        qbar_off, total;
 };
 
-// `sorted`: room for the size-sorted walk (expert order and its tile prefix).
-__host__ __device__ inline SmemPlan smem_plan(int BM, int BN, int stages, int E, bool sorted = false) {
+// `sorted`: room for the size-sorted walk (expert order and its tile
+// prefix).  `mixed`: room for the second class prefix (at ord_off) and the
+// tile queue (kQueueDepth 16-byte descriptors, then q_full[Q], q_empty[Q]).
+__host__ __device__ inline SmemPlan smem_plan(int BM, int BN, int stages, int E, bool sorted = false,
+                                              bool mixed = false) {
     SmemPlan p;
+    const uint32_t ex = 4u * static_cast<uint32_t>(E + 1);
     p.a_stage = static_cast<uint32_t>(BM) * 128u;
     p.b_stage = static_cast<uint32_t>(BN) * 128u;
     p.a_off = 0;
@@ -93,10 +103,12 @@ __host__ __device__ inline SmemPlan smem_plan(int BM, int BN, int stages, int E,
     p.bar_off = p.b_off + stages * p.b_stage;          // full[S], empty[S], acc_full[2], acc_empty[2], drain
     p.misc_off = p.bar_off + 8u * (2u * stages + 5u);   // tmem base, abort flag (16 B reserved)
     p.off_off = p.misc_off + 16u;
-    p.pre_off = p.off_off + 4u * static_cast<uint32_t>(E + 1);
-    p.ord_off = p.pre_off + 4u * static_cast<uint32_t>(E + 1);
-    p.spre_off = p.ord_off + (sorted ? 4u * static_cast<uint32_t>(E + 1) : 0u);
-    p.total = p.spre_off + (sorted ? 4u * static_cast<uint32_t>(E + 1) : 0u);
+    p.pre_off = p.off_off + ex;
+    p.ord_off = p.pre_off + ex;
+    p.spre_off = p.ord_off + ((sorted || mixed) ? ex : 0u);
+    p.q_off = (p.spre_off + (sorted ? ex : 0u) + 15u) & ~15u;
+    p.qbar_off = p.q_off + (mixed ? 16u * kQueueDepth : 0u);
+    p.total = p.qbar_off + (mixed ? 16u * kQueueDepth : 0u);
     return p;
 }
 
@@ -128,12 +140,16 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
 // Kernels on clusters of two CTAs: as wait_or_abort, and a timeout also raises
 // the other CTA's abort flag (its shared::cluster address), so both leave
 // their loops instead of waiting on arrivals that will not come.
+// kClusterAcquire: the barrier is arrived on by the other CTA after it wrote
+// (or read) this CTA's shared memory, so the wait acquires at cluster scope.
+template <bool kClusterAcquire = false>
 __device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                    uint32_t peer_flag_cluster, int32_t* status, uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto probe = [&]() { return kClusterAcquire ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (probe()) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (probe()) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > timeout_ns) {
             *abort_flag = 1u;
@@ -163,11 +179,12 @@ struct TileConfig {
     static constexpr uint32_t kPanelB = static_cast<uint32_t>(kKStage) * 128u;  // bytes per W panel
     static constexpr uint32_t kBStep = kFp8 ? 4096u : 2048u;  // B start advance per MMA (32 or 16 K rows)
     static constexpr uint32_t kTmemCols = (2 * BN <= 256) ? 256u : 512u;  // two accumulator buffers
-    static constexpr uint32_t kStageTx = static_cast<uint32_t>((BM + BN) * 128);
-    static constexpr uint32_t kStageTx64 = static_cast<uint32_t>((64 + BN) * 128);  // 64-row tail tile
-    static constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(BM, BN, true) : idesc_bf16_f32(BM, BN, true);
-    static constexpr uint32_t kIdesc64 = kFp8 ? idesc_e4m3_f32(64, BN, true) : idesc_bf16_f32(64, BN, true);
+    // Instruction descriptor for an M x n MMA (n = the panels a tile loads x kPanelN).
+    __host__ __device__ static constexpr uint32_t idesc(int m, int n) {
+        return kFp8 ? idesc_e4m3_f32(m, n, true) : idesc_bf16_f32(m, n, true);
+    }
 };
+
 
 constexpr int kMmasPerStage = 4;  // K = 16 (bf16) or 32 (FP8) per instruction
 
@@ -186,6 +203,19 @@ __device__ __forceinline__ bool runs_as_64_rows(const GemmArgs& args, const Tile
 // epilogue writes silu(gate) * up.
 constexpr int kEpiPlain = 0;
 constexpr int kEpiSwiGLU = 1;
+
+// Weight panels a tile loads and multiplies.  A plain tile whose columns run
+// past N (the last N tile of an expert) loads only the panels that hold
+// columns below N and issues an MMA of that width, so neither the copies nor
+// the MMAs of the columns past N are paid for (on N = 2688 with 256-column
+// tiles every expert's eleventh N tile is half empty).  The fused gate-up
+// tile keeps its gate | up panel layout and loads them all.
+template <int kPanels, int kPanelN, int kEpi>
+__device__ __forceinline__ int tile_panels(int32_t col0, int32_t N) {
+    if (kEpi != kEpiPlain) return kPanels;
+    const int32_t need = (N - col0 + kPanelN - 1) / kPanelN;
+    return need < kPanels ? static_cast<int>(need) : kPanels;
+}
 
 // Epilogue warps of the 1-CTA kernel.  Four (one per TMEM lane quadrant)
 // keep pace with the main loop for plain bf16 outputs.  The FP8 epilogue also
@@ -224,6 +254,7 @@ __device__ __forceinline__ void epilogue_store_tile(const GemmArgs& args, const 
     __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0;
 #pragma unroll 1
     for (int cc = cc0; cc < cc0 + kPartCols; cc += 32) {
+        if (c.col0 + cc >= N) break;  // columns past N: not computed (tile_panels), not stored
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
         if (kEpi == kEpiSwiGLU) {
@@ -293,11 +324,18 @@ __device__ __forceinline__ void epilogue_store_tile(const GemmArgs& args, const 
 constexpr int kGatherNone = 0;
 constexpr int kGatherTma = 1;
 
-template <int BM, int BN, int kEpi = kEpiPlain, bool kFp8 = false, int kGather = kGatherNone>
+// kDyn: the 1-CTA kernel of the mixed launch (rgg_sched.cuh).  Its producer
+// claims tiles from the device counters and hands each tile's descriptor to
+// the MMA thread and the epilogue warps through a small shared-memory queue
+// (q_full / q_empty barriers per slot); a descriptor with expert -1 ends the
+// walk.  Otherwise each role decodes the static walk t = cta, cta + grid, ...
+template <int BM, int BN, int kEpi = kEpiPlain, bool kFp8 = false, int kGather = kGatherNone, bool kDyn = false>
 __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
                         const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
     using Cfg = TileConfig<BM, BN, kFp8>;
+    static_assert(!kDyn || (BM == 128 && BN == kMixedBN && kEpi == kEpiPlain && !kFp8 && kGather == kGatherNone),
+                  "the mixed launch's 1-CTA kernel runs plain bf16 128 x 256 tiles");
     static_assert(kEpi == kEpiPlain || (BN % 128) == 0, "fused gate-up tiles hold whole gate and up panels");
     static_assert(!(kFp8 && kEpi == kEpiSwiGLU), "the fused gate-up epilogue is bf16 only");
     static_assert(!(kFp8 && kGather != kGatherNone), "the token gather is bf16 only");
@@ -320,7 +358,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const SmemPlan sp = smem_plan(BM, BN, S, E, args.walk_order == 3);
+    const SmemPlan sp = smem_plan(BM, BN, S, E, !kDyn && args.walk_order == 3, kDyn);
     const uint32_t a0 = base + sp.a_off;
     const uint32_t b0 = base + sp.b_off;
     const uint32_t bars = base + sp.bar_off;
@@ -332,19 +370,38 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + sp.misc_off);
     int32_t* s_off = reinterpret_cast<int32_t*>(gbase + sp.off_off);
     int32_t* s_pre = reinterpret_cast<int32_t*>(gbase + sp.pre_off);
-    int32_t* s_order = reinterpret_cast<int32_t*>(gbase + sp.ord_off);  // walk order 3 only
+    int32_t* s_order = reinterpret_cast<int32_t*>(gbase + sp.ord_off);  // walk order 3; mixed: class S prefix
     int32_t* s_spre = reinterpret_cast<int32_t*>(gbase + sp.spre_off);
+    int32_t* q_desc = reinterpret_cast<int32_t*>(gbase + sp.q_off);     // mixed: tile queue
+    auto qfull_bar = [&](int i) { return base + sp.qbar_off + 8u * i; };
+    auto qempty_bar = [&](int i) { return base + sp.qbar_off + 8u * (kQueueDepth + i); };
 
     // S1: group offsets -> validated per-expert tile prefix.
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
         if (threadIdx.x == 0) atomicCAS(args.status, 0, kStatusBadOffsets);
+        if constexpr (kDyn) pdl_wait_prerequisites();
         return;
     }
-    if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
-    __syncthreads();
-    const int32_t T = s_pre[E];
-    if (args.walk_order == 3) build_size_order(s_off, s_order, s_spre, E, BM, args.n_tiles_n);
-    if (static_cast<int32_t>(blockIdx.x) >= T) return;  // uniform over the CTA
+    ClassLists L;
+    int32_t T;
+    if constexpr (kDyn) {
+        // both class lists (class P in s_pre, class S in s_order)
+        if (warp == 0) build_class_prefix_warp(s_off, s_pre, E, 256, args.n_tiles_n, args.pair_min_rows, 0x7fffffff);
+        if (warp == 1) build_class_prefix_warp(s_off, s_order, E, 128, args.n_tiles_n, 0, args.pair_min_rows);
+        __syncthreads();
+        L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E]};
+        T = L.nP + L.nS;
+        if (T == 0) {
+            pdl_wait_prerequisites();
+            return;
+        }
+    } else {
+        if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
+        __syncthreads();
+        T = s_pre[E];
+        if (args.walk_order == 3) build_size_order(s_off, s_order, s_spre, E, BM, args.n_tiles_n);
+        if (static_cast<int32_t>(blockIdx.x) >= T) return;  // uniform over the CTA
+    }
 
     if (threadIdx.x == 32) {
         for (int s = 0; s < S; ++s) {
@@ -356,6 +413,12 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             mbar_init(acce_bar(a), epilogue_warps<kEpi, kFp8>());
         }
         mbar_init(drain_bar, 1);
+        if constexpr (kDyn) {
+            for (int i = 0; i < kQueueDepth; ++i) {
+                mbar_init(qfull_bar(i), 1);
+                mbar_init(qempty_bar(i), 1 + epilogue_warps<kEpi, kFp8>());
+            }
+        }
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -381,6 +444,30 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     // The tile visited at walk position p.
     auto tile_at = [&](int32_t p) -> TileCoord {
         return walk_decode(s_off, s_pre, s_order, s_spre, E, BM, kOutN, nN, T, WO, WS, p);
+    };
+    // Mixed launch: a consumer takes the next descriptor from the queue
+    // (`warp_wide`: all lanes of an epilogue warp wait, lane 0 releases the
+    // slot for the warp).  False on an abort; expert -1 ends the walk.
+    auto q_pop = [&](int& qs, uint32_t& qp, TileCoord& c, bool warp_wide) -> bool {
+        bool ok = wait_or_abort(qfull_bar(qs), qp, abort_flag, args.status, args.timeout_ns);
+        if (warp_wide) ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        const volatile int32_t* d = q_desc + 4 * qs;
+        c.expert = d[0];
+        c.row0 = d[1];
+        c.rows = d[2];
+        c.col0 = d[3];
+        if (warp_wide) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qs));
+        } else {
+            mbar_arrive(qempty_bar(qs));
+        }
+        if (++qs == kQueueDepth) {
+            qs = 0;
+            qp ^= 1u;
+        }
+        return true;
     };
 
     if (kGather == kGatherTma && warp == 0) {
@@ -422,7 +509,8 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
                 const int groups = (c.rows + 3) >> 2;
                 if (bad && 4 * lane < c.rows) atomicCAS(args.status, 0, kStatusBadRowIndex);
                 if (t + static_cast<int32_t>(gridDim.x) < T) fetch(t + gridDim.x);
-                const uint32_t tx_bytes = static_cast<uint32_t>(groups) * 512u + static_cast<uint32_t>(BN) * 128u;
+                const int np = tile_panels<kPanels, Cfg::kPanelN, kEpi>(c.col0, args.N);
+                const uint32_t tx_bytes = static_cast<uint32_t>(groups) * 512u + np * Cfg::kPanelB;
                 for (int kb = 0; kb < KB; ++kb) {
                     int got = 1;
                     if (lane == 0) got = wait_or_abort(empty_bar(st), ph ^ 1u, abort_flag, args.status, args.timeout_ns);
@@ -438,8 +526,9 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
                     if (lane == 0) {
 #pragma unroll
                         for (int p = 0; p < kPanels; ++p)
-                            tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st),
-                                        w_col(c.col0, p), kb * Cfg::kKStage, c.expert);
+                            if (p < np)
+                                tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st),
+                                            w_col(c.col0, p), kb * Cfg::kKStage, c.expert);
                     }
                     ++issued;
                     if (++st == S) {
@@ -463,10 +552,10 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = true;
-            for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
-                const TileCoord c = tile_at(t);
+            auto produce = [&](const TileCoord& c) {
                 const bool half = runs_as_64_rows<BM>(args, c);
-                const uint32_t tx_bytes = half ? Cfg::kStageTx64 : Cfg::kStageTx;
+                const int np = tile_panels<kPanels, Cfg::kPanelN, kEpi>(c.col0, args.N);
+                const uint32_t tx_bytes = (half ? 64u : static_cast<uint32_t>(BM)) * 128u + np * Cfg::kPanelB;
                 const CUtensorMap* xmap = (BM == 128 && half) ? &tmap_x64 : &tmap_x;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_or_abort(empty_bar(st), ph ^ 1u, abort_flag, args.status, args.timeout_ns)) {
@@ -477,14 +566,45 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
                     tma_load_2d(a0 + st * sp.a_stage, xmap, full_bar(st), kb * Cfg::kKStage, c.row0);
 #pragma unroll
                     for (int p = 0; p < kPanels; ++p)
-                        tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st),
-                                    w_col(c.col0, p), kb * Cfg::kKStage, c.expert);
+                        if (p < np)
+                            tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st),
+                                        w_col(c.col0, p), kb * Cfg::kKStage, c.expert);
                     ++issued;
                     if (++st == S) {
                         st = 0;
                         ph ^= 1u;
                     }
                 }
+            };
+            if constexpr (kDyn) {
+                // claim, hand the descriptor to the consumers, load the tile
+                TileClaimer cl;
+                cl.init(args.sched, L, false);
+                int qs = 0;
+                uint32_t qp = 0;
+                TileCoord c = cl.next(L);
+                while (ok) {
+                    if (!wait_or_abort(qempty_bar(qs), qp ^ 1u, abort_flag, args.status, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    int32_t* d = q_desc + 4 * qs;
+                    d[0] = c.expert;
+                    d[1] = c.row0;
+                    d[2] = c.rows;
+                    d[3] = c.col0;
+                    mbar_arrive(qfull_bar(qs));
+                    if (++qs == kQueueDepth) {
+                        qs = 0;
+                        qp ^= 1u;
+                    }
+                    if (c.expert < 0) break;
+                    cl.prefetch();
+                    produce(c);
+                    if (ok) c = cl.next(L);
+                }
+            } else {
+                for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) produce(tile_at(t));
             }
             if (!ok) {
                 // Let the copies already issued land before the CTA can exit.
@@ -502,19 +622,19 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             int acc = 0;
             uint32_t acc_ph = 0;
             bool ok = true;
-            for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) {
-                const TileCoord c = tile_at(t);
-                const uint32_t idesc = runs_as_64_rows<BM>(args, c) ? Cfg::kIdesc64 : Cfg::kIdesc;
+            auto mma_tile = [&](const TileCoord& c) {
+                const int np = tile_panels<kPanels, Cfg::kPanelN, kEpi>(c.col0, args.N);
+                const uint32_t idesc = Cfg::idesc(runs_as_64_rows<BM>(args, c) ? 64 : BM, np * Cfg::kPanelN);
                 if (!wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, args.status, args.timeout_ns)) {
                     ok = false;
-                    break;
+                    return;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_or_abort(full_bar(st), ph, abort_flag, args.status, args.timeout_ns)) {
                         ok = false;
-                        break;
+                        return;
                     }
                     tc_fence_after_sync();
                     const uint32_t a_st = a0 + st * sp.a_stage;
@@ -534,12 +654,26 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
                         ph ^= 1u;
                     }
                 }
-                if (!ok) break;
                 mma_commit(accf_bar(acc));      // accumulator buffer ready for the epilogue
                 if (++acc == 2) {
                     acc = 0;
                     acc_ph ^= 1u;
                 }
+            };
+            if constexpr (kDyn) {
+                int qs = 0;
+                uint32_t qp = 0;
+                TileCoord c;
+                while (ok) {
+                    if (!q_pop(qs, qp, c, false)) {
+                        ok = false;
+                        break;
+                    }
+                    if (c.expert < 0) break;
+                    mma_tile(c);
+                }
+            } else {
+                for (int32_t t = blockIdx.x; ok && t < T; t += gridDim.x) mma_tile(tile_at(t));
             }
             if (!ok) {
                 mma_commit(drain_bar);
@@ -556,15 +690,15 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
         const int cc0 = ((warp - 2) >> 2) * kPartCols;
         int acc = 0;
         uint32_t acc_ph = 0;
-        for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
-            const TileCoord c = tile_at(t);
+        // false when the CTA aborts
+        auto epi_tile = [&](const TileCoord& c) -> bool {
             // M = 128: tile row 32q + lane sits in TMEM lane 32q + lane.  M = 64:
             // tile row 16q + i sits in TMEM lane 32q + i (i < 16).
             const bool half = runs_as_64_rows<BM>(args, c);
             const int r_local = half ? (q * 16 + (lane & 15)) : (q * 32 + lane);
             bool ok = wait_or_abort(accf_bar(acc), acc_ph, abort_flag, args.status, args.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
+            if (!ok) return false;
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             epilogue_store_tile<BN, kEpi, kFp8>(args, c, half, r_local, t_row, lane, cc0, true);
@@ -575,6 +709,17 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
                 acc = 0;
                 acc_ph ^= 1u;
             }
+            return true;
+        };
+        if constexpr (kDyn) {
+            int qs = 0;
+            uint32_t qp = 0;
+            TileCoord c;
+            while (q_pop(qs, qp, c, true) && c.expert >= 0)
+                if (!epi_tile(c)) break;
+        } else {
+            for (int32_t t = blockIdx.x; t < T; t += gridDim.x)
+                if (!epi_tile(tile_at(t))) break;
         }
     }
 
@@ -584,6 +729,9 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, Cfg::kTmemCols);
     }
+    // The mixed launch's 1-CTA kernel may start before the pair kernel ends;
+    // it does not end before it, so the stream's later work sees both done.
+    if constexpr (kDyn) pdl_wait_prerequisites();
 }
 
 }  // namespace rgg

@@ -41,11 +41,18 @@ struct PairConfig {
     static constexpr uint32_t kPanelB = static_cast<uint32_t>(kKStage) * 128u;  // bytes per W panel
     static constexpr uint32_t kBStep = 2048u;       // B start advance per MMA (16 K rows)
     static constexpr uint32_t kTmemCols = 512;      // two BN-column fp32 buffers (BN <= 256)
-    static constexpr uint32_t kStageBytesPerCta = static_cast<uint32_t>((128 + kHalfN) * 128);
-    static constexpr uint32_t kStageBytesPerCta64 = static_cast<uint32_t>((64 + kHalfN) * 128);
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(256, BN, true);
-    static constexpr uint32_t kIdesc128 = idesc_bf16_f32(128, BN, true);  // 64 rows per CTA
 };
+
+// Columns a pair tile multiplies: BN, or for a plain tile whose columns run
+// past N (an expert's last N tile) the columns below N rounded up to 128, so
+// that each CTA still holds whole 64-column panels (N/2 of them per CTA).
+// The copies and MMAs of the columns past that are not issued.
+template <int BN, int kEpi>
+__device__ __forceinline__ int pair_tile_cols(int32_t col0, int32_t N) {
+    if (kEpi != kEpiPlain) return BN;
+    const int32_t need = (N - col0 + 127) / 128 * 128;
+    return need < BN ? static_cast<int>(need) : BN;
+}
 
 // A pair tile whose rows are the last <= 128 of its expert runs as an M = 128
 // pair MMA (args.tail64): each CTA loads and computes 64 rows, which halves
@@ -68,11 +75,21 @@ __host__ __device__ constexpr int pair_epilogue_warps() {
     return kEpi == kEpiSwiGLU ? 8 : 4;
 }
 
-template <int BN, int kEpi = kEpiPlain>
+// kDyn: the pair kernel of the mixed launch (rgg_sched.cuh).  The leader's
+// producer claims tiles from the device counters (class P first, then the
+// 1-CTA class as M = 128 pair tiles) and writes each descriptor into both
+// CTAs' tile queues; the leader's MMA thread, the peer's producer and both
+// CTAs' epilogue warps take it from their own CTA's queue and release the slot
+// on the leader's q_empty.  A descriptor with expert -1 ends the walk.
+template <int BN, int kEpi = kEpiPlain, bool kDyn = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilogue_warps<kEpi>(), 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
                              const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
     using Cfg = PairConfig<BN>;
+    static_assert(!kDyn || (BN == kMixedBN && kEpi == kEpiPlain), "the mixed launch's pairs run plain 256 x 256 tiles");
+    // The mixed launch's 1-CTA kernel, launched after this one, may start as
+    // soon as every CTA of this grid is running.
+    if constexpr (kDyn) pdl_launch_dependents();
     constexpr int BM = 256;  // rows per pair tile
     constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;  // output columns per tile
     auto half_tile = [&](const TileCoord& c) { return kEpi == kEpiPlain && pair_runs_as_128_rows(args, c); };
@@ -89,7 +106,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const SmemPlan sp = smem_plan(128, Cfg::kHalfN, S, E, args.walk_order == 3);
+    const SmemPlan sp = smem_plan(128, Cfg::kHalfN, S, E, !kDyn && args.walk_order == 3, kDyn);
     const uint32_t a0 = base + sp.a_off;
     const uint32_t b0 = base + sp.b_off;
     const uint32_t bars = base + sp.bar_off;
@@ -101,19 +118,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + sp.misc_off);
     int32_t* s_off = reinterpret_cast<int32_t*>(gbase + sp.off_off);
     int32_t* s_pre = reinterpret_cast<int32_t*>(gbase + sp.pre_off);
-    int32_t* s_order = reinterpret_cast<int32_t*>(gbase + sp.ord_off);  // walk order 3 only
+    int32_t* s_order = reinterpret_cast<int32_t*>(gbase + sp.ord_off);  // walk order 3; mixed: class S prefix
     int32_t* s_spre = reinterpret_cast<int32_t*>(gbase + sp.spre_off);
+    int32_t* q_desc = reinterpret_cast<int32_t*>(gbase + sp.q_off);     // mixed: tile queue
+    auto qfull_bar = [&](int i) { return base + sp.qbar_off + 8u * i; };
+    auto qempty_bar = [&](int i) { return base + sp.qbar_off + 8u * (kQueueDepth + i); };
 
     // S1, identical in both CTAs, so every early exit below is pair-uniform.
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
         if (threadIdx.x == 0 && rank == 0) atomicCAS(args.status, 0, kStatusBadOffsets);
         return;
     }
-    if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
-    __syncthreads();
-    const int32_t T = s_pre[E];
-    if (args.walk_order == 3) build_size_order(s_off, s_order, s_spre, E, BM, args.n_tiles_n);
-    if (static_cast<int32_t>(pair) >= T) return;
+    ClassLists L;
+    int32_t T;
+    if constexpr (kDyn) {
+        // both class lists (class P in s_pre, class S in s_order)
+        if (warp == 0) build_class_prefix_warp(s_off, s_pre, E, 256, args.n_tiles_n, args.pair_min_rows, 0x7fffffff);
+        if (warp == 1) build_class_prefix_warp(s_off, s_order, E, 128, args.n_tiles_n, 0, args.pair_min_rows);
+        __syncthreads();
+        L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E]};
+        T = L.nP + L.nS;
+        if (T == 0) return;
+    } else {
+        if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
+        __syncthreads();
+        T = s_pre[E];
+        if (args.walk_order == 3) build_size_order(s_off, s_order, s_spre, E, BM, args.n_tiles_n);
+        if (static_cast<int32_t>(pair) >= T) return;
+    }
 
     if (threadIdx.x == 32) {
         for (int s = 0; s < S; ++s) {
@@ -125,6 +157,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             mbar_init(acce_bar(a), 2 * pair_epilogue_warps<kEpi>());
         }
         mbar_init(drain_bar, 1);
+        if constexpr (kDyn) {
+            // q_empty (used in the leader) counts the leader's MMA thread and
+            // epilogue warps and the peer's producer and epilogue warps
+            for (int i = 0; i < kQueueDepth; ++i) {
+                mbar_init(qfull_bar(i), 1);
+                mbar_init(qempty_bar(i), 2 + 2 * pair_epilogue_warps<kEpi>());
+            }
+        }
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -150,6 +190,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     auto tile_at = [&](int32_t p) -> TileCoord {
         return walk_decode(s_off, s_pre, s_order, s_spre, E, BM, kOutN, nN, T, WO, WS, p);
     };
+    // Mixed launch: take the next descriptor from this CTA's queue and
+    // release the slot on the leader's q_empty (`warp_wide`: all lanes of an
+    // epilogue warp wait, lane 0 releases).  False on an abort.
+    auto q_pop = [&](int& qs, uint32_t& qp, TileCoord& c, bool warp_wide) -> bool {
+        bool ok = pair_wait_or_abort<true>(qfull_bar(qs), qp, abort_flag, peer_flag, args.status, args.timeout_ns);
+        if (warp_wide) ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        const volatile int32_t* d = q_desc + 4 * qs;
+        c.expert = d[0];
+        c.row0 = d[1];
+        c.rows = d[2];
+        c.col0 = d[3];
+        if (warp_wide) __syncwarp();
+        if (!warp_wide || lane == 0) {
+            if (rank == 0) mbar_arrive(qempty_bar(qs));
+            else mbar_arrive_cluster(map_to_rank(qempty_bar(qs), 0));
+        }
+        if (++qs == kQueueDepth) {
+            qs = 0;
+            qp ^= 1u;
+        }
+        return true;
+    };
 
     if (warp == 0) {
         // ---------------------------------------------------- S4: TMA producer
@@ -158,15 +221,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = true;
-            for (int32_t t = pair; ok && t < T; t += npairs) {
-                const TileCoord c = tile_at(t);
+            auto produce = [&](const TileCoord& c) {
                 const bool half = half_tile(c);
                 const int32_t a_row = c.row0 + (half ? 64 : 128) * static_cast<int32_t>(rank);
+                const int ncols = pair_tile_cols<BN, kEpi>(c.col0, args.N);
+                const int np = ncols / (2 * Cfg::kPanelN);  // panels this CTA loads
                 // plain: this CTA's half of the tile's columns; SwiGLU: the gate (CTA 0) or up (CTA 1) columns
                 const int32_t b_col = (kEpi == kEpiSwiGLU) ? c.col0 + (rank ? args.N : 0)
-                                                           : c.col0 + Cfg::kHalfN * static_cast<int32_t>(rank);
+                                                           : c.col0 + (ncols / 2) * static_cast<int32_t>(rank);
                 const CUtensorMap* xmap = half ? &tmap_x64 : &tmap_x;
-                const uint32_t tx_bytes = 2u * (half ? Cfg::kStageBytesPerCta64 : Cfg::kStageBytesPerCta);
+                const uint32_t tx_bytes = 2u * ((half ? 64u : 128u) * 128u + np * Cfg::kPanelB);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!pair_wait_or_abort(empty_bar(st), ph ^ 1u, abort_flag, peer_flag, args.status,
                                             args.timeout_ns)) {
@@ -178,14 +242,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                     tma_load_2d_pair(a0 + st * sp.a_stage, xmap, full_leader, kb * Cfg::kKStage, a_row);
 #pragma unroll
                     for (int p = 0; p < Cfg::kPanels; ++p)
-                        tma_load_3d_pair(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_leader,
-                                         b_col + Cfg::kPanelN * p, kb * Cfg::kKStage, c.expert);
+                        if (p < np)
+                            tma_load_3d_pair(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_leader,
+                                             b_col + Cfg::kPanelN * p, kb * Cfg::kKStage, c.expert);
                     ++issued;
                     if (++st == S) {
                         st = 0;
                         ph ^= 1u;
                     }
                 }
+            };
+            if constexpr (kDyn) {
+                int qs = 0;
+                uint32_t qp = 0;
+                if (rank == 0) {
+                    // claim, write the descriptor into both CTAs' queues, load the leader's half
+                    TileClaimer cl;
+                    cl.init(args.sched, L, true);
+                    TileCoord c = cl.next(L);
+                    while (ok) {
+                        if (!pair_wait_or_abort<true>(qempty_bar(qs), qp ^ 1u, abort_flag, peer_flag, args.status,
+                                                      args.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        int32_t* d = q_desc + 4 * qs;
+                        d[0] = c.expert;
+                        d[1] = c.row0;
+                        d[2] = c.rows;
+                        d[3] = c.col0;
+                        st_shared_cluster_v4(map_to_rank(smem_addr(d), 1), c.expert, c.row0, c.rows, c.col0);
+                        mbar_arrive(qfull_bar(qs));
+                        mbar_arrive_cluster(map_to_rank(qfull_bar(qs), 1));
+                        if (++qs == kQueueDepth) {
+                            qs = 0;
+                            qp ^= 1u;
+                        }
+                        if (c.expert < 0) break;
+                        cl.prefetch();
+                        produce(c);
+                        if (ok) c = cl.next(L);
+                    }
+                } else {
+                    TileCoord c;
+                    while (ok) {
+                        if (!q_pop(qs, qp, c, false)) {
+                            ok = false;
+                            break;
+                        }
+                        if (c.expert < 0) break;
+                        produce(c);
+                    }
+                }
+            } else {
+                for (int32_t t = pair; ok && t < T; t += npairs) produce(tile_at(t));
             }
             if (!ok) {
                 // The leader's full barriers count both CTAs' bytes: it waits
@@ -209,21 +319,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             int acc = 0;
             uint32_t acc_ph = 0;
             bool ok = true;
-            for (int32_t t = pair; ok && t < T; t += npairs) {
-                const uint32_t idesc =
-                    half_tile(tile_at(t)) ? Cfg::kIdesc128
-                                                                                              : Cfg::kIdesc;
+            auto mma_tile = [&](const TileCoord& c) {
+                const uint32_t idesc = idesc_bf16_f32(half_tile(c) ? 128 : 256, pair_tile_cols<BN, kEpi>(c.col0, args.N),
+                                                      true);
                 if (!pair_wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, peer_flag, args.status,
                                         args.timeout_ns)) {
                     ok = false;
-                    break;
+                    return;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!pair_wait_or_abort(full_bar(st), ph, abort_flag, peer_flag, args.status, args.timeout_ns)) {
                         ok = false;
-                        break;
+                        return;
                     }
                     tc_fence_after_sync();
                     const uint32_t a_st = a0 + st * sp.a_stage;
@@ -240,12 +349,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                         ph ^= 1u;
                     }
                 }
-                if (!ok) break;
                 mma_commit_pair(accf_bar(acc), 0x3);
                 if (++acc == 2) {
                     acc = 0;
                     acc_ph ^= 1u;
                 }
+            };
+            if constexpr (kDyn) {
+                int qs = 0;
+                uint32_t qp = 0;
+                TileCoord c;
+                while (ok) {
+                    if (!q_pop(qs, qp, c, false)) {
+                        ok = false;
+                        break;
+                    }
+                    if (c.expert < 0) break;
+                    mma_tile(c);
+                }
+            } else {
+                for (int32_t t = pair; ok && t < T; t += npairs) mma_tile(tile_at(t));
             }
             if (!ok) {
                 mma_commit_pair(drain_bar, 0x1);
@@ -259,11 +382,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
         const int N = args.N;
         int acc = 0;
         uint32_t acc_ph = 0;
-        for (int32_t t = pair; t < T; t += npairs) {
-            const TileCoord c = tile_at(t);
+        // false when the pair aborts
+        auto epi_tile = [&](const TileCoord& c) -> bool {
             bool ok = pair_wait_or_abort(accf_bar(acc), acc_ph, abort_flag, peer_flag, args.status, args.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
+            if (!ok) return false;
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             // M = 256: this CTA's 128 rows, one per TMEM lane, all BN columns.
@@ -274,8 +397,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             const bool half = half_tile(c);
             const int r_local = half ? 64 * static_cast<int>(rank) + 32 * (q & 1) + lane
                                      : 128 * static_cast<int>(rank) + q * 32 + lane;
-            const int ncols = half ? BN / 2 : kOutN;
-            const int cbase = half ? (q >> 1) * (BN / 2) : 0;  // first tile column this warp holds
+            const int tcols = (kEpi == kEpiSwiGLU) ? kOutN : pair_tile_cols<BN, kEpi>(c.col0, N);
+            const int ncols = half ? tcols / 2 : tcols;
+            const int cbase = half ? (q >> 1) * (tcols / 2) : 0;  // first tile column this warp holds
             const bool row_ok = r_local < c.rows;
             __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0 + cbase;
             constexpr int kParts = pair_epilogue_warps<kEpi>() / 4;  // warps per lane quadrant
@@ -283,6 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             const int c0 = ((warp - 2) >> 2) * pc;
 #pragma unroll 1
             for (int cc = c0; cc < c0 + pc; cc += 32) {
+                if (c.col0 + cbase + cc >= N) break;  // columns past N: not computed, not stored
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
                 if constexpr (kEpi == kEpiSwiGLU) {
@@ -324,6 +449,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                 acc = 0;
                 acc_ph ^= 1u;
             }
+            return true;
+        };
+        if constexpr (kDyn) {
+            int qs = 0;
+            uint32_t qp = 0;
+            TileCoord c;
+            while (q_pop(qs, qp, c, true) && c.expert >= 0)
+                if (!epi_tile(c)) break;
+        } else {
+            for (int32_t t = pair; t < T; t += npairs)
+                if (!epi_tile(tile_at(t))) break;
         }
     }
 

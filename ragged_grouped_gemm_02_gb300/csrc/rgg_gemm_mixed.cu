@@ -1,0 +1,49 @@
+// The mixed launch (rgg_sched.cuh): 256-row tiles of the large experts on CTA
+// pairs beside 128-row tiles of the small ones on single CTAs, two kernels on
+// disjoint SMs that claim tiles from the same two device counters.
+#include "rgg_gemm_2cta.cuh"
+#include "rgg_internal.h"
+
+namespace rgg {
+
+cudaError_t launch_gemm_mixed(int pair_grid, size_t pair_smem, const GemmArgs& pair_args, int single_grid,
+                              size_t single_smem, const GemmArgs& single_args, cudaStream_t stream,
+                              const CUtensorMap& tmap_x, const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w) {
+    if (pair_grid < 0 || pair_grid % 2 != 0 || single_grid < 0 || pair_grid + single_grid == 0)
+        return cudaErrorInvalidValue;
+    if (pair_grid > 0) {
+        auto kernel = grouped_gemm_pair_kernel<kMixedBN, kEpiPlain, true>;
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(pair_smem));
+        if (err != cudaSuccess) return err;
+        kernel<<<pair_grid, 64 + 32 * pair_epilogue_warps<kEpiPlain>(), pair_smem, stream>>>(tmap_x, tmap_x64,
+                                                                                             tmap_w, pair_args);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    if (single_grid > 0) {
+        auto kernel = grouped_gemm_kernel<128, kMixedBN, kEpiPlain, false, kGatherNone, true>;
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(single_smem));
+        if (err != cudaSuccess) return err;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(single_grid, 1, 1);
+        cfg.blockDim = dim3(cta_threads<kEpiPlain, false>(), 1, 1);
+        cfg.dynamicSmemBytes = single_smem;
+        cfg.stream = stream;
+        // After the pair kernel: may start once every pair CTA is running, so
+        // the two kernels share the GPU (each kernel ends no earlier than the
+        // pair kernel, see pdl_wait_prerequisites).
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pair_grid > 0 ? 1 : 0;
+        err = cudaLaunchKernelEx(&cfg, kernel, tmap_x, tmap_x64, tmap_w, single_args);
+        if (err != cudaSuccess) return err;
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
+}
+
+}  // namespace rgg

@@ -53,6 +53,14 @@ cudaError_t launch_gemm_pair(int bn, int grid, size_t smem, cudaStream_t stream,
 cudaError_t launch_gemm_pair_swiglu(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,
                                     const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w, const GemmArgs& args);
 
+// The mixed launch: the pair kernel (pair_grid CTAs, even; may be 0) and,
+// after it with programmatic stream serialisation, the 1-CTA kernel
+// (single_grid CTAs; may be 0), both 256-column tiles claiming from the two
+// counters at pair_args.sched (zeroed by the caller before the launch).
+cudaError_t launch_gemm_mixed(int pair_grid, size_t pair_smem, const GemmArgs& pair_args, int single_grid,
+                              size_t single_smem, const GemmArgs& single_args, cudaStream_t stream,
+                              const CUtensorMap& tmap_x, const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w);
+
 // The flat tile list written out by the same device code the GEMM uses, in
 // list order (walk_order 0) or in the order walk_order visits it.
 cudaError_t launch_export_tiles(const int32_t* offsets, int E, int64_t M_tot, int N, int bm, int bn,

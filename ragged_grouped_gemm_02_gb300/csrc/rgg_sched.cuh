@@ -1,0 +1,131 @@
+// rgg_sched.cuh -- the tile claims of the mixed launch: CTA pairs for large
+// experts beside 1-CTA tiles for small ones, two kernels that run side by
+// side on disjoint SMs and take tiles from two device-wide counters.
+//
+// "Grouped GEMM for Imbalanced Experts on Blackwell: A WIP Worklog", sections
+// 2.1 and 7: under skewed routing one BM wastes either rows (large tiles on
+// small experts) or bandwidth (small tiles on large experts), and BM should
+// follow the expert sizes.  "Pearl's grouped GEMM kernel for MoE models,
+// explained", "Four changes, three of them measured": 64-row tiles on a single
+// CTA for small groups, the two-CTA mode for large ones.  A tcgen05 kernel
+// uses one cta_group throughout, so the two tile shapes run as two kernels:
+//
+//   class P (m_e >= pair_min_rows): 256-row tiles on CTA pairs (the last tile
+//     of an expert, when it holds <= 128 rows, as an M = 128 pair MMA);
+//   class S (the other experts): 128-row tiles on one CTA (<= 64-row tails as
+//     M = 64 MMAs).
+//
+// Each kernel builds both class lists from the device offsets (the routed
+// counts never reach the host) and claims tiles of its own class first, in
+// list order with each expert's tiles N tile by N tile, from a device counter
+// (atomicAdd); when its class runs out it takes tiles of the other class: the
+// pair kernel runs a class-S tile (<= 128 rows) as an M = 128 pair tile, the
+// 1-CTA kernel runs a class-P tile as two 128-row tiles.  Every tile of both
+// lists is claimed exactly once (the counter hands out each index once; an
+// index past the end ends that class), so the result does not depend on how
+// the SMs are split between the kernels or on whether they overlap at all.
+// Claimed in list order, the tiles in flight at any moment are a contiguous
+// window of the lists: the M tiles that read one weight panel run side by
+// side, so the panel is read from HBM about once however the SMs drift.
+//
+// The counters (two int32) are zeroed before each launch by the host.
+#pragma once
+
+#include <cstdint>
+
+#include "rgg_tiles.cuh"
+
+namespace rgg {
+
+constexpr int kQueueDepth = 8;          // tile descriptors between a CTA's producer and its consumers
+constexpr int kMixedBN = 256;           // both classes: 256-column tiles (the last N tile narrowed)
+constexpr int kPairMinRowsDefault = 256;
+
+struct ClassLists {
+    const int32_t* s_off;
+    const int32_t* s_preP;  // class P prefix of 256-row tiles
+    const int32_t* s_preS;  // class S prefix of 128-row tiles
+    int E, nN;
+    int32_t nP, nS;
+
+    __device__ __forceinline__ TileCoord decode_p(int32_t t) const {
+        return decode_tile(s_off, s_preP, E, 256, kMixedBN, nN, t, true);
+    }
+    __device__ __forceinline__ TileCoord decode_s(int32_t t) const {
+        return decode_tile(s_off, s_preS, E, 128, kMixedBN, nN, t, true);
+    }
+};
+
+__device__ __forceinline__ TileCoord sentinel_tile() {
+    TileCoord c;
+    c.expert = -1;
+    c.row0 = 0;
+    c.rows = 0;
+    c.col0 = 0;
+    return c;
+}
+
+// Claims of one CTA (the pair kernel: of the leader CTA).  `own_first_p`:
+// the pair kernel claims class P first, the 1-CTA kernel class S first.
+// `split_p`: class-P tiles are handed out as up to two 128-row tiles (the
+// 1-CTA kernel).  prefetch() issues the atomic of the next claim early so its
+// latency hides under the current tile's loads; next() resolves it.
+struct TileClaimer {
+    int32_t* ctr_first;
+    int32_t* ctr_second;
+    int32_t n_first, n_second;
+    bool first_is_p, split_p;
+    int phase;          // 0: first class, 1: second class, 2: done
+    bool has_half;      // the second 128-row half of a split class-P tile is due
+    TileCoord half;
+    bool ticket_valid;
+    int32_t ticket;
+
+    __device__ __forceinline__ void init(int32_t* sched, const ClassLists& L, bool pair_kernel) {
+        first_is_p = pair_kernel;
+        split_p = !pair_kernel;
+        ctr_first = pair_kernel ? sched : sched + 1;
+        ctr_second = pair_kernel ? sched + 1 : sched;
+        n_first = pair_kernel ? L.nP : L.nS;
+        n_second = pair_kernel ? L.nS : L.nP;
+        phase = 0;
+        has_half = false;
+        ticket_valid = false;
+        ticket = 0;
+    }
+
+    __device__ __forceinline__ void prefetch() {
+        ticket_valid = false;
+        if (has_half || phase >= 2) return;
+        ticket = atomicAdd(phase == 0 ? ctr_first : ctr_second, 1);
+        ticket_valid = true;
+    }
+
+    __device__ __forceinline__ TileCoord next(const ClassLists& L) {
+        if (has_half) {
+            has_half = false;
+            return half;
+        }
+        while (phase < 2) {
+            const int32_t t = ticket_valid ? ticket : atomicAdd(phase == 0 ? ctr_first : ctr_second, 1);
+            ticket_valid = false;
+            const bool is_p = (phase == 0) == first_is_p;
+            if (t >= (phase == 0 ? n_first : n_second)) {
+                ++phase;
+                continue;
+            }
+            TileCoord c = is_p ? L.decode_p(t) : L.decode_s(t);
+            if (is_p && split_p && c.rows > 128) {
+                half = c;
+                half.row0 = c.row0 + 128;
+                half.rows = c.rows - 128;
+                has_half = true;
+                c.rows = 128;
+            }
+            return c;
+        }
+        return sentinel_tile();
+    }
+};
+
+}  // namespace rgg

@@ -75,6 +75,37 @@ __device__ __forceinline__ void build_tile_prefix_warp(const int32_t* s_off, int
     if (lane == 31) s_pre[E] = incl;
 }
 
+// The same prefix over one class of experts: expert e counts only when
+// lo <= m_e < hi (its tiles of BM rows), the others add no tiles.  Used by the
+// mixed launch, whose CTA pairs take the experts of at least `pair_min_rows`
+// rows in 256-row tiles and whose 1-CTA kernel takes the rest in 128-row
+// tiles, each class with its own flat list in the worklog's order.
+__device__ __forceinline__ void build_class_prefix_warp(const int32_t* s_off, int32_t* s_pre, int E, int BM,
+                                                        int n_tiles_n, int32_t lo, int32_t hi) {
+    const int lane = threadIdx.x & 31;
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per);
+    const int e1 = min(E, e0 + per);
+    auto tiles = [&](int e) -> int32_t {
+        const int32_t m = s_off[e + 1] - s_off[e];
+        return (m >= lo && m < hi) ? ((m + BM - 1) / BM) * n_tiles_n : 0;
+    };
+    int32_t local = 0;
+    for (int e = e0; e < e1; ++e) local += tiles(e);
+    int32_t incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    int32_t run = incl - local;
+    for (int e = e0; e < e1; ++e) {
+        s_pre[e] = run;
+        run += tiles(e);
+    }
+    if (lane == 31) s_pre[E] = incl;
+}
+
 // Decode flat tile t (0 <= t < s_pre[E]).  The expert is the last e with
 // s_pre[e] <= t, which skips empty experts because they add no tiles.
 // `n_major` (walk order 4) visits an expert's tiles N tile by N tile (all M

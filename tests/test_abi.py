@@ -267,3 +267,45 @@ def test_plan_reports_the_launch_block_size(lib):
     assert rgg.rgg_plan(64, 16384, 1024, 2688, op="fp8")["threads"] == 320
     assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu", bm=128)["threads"] == 320
     assert rgg.rgg_plan(32, 32768, 6144, 2048, op="swiglu")["threads"] == 320  # pairs, per CTA
+
+
+def test_plan_mixed_launch(lib):
+    # the mixed launch: pairs for the experts of >= pair_min_rows rows, single CTAs for the rest
+    from ragged_grouped_gemm_02_gb300 import workloads as wl
+    skew = wl.workload_counts("skew16k")
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=skew, mixed=1)
+    assert p["mixed"] == 1 and p["bm"] == 256 and p["bn"] == 256 and p["tail64"] == 1
+    assert p["grid"] % 2 == 0 and 0 < p["grid"] < 152 and p["grid"] + p["single_grid"] == 152
+    assert p["stages"] >= 4 and p["single_stages"] >= 3 and p["pair_min_rows"] == 256
+    assert p["smem_bytes"] <= 232448 and p["single_smem_bytes"] <= 232448 and p["tmem_cols"] == 512
+    # every expert large: all SMs to the pairs; every expert small: all to single CTAs
+    assert (rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=[256] * 64, mixed=1)["grid"],
+            rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=[256] * 64, mixed=1)["single_grid"]) == (152, 0)
+    q = rgg.rgg_plan(32, 512, 6144, 4096, host_counts=[16] * 32, mixed=1)
+    assert (q["grid"], q["single_grid"]) == (0, 152)
+    # without host counts the experts are taken as balanced
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, mixed=1)["grid"] == 152
+    assert rgg.rgg_plan(64, 2048, 1024, 2688, mixed=1)["single_grid"] == 152
+    # an explicit split, a threshold, a grid cap
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, mixed=1, mixed_pair_sms=76, pair_min_rows=1000)
+    assert (p["grid"], p["single_grid"], p["pair_min_rows"]) == (76, 76, 1000)
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, mixed=1, mixed_pair_sms=-1)
+    assert (p["grid"], p["single_grid"]) == (0, 152)
+    p = rgg.rgg_plan(4, 256, 256, 512, host_counts=[100, 0, 300, 1], mixed=1, max_ctas=3)
+    assert p["grid"] == 2 and p["single_grid"] == 1
+    # off by default
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=skew)["mixed"] == 0
+
+
+@pytest.mark.parametrize("kw,status", [(dict(bm=128), "INVALID_ARG"), (dict(bn=128), "INVALID_ARG"),
+                                       (dict(tail64=-1), "INVALID_ARG"), (dict(mixed_pair_sms=3), "INVALID_ARG"),
+                                       (dict(mixed_pair_sms=154), "INVALID_ARG"),
+                                       (dict(mixed_pair_sms=-2), "INVALID_ARG"),
+                                       (dict(pair_min_rows=-1), "INVALID_ARG"), (dict(mixed=2), "INVALID_ARG"),
+                                       (dict(op="swiglu"), "UNSUPPORTED"), (dict(op="fp8"), "UNSUPPORTED")])
+def test_plan_mixed_rejects(lib, kw, status):
+    args = dict(mixed=1)
+    args.update(kw)
+    with pytest.raises(rgg.RggError) as ei:
+        rgg.rgg_plan(64, 16384, 1024, 2688, **args)
+    assert ei.value.status == getattr(rgg, "RGG_ERR_" + status)

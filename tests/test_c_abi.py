@@ -22,13 +22,15 @@ PROGRAM = r"""
 
 static char ws_marker[16]; /* rgg_plan only reads whether a gather workspace is given */
 
-static void plan(int E, int64_t M, int K, int N, const int32_t* counts, int op, int bm, int walk, int ws) {
+static void plan(int E, int64_t M, int K, int N, const int32_t* counts, int op, int bm, int walk, int ws,
+                 int mixed) {
     rgg_options o;
     memset(&o, 0, sizeof(o));
     o.host_counts = counts;
     o.op = op;
     o.bm = bm;
     o.walk_order = walk;
+    o.mixed = mixed;
     if (ws) {
         o.workspace = ws_marker;
         o.workspace_bytes = (int64_t)1 << 62;
@@ -36,9 +38,10 @@ static void plan(int E, int64_t M, int K, int N, const int32_t* counts, int op, 
     rgg_plan_info p;
     memset(&p, 0, sizeof(p));
     rgg_status s = rgg_plan(0, 0, E, M, K, N, &o, &p);
-    printf("%d %d %d %d %d %d %d %d %lld %d %d %d %lld\n", (int)s, p.bm, p.bn, p.bk, p.stages, p.grid,
-           p.threads, p.smem_bytes, (long long)p.max_tiles, p.tail64, p.walk_order, p.gather_mode,
-           (long long)p.workspace_bytes);
+    printf("%d %d %d %d %d %d %d %d %lld %d %d %d %lld %d %d %d %d %d\n", (int)s, p.bm, p.bn, p.bk, p.stages,
+           p.grid, p.threads, p.smem_bytes, (long long)p.max_tiles, p.tail64, p.walk_order, p.gather_mode,
+           (long long)p.workspace_bytes, p.mixed, p.single_grid, p.single_stages, p.single_smem_bytes,
+           p.pair_min_rows);
 }
 
 int main(void) {
@@ -47,15 +50,17 @@ int main(void) {
     for (int e = 0; e < 64; ++e)
         if (fscanf(f, "%d", &skew[e]) != 1) return 2;
     fclose(f);
-    plan(32, 512, 6144, 4096, NULL, 0, 0, 0, 0);
-    plan(64, 16384, 1024, 2688, NULL, 0, 0, 0, 0);
-    plan(64, 16384, 1024, 2688, skew, 0, 0, 0, 0);
-    plan(64, 16384, 1024, 2688, skew, 2, 0, 0, 0);
-    plan(64, 16384, 1024, 1344, skew, 1, 0, 0, 0);
-    plan(64, 16384, 1024, 2688, skew, 3, 0, 0, 0);
-    plan(64, 16384, 1024, 2688, skew, 3, 0, 0, 1);
-    plan(32, 32768, 6144, 4096, NULL, 0, 0, 0, 0);
-    plan(4, 256, 256, 512, NULL, 0, 64, 5, 0);
+    plan(32, 512, 6144, 4096, NULL, 0, 0, 0, 0, 0);
+    plan(64, 16384, 1024, 2688, NULL, 0, 0, 0, 0, 0);
+    plan(64, 16384, 1024, 2688, skew, 0, 0, 0, 0, 0);
+    plan(64, 16384, 1024, 2688, skew, 2, 0, 0, 0, 0);
+    plan(64, 16384, 1024, 1344, skew, 1, 0, 0, 0, 0);
+    plan(64, 16384, 1024, 2688, skew, 3, 0, 0, 0, 0);
+    plan(64, 16384, 1024, 2688, skew, 3, 0, 0, 1, 0);
+    plan(32, 32768, 6144, 4096, NULL, 0, 0, 0, 0, 0);
+    plan(4, 256, 256, 512, NULL, 0, 64, 5, 0, 0);
+    plan(64, 16384, 1024, 2688, skew, 0, 0, 0, 0, 1);
+    plan(64, 16384, 1024, 2688, skew, 2, 0, 0, 0, 1);
     printf("%s|%s\n", rgg_status_string(RGG_ERR_BAD_OFFSETS), rgg_status_string(RGG_OK));
     return 0;
 }
@@ -71,6 +76,8 @@ CASES = [
     dict(E=64, M=16384, K=1024, N=2688, counts=True, op="gather", ws=True),
     dict(E=32, M=32768, K=6144, N=4096),
     dict(E=4, M=256, K=256, N=512, bm=64, walk_order=5),
+    dict(E=64, M=16384, K=1024, N=2688, counts=True, mixed=1),
+    dict(E=64, M=16384, K=1024, N=2688, counts=True, op="fp8", mixed=1),
 ]
 
 
@@ -100,7 +107,7 @@ def test_c_program_sees_the_same_plans_as_python(c_output):
     for line, case in zip(lines, CASES):
         vals = [int(v) for v in line.split()]
         kw = dict(op=case.get("op", "gemm"), bm=case.get("bm", 0), walk_order=case.get("walk_order", 0),
-                  workspace=True if case.get("ws") else None)
+                  workspace=True if case.get("ws") else None, mixed=case.get("mixed", 0))
         if case.get("counts"):
             kw["host_counts"] = counts
         if vals[0] != rgg.RGG_OK:
@@ -110,7 +117,8 @@ def test_c_program_sees_the_same_plans_as_python(c_output):
             continue
         p = rgg.rgg_plan(case["E"], case["M"], case["K"], case["N"], **kw)
         fields = ["bm", "bn", "bk", "stages", "grid", "threads", "smem_bytes", "max_tiles", "tail64", "walk_order",
-                  "gather_mode", "workspace_bytes"]
+                  "gather_mode", "workspace_bytes", "mixed", "single_grid", "single_stages", "single_smem_bytes",
+                  "pair_min_rows"]
         assert vals[1:] == [p[f] for f in fields], (case, vals, p)
 
 
