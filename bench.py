@@ -74,6 +74,11 @@ def parse_args():
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--tail64", type=int, default=0, help="0 auto, 1 on, -1 off")
     p.add_argument("--gather-mode", type=int, default=0, help="gather ops: 0 auto, 1 TMA gather4, 2 two-pass")
+    p.add_argument("--mixed", type=int, default=0,
+                   help="plain GEMM: 0 auto, 1 the mixed launch (large experts on CTA pairs beside small ones "
+                        "on single CTAs, tiles claimed on the device), -1 off")
+    p.add_argument("--mixed-pair-sms", type=int, default=0,
+                   help="mixed launch: SMs of the pair kernel (0: split by estimated work, -1: none)")
     p.add_argument("--walk-order", type=int, default=0,
                    help="0 auto, -1 list order, 1 front/back interleave, 2 scatter, 3 size-sorted interleave, "
                         "4 N-major within each expert")
@@ -277,6 +282,8 @@ def run_profile(args):
     Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device=dev)
     opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
                 walk_order=args.walk_order, host_counts=inp.counts)
+    if args.op == "gemm":
+        opts.update(mixed=args.mixed, mixed_pair_sms=args.mixed_pair_sms)
     if args.op == "gather":
         # the same recipe as the timed gather op: M_tot tokens, distinct tokens per expert
         gen = torch.Generator().manual_seed(inp.workload.seed + 7)
@@ -370,6 +377,8 @@ class Step:
         # alone); the kernel itself reads the offsets on the device.
         self.opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
                          walk_order=args.walk_order, host_counts=inp.counts if host_counts else None)
+        if op == "gemm":
+            self.opts.update(mixed=args.mixed, mixed_pair_sms=args.mixed_pair_sms)
         self.plan_from = ("host-side routed counts (tile shape only)" if host_counts
                           else "device offsets only (no host counts)")
         if self.gather:
@@ -380,8 +389,12 @@ class Step:
                                  num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
                                  op=op, **self.opts)
         # launches of this library's kernels in one step: the two-pass gather runs
-        # its row gather and then the grouped GEMM, every other op one kernel
-        self.per_step = 2 if self.plan.get("gather_mode") == 2 else 1
+        # its row gather and then the grouped GEMM, the mixed launch its pair
+        # kernel and its 1-CTA kernel (each when it has SMs), every other op one kernel
+        if self.plan.get("mixed"):
+            self.per_step = int(self.plan["grid"] > 0) + int(self.plan["single_grid"] > 0)
+        else:
+            self.per_step = 2 if self.plan.get("gather_mode") == 2 else 1
 
     def launch(self, stream):
         self.gemm(self.X, self.W, self.off, self.Y, stream=stream, **self.opts)
@@ -480,8 +493,13 @@ def roofline_of(step, launch_ms, peaks):
     roof["peak_source"] = peaks["source"] + (" bf16 x 2 (nominal fp8/bf16 ratio)" if op == "fp8" else "")
     roof["algorithmic_per_launch"] = {"flops": step.flops, "bytes": step.bytes}
     roof["launch_ms"] = round(launch_ms, 5)
-    roof["launch_scope"] = ("one step of the CUDA-graph timed region: the row gather and the GEMM"
-                            if step.per_step == 2 else "one GEMM launch in the CUDA-graph timed region")
+    if step.plan.get("mixed"):
+        roof["launch_scope"] = ("one step of the CUDA-graph timed region: the mixed launch (its pair kernel and "
+                                "its 1-CTA kernel side by side)")
+    elif step.per_step == 2:
+        roof["launch_scope"] = "one step of the CUDA-graph timed region: the row gather and the GEMM"
+    else:
+        roof["launch_scope"] = "one GEMM launch in the CUDA-graph timed region"
     roof["hbm_gbs"] = round(step.bytes / (launch_ms / 1e3) / 1e9, 1)
     roof["hbm_frac"] = round(step.bytes / (launch_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
     roof["tensor_frac"] = round(step.flops / (launch_ms / 1e3) / 1e12 / tc_peak, 4)

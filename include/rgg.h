@@ -51,8 +51,11 @@ typedef enum rgg_status {
     RGG_ERR_BAD_OFFSETS = 4,     /* device-detected: group offsets not valid; nothing was written */
     RGG_ERR_DEVICE_TIMEOUT = 5,  /* device-detected: a pipeline wait exceeded the time limit; Y is incomplete */
     RGG_ERR_CAPACITY = 6,        /* rgg_export_tiles: more tiles than the output capacity (count still exact) */
-    RGG_ERR_BAD_ROW_INDEX = 7    /* device-detected (gather calls): a token index read was outside [0, T); the
+    RGG_ERR_BAD_ROW_INDEX = 7,   /* device-detected (gather calls): a token index read was outside [0, T); the
                                     rows with such an index hold unspecified values, all other rows are right */
+    RGG_ERR_DEVICE_BOUNDS = 8    /* device-detected, debug build (librgg_debug.so) only: a copy, store, TMEM load
+                                    or tile descriptor failed its bounds check and was not issued; Y is
+                                    incomplete.  The release build never reports it. */
 } rgg_status;
 
 typedef struct rgg_handle rgg_handle;
@@ -144,14 +147,18 @@ typedef struct rgg_plan_info {
 /*
  * Create a handle bound to CUDA device `device`: queries the SM count and the
  * shared-memory limit, checks for compute capability 10.3 (sm_103), and
- * allocates the device status word (once per handle; no call allocates device
- * memory after this).  On success *out owns the handle; release it with
- * rgg_destroy.  Returns RGG_ERR_UNSUPPORTED on any other GPU.
+ * allocates the handle's 256-byte device word, zeroed (once per handle; no
+ * call allocates device memory after this).  Its first int32 is the status
+ * word; three int32 at byte 64 are the mixed launch's tile counters, which
+ * each mixed launch leaves at zero again when its last CTA ends.  On success
+ * *out owns the handle; release it with rgg_destroy.  Returns
+ * RGG_ERR_UNSUPPORTED on any other GPU.
  *
  * Concurrency: calls on one handle may run on any streams, but they share the
  * handle's status word (rgg_query_status returns the first error any of them
- * recorded).  Use a handle from several host threads only under the caller's
- * own lock.
+ * recorded); mixed launches (rgg_options.mixed) on one handle must not overlap
+ * on the GPU, since they share the tile counters: order them on one stream.
+ * Use a handle from several host threads only under the caller's own lock.
  */
 rgg_status rgg_create(rgg_handle** out, int device);
 

@@ -22,7 +22,8 @@ __all__ = [
     "rgg_query_status",
     "rgg_plan", "rgg_status_string", "library_path", "load_library", "EXPORTED_SYMBOLS",
     "RGG_OK", "RGG_ERR_INVALID_ARG", "RGG_ERR_UNSUPPORTED", "RGG_ERR_CUDA", "RGG_ERR_BAD_OFFSETS",
-    "RGG_ERR_DEVICE_TIMEOUT", "RGG_ERR_CAPACITY", "RGG_ERR_BAD_ROW_INDEX",
+    "RGG_ERR_DEVICE_TIMEOUT", "RGG_ERR_CAPACITY", "RGG_ERR_BAD_ROW_INDEX", "RGG_ERR_DEVICE_BOUNDS",
+    "open_library", "debug_library_path",
 ]
 
 RGG_OK = 0
@@ -33,10 +34,12 @@ RGG_ERR_BAD_OFFSETS = 4
 RGG_ERR_DEVICE_TIMEOUT = 5
 RGG_ERR_CAPACITY = 6
 RGG_ERR_BAD_ROW_INDEX = 7
+RGG_ERR_DEVICE_BOUNDS = 8
 RGG_DEBUG_PRODUCER_STALL = 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "librgg.so")
+_DEBUG_LIB_PATH = os.path.join(_PKG, "librgg_debug.so")
 
 # The C ABI entry points declared in include/rgg.h.
 EXPORTED_SYMBOLS = (
@@ -85,40 +88,51 @@ def load_library() -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(_LIB_PATH):
-            raise RuntimeError("librgg.so is not built (%s): run __graft_entry__.build() first" % _LIB_PATH)
-        lib = ctypes.CDLL(_LIB_PATH)
-        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-        lib.rgg_create.argtypes = [ctypes.POINTER(ctypes.c_void_p), I]
-        lib.rgg_create.restype = I
-        lib.rgg_destroy.argtypes = [P]
-        lib.rgg_destroy.restype = None
-        lib.rgg_grouped_gemm.argtypes = [P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
-        lib.rgg_grouped_gemm.restype = I
-        lib.rgg_export_tiles.argtypes = [P, P, I, I64, I, I, I, P, I64, P, P]
-        lib.rgg_export_tiles.restype = I
-        lib.rgg_export_walk.argtypes = [P, P, I, I64, I, I, I, I, P, I64, P, P]
-        lib.rgg_export_walk.restype = I
-        lib.rgg_query_status.argtypes = [P, P]
-        lib.rgg_query_status.restype = I
-        lib.rgg_plan.argtypes = [I, I, I, I64, I, I, ctypes.POINTER(_Options), ctypes.POINTER(_PlanInfo)]
-        lib.rgg_plan.restype = I
-        lib.rgg_status_string.argtypes = [I]
-        lib.rgg_status_string.restype = ctypes.c_char_p
-        lib.rgg_last_cuda_error.argtypes = []
-        lib.rgg_last_cuda_error.restype = ctypes.c_char_p
-        lib.rgg_grouped_gemm_swiglu.argtypes = [P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
-        lib.rgg_grouped_gemm_swiglu.restype = I
-        lib.rgg_grouped_gemm_fp8.argtypes = [P, P, P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
-        lib.rgg_grouped_gemm_fp8.restype = I
-        for name in ("rgg_grouped_gemm_gather", "rgg_grouped_gemm_swiglu_gather"):
-            fn = getattr(lib, name)
-            fn.argtypes = [P, P, I64, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
-            fn.restype = I
-        lib.rgg_grouped_gemm_noalloc.argtypes = [P, P, P, P, I, I64, I, I, P, P]
-        lib.rgg_grouped_gemm_noalloc.restype = I
-        _lib = lib
-        return lib
+        _lib = open_library(_LIB_PATH)
+        return _lib
+
+
+def open_library(path: str) -> ctypes.CDLL:
+    """Open a build of the C ABI (librgg.so, or librgg_debug.so: the same
+    entry points with every device access bounds-checked) and declare its
+    entry points' argument types."""
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built: run __graft_entry__.build() first" % path)
+    lib = ctypes.CDLL(path)
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.rgg_create.argtypes = [ctypes.POINTER(ctypes.c_void_p), I]
+    lib.rgg_create.restype = I
+    lib.rgg_destroy.argtypes = [P]
+    lib.rgg_destroy.restype = None
+    lib.rgg_grouped_gemm.argtypes = [P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
+    lib.rgg_grouped_gemm.restype = I
+    lib.rgg_export_tiles.argtypes = [P, P, I, I64, I, I, I, P, I64, P, P]
+    lib.rgg_export_tiles.restype = I
+    lib.rgg_export_walk.argtypes = [P, P, I, I64, I, I, I, I, P, I64, P, P]
+    lib.rgg_export_walk.restype = I
+    lib.rgg_query_status.argtypes = [P, P]
+    lib.rgg_query_status.restype = I
+    lib.rgg_plan.argtypes = [I, I, I, I64, I, I, ctypes.POINTER(_Options), ctypes.POINTER(_PlanInfo)]
+    lib.rgg_plan.restype = I
+    lib.rgg_status_string.argtypes = [I]
+    lib.rgg_status_string.restype = ctypes.c_char_p
+    lib.rgg_last_cuda_error.argtypes = []
+    lib.rgg_last_cuda_error.restype = ctypes.c_char_p
+    lib.rgg_grouped_gemm_swiglu.argtypes = [P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
+    lib.rgg_grouped_gemm_swiglu.restype = I
+    lib.rgg_grouped_gemm_fp8.argtypes = [P, P, P, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
+    lib.rgg_grouped_gemm_fp8.restype = I
+    for name in ("rgg_grouped_gemm_gather", "rgg_grouped_gemm_swiglu_gather"):
+        fn = getattr(lib, name)
+        fn.argtypes = [P, P, I64, P, P, P, P, I, I64, I, I, P, ctypes.POINTER(_Options)]
+        fn.restype = I
+    lib.rgg_grouped_gemm_noalloc.argtypes = [P, P, P, P, I, I64, I, I, P, P]
+    lib.rgg_grouped_gemm_noalloc.restype = I
+    return lib
+
+
+def debug_library_path() -> str:
+    return _DEBUG_LIB_PATH
 
 
 def rgg_status_string(status: int) -> str:

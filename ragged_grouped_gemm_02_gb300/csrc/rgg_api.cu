@@ -580,15 +580,21 @@ rgg_status host_grouped_gemm(int num_sms, int smem_optin, int32_t* status, const
     a.tail64 = p.tail64;
     a.walk_order = p.walk_order;
     if (p.mixed) {
-        // two claim counters after the status word (the device word's first 64 bytes), zeroed per call
+        // the claim counters and the count of finished CTAs sit 64 bytes after the status word; they
+        // start at zero and the launch's last CTA sets them back to zero
         a.sched = status + 16;
+        a.sched_total = p.grid + p.single_grid;
         a.pair_min_rows = p.pair_min_rows;
-        cudaError_t err = cudaMemsetAsync(a.sched, 0, 2 * sizeof(int32_t), st);
-        if (err != cudaSuccess) return cuda_failure(err, "cudaMemsetAsync(tile counters)");
         GemmArgs as = a;
         as.stages = p.single_stages;
-        err = launch_gemm_mixed(p.grid, p.smem_bytes, a, p.single_grid, p.single_smem, as, st, tx, tx64, tw);
-        return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm (mixed) launch");
+        cudaError_t err = launch_gemm_mixed(p.grid, p.smem_bytes, a, p.single_grid, p.single_smem, as, st, tx, tx64,
+                                            tw);
+        if (err != cudaSuccess) {
+            // a kernel that did launch still counts its CTAs: zero the counters behind it
+            cudaMemsetAsync(a.sched, 0, 3 * sizeof(int32_t), st);
+            return cuda_failure(err, "grouped_gemm (mixed) launch");
+        }
+        return RGG_OK;
     }
     cudaError_t err = (p.bm == 256)   ? launch_gemm_pair(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
                       : (p.bm == 128) ? launch_gemm_bm128(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
@@ -610,6 +616,8 @@ const char* rgg_status_string(rgg_status s) {
         case RGG_ERR_DEVICE_TIMEOUT: return "RGG_ERR_DEVICE_TIMEOUT: a device pipeline wait exceeded its limit";
         case RGG_ERR_CAPACITY: return "RGG_ERR_CAPACITY: more tiles than the output capacity";
         case RGG_ERR_BAD_ROW_INDEX: return "RGG_ERR_BAD_ROW_INDEX: a token index is outside [0, T)";
+        case RGG_ERR_DEVICE_BOUNDS:
+            return "RGG_ERR_DEVICE_BOUNDS: a device access failed its bounds check (debug build) and was skipped";
     }
     return "unknown rgg_status";
 }

@@ -41,6 +41,7 @@
 
 #include <cstdint>
 
+#include "rgg_checks.cuh"
 #include "rgg_ptx.cuh"
 #include "rgg_sched.cuh"
 #include "rgg_tiles.cuh"
@@ -76,8 +77,10 @@ struct GemmArgs {
     const int32_t* row_index = nullptr;  // gather kernels: token row of each routed row [M_tot]
     int32_t t_rows = 0;                  // gather kernels: rows of the token matrix
     // Mixed launch (rgg_sched.cuh): tiles claimed from two device counters
-    // sched[0] (class P) and sched[1] (class S), zeroed before the launch.
+    // sched[0] (class P) and sched[1] (class S); sched[2] counts finished CTAs
+    // of the sched_total CTAs of both kernels (the last one resets all three).
     int32_t* sched = nullptr;
+    int32_t sched_total = 0;
     int32_t pair_min_rows = kPairMinRowsDefault;
 };
 
@@ -244,33 +247,48 @@ __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-
 // registers to Y with 256-bit stores ("Pearl's grouped GEMM kernel for MoE
 // models, explained").  Rows past the tile's valid rows, and every row when
 // `store` is false, are read from TMEM but not written.
+//
+// [row_lo, row_hi) are the expert's rows and tcol the buffer's first TMEM
+// column, read only by the bounds checks of the debug build.
 template <int BN, int kEpi, bool kFp8>
 __device__ __forceinline__ void epilogue_store_tile(const GemmArgs& args, const TileCoord& c, bool half, int r_local,
-                                                    uint32_t t_row, int lane, int cc0, bool store) {
+                                                    uint32_t t_row, int lane, int cc0, bool store, int32_t row_lo,
+                                                    int32_t row_hi, uint32_t tcol) {
     constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;
     constexpr int kPartCols = kOutN / (epilogue_warps<kEpi, kFp8>() / 4);
+    constexpr uint32_t kTmemCols = TileConfig<64, BN, kFp8>::kTmemCols;
     const int N = args.N;
     const bool row_ok = store && (!half || lane < 16) && (r_local < c.rows);
-    __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0;
+    const int64_t row = static_cast<int64_t>(c.row0) + r_local;
+    __nv_bfloat16* yrow = args.Y + row * N + c.col0;
 #pragma unroll 1
     for (int cc = cc0; cc < cc0 + kPartCols; cc += 32) {
         if (c.col0 + cc >= N) break;  // columns past N: not computed (tile_panels), not stored
         uint32_t v[32];
-        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
+        const bool ld_ok = RGG_BOUNDS_OK(tmem_cols_ok(tcol + cc, 32, kTmemCols), args.status);
+        if (ld_ok) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
         if (kEpi == kEpiSwiGLU) {
             // gate in columns [cc, cc+32), up in [kOutN + cc, kOutN + cc + 32)
             uint32_t u[32];
-            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kOutN + cc), u);
+            const bool ldu_ok = RGG_BOUNDS_OK(tmem_cols_ok(tcol + kOutN + cc, 32, kTmemCols), args.status);
+            if (ldu_ok) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kOutN + cc), u);
             tmem_ld_wait();
+            if (!ldu_ok)
+                for (int i = 0; i < 32; ++i) u[i] = 0u;
+            if (!ld_ok)
+                for (int i = 0; i < 32; ++i) v[i] = 0u;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 v[i] = __float_as_uint(silu_f32(__uint_as_float(v[i])) * __uint_as_float(u[i]));
         } else {
             tmem_ld_wait();
+            if (!ld_ok)
+                for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
         if constexpr (kFp8) {
             // dequantise: row scale of X times the expert's column scale of W
-            if (row_ok) {
+            if (row_ok && RGG_BOUNDS_OK(store_ok(row, c.col0 + cc, 0, row_lo, row_hi, N) && c.col0 + cc + 16 <= N,
+                                        args.status)) {
                 const float rs = __ldg(args.sx + c.row0 + r_local);
                 const float* swp = args.sw + static_cast<int64_t>(c.expert) * N + c.col0 + cc;
 #pragma unroll
@@ -298,14 +316,17 @@ __device__ __forceinline__ void epilogue_store_tile(const GemmArgs& args, const 
                 for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
                 __nv_bfloat16* dst = yrow + cc + 16 * h;
                 if (col + 16 <= N) {
-                    if (args.y_vec32) {
-                        st_global_v8(dst, w);
-                    } else {
-                        st_global_v4(dst, w[0], w[1], w[2], w[3]);
-                        st_global_v4(dst + 8, w[4], w[5], w[6], w[7]);
+                    if (RGG_BOUNDS_OK(store_ok(row, col, 16, row_lo, row_hi, N), args.status)) {
+                        if (args.y_vec32) {
+                            st_global_v8(dst, w);
+                        } else {
+                            st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                            st_global_v4(dst + 8, w[4], w[5], w[6], w[7]);
+                        }
                     }
                 } else if (col + 8 <= N) {
-                    st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                    if (RGG_BOUNDS_OK(store_ok(row, col, 8, row_lo, row_hi, N), args.status))
+                        st_global_v4(dst, w[0], w[1], w[2], w[3]);
                 }
             }
         }
@@ -342,6 +363,13 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     static_assert(BM / 4 <= 32, "one producer lane per group of four tile rows");
     constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;  // output columns per tile
     constexpr int kPanels = BN / Cfg::kPanelN;
+    constexpr int kElemBytes = kFp8 ? 1 : 2;
+    const int64_t kNw = (kEpi == kEpiSwiGLU) ? 2 * static_cast<int64_t>(args.N) : args.N;  // columns of W
+    (void)kNw;
+    // A plain tile loads only panels below N (tile_panels); the fused gate-up
+    // tile's last up panel of an expert's last N tile can start past column
+    // 2N, a box the copy zero-fills.
+    constexpr int64_t kWOverhang = (kEpi == kEpiSwiGLU) ? Cfg::kPanelN : 0;
     // Column of W read by B panel p of a tile whose first output column is col0.
     auto w_col = [&](int32_t col0, int p) -> int32_t {
         if (kEpi == kEpiSwiGLU)
@@ -379,7 +407,10 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     // S1: group offsets -> validated per-expert tile prefix.
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
         if (threadIdx.x == 0) atomicCAS(args.status, 0, kStatusBadOffsets);
-        if constexpr (kDyn) pdl_wait_prerequisites();
+        if constexpr (kDyn) {
+            if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);
+            pdl_wait_prerequisites();
+        }
         return;
     }
     ClassLists L;
@@ -392,6 +423,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
         L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E]};
         T = L.nP + L.nS;
         if (T == 0) {
+            if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);
             pdl_wait_prerequisites();
             return;
         }
@@ -520,13 +552,18 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
                     }
                     if (lane == 0) mbar_arrive_expect_tx(full_bar(st), tx_bytes);
                     __syncwarp();
-                    if (lane < groups)
+                    if (lane < groups &&
+                        RGG_BOUNDS_OK(x_box_ok(kb * Cfg::kKStage, tok[0], args.K, args.t_rows, kElemBytes) &&
+                                          x_box_ok(kb * Cfg::kKStage, tok[3], args.K, args.t_rows, kElemBytes),
+                                      args.status))
                         tma_gather4(a0 + st * sp.a_stage + 512u * lane, &tmap_x, full_bar(st), kb * Cfg::kKStage,
                                     tok[0], tok[1], tok[2], tok[3]);
                     if (lane == 0) {
 #pragma unroll
                         for (int p = 0; p < kPanels; ++p)
-                            if (p < np)
+                            if (p < np && RGG_BOUNDS_OK(w_box_ok(w_col(c.col0, p), kb * Cfg::kKStage, c.expert, kNw,
+                                                                 args.K, E, kElemBytes, kWOverhang),
+                                                        args.status))
                                 tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st),
                                             w_col(c.col0, p), kb * Cfg::kKStage, c.expert);
                     }
@@ -553,6 +590,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             uint32_t issued = 0;
             bool ok = true;
             auto produce = [&](const TileCoord& c) {
+                (void)RGG_BOUNDS_OK(tile_ok(c.expert, c.row0, c.rows, c.col0, s_off, E, args.N), args.status);
                 const bool half = runs_as_64_rows<BM>(args, c);
                 const int np = tile_panels<kPanels, Cfg::kPanelN, kEpi>(c.col0, args.N);
                 const uint32_t tx_bytes = (half ? 64u : static_cast<uint32_t>(BM)) * 128u + np * Cfg::kPanelB;
@@ -563,10 +601,14 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full_bar(st), tx_bytes);
-                    tma_load_2d(a0 + st * sp.a_stage, xmap, full_bar(st), kb * Cfg::kKStage, c.row0);
+                    if (RGG_BOUNDS_OK(x_box_ok(kb * Cfg::kKStage, c.row0, args.K, args.M_tot, kElemBytes),
+                                      args.status))
+                        tma_load_2d(a0 + st * sp.a_stage, xmap, full_bar(st), kb * Cfg::kKStage, c.row0);
 #pragma unroll
                     for (int p = 0; p < kPanels; ++p)
-                        if (p < np)
+                        if (p < np && RGG_BOUNDS_OK(w_box_ok(w_col(c.col0, p), kb * Cfg::kKStage, c.expert, kNw,
+                                                             args.K, E, kElemBytes, kWOverhang),
+                                                    args.status))
                             tma_load_3d(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_bar(st),
                                         w_col(c.col0, p), kb * Cfg::kKStage, c.expert);
                     ++issued;
@@ -701,7 +743,8 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             if (!ok) return false;
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            epilogue_store_tile<BN, kEpi, kFp8>(args, c, half, r_local, t_row, lane, cc0, true);
+            epilogue_store_tile<BN, kEpi, kFp8>(args, c, half, r_local, t_row, lane, cc0, true, s_off[c.expert],
+                                                s_off[c.expert + 1], static_cast<uint32_t>(acc * BN));
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));
@@ -731,7 +774,10 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     }
     // The mixed launch's 1-CTA kernel may start before the pair kernel ends;
     // it does not end before it, so the stream's later work sees both done.
-    if constexpr (kDyn) pdl_wait_prerequisites();
+    if constexpr (kDyn) {
+        if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);  // after the producer's last claim
+        pdl_wait_prerequisites();
+    }
 }
 
 }  // namespace rgg

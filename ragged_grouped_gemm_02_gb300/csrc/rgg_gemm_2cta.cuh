@@ -127,6 +127,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     // S1, identical in both CTAs, so every early exit below is pair-uniform.
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
         if (threadIdx.x == 0 && rank == 0) atomicCAS(args.status, 0, kStatusBadOffsets);
+        if constexpr (kDyn)
+            if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);
         return;
     }
     ClassLists L;
@@ -138,7 +140,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
         __syncthreads();
         L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E]};
         T = L.nP + L.nS;
-        if (T == 0) return;
+        if (T == 0) {
+            if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);
+            return;
+        }
     } else {
         if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
         __syncthreads();
@@ -222,6 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             uint32_t issued = 0;
             bool ok = true;
             auto produce = [&](const TileCoord& c) {
+                (void)RGG_BOUNDS_OK(tile_ok(c.expert, c.row0, c.rows, c.col0, s_off, E, args.N), args.status);
                 const bool half = half_tile(c);
                 const int32_t a_row = c.row0 + (half ? 64 : 128) * static_cast<int32_t>(rank);
                 const int ncols = pair_tile_cols<BN, kEpi>(c.col0, args.N);
@@ -239,10 +245,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                     }
                     const uint32_t full_leader = map_to_rank(full_bar(st), 0);
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(st), tx_bytes);
-                    tma_load_2d_pair(a0 + st * sp.a_stage, xmap, full_leader, kb * Cfg::kKStage, a_row);
+                    // the second CTA's rows may start past M_tot (a short tile at the end of X): the copy
+                    // zero-fills them, so the row check allows one tile of overhang
+                    if (RGG_BOUNDS_OK(x_box_ok(kb * Cfg::kKStage, a_row, args.K, args.M_tot + 128, 2), args.status))
+                        tma_load_2d_pair(a0 + st * sp.a_stage, xmap, full_leader, kb * Cfg::kKStage, a_row);
 #pragma unroll
                     for (int p = 0; p < Cfg::kPanels; ++p)
-                        if (p < np)
+                        if (p < np && RGG_BOUNDS_OK(w_box_ok(b_col + Cfg::kPanelN * p, kb * Cfg::kKStage, c.expert,
+                                                             kEpi == kEpiSwiGLU ? 2 * int64_t(args.N) : args.N,
+                                                             args.K, E, 2, Cfg::kPanelN),
+                                                    args.status))
                             tma_load_3d_pair(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_leader,
                                              b_col + Cfg::kPanelN * p, kb * Cfg::kKStage, c.expert);
                     ++issued;
@@ -401,7 +413,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             const int ncols = half ? tcols / 2 : tcols;
             const int cbase = half ? (q >> 1) * (tcols / 2) : 0;  // first tile column this warp holds
             const bool row_ok = r_local < c.rows;
-            __nv_bfloat16* yrow = args.Y + static_cast<int64_t>(c.row0 + r_local) * N + c.col0 + cbase;
+            const int64_t row = static_cast<int64_t>(c.row0) + r_local;
+            const int32_t row_lo = s_off[c.expert], row_hi = s_off[c.expert + 1];  // the debug build's row bounds
+            (void)row_lo;
+            (void)row_hi;
+            __nv_bfloat16* yrow = args.Y + row * N + c.col0 + cbase;
             constexpr int kParts = pair_epilogue_warps<kEpi>() / 4;  // warps per lane quadrant
             const int pc = ncols / kParts;                                // columns each of them writes
             const int c0 = ((warp - 2) >> 2) * pc;
@@ -409,17 +425,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             for (int cc = c0; cc < c0 + pc; cc += 32) {
                 if (c.col0 + cbase + cc >= N) break;  // columns past N: not computed, not stored
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
+                const uint32_t tcol = static_cast<uint32_t>(acc * BN + cc);
+                const bool ld_ok = RGG_BOUNDS_OK(tmem_cols_ok(tcol, 32, Cfg::kTmemCols), args.status);
+                if (ld_ok) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
                 if constexpr (kEpi == kEpiSwiGLU) {
                     // gate in columns [cc, cc+32), up in [kOutN + cc, kOutN + cc + 32)
                     uint32_t u[32];
-                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kOutN + cc), u);
+                    const bool ldu_ok = RGG_BOUNDS_OK(tmem_cols_ok(tcol + kOutN, 32, Cfg::kTmemCols), args.status);
+                    if (ldu_ok) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kOutN + cc), u);
                     tmem_ld_wait();
+                    if (!ldu_ok)
+                        for (int i = 0; i < 32; ++i) u[i] = 0u;
+                    if (!ld_ok)
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[i] = __float_as_uint(silu_f32(__uint_as_float(v[i])) * __uint_as_float(u[i]));
                 } else {
                     tmem_ld_wait();
+                    if (!ld_ok)
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
                 }
                 if (row_ok) {
 #pragma unroll
@@ -430,14 +455,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                         for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
                         __nv_bfloat16* dst = yrow + cc + 16 * h;
                         if (col + 16 <= N) {
-                            if (args.y_vec32) {
-                                st_global_v8(dst, w);
-                            } else {
-                                st_global_v4(dst, w[0], w[1], w[2], w[3]);
-                                st_global_v4(dst + 8, w[4], w[5], w[6], w[7]);
+                            if (RGG_BOUNDS_OK(store_ok(row, col, 16, row_lo, row_hi, N), args.status)) {
+                                if (args.y_vec32) {
+                                    st_global_v8(dst, w);
+                                } else {
+                                    st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                                    st_global_v4(dst + 8, w[4], w[5], w[6], w[7]);
+                                }
                             }
                         } else if (col + 8 <= N) {
-                            st_global_v4(dst, w[0], w[1], w[2], w[3]);
+                            if (RGG_BOUNDS_OK(store_ok(row, col, 8, row_lo, row_hi, N), args.status))
+                                st_global_v4(dst, w[0], w[1], w[2], w[3]);
                         }
                     }
                 }
@@ -469,6 +497,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
         tc_fence_after_sync();
         tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
     }
+    if constexpr (kDyn)
+        if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);  // after the leader's last claim
 }
 
 }  // namespace rgg

@@ -28,7 +28,13 @@
 // window of the lists: the M tiles that read one weight panel run side by
 // side, so the panel is read from HBM about once however the SMs drift.
 //
-// The counters (two int32) are zeroed before each launch by the host.
+// The counters need no reset from the host between launches: sched[2]
+// counts the CTAs of both kernels that have finished, and the last one
+// (sched[2] reaching sched_total - 1) sets all three back to zero.  Every CTA
+// takes part exactly once, on every exit path (a bounded wait that timed out
+// and bad offsets included), after its last claim; a launch of the next call
+// on the stream starts after both kernels end, so it finds the counters at
+// zero.  (The host zeroes them once, with the handle's device word.)
 #pragma once
 
 #include <cstdint>
@@ -55,6 +61,18 @@ struct ClassLists {
         return decode_tile(s_off, s_preS, E, 128, kMixedBN, nN, t, true);
     }
 };
+
+// One CTA of a mixed launch is done with the counters (thread 0, once per
+// CTA, after the CTA's last claim).
+__device__ __forceinline__ void sched_cta_done(int32_t* sched, int32_t sched_total) {
+    __threadfence();  // this CTA's claims before its count
+    if (atomicAdd(sched + 2, 1) == sched_total - 1) {
+        __threadfence();  // every other CTA's claims and counts before the reset
+        atomicExch(sched + 0, 0);
+        atomicExch(sched + 1, 0);
+        atomicExch(sched + 2, 0);
+    }
+}
 
 __device__ __forceinline__ TileCoord sentinel_tile() {
     TileCoord c;

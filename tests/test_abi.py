@@ -42,6 +42,79 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), "librgg.so does not export %s" % name
 
 
+def test_debug_library_exports_every_declared_symbol(lib):
+    # librgg_debug.so: the same ABI with every device access bounds-checked
+    dbg = rgg.open_library(rgg.debug_library_path())
+    for name in _declared_functions():
+        assert hasattr(dbg, name), "librgg_debug.so does not export %s" % name
+    assert dbg.rgg_status_string(rgg.RGG_ERR_DEVICE_BOUNDS).decode().startswith("RGG_ERR_DEVICE_BOUNDS")
+
+
+CHECKS_PROGRAM = r"""
+#include <cstdio>
+#include "rgg_checks.cuh"
+using namespace rgg;
+#define EXPECT(c) do { if (!(c)) { std::printf("failed: %s (line %d)\n", #c, __LINE__); return 1; } } while (0)
+int main() {
+    // X box: K coordinate inside [0, K) on a 16-byte boundary, first row inside [0, rows)
+    EXPECT(x_box_ok(0, 0, 264, 10, 2));
+    EXPECT(x_box_ok(256, 9, 264, 10, 2));
+    EXPECT(!x_box_ok(264, 0, 264, 10, 2));
+    EXPECT(!x_box_ok(4, 0, 264, 10, 2));      // 8 bytes: not a 16-byte boundary
+    EXPECT(x_box_ok(16, 0, 272, 10, 1));      // FP8: 16 elements
+    EXPECT(!x_box_ok(8, 0, 272, 10, 1));
+    EXPECT(!x_box_ok(0, 10, 264, 10, 2));
+    EXPECT(!x_box_ok(0, -1, 264, 10, 2));
+    // W box: column, K coordinate, expert
+    EXPECT(w_box_ok(512, 192, 3, 520, 264, 4, 2));
+    EXPECT(!w_box_ok(520, 0, 0, 520, 264, 4, 2));
+    EXPECT(!w_box_ok(4, 0, 0, 520, 264, 4, 2));
+    EXPECT(!w_box_ok(0, 0, 4, 520, 264, 4, 2));
+    EXPECT(!w_box_ok(0, 0, -1, 520, 264, 4, 2));
+    EXPECT(w_box_ok(576, 0, 0, 520, 264, 4, 2, 64));   // a pair's second half past the last column
+    EXPECT(!w_box_ok(584, 0, 0, 520, 264, 4, 2, 64));
+    // stores: the expert's rows, columns inside [0, N)
+    EXPECT(store_ok(37, 504, 16, 37, 38, 520));
+    EXPECT(!store_ok(37, 512, 16, 37, 38, 520));
+    EXPECT(store_ok(37, 512, 8, 37, 38, 520));
+    EXPECT(!store_ok(38, 0, 8, 37, 38, 520));
+    EXPECT(!store_ok(36, 0, 8, 37, 38, 520));
+    EXPECT(!store_ok(37, -16, 16, 37, 38, 520));
+    // TMEM columns
+    EXPECT(tmem_cols_ok(480, 32, 512));
+    EXPECT(!tmem_cols_ok(481, 32, 512));
+    // tile descriptors against the offsets {0, 0, 37, 101}
+    const int32_t off[4] = {0, 0, 37, 101};
+    EXPECT(tile_ok(1, 0, 37, 0, off, 3, 520));
+    EXPECT(tile_ok(2, 37, 64, 512, off, 3, 520));
+    EXPECT(!tile_ok(0, 0, 1, 0, off, 3, 520));    // an empty expert has no rows
+    EXPECT(!tile_ok(2, 37, 65, 0, off, 3, 520));  // past the expert's last row
+    EXPECT(!tile_ok(2, 36, 1, 0, off, 3, 520));   // before its first
+    EXPECT(!tile_ok(2, 37, 1, 520, off, 3, 520));
+    EXPECT(!tile_ok(3, 0, 1, 0, off, 3, 520));
+    EXPECT(!tile_ok(-1, 0, 1, 0, off, 3, 520));
+    std::printf("ok\n");
+    return 0;
+}
+"""
+
+
+def test_bounds_check_predicates_on_the_host(tmp_path):
+    # the debug build's predicates are plain host/device functions: their arithmetic is checked here
+    import shutil
+    import subprocess
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("no C++ compiler")
+    (tmp_path / "checks.cc").write_text(CHECKS_PROGRAM)
+    csrc = os.path.join(ROOT, "ragged_grouped_gemm_02_gb300", "csrc")
+    r = subprocess.run([gxx, "-std=c++17", "-Wall", "-Werror", "-I", csrc, str(tmp_path / "checks.cc"), "-o",
+                        str(tmp_path / "checks")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(tmp_path / "checks")], capture_output=True, text=True, timeout=30)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout
+
+
 def test_library_has_no_runtime_cuda_dependency():
     # the CUDA runtime is linked statically; the library loads on a machine
     # without a GPU or a driver and reaches the driver only when called
@@ -51,7 +124,7 @@ def test_library_has_no_runtime_cuda_dependency():
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         s = rgg.rgg_status_string(code)
         assert s.startswith("RGG_")
     assert rgg.rgg_status_string(99) == "unknown rgg_status"

@@ -88,7 +88,7 @@ def test_random_inputs_with_k_and_n_tails(opts):
 
 
 def test_offsets_that_leave_rows_uncovered():
-    counts = [300, 0, 40, 600, 7]
+    counts = [300, 0, 40, 600, 37]
     inp = wl.make_custom(counts, K=64, N=256, seed=164, integer_valued=True, spare_rows=0)
     off = inp.offsets.copy()
     M = int(off[-1])
