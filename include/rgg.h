@@ -297,12 +297,14 @@ const char* rgg_last_cuda_error(void);
  * word.  This call takes no handle and allocates nothing: no cudaMalloc, no
  * cudaFree, no allocating library routine.
  *
- * Scratch: the kernel's only scratch (its 4-byte status word) lives in a
- * file-scope device array of 256 bytes that every GPU which loads librgg.so
- * holds until the process exits.  The scratch need does not grow with the
- * problem, so only the kernel's own limits bound a call (1 <= E <= 4096,
- * 0 <= M_tot < 2^31, K and N multiples of 8): other sizes are rejected with
- * RGG_ERR_INVALID_ARG or RGG_ERR_UNSUPPORTED before anything is launched.
+ * Scratch: the kernels' only scratch -- the 4-byte status word and, when the
+ * plan is the mixed launch, three int32 tile counters that the launch leaves
+ * at zero when it ends -- lives in a file-scope device array of 256 bytes that
+ * every GPU which loads librgg.so holds until the process exits.  The scratch
+ * need does not grow with the problem, so only the kernel's own limits bound
+ * a call (1 <= E <= 4096, 0 <= M_tot < 2^31, K and N multiples of 8): other
+ * sizes are rejected with RGG_ERR_INVALID_ARG or RGG_ERR_UNSUPPORTED before
+ * anything is launched.
  *
  * The call runs on the current CUDA device.  Its first call on a device sets
  * up that device (it looks up the array's device address with
@@ -313,8 +315,8 @@ const char* rgg_last_cuda_error(void);
  * and, when status_out is not NULL, copies the final status word into
  * *status_out (device memory or pinned host memory, int32): RGG_OK,
  * RGG_ERR_BAD_OFFSETS or RGG_ERR_DEVICE_TIMEOUT, valid once the stream has
- * reached that point.  All calls share the one status word, so calls that
- * overlap on the GPU (other streams, other threads) race on it.
+ * reached that point.  All calls share the one array, so calls that overlap
+ * on the GPU (other streams, other threads) race on it.
  *
  * Arguments, layouts and ownership as for rgg_grouped_gemm; asynchronous on
  * `stream` (a cudaStream_t, NULL = legacy default stream).

@@ -327,6 +327,18 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
         if (skewed) walk = 3;
     }
     if (walk == 0 && !keep_list && !skewed && avg >= 3.0 * bm) walk = 4;
+    // Large experts on CTA pairs, walked N-major: the mixed launch instead
+    // (its pair kernel; the 1-CTA kernel only if host counts show small
+    // experts), whose tiles are claimed in list order from a device counter.
+    // The M tiles that share a weight panel then run side by side whatever
+    // the drift between SMs: measured on prefill (E = 32, ~1 024 rows per
+    // expert, K = 6144), DRAM reads of 2.75-2.92 GB per launch against 2.07 GB
+    // (2.28 GB algorithmic in all), 1 444-1 466 -> 1 494-1 507 TFLOP/s.  Where
+    // experts fill only one or two M tiles the static walk stays ahead (uniform
+    // 256 rows per expert: 1 093-1 108 static, 1 048 claimed).
+    if (want_mixed == 0 && kind == 0 && pair && bn == 256 && walk == 4 && want_walk == 0 && want_tail != -1 &&
+        (want_stages == 0))
+        return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out);
     const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;  // persistent CTAs or CTA pairs
 
     const int64_t max_tiles = tile_bound(E, M_tot, N, bm, bn);
@@ -584,6 +596,8 @@ rgg_status host_grouped_gemm(int num_sms, int smem_optin, int32_t* status, const
         // start at zero and the launch's last CTA sets them back to zero
         a.sched = status + 16;
         a.sched_total = p.grid + p.single_grid;
+        a.sched_pairs = p.grid / 2;
+        a.sched_singles = p.single_grid;
         a.pair_min_rows = p.pair_min_rows;
         GemmArgs as = a;
         as.stages = p.single_stages;

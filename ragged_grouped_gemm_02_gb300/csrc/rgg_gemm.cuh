@@ -81,6 +81,8 @@ struct GemmArgs {
     // of the sched_total CTAs of both kernels (the last one resets all three).
     int32_t* sched = nullptr;
     int32_t sched_total = 0;
+    int32_t sched_pairs = 0;    // clusters of the pair kernel (each takes its first class-P tile without a claim)
+    int32_t sched_singles = 0;  // CTAs of the 1-CTA kernel (each takes its first class-S tile without a claim)
     int32_t pair_min_rows = kPairMinRowsDefault;
 };
 
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             if constexpr (kDyn) {
                 // claim, hand the descriptor to the consumers, load the tile
                 TileClaimer cl;
-                cl.init(args.sched, L, false);
+                cl.init(args.sched, L, false, blockIdx.x, args.sched_pairs, args.sched_singles);
                 int qs = 0;
                 uint32_t qp = 0;
                 TileCoord c = cl.next(L);

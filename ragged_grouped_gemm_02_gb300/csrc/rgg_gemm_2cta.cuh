@@ -270,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                 if (rank == 0) {
                     // claim, write the descriptor into both CTAs' queues, load the leader's half
                     TileClaimer cl;
-                    cl.init(args.sched, L, true);
+                    cl.init(args.sched, L, true, static_cast<int32_t>(pair), args.sched_pairs, args.sched_singles);
                     TileCoord c = cl.next(L);
                     while (ok) {
                         if (!pair_wait_or_abort<true>(qempty_bar(qs), qp ^ 1u, abort_flag, peer_flag, args.status,

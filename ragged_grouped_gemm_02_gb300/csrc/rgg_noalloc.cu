@@ -7,9 +7,9 @@
 // memory is entirely owned by a pool allocator that other code may not go
 // around.  rgg_grouped_gemm needs a handle, and rgg_create allocates the
 // handle's device status word with cudaMalloc.  This entry point needs no
-// handle: the only scratch the kernel uses beyond its inputs and outputs --
-// the status word that records bad offsets or a timed-out wait -- lives in a
-// file-scope device array instead.
+// handle: the only scratch the kernels use beyond their inputs and outputs --
+// the status word that records bad offsets or a timed-out wait, and the mixed
+// launch's tile counters -- lives in a file-scope device array instead.
 //
 // The array is small and fixed: every GPU that loads librgg.so holds it until
 // the process exits.  All calls share it, so calls that run at the same time
@@ -26,8 +26,10 @@
 
 namespace {
 
-// 256 bytes of device scratch per GPU.  The kernel uses the first int32 as
-// its status word (zero = OK); the rest is reserved.
+// 256 bytes of device scratch per GPU.  The kernels use the first int32 as
+// the status word (zero = OK) and, for the mixed launch, the three int32 at
+// byte 64 as its tile counters (zero here at load, and zero again after every
+// mixed launch); the rest is reserved.
 constexpr int kNoallocScratchWords = 64;
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoallocScratchWords];
 
@@ -85,10 +87,10 @@ extern "C" rgg_status rgg_grouped_gemm_noalloc(const void* X, const void* W, con
     rgg_status s = rgg::host_check_gemm_args(X, W, group_offsets, Y, E, M_tot, K, N);
     if (s != RGG_OK) return s;
     if (status_out && (reinterpret_cast<uintptr_t>(status_out) % 4) != 0) return RGG_ERR_INVALID_ARG;
-    // The kernel's scratch need does not grow with the problem: one status
-    // word.  Sizes the kernel itself cannot take (E > 4096, M_tot >= 2^31,
-    // K or N not a multiple of 8) were rejected above.
-    if (kStatusWordBytes > sizeof(g_noalloc_scratch)) {
+    // The kernels' scratch need does not grow with the problem: the status
+    // word and three counters.  Sizes the kernels cannot take (E > 4096,
+    // M_tot >= 2^31, K or N not a multiple of 8) were rejected above.
+    if (kStatusWordBytes > sizeof(g_noalloc_scratch) || 19 * sizeof(int32_t) > sizeof(g_noalloc_scratch)) {
         rgg::host_set_last_error("rgg_grouped_gemm_noalloc: request needs more than the 256-byte scratch");
         return RGG_ERR_UNSUPPORTED;
     }

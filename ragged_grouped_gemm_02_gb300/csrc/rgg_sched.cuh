@@ -83,39 +83,53 @@ __device__ __forceinline__ TileCoord sentinel_tile() {
     return c;
 }
 
-// Claims of one CTA (the pair kernel: of the leader CTA).  `own_first_p`:
-// the pair kernel claims class P first, the 1-CTA kernel class S first.
-// `split_p`: class-P tiles are handed out as up to two 128-row tiles (the
-// 1-CTA kernel).  prefetch() issues the atomic of the next claim early so its
-// latency hides under the current tile's loads; next() resolves it.
+// Claims of one CTA (the pair kernel: of the leader CTA).  The pair kernel
+// claims class P first, the 1-CTA kernel class S first; `split_p` (the 1-CTA
+// kernel) hands class-P tiles out as up to two 128-row tiles.  The first
+// `off_p` tiles of class P belong to the pair kernel's clusters and the first
+// `off_s` tiles of class S to the 1-CTA kernel's CTAs, one each, taken without
+// an atomic (cluster or CTA k takes tile k of its own class), so no CTA waits
+// for a counter before its first loads; claimed indices start after them.
+// prefetch() issues the atomic of the next claim early so its latency hides
+// under the current tile's loads; next() resolves it.
 struct TileClaimer {
     int32_t* ctr_first;
     int32_t* ctr_second;
     int32_t n_first, n_second;
+    int32_t off_first, off_second;
     bool first_is_p, split_p;
     int phase;          // 0: first class, 1: second class, 2: done
+    int32_t own;        // this claimer's own first tile of its class, or -1 once taken
     bool has_half;      // the second 128-row half of a split class-P tile is due
     TileCoord half;
     bool ticket_valid;
     int32_t ticket;
 
-    __device__ __forceinline__ void init(int32_t* sched, const ClassLists& L, bool pair_kernel) {
+    __device__ __forceinline__ void init(int32_t* sched, const ClassLists& L, bool pair_kernel, int32_t own_index,
+                                         int32_t off_p, int32_t off_s) {
         first_is_p = pair_kernel;
         split_p = !pair_kernel;
         ctr_first = pair_kernel ? sched : sched + 1;
         ctr_second = pair_kernel ? sched + 1 : sched;
         n_first = pair_kernel ? L.nP : L.nS;
         n_second = pair_kernel ? L.nS : L.nP;
+        off_first = pair_kernel ? off_p : off_s;
+        off_second = pair_kernel ? off_s : off_p;
         phase = 0;
+        own = own_index;
         has_half = false;
         ticket_valid = false;
         ticket = 0;
     }
 
+    __device__ __forceinline__ int32_t claim() {
+        return phase == 0 ? atomicAdd(ctr_first, 1) + off_first : atomicAdd(ctr_second, 1) + off_second;
+    }
+
     __device__ __forceinline__ void prefetch() {
         ticket_valid = false;
-        if (has_half || phase >= 2) return;
-        ticket = atomicAdd(phase == 0 ? ctr_first : ctr_second, 1);
+        if (has_half || phase >= 2 || own >= 0) return;
+        ticket = claim();
         ticket_valid = true;
     }
 
@@ -125,13 +139,20 @@ struct TileClaimer {
             return half;
         }
         while (phase < 2) {
-            const int32_t t = ticket_valid ? ticket : atomicAdd(phase == 0 ? ctr_first : ctr_second, 1);
-            ticket_valid = false;
-            const bool is_p = (phase == 0) == first_is_p;
-            if (t >= (phase == 0 ? n_first : n_second)) {
-                ++phase;
-                continue;
+            int32_t t;
+            if (own >= 0) {
+                t = own;
+                own = -1;
+                if (t >= n_first) continue;  // no own tile: claim (indices past off_first)
+            } else {
+                t = ticket_valid ? ticket : claim();
+                ticket_valid = false;
+                if (t >= (phase == 0 ? n_first : n_second)) {
+                    ++phase;
+                    continue;
+                }
             }
+            const bool is_p = (phase == 0) == first_is_p;
             TileCoord c = is_p ? L.decode_p(t) : L.decode_s(t);
             if (is_p && split_p && c.rows > 128) {
                 half = c;

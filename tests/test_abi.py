@@ -210,11 +210,15 @@ def test_plan_grid_never_exceeds_tiles_or_sms(lib):
 
 def test_plan_walk_order_choice(lib):
     from ragged_grouped_gemm_02_gb300 import workloads as wl
-    # experts of three M tiles or more: each expert's tiles walked N-major
+    # experts of three M tiles or more on CTA pairs: the mixed launch's claims in list order, each
+    # expert N-major (the static walk order 4 when the mixed launch is off or cannot run)
     p = rgg.rgg_plan(32, 32768, 6144, 4096, host_counts=wl.workload_counts("prefill"))
-    assert p["walk_order"] == 4
+    assert p["mixed"] == 1 and (p["grid"], p["single_grid"]) == (152, 0)
+    assert rgg.rgg_plan(32, 32768, 6144, 4096)["mixed"] == 1  # balanced estimate without counts
+    for kw in (dict(mixed=-1), dict(stages=6), dict(tail64=-1)):
+        p = rgg.rgg_plan(32, 32768, 6144, 4096, host_counts=wl.workload_counts("prefill"), **kw)
+        assert p["mixed"] == 0 and p["walk_order"] == 4, kw
     assert rgg.rgg_plan(32, 32768, 6144, 4096, host_counts=wl.workload_counts("prefill"), op="fp8")["walk_order"] == 4
-    assert rgg.rgg_plan(32, 32768, 6144, 4096)["walk_order"] == 4  # balanced estimate without counts
     # one or two M tiles per expert: list order
     assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("uniform"))["walk_order"] == 0
     assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("uniform"), op="fp8")["walk_order"] == 0
