@@ -110,8 +110,11 @@ typedef struct rgg_options {
                                     tails as 64-row MMAs), as two kernels on disjoint SMs that claim tiles
                                     from two device counters and take each other's tiles when their own
                                     class runs out.  The classes are formed on the device from the offsets.
-                                    0 = auto (the planner's choice), -1 = off.  On: bm and bn must be 0 or
-                                    256, tail64 must not be -1, walk_order is not used. */
+                                    2 = the same two kernels without claims: each walks its own class in a
+                                    fixed order (and the other class too when the other kernel has no
+                                    SMs), so the split of the SMs decides the balance.  0 = auto (the
+                                    planner's choice), -1 = off.  On: bm and bn must be 0 or 256, tail64
+                                    must not be -1, walk_order is not used. */
     int mixed_pair_sms;          /* mixed launch: SMs given to the pair kernel (even; the 1-CTA kernel gets
                                     the rest).  0 = split by the estimated work of each class (from
                                     host_counts, else balanced experts), -1 = no pair kernel. */
@@ -136,8 +139,9 @@ typedef struct rgg_plan_info {
     int64_t workspace_bytes;     /* gather ops: the workspace the two-pass mode needs when it is asked
                                     for, or when the automatic choice prefers it (it runs only with a
                                     caller workspace); else 0 */
-    int mixed;                   /* 1 for the mixed launch: then bm, bn, stages, grid, smem_bytes describe
-                                    its pair kernel (grid 0: none) and the next three its 1-CTA kernel */
+    int mixed;                   /* 1 (claims) or 2 (fixed walks) for the mixed launch: then bm, bn, stages,
+                                    grid, smem_bytes describe its pair kernel (grid 0: none) and the next
+                                    three its 1-CTA kernel */
     int single_grid;             /* mixed launch: CTAs of the 1-CTA kernel (0: none) */
     int single_stages;           /* mixed launch: ring depth of the 1-CTA kernel */
     int single_smem_bytes;       /* mixed launch: dynamic shared memory per CTA of the 1-CTA kernel */

@@ -118,10 +118,17 @@ int stages_that_fit(int smem_optin, uint32_t fixed, int64_t per_stage) {
 // into shared memory per tile (the quantity that set the pace of both tile
 // shapes on a GB300): (128 + cols/2) per CTA of a pair tile (64 + cols/2 for
 // a tile of <= 128 rows), 128 + cols per 1-CTA tile (64 + cols for <= 64
-// rows).  The kernels steal each other's tiles when their own class runs out,
-// so an inexact split costs only the less efficient shape on the stolen
-// tiles.  Without host counts the experts are taken as balanced.
-rgg_status plan_mixed(int grid_cap, int smem_optin, int E, int64_t M_tot, int N, const rgg_options* opt, Plan* out) {
+// rows), the pair tiles' count weighted by kPairCostFactor: on the skewed
+// 16k workload a pair tile's unit took 1.12 times a 1-CTA tile's (per-CTA
+// traces: 12.8 SM-us per 512 units against 8.6 per 384), and the split it
+// gives (88 of 152 SMs on pairs) was the measured best, 906 TFLOP/s (84: 876,
+// 80: 872, 92: 882, 100: 824).  With claims the kernels steal each other's
+// tiles when their own class runs out, so an inexact split costs only the
+// less efficient shape on the stolen tiles; the fixed walks depend on it.
+// Without host counts the experts are taken as balanced.
+constexpr double kPairCostFactor = 1.12;
+rgg_status plan_mixed(int grid_cap, int smem_optin, int E, int64_t M_tot, int N, const rgg_options* opt, Plan* out,
+                      int mode) {
     const int want_bm = opt ? opt->bm : 0;
     const int want_bn = opt ? opt->bn : 0;
     const int want_tail = opt ? opt->tail64 : 0;
@@ -160,6 +167,7 @@ rgg_status plan_mixed(int grid_cap, int smem_optin, int E, int64_t M_tot, int N,
         } else {
             add_expert(M_tot / E, static_cast<double>(E));
         }
+        cost_p *= kPairCostFactor;
         if (cost_p <= 0.0) {
             pair_sms = 0;
         } else if (cost_s <= 0.0) {
@@ -195,7 +203,7 @@ rgg_status plan_mixed(int grid_cap, int smem_optin, int E, int64_t M_tot, int N,
     out->max_tiles = tile_bound(E, M_tot, N, 128, rgg::kMixedBN);
     out->tail64 = 1;
     out->walk_order = 0;
-    out->mixed = 1;
+    out->mixed = mode;
     out->single_grid = single;
     out->single_stages = st_s;
     out->single_smem = smem_s;
@@ -239,10 +247,10 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (want_walk == 3 && E > rgg::kMaxSortedExperts) return RGG_ERR_UNSUPPORTED;
     int grid_cap = max_ctas > 0 ? std::min(max_ctas, num_sms) : num_sms;
     const int want_mixed = opt ? opt->mixed : 0;
-    if (want_mixed < -1 || want_mixed > 1 || (opt && opt->pair_min_rows < 0)) return RGG_ERR_INVALID_ARG;
-    if (want_mixed == 1) {
+    if (want_mixed < -1 || want_mixed > 2 || (opt && opt->pair_min_rows < 0)) return RGG_ERR_INVALID_ARG;
+    if (want_mixed >= 1) {
         if (kind != 0) return RGG_ERR_UNSUPPORTED;  // the plain bf16 GEMM only
-        return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out);
+        return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out, want_mixed);
     }
 
     // Per-expert M tiles at each BM: exact with host counts, else the
@@ -338,7 +346,21 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     // 256 rows per expert: 1 093-1 108 static, 1 048 claimed).
     if (want_mixed == 0 && kind == 0 && pair && bn == 256 && walk == 4 && want_walk == 0 && want_tail != -1 &&
         (want_stages == 0))
-        return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out);
+        return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out, 1);
+    // A strong skew (host counts: the largest expert above four times the
+    // mean) over experts that fill 128-row tiles: the large experts on CTA
+    // pairs beside the small ones on single CTAs, each kernel walking its own
+    // class (measured on the skewed 16k workload: 855-868 TFLOP/s for the
+    // size-sorted 128 x 256 walk, 906 for the mixed launch with fixed walks,
+    // 841 with claims, whose descriptor queue costs a few microseconds).
+    if (want_mixed == 0 && kind == 0 && skewed && bm == 128 && want_bm == 0 && (want_bn == 0 || want_bn == 256) &&
+        want_walk == 0 && want_tail != -1 && want_stages == 0) {
+        Plan mp;
+        if (plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, &mp, 2) == RGG_OK && mp.grid > 0 && mp.single_grid > 0) {
+            *out = mp;
+            return RGG_OK;
+        }
+    }
     const int units = pair ? std::max(1, grid_cap / 2) : grid_cap;  // persistent CTAs or CTA pairs
 
     const int64_t max_tiles = tile_bound(E, M_tot, N, bm, bn);
@@ -598,6 +620,7 @@ rgg_status host_grouped_gemm(int num_sms, int smem_optin, int32_t* status, const
         a.sched_total = p.grid + p.single_grid;
         a.sched_pairs = p.grid / 2;
         a.sched_singles = p.single_grid;
+        a.sched_claims = (p.mixed == 1) ? 1 : 0;
         a.pair_min_rows = p.pair_min_rows;
         GemmArgs as = a;
         as.stages = p.single_stages;

@@ -83,6 +83,7 @@ struct GemmArgs {
     int32_t sched_total = 0;
     int32_t sched_pairs = 0;    // clusters of the pair kernel (each takes its first class-P tile without a claim)
     int32_t sched_singles = 0;  // CTAs of the 1-CTA kernel (each takes its first class-S tile without a claim)
+    int32_t sched_claims = 1;   // 0: each kernel walks its own class statically (no counters, no queue)
     int32_t pair_min_rows = kPairMinRowsDefault;
 };
 
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
         if (threadIdx.x == 0) atomicCAS(args.status, 0, kStatusBadOffsets);
         if constexpr (kDyn) {
-            if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);
+            if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);
             pdl_wait_prerequisites();
         }
         return;
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
         L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E]};
         T = L.nP + L.nS;
         if (T == 0) {
-            if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);
+            if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);
             pdl_wait_prerequisites();
             return;
         }
@@ -620,7 +621,14 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
                     }
                 }
             };
-            if constexpr (kDyn) {
+            if (kDyn && !args.sched_claims) {
+                ClassWalk cw;
+                cw.init(L, false, args.sched_pairs > 0);
+                for (int32_t p = blockIdx.x; ok && p < cw.n_positions; p += gridDim.x) {
+                    const TileCoord c = cw.at(L, p);
+                    if (c.rows > 0) produce(c);
+                }
+            } else if constexpr (kDyn) {
                 // claim, hand the descriptor to the consumers, load the tile
                 TileClaimer cl;
                 cl.init(args.sched, L, false, blockIdx.x, args.sched_pairs, args.sched_singles);
@@ -704,7 +712,14 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
                     acc_ph ^= 1u;
                 }
             };
-            if constexpr (kDyn) {
+            if (kDyn && !args.sched_claims) {
+                ClassWalk cw;
+                cw.init(L, false, args.sched_pairs > 0);
+                for (int32_t p = blockIdx.x; ok && p < cw.n_positions; p += gridDim.x) {
+                    const TileCoord c = cw.at(L, p);
+                    if (c.rows > 0) mma_tile(c);
+                }
+            } else if constexpr (kDyn) {
                 int qs = 0;
                 uint32_t qp = 0;
                 TileCoord c;
@@ -756,7 +771,14 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             }
             return true;
         };
-        if constexpr (kDyn) {
+        if (kDyn && !args.sched_claims) {
+            ClassWalk cw;
+            cw.init(L, false, args.sched_pairs > 0);
+            for (int32_t p = blockIdx.x; p < cw.n_positions; p += gridDim.x) {
+                const TileCoord c = cw.at(L, p);
+                if (c.rows > 0 && !epi_tile(c)) break;
+            }
+        } else if constexpr (kDyn) {
             int qs = 0;
             uint32_t qp = 0;
             TileCoord c;
@@ -777,7 +799,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     // The mixed launch's 1-CTA kernel may start before the pair kernel ends;
     // it does not end before it, so the stream's later work sees both done.
     if constexpr (kDyn) {
-        if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);  // after the producer's last claim
+        if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);  // after the producer's last claim
         pdl_wait_prerequisites();
     }
 }

@@ -128,7 +128,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {
         if (threadIdx.x == 0 && rank == 0) atomicCAS(args.status, 0, kStatusBadOffsets);
         if constexpr (kDyn)
-            if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);
+            if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);
         return;
     }
     ClassLists L;
@@ -141,7 +141,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
         L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E]};
         T = L.nP + L.nS;
         if (T == 0) {
-            if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);
+            if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);
             return;
         }
     } else {
@@ -264,7 +264,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                     }
                 }
             };
-            if constexpr (kDyn) {
+            if (kDyn && !args.sched_claims) {
+                ClassWalk cw;
+                cw.init(L, true, args.sched_singles > 0);
+                for (int32_t p = pair; ok && p < cw.n_positions; p += npairs) produce(cw.at(L, p));
+            } else if constexpr (kDyn) {
                 int qs = 0;
                 uint32_t qp = 0;
                 if (rank == 0) {
@@ -367,7 +371,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                     acc_ph ^= 1u;
                 }
             };
-            if constexpr (kDyn) {
+            if (kDyn && !args.sched_claims) {
+                ClassWalk cw;
+                cw.init(L, true, args.sched_singles > 0);
+                for (int32_t p = pair; ok && p < cw.n_positions; p += npairs) mma_tile(cw.at(L, p));
+            } else if constexpr (kDyn) {
                 int qs = 0;
                 uint32_t qp = 0;
                 TileCoord c;
@@ -479,7 +487,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             }
             return true;
         };
-        if constexpr (kDyn) {
+        if (kDyn && !args.sched_claims) {
+            ClassWalk cw;
+            cw.init(L, true, args.sched_singles > 0);
+            for (int32_t p = pair; p < cw.n_positions; p += npairs)
+                if (!epi_tile(cw.at(L, p))) break;
+        } else if constexpr (kDyn) {
             int qs = 0;
             uint32_t qp = 0;
             TileCoord c;
@@ -498,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
         tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
     }
     if constexpr (kDyn)
-        if (threadIdx.x == 0) sched_cta_done(args.sched, args.sched_total);  // after the leader's last claim
+        if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);  // after the leader's last claim
 }
 
 }  // namespace rgg

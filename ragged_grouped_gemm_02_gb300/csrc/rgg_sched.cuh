@@ -28,6 +28,11 @@
 // window of the lists: the M tiles that read one weight panel run side by
 // side, so the panel is read from HBM about once however the SMs drift.
 //
+// Without claims (GemmArgs::sched_claims = 0) each kernel walks its own
+// class statically instead (ClassWalk), with no counters and no descriptor
+// queue; a kernel whose partner has no CTAs walks the other class too, so the
+// result never depends on how the SMs were split.
+//
 // The counters need no reset from the host between launches: sched[2]
 // counts the CTAs of both kernels that have finished, and the last one
 // (sched[2] reaching sched_total - 1) sets all three back to zero.  Every CTA
@@ -73,6 +78,38 @@ __device__ __forceinline__ void sched_cta_done(int32_t* sched, int32_t sched_tot
         atomicExch(sched + 2, 0);
     }
 }
+
+// Static walk over a kernel's share of the two classes (the launch without
+// claims): positions [0, n_own) are the kernel's own class; when the other
+// kernel has no CTAs, the other class follows (on the 1-CTA kernel each
+// class-P tile as two positions, its two 128-row halves; an empty second half
+// has rows <= 0 and is skipped by every role alike).  CTA or cluster k of a
+// kernel of n takes positions k, k + n, ...
+struct ClassWalk {
+    bool pair_kernel;
+    int32_t n_own, n_positions;
+
+    __device__ __forceinline__ void init(const ClassLists& L, bool is_pair_kernel, bool other_kernel_has_ctas) {
+        pair_kernel = is_pair_kernel;
+        n_own = pair_kernel ? L.nP : L.nS;
+        const int32_t other = other_kernel_has_ctas ? 0 : (pair_kernel ? L.nS : 2 * L.nP);
+        n_positions = n_own + other;
+    }
+
+    __device__ __forceinline__ TileCoord at(const ClassLists& L, int32_t p) const {
+        if (p < n_own) return pair_kernel ? L.decode_p(p) : L.decode_s(p);
+        const int32_t q = p - n_own;
+        if (pair_kernel) return L.decode_s(q);
+        TileCoord c = L.decode_p(q >> 1);
+        if (q & 1) {
+            c.row0 += 128;
+            c.rows -= 128;
+        } else if (c.rows > 128) {
+            c.rows = 128;
+        }
+        return c;
+    }
+};
 
 __device__ __forceinline__ TileCoord sentinel_tile() {
     TileCoord c;

@@ -165,11 +165,15 @@ def test_plan_large_balanced_groups_use_cta_pairs(lib):
 
 
 def test_plan_skewed_counts_prefer_128_row_tiles(lib):
-    # the same total under rank^-1.2 skew: 256-row tiles would be 40 % padding
+    # the same total under rank^-1.2 skew: 256-row tiles on every expert would be 40 % padding,
+    # so the static plan takes 128-row tiles with the size-sorted walk; the automatic plan runs the
+    # large experts on CTA pairs beside them instead (the mixed launch with fixed walks)
     from ragged_grouped_gemm_02_gb300 import workloads as wl
     counts = wl.workload_counts("skew16k")
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=counts, mixed=-1)
+    assert p["bm"] == 128 and p["bn"] == 256 and p["tail64"] == 1 and p["walk_order"] == 3
     p = rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=counts)
-    assert p["bm"] == 128 and p["bn"] == 256 and p["tail64"] == 1
+    assert p["mixed"] == 2 and p["bm"] == 256 and p["bn"] == 256 and p["grid"] == 88 and p["single_grid"] == 64
     # experts of 128 rows: a pair tile would be half empty
     p = rgg.rgg_plan(32, 4096, 6144, 4096, host_counts=[128] * 32)
     assert p["bm"] == 128
@@ -223,8 +227,9 @@ def test_plan_walk_order_choice(lib):
     assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("uniform"))["walk_order"] == 0
     assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("uniform"), op="fp8")["walk_order"] == 0
     assert rgg.rgg_plan(32, 512, 6144, 4096, host_counts=wl.workload_counts("decode"))["walk_order"] == 0
-    # strong skew: the size-sorted interleave
-    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("skew16k"))["walk_order"] == 3
+    # strong skew: the size-sorted interleave (when the mixed launch is off)
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=wl.workload_counts("skew16k"),
+                        mixed=-1)["walk_order"] == 3
     # an explicit order is kept; -1 asks for list order
     assert rgg.rgg_plan(32, 32768, 6144, 4096, walk_order=1)["walk_order"] == 1
     assert rgg.rgg_plan(32, 32768, 6144, 4096, walk_order=-1)["walk_order"] == 0
@@ -370,15 +375,24 @@ def test_plan_mixed_launch(lib):
     assert (p["grid"], p["single_grid"]) == (0, 152)
     p = rgg.rgg_plan(4, 256, 256, 512, host_counts=[100, 0, 300, 1], mixed=1, max_ctas=3)
     assert p["grid"] == 2 and p["single_grid"] == 1
-    # off by default
-    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=skew)["mixed"] == 0
+    # chosen by the planner: fixed walks for a strong skew over 128-row tiles (host counts only),
+    # claims for experts of three or more 256-row tiles; off for balanced mid-size experts,
+    # small groups, and without counts unless the experts average three 256-row tiles
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=skew)["mixed"] == 2
+    assert rgg.rgg_plan(64, 16384, 1024, 2688)["mixed"] == 0
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=[256] * 64)["mixed"] == 0
+    assert rgg.rgg_plan(64, 2048, 1024, 2688, host_counts=wl.workload_counts("skew2k"))["mixed"] == 0
+    assert rgg.rgg_plan(32, 32768, 6144, 4096)["mixed"] == 1
+    # the fixed walks on request
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=skew, mixed=2, mixed_pair_sms=76)
+    assert (p["mixed"], p["grid"], p["single_grid"]) == (2, 76, 76)
 
 
 @pytest.mark.parametrize("kw,status", [(dict(bm=128), "INVALID_ARG"), (dict(bn=128), "INVALID_ARG"),
                                        (dict(tail64=-1), "INVALID_ARG"), (dict(mixed_pair_sms=3), "INVALID_ARG"),
                                        (dict(mixed_pair_sms=154), "INVALID_ARG"),
                                        (dict(mixed_pair_sms=-2), "INVALID_ARG"),
-                                       (dict(pair_min_rows=-1), "INVALID_ARG"), (dict(mixed=2), "INVALID_ARG"),
+                                       (dict(pair_min_rows=-1), "INVALID_ARG"), (dict(mixed=3), "INVALID_ARG"),
                                        (dict(op="swiglu"), "UNSUPPORTED"), (dict(op="fp8"), "UNSUPPORTED")])
 def test_plan_mixed_rejects(lib, kw, status):
     args = dict(mixed=1)

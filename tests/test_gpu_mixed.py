@@ -2,11 +2,13 @@
 
 The mixed launch runs the experts of at least pair_min_rows rows as 256 x 256
 tiles on CTA pairs and the other experts as 128 x 256 tiles on single CTAs:
-two kernels that share the GPU and claim tiles from two device counters,
-each taking the other class's tiles once its own runs out.  Whatever the
-split of the SMs (all to pairs, all to single CTAs, or anything between),
-whether the kernels overlap, and whichever kernel ends up running a tile,
-every tile must be computed exactly once:
+two kernels that share the GPU and either claim tiles from two device
+counters, each taking the other class's tiles once its own runs out
+(mixed = 1), or walk their own class in a fixed order (mixed = 2; a kernel
+whose partner has no SMs walks both classes).  Whatever the split of the SMs
+(all to pairs, all to single CTAs, or anything between), whether the kernels
+overlap, whichever kernel ends up running a tile, and whatever the host
+counts claim, every tile must be computed exactly once:
 
 * integer-valued inputs with K <= 64 are exact in fp32 and bf16, so the result
   must equal the oracle bit for bit (this also pins the 128-row pair tail
@@ -36,11 +38,11 @@ def gpu():
     oracle.build()
 
 
-def _run(inp, offsets=None, **opts):
+def _run(inp, offsets=None, mixed=1, **opts):
     off = inp.offsets if offsets is None else np.asarray(offsets, dtype=np.int32)
     X, W = inp.X.cuda(), inp.W.cuda()
     Y = torch.full((X.shape[0], W.shape[2]), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
-    rgg.rgg_grouped_gemm(X, W, torch.from_numpy(off).cuda(), Y, check=True, mixed=1, **opts)
+    rgg.rgg_grouped_gemm(X, W, torch.from_numpy(off).cuda(), Y, check=True, mixed=mixed, **opts)
     torch.cuda.synchronize()
     return Y.cpu()
 
@@ -67,21 +69,34 @@ SPLITS = [dict(), dict(mixed_pair_sms=-1), dict(mixed_pair_sms=2), dict(mixed_pa
 SPLIT_IDS = ["auto", "no-pairs", "pairs-2", "pairs-76", "pairs-146", "3-ctas", "9-ctas-4-pairs"]
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["claims", "fixed-walks"])
 @pytest.mark.parametrize("opts", SPLITS, ids=SPLIT_IDS)
 @pytest.mark.parametrize("N", [512, 520, 136])
-def test_integer_inputs_bit_exact(opts, N):
+def test_integer_inputs_bit_exact(opts, N, mode):
     inp = wl.make_custom(COUNTS, K=64, N=N, seed=161, integer_valued=True, spare_rows=5)
-    _check(inp, _run(inp, host_counts=inp.counts, **opts), exact=True)
+    _check(inp, _run(inp, mixed=mode, host_counts=inp.counts, **opts), exact=True)
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["claims", "fixed-walks"])
+@pytest.mark.parametrize("wrong", [[1000] * 19, [10] * 19, list(range(19)), [0] * 18 + [10000]],
+                         ids=["all-large", "all-small", "ramp", "one-large"])
+def test_host_counts_that_disagree_with_the_device_offsets(mode, wrong):
+    # the host counts only size the split: the classes come from the device offsets, and a
+    # kernel whose partner got no SMs runs both classes
+    inp = wl.make_custom(COUNTS, K=64, N=264, seed=169, integer_valued=True, spare_rows=1)
+    _check(inp, _run(inp, mixed=mode, host_counts=np.asarray(wrong)), exact=True)
 
 
 @pytest.mark.parametrize("pmin", [1, 64, 129, 256, 1000, 1 << 20])
 def test_class_threshold_moves_experts_between_kernels(pmin):
     inp = wl.make_custom(COUNTS, K=64, N=264, seed=162, integer_valued=True, spare_rows=2)
-    _check(inp, _run(inp, pair_min_rows=pmin), exact=True)
-    _check(inp, _run(inp, pair_min_rows=pmin, host_counts=inp.counts), exact=True)
+    for mode in (1, 2):
+        _check(inp, _run(inp, mixed=mode, pair_min_rows=pmin), exact=True)
+        _check(inp, _run(inp, mixed=mode, pair_min_rows=pmin, host_counts=inp.counts), exact=True)
 
 
-@pytest.mark.parametrize("opts", [dict(), dict(mixed_pair_sms=-1), dict(mixed_pair_sms=76)])
+@pytest.mark.parametrize("opts", [dict(), dict(mixed_pair_sms=-1), dict(mixed_pair_sms=76), dict(mixed=2),
+                                  dict(mixed=2, mixed_pair_sms=76)])
 def test_random_inputs_with_k_and_n_tails(opts):
     inp = wl.make_custom(COUNTS, K=264, N=520, seed=163, spare_rows=3)
     _check(inp, _run(inp, host_counts=inp.counts, **opts), exact=False)
@@ -113,17 +128,18 @@ def test_no_rows_and_bad_offsets():
     assert bool((Y.view(torch.int16) == CANARY).all())
 
 
-@pytest.mark.parametrize("opts", [dict(), dict(mixed_pair_sms=-1), dict(mixed_pair_sms=76)])
+@pytest.mark.parametrize("opts", [dict(), dict(mixed_pair_sms=-1), dict(mixed_pair_sms=76), dict(mixed=2)])
 def test_bounded_wait_reports_timeout_and_context_survives(opts):
     inp = wl.make_custom([300, 37, 0, 64], K=256, N=512, seed=166)
     X, W = inp.X.cuda(), inp.W.cuda()
     off = torch.from_numpy(inp.offsets).cuda()
+    mode = opts.pop("mixed", 1)
     with pytest.raises(rgg.RggError) as ei:
-        rgg.rgg_grouped_gemm(X, W, off, check=True, mixed=1, timeout_ns=20_000_000,
+        rgg.rgg_grouped_gemm(X, W, off, check=True, mixed=mode, timeout_ns=20_000_000,
                              debug_flags=rgg.RGG_DEBUG_PRODUCER_STALL, host_counts=inp.counts, **opts)
     assert ei.value.status == rgg.RGG_ERR_DEVICE_TIMEOUT
     assert rgg.rgg_query_status() == rgg.RGG_OK
-    _check(inp, _run(inp, host_counts=inp.counts, **opts), exact=False)
+    _check(inp, _run(inp, mixed=mode, host_counts=inp.counts, **opts), exact=False)
 
 
 def test_repeated_calls_and_graph_replay():
@@ -158,9 +174,9 @@ def test_full_size(name):
     ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
     X, W = inp.X.cuda(), inp.W.cuda()
     off = torch.from_numpy(inp.offsets).cuda()
-    for opts in (dict(host_counts=inp.counts), dict()):
+    for opts in (dict(host_counts=inp.counts, mixed=1), dict(mixed=1), dict(host_counts=inp.counts, mixed=2)):
         Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device="cuda")
-        rgg.rgg_grouped_gemm(X, W, off, Y, check=True, mixed=1, **opts)
+        rgg.rgg_grouped_gemm(X, W, off, Y, check=True, **opts)
         torch.cuda.synchronize()
         got = Y.double().cpu().numpy()
         err = np.abs(got - ref)
