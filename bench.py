@@ -75,8 +75,9 @@ def parse_args():
     p.add_argument("--tail64", type=int, default=0, help="0 auto, 1 on, -1 off")
     p.add_argument("--gather-mode", type=int, default=0, help="gather ops: 0 auto, 1 TMA gather4, 2 two-pass")
     p.add_argument("--mixed", type=int, default=0,
-                   help="plain GEMM: 0 auto, 1 the mixed launch (large experts on CTA pairs beside small ones "
-                        "on single CTAs, tiles claimed on the device), -1 off")
+                   help="plain GEMM and fused gate-up: 0 auto, 1 the mixed launch (large experts on CTA pairs "
+                        "beside small ones on single CTAs, tiles claimed on the device), 2 the same with fixed "
+                        "walks, -1 off")
     p.add_argument("--mixed-pair-sms", type=int, default=0,
                    help="mixed launch: SMs of the pair kernel (0: split by estimated work, -1: none)")
     p.add_argument("--walk-order", type=int, default=0,
@@ -282,7 +283,7 @@ def run_profile(args):
     Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device=dev)
     opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
                 walk_order=args.walk_order, host_counts=inp.counts)
-    if args.op == "gemm":
+    if args.op in ("gemm", "swiglu"):
         opts.update(mixed=args.mixed, mixed_pair_sms=args.mixed_pair_sms)
     if args.op == "gather":
         # the same recipe as the timed gather op: M_tot tokens, distinct tokens per expert
@@ -377,7 +378,7 @@ class Step:
         # alone); the kernel itself reads the offsets on the device.
         self.opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
                          walk_order=args.walk_order, host_counts=inp.counts if host_counts else None)
-        if op == "gemm":
+        if op in ("gemm", "swiglu"):
             self.opts.update(mixed=args.mixed, mixed_pair_sms=args.mixed_pair_sms)
         self.plan_from = ("host-side routed counts (tile shape only)" if host_counts
                           else "device offsets only (no host counts)")

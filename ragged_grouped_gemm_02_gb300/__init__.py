@@ -239,7 +239,8 @@ def rgg_grouped_gemm(X, W, group_offsets, Y=None, *, bm=0, bn=0, stages=0, max_c
 
 
 def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages=0, max_ctas=0, timeout_ns=0,
-                            host_counts=None, debug_flags=0, tail64=0, walk_order=0, stream=None, check=False):
+                            host_counts=None, debug_flags=0, tail64=0, walk_order=0, mixed=0, mixed_pair_sms=0,
+                            pair_min_rows=0, stream=None, check=False):
     """H = silu(X_e . W13_e[:, :N]) * (X_e . W13_e[:, N:]) for every expert,
     one kernel launch (the fused gate-up projection with SiLU activation).
 
@@ -264,7 +265,8 @@ def rgg_grouped_gemm_swiglu(X, W13, group_offsets, H=None, *, bm=0, bn=0, stages
     elif H.shape != (M_tot, N) or H.dtype != torch.bfloat16 or not H.is_contiguous() or not H.is_cuda:
         raise ValueError("H must be a contiguous bf16 CUDA tensor of shape [M_tot, N]")
     lib = load_library()
-    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order)
+    opt, keep = _options(bm, bn, stages, max_ctas, timeout_ns, host_counts, debug_flags, tail64, 0, walk_order,
+                         mixed=mixed, mixed_pair_sms=mixed_pair_sms, pair_min_rows=pair_min_rows)
     st = _stream_ptr(stream, device)
     s = lib.rgg_grouped_gemm_swiglu(_handle(device), X.data_ptr(), W13.data_ptr(), group_offsets.data_ptr(),
                                     H.data_ptr(), E, M_tot, K, N, st, ctypes.byref(opt))

@@ -249,7 +249,7 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     const int want_mixed = opt ? opt->mixed : 0;
     if (want_mixed < -1 || want_mixed > 2 || (opt && opt->pair_min_rows < 0)) return RGG_ERR_INVALID_ARG;
     if (want_mixed >= 1) {
-        if (kind != 0) return RGG_ERR_UNSUPPORTED;  // the plain bf16 GEMM only
+        if ((kind & ~kPlanNoBn192) != 0) return RGG_ERR_UNSUPPORTED;  // bf16 plain or fused gate-up only
         return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out, want_mixed);
     }
 
@@ -341,10 +341,12 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     // The M tiles that share a weight panel then run side by side whatever
     // the drift between SMs: measured on prefill (E = 32, ~1 024 rows per
     // expert, K = 6144), DRAM reads of 2.75-2.92 GB per launch against 2.07 GB
-    // (2.28 GB algorithmic in all), 1 444-1 466 -> 1 494-1 507 TFLOP/s.  Where
-    // experts fill only one or two M tiles the static walk stays ahead (uniform
-    // 256 rows per expert: 1 093-1 108 static, 1 048 claimed).
-    if (want_mixed == 0 && kind == 0 && pair && bn == 256 && walk == 4 && want_walk == 0 && want_tail != -1 &&
+    // (2.28 GB algorithmic in all), 1 444-1 466 -> 1 494-1 507 TFLOP/s; the
+    // fused gate-up op 1 474 -> 1 522-1 548.  Where experts fill only one or
+    // two M tiles the static walk stays ahead (uniform 256 rows per expert:
+    // 1 093-1 108 static, 1 048 claimed).
+    const bool mixed_kind = (kind & ~kPlanNoBn192) == 0;  // the plain and fused gate-up bf16 ops
+    if (want_mixed == 0 && mixed_kind && pair && bn == 256 && walk == 4 && want_walk == 0 && want_tail != -1 &&
         (want_stages == 0))
         return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out, 1);
     // A strong skew (host counts: the largest expert above four times the
@@ -352,7 +354,9 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     // pairs beside the small ones on single CTAs, each kernel walking its own
     // class (measured on the skewed 16k workload: 855-868 TFLOP/s for the
     // size-sorted 128 x 256 walk, 906 for the mixed launch with fixed walks,
-    // 841 with claims, whose descriptor queue costs a few microseconds).
+    // 841 with claims, whose descriptor queue costs a few microseconds).  The
+    // plain op only: the fused gate-up op's pair tiles keep 256-row tails, and
+    // there it lost (867 -> 730 TFLOP/s).
     if (want_mixed == 0 && kind == 0 && skewed && bm == 128 && want_bm == 0 && (want_bn == 0 || want_bn == 256) &&
         want_walk == 0 && want_tail != -1 && want_stages == 0) {
         Plan mp;
@@ -805,6 +809,24 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
     a.debug_flags = opt ? (opt->debug_flags & RGG_DEBUG_PRODUCER_STALL) : 0;
     a.tail64 = p.tail64;
     a.walk_order = p.walk_order;
+    if (p.mixed) {
+        // as for rgg_grouped_gemm's mixed launch; the pair kernel keeps 256-row tail tiles here
+        a.sched = h->d_status + 16;
+        a.sched_total = p.grid + p.single_grid;
+        a.sched_pairs = p.grid / 2;
+        a.sched_singles = p.single_grid;
+        a.sched_claims = (p.mixed == 1) ? 1 : 0;
+        a.pair_min_rows = p.pair_min_rows;
+        rgg::GemmArgs as = a;
+        as.stages = p.single_stages;
+        cudaError_t err = rgg::launch_gemm_mixed_swiglu(p.grid, p.smem_bytes, a, p.single_grid, p.single_smem, as, st,
+                                                        tx, tx64, tw);
+        if (err != cudaSuccess) {
+            cudaMemsetAsync(a.sched, 0, 3 * sizeof(int32_t), st);
+            return cuda_failure(err, "grouped_gemm_swiglu (mixed) launch");
+        }
+        return RGG_OK;
+    }
     if (p.bm == 256) a.tail64 = 0;  // the pair's 128-row tail layout splits gate and up across warps
     cudaError_t err = (p.bm == 256) ? rgg::launch_gemm_pair_swiglu(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
                                     : rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);

@@ -358,8 +358,8 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
                         const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
     using Cfg = TileConfig<BM, BN, kFp8>;
-    static_assert(!kDyn || (BM == 128 && BN == kMixedBN && kEpi == kEpiPlain && !kFp8 && kGather == kGatherNone),
-                  "the mixed launch's 1-CTA kernel runs plain bf16 128 x 256 tiles");
+    static_assert(!kDyn || (BM == 128 && BN == kMixedBN && !kFp8 && kGather == kGatherNone),
+                  "the mixed launch's 1-CTA kernel runs bf16 128 x 256 tiles (plain or fused gate-up)");
     static_assert(kEpi == kEpiPlain || (BN % 128) == 0, "fused gate-up tiles hold whole gate and up panels");
     static_assert(!(kFp8 && kEpi == kEpiSwiGLU), "the fused gate-up epilogue is bf16 only");
     static_assert(!(kFp8 && kGather != kGatherNone), "the token gather is bf16 only");
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
         if (warp == 0) build_class_prefix_warp(s_off, s_pre, E, 256, args.n_tiles_n, args.pair_min_rows, 0x7fffffff);
         if (warp == 1) build_class_prefix_warp(s_off, s_order, E, 128, args.n_tiles_n, 0, args.pair_min_rows);
         __syncthreads();
-        L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E]};
+        L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E], kOutN};
         T = L.nP + L.nS;
         if (T == 0) {
             if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);

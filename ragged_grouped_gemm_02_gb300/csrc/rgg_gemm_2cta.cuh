@@ -86,7 +86,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
                              const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
     using Cfg = PairConfig<BN>;
-    static_assert(!kDyn || (BN == kMixedBN && kEpi == kEpiPlain), "the mixed launch's pairs run plain 256 x 256 tiles");
+    static_assert(!kDyn || BN == kMixedBN, "the mixed launch's pairs run 256-column MMAs");
     // The mixed launch's 1-CTA kernel, launched after this one, may start as
     // soon as every CTA of this grid is running.
     if constexpr (kDyn) pdl_launch_dependents();
@@ -138,7 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
         if (warp == 0) build_class_prefix_warp(s_off, s_pre, E, 256, args.n_tiles_n, args.pair_min_rows, 0x7fffffff);
         if (warp == 1) build_class_prefix_warp(s_off, s_order, E, 128, args.n_tiles_n, 0, args.pair_min_rows);
         __syncthreads();
-        L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E]};
+        L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E], kOutN};
         T = L.nP + L.nS;
         if (T == 0) {
             if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);

@@ -6,29 +6,31 @@
 
 namespace rgg {
 
-cudaError_t launch_gemm_mixed(int pair_grid, size_t pair_smem, const GemmArgs& pair_args, int single_grid,
-                              size_t single_smem, const GemmArgs& single_args, cudaStream_t stream,
-                              const CUtensorMap& tmap_x, const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w) {
+template <int kEpi>
+static cudaError_t launch_mixed_instance(int pair_grid, size_t pair_smem, const GemmArgs& pair_args, int single_grid,
+                                         size_t single_smem, const GemmArgs& single_args, cudaStream_t stream,
+                                         const CUtensorMap& tmap_x, const CUtensorMap& tmap_x64,
+                                         const CUtensorMap& tmap_w) {
     if (pair_grid < 0 || pair_grid % 2 != 0 || single_grid < 0 || pair_grid + single_grid == 0)
         return cudaErrorInvalidValue;
     if (pair_grid > 0) {
-        auto kernel = grouped_gemm_pair_kernel<kMixedBN, kEpiPlain, true>;
+        auto kernel = grouped_gemm_pair_kernel<kMixedBN, kEpi, true>;
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(pair_smem));
         if (err != cudaSuccess) return err;
-        kernel<<<pair_grid, 64 + 32 * pair_epilogue_warps<kEpiPlain>(), pair_smem, stream>>>(tmap_x, tmap_x64,
-                                                                                             tmap_w, pair_args);
+        kernel<<<pair_grid, 64 + 32 * pair_epilogue_warps<kEpi>(), pair_smem, stream>>>(tmap_x, tmap_x64, tmap_w,
+                                                                                        pair_args);
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
     if (single_grid > 0) {
-        auto kernel = grouped_gemm_kernel<128, kMixedBN, kEpiPlain, false, kGatherNone, true>;
+        auto kernel = grouped_gemm_kernel<128, kMixedBN, kEpi, false, kGatherNone, true>;
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(single_smem));
         if (err != cudaSuccess) return err;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(single_grid, 1, 1);
-        cfg.blockDim = dim3(cta_threads<kEpiPlain, false>(), 1, 1);
+        cfg.blockDim = dim3(cta_threads<kEpi, false>(), 1, 1);
         cfg.dynamicSmemBytes = single_smem;
         cfg.stream = stream;
         // After the pair kernel: may start once every pair CTA is running, so
@@ -44,6 +46,21 @@ cudaError_t launch_gemm_mixed(int pair_grid, size_t pair_smem, const GemmArgs& p
         return cudaGetLastError();
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_gemm_mixed(int pair_grid, size_t pair_smem, const GemmArgs& pair_args, int single_grid,
+                              size_t single_smem, const GemmArgs& single_args, cudaStream_t stream,
+                              const CUtensorMap& tmap_x, const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w) {
+    return launch_mixed_instance<kEpiPlain>(pair_grid, pair_smem, pair_args, single_grid, single_smem, single_args,
+                                            stream, tmap_x, tmap_x64, tmap_w);
+}
+
+cudaError_t launch_gemm_mixed_swiglu(int pair_grid, size_t pair_smem, const GemmArgs& pair_args, int single_grid,
+                                     size_t single_smem, const GemmArgs& single_args, cudaStream_t stream,
+                                     const CUtensorMap& tmap_x, const CUtensorMap& tmap_x64,
+                                     const CUtensorMap& tmap_w) {
+    return launch_mixed_instance<kEpiSwiGLU>(pair_grid, pair_smem, pair_args, single_grid, single_smem, single_args,
+                                             stream, tmap_x, tmap_x64, tmap_w);
 }
 
 }  // namespace rgg

@@ -60,6 +60,12 @@ cudaError_t launch_gemm_pair_swiglu(int bn, int grid, size_t smem, cudaStream_t 
 cudaError_t launch_gemm_mixed(int pair_grid, size_t pair_smem, const GemmArgs& pair_args, int single_grid,
                               size_t single_smem, const GemmArgs& single_args, cudaStream_t stream,
                               const CUtensorMap& tmap_x, const CUtensorMap& tmap_x64, const CUtensorMap& tmap_w);
+// The same with the fused gate-up + SiLU epilogue (tmap_w spans 2N columns;
+// 128 output columns per tile; pair tail tiles stay 256 rows).
+cudaError_t launch_gemm_mixed_swiglu(int pair_grid, size_t pair_smem, const GemmArgs& pair_args, int single_grid,
+                                     size_t single_smem, const GemmArgs& single_args, cudaStream_t stream,
+                                     const CUtensorMap& tmap_x, const CUtensorMap& tmap_x64,
+                                     const CUtensorMap& tmap_w);
 
 // The flat tile list written out by the same device code the GEMM uses, in
 // list order (walk_order 0) or in the order walk_order visits it.

@@ -49,7 +49,8 @@
 namespace rgg {
 
 constexpr int kQueueDepth = 8;          // tile descriptors between a CTA's producer and its consumers
-constexpr int kMixedBN = 256;           // both classes: 256-column tiles (the last N tile narrowed)
+constexpr int kMixedBN = 256;           // both classes: MMAs 256 columns wide (plain: the last N tile narrowed;
+                                        // fused gate-up: 128 gate + 128 up columns, 128 outputs)
 constexpr int kPairMinRowsDefault = 256;
 
 struct ClassLists {
@@ -58,12 +59,13 @@ struct ClassLists {
     const int32_t* s_preS;  // class S prefix of 128-row tiles
     int E, nN;
     int32_t nP, nS;
+    int out_cols;           // output columns per tile: kMixedBN, or half of it for the fused gate-up op
 
     __device__ __forceinline__ TileCoord decode_p(int32_t t) const {
-        return decode_tile(s_off, s_preP, E, 256, kMixedBN, nN, t, true);
+        return decode_tile(s_off, s_preP, E, 256, out_cols, nN, t, true);
     }
     __device__ __forceinline__ TileCoord decode_s(int32_t t) const {
-        return decode_tile(s_off, s_preS, E, 128, kMixedBN, nN, t, true);
+        return decode_tile(s_off, s_preS, E, 128, out_cols, nN, t, true);
     }
 };
 

@@ -383,6 +383,11 @@ def test_plan_mixed_launch(lib):
     assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=[256] * 64)["mixed"] == 0
     assert rgg.rgg_plan(64, 2048, 1024, 2688, host_counts=wl.workload_counts("skew2k"))["mixed"] == 0
     assert rgg.rgg_plan(32, 32768, 6144, 4096)["mixed"] == 1
+    # the fused gate-up op: claims for the large experts, but no fixed walks for a skew
+    assert rgg.rgg_plan(32, 32768, 6144, 2048, op="swiglu")["mixed"] == 1
+    assert rgg.rgg_plan(64, 16384, 1024, 1344, host_counts=skew, op="swiglu")["mixed"] == 0
+    p = rgg.rgg_plan(64, 16384, 1024, 1344, host_counts=skew, op="swiglu", mixed=2)
+    assert p["mixed"] == 2 and p["grid"] > 0 and p["single_grid"] > 0
     # the fixed walks on request
     p = rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=skew, mixed=2, mixed_pair_sms=76)
     assert (p["mixed"], p["grid"], p["single_grid"]) == (2, 76, 76)
@@ -393,7 +398,7 @@ def test_plan_mixed_launch(lib):
                                        (dict(mixed_pair_sms=154), "INVALID_ARG"),
                                        (dict(mixed_pair_sms=-2), "INVALID_ARG"),
                                        (dict(pair_min_rows=-1), "INVALID_ARG"), (dict(mixed=3), "INVALID_ARG"),
-                                       (dict(op="swiglu"), "UNSUPPORTED"), (dict(op="fp8"), "UNSUPPORTED")])
+                                       (dict(op="gather", gather_mode=1), "UNSUPPORTED"), (dict(op="fp8"), "UNSUPPORTED")])
 def test_plan_mixed_rejects(lib, kw, status):
     args = dict(mixed=1)
     args.update(kw)

@@ -60,7 +60,8 @@ def _canary(M, N):
 GEMM_OPTS = [dict(bm=64, bn=128), dict(bm=64, bn=256), dict(bm=128, bn=192), dict(bm=128, bn=256),
              dict(bm=128, bn=256, tail64=-1), dict(bm=256, bn=128), dict(bm=256, bn=256), dict(walk_order=3),
              dict(walk_order=4, bm=256), dict(mixed=1), dict(mixed=1, mixed_pair_sms=-1),
-             dict(mixed=1, mixed_pair_sms=2), dict(mixed=1, max_ctas=5)]
+             dict(mixed=1, mixed_pair_sms=2), dict(mixed=1, max_ctas=5), dict(mixed=2), dict(mixed=2, mixed_pair_sms=-1),
+             dict(mixed=2, mixed_pair_sms=4, max_ctas=7)]
 
 
 @pytest.mark.parametrize("opts", GEMM_OPTS, ids=[str(o) for o in GEMM_OPTS])
@@ -75,11 +76,15 @@ def test_grouped_gemm_edges(opts, K, integer):
     _check(Y.cpu(), ref, 0, int(inp.offsets[-1]), integer)
 
 
-@pytest.mark.parametrize("opts", [dict(bm=64, bn=128), dict(bm=128, bn=256), dict(bm=256, bn=256)])
+@pytest.mark.parametrize("opts", [dict(bm=64, bn=128), dict(bm=128, bn=256), dict(bm=256, bn=256), dict(mixed=1),
+                                  dict(mixed=2, host_counts=True), dict(mixed=1, mixed_pair_sms=-1)])
 def test_swiglu_edges(opts):
     inp = wl.make_custom(EDGE_PAIRS, K=264, N=2 * 520, seed=172, spare_rows=2)
     X, W = inp.X.cuda(), inp.W.cuda()
     H = _canary(X.shape[0], 520)
+    opts = dict(opts)
+    if opts.pop("host_counts", False):
+        opts["host_counts"] = inp.counts
     rgg.rgg_grouped_gemm_swiglu(X, W, torch.from_numpy(inp.offsets).cuda(), H, check=True, **opts)
     torch.cuda.synchronize()
     ref = oracle.grouped_swiglu(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)

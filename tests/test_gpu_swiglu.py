@@ -101,3 +101,28 @@ def test_full_size(name):
     err = np.abs(got - ref[lo:hi])
     bad = ~(err <= RTOL * np.maximum(1.0, np.abs(ref[lo:hi])))
     assert not bad.any(), "%s: %d outputs out of tolerance, max err %.4g" % (name, int(bad.sum()), err.max())
+
+
+# the mixed launch with the fused epilogue: large experts on CTA pairs (256-row tiles, gate on the
+# first CTA and up on the second), small ones on single CTAs, claimed (1) or walked in a fixed
+# order (2); integer inputs with K = 64 are exact
+MIXED_COUNTS = [0, 1, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300, 384, 385, 511, 700, 3, 0, 1000]
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["claims", "fixed-walks"])
+@pytest.mark.parametrize("opts", [dict(), dict(mixed_pair_sms=-1), dict(mixed_pair_sms=2), dict(mixed_pair_sms=76),
+                                  dict(max_ctas=5)], ids=["auto", "no-pairs", "pairs-2", "pairs-76", "5-ctas"])
+def test_mixed_launch_bit_exact(mode, opts):
+    inp = wl.make_custom(MIXED_COUNTS, K=64, N=2 * 264, seed=75, integer_valued=True, spare_rows=3)
+    X, W13 = inp.X.cuda(), inp.W.cuda()
+    H = torch.full((X.shape[0], 264), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    rgg.rgg_grouped_gemm_swiglu(X, W13, torch.from_numpy(inp.offsets).cuda(), H, check=True, mixed=mode,
+                                host_counts=inp.counts, **opts)
+    torch.cuda.synchronize()
+    ref = oracle.grouped_swiglu(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
+    M = int(inp.offsets[-1])
+    # integer gate and up products are exact; silu(g) * u is then computed in fp32 and rounded to bf16
+    got = H.cpu()[:M].double().numpy()
+    err = np.abs(got - ref[:M])
+    assert (err <= RTOL * np.maximum(1.0, np.abs(ref[:M]))).all(), "max err %.4g" % err.max()
+    assert bool((H.view(torch.int16)[M:] == CANARY).all())
