@@ -85,6 +85,11 @@ struct GemmArgs {
     int32_t sched_singles = 0;  // CTAs of the 1-CTA kernel (each takes its first class-S tile without a claim)
     int32_t sched_claims = 1;   // 0: each kernel walks its own class statically (no counters, no queue)
     int32_t pair_min_rows = kPairMinRowsDefault;
+    // 1: the kernel waits for the grid before it on the stream before its
+    // first global memory access (programmatic dependent launch, see
+    // pdl_wait_prerequisites); 0 only for the mixed launch's 1-CTA kernel
+    // beside a pair kernel, which waits at its end instead.
+    int32_t pdl_wait_first = 1;
 };
 
 // Shared-memory carve-up shared by the host planner and the kernel.  Offsets
@@ -406,6 +411,14 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     int32_t* q_desc = reinterpret_cast<int32_t*>(gbase + sp.q_off);     // mixed: tile queue
     auto qfull_bar = [&](int i) { return base + sp.qbar_off + 8u * i; };
     auto qempty_bar = [&](int i) { return base + sp.qbar_off + 8u * (kQueueDepth + i); };
+
+    // Launched with programmatic stream serialisation: the grid may be
+    // resident before the kernel ahead of it on the stream has finished, so
+    // it touches no global memory before that kernel's writes are visible.
+    // Then the grid after it may launch; its CTAs take the SMs this grid's
+    // CTAs leave and wait the same way.
+    if (args.pdl_wait_first) pdl_wait_prerequisites();
+    pdl_launch_dependents();
 
     // S1: group offsets -> validated per-expert tile prefix.
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {

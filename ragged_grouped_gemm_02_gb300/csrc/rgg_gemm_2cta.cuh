@@ -87,9 +87,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                              const __grid_constant__ CUtensorMap tmap_w, const GemmArgs args) {
     using Cfg = PairConfig<BN>;
     static_assert(!kDyn || BN == kMixedBN, "the mixed launch's pairs run 256-column MMAs");
-    // The mixed launch's 1-CTA kernel, launched after this one, may start as
-    // soon as every CTA of this grid is running.
-    if constexpr (kDyn) pdl_launch_dependents();
     constexpr int BM = 256;  // rows per pair tile
     constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;  // output columns per tile
     auto half_tile = [&](const TileCoord& c) { return kEpi == kEpiPlain && pair_runs_as_128_rows(args, c); };
@@ -123,6 +120,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     int32_t* q_desc = reinterpret_cast<int32_t*>(gbase + sp.q_off);     // mixed: tile queue
     auto qfull_bar = [&](int i) { return base + sp.qbar_off + 8u * i; };
     auto qempty_bar = [&](int i) { return base + sp.qbar_off + 8u * (kQueueDepth + i); };
+
+    // No global memory access before the kernel ahead on the stream has
+    // finished (programmatic stream serialisation, as in the 1-CTA kernel);
+    // then the next grid may launch: the mixed launch's 1-CTA kernel starts
+    // beside this one as soon as every pair CTA has got here.
+    pdl_wait_prerequisites();
+    pdl_launch_dependents();
 
     // S1, identical in both CTAs, so every early exit below is pair-uniform.
     if (!load_and_check_offsets(args.offsets, s_off, E, args.M_tot)) {

@@ -13,8 +13,7 @@ cudaError_t launch_gemm_instance(int grid, size_t smem, cudaStream_t stream, con
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kernel<<<grid, cta_threads<kEpi, kFp8>(), smem, stream>>>(tmap_x, tmap_x64, tmap_w, args);
-    return cudaGetLastError();
+    return launch_chained(kernel, grid, cta_threads<kEpi, kFp8>(), smem, stream, tmap_x, tmap_x64, tmap_w, args);
 }
 
 }  // namespace rgg

@@ -18,9 +18,8 @@ static cudaError_t launch_mixed_instance(int pair_grid, size_t pair_smem, const 
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(pair_smem));
         if (err != cudaSuccess) return err;
-        kernel<<<pair_grid, 64 + 32 * pair_epilogue_warps<kEpi>(), pair_smem, stream>>>(tmap_x, tmap_x64, tmap_w,
-                                                                                        pair_args);
-        err = cudaGetLastError();
+        err = launch_chained(kernel, pair_grid, 64 + 32 * pair_epilogue_warps<kEpi>(), pair_smem, stream, tmap_x,
+                             tmap_x64, tmap_w, pair_args);
         if (err != cudaSuccess) return err;
     }
     if (single_grid > 0) {
@@ -28,22 +27,15 @@ static cudaError_t launch_mixed_instance(int pair_grid, size_t pair_smem, const 
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(single_smem));
         if (err != cudaSuccess) return err;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(single_grid, 1, 1);
-        cfg.blockDim = dim3(cta_threads<kEpi, false>(), 1, 1);
-        cfg.dynamicSmemBytes = single_smem;
-        cfg.stream = stream;
-        // After the pair kernel: may start once every pair CTA is running, so
-        // the two kernels share the GPU (each kernel ends no earlier than the
-        // pair kernel, see pdl_wait_prerequisites).
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = pair_grid > 0 ? 1 : 0;
-        err = cudaLaunchKernelEx(&cfg, kernel, tmap_x, tmap_x64, tmap_w, single_args);
-        if (err != cudaSuccess) return err;
-        return cudaGetLastError();
+        // After the pair kernel: starts once every pair CTA has passed its own
+        // wait for the work ahead on the stream, so the two kernels share the
+        // GPU; it does not wait for the pair kernel before its loads, only
+        // before it ends (so the stream's later work sees both done).  Alone
+        // (no pair CTAs) it waits first, like every other kernel.
+        GemmArgs a = single_args;
+        a.pdl_wait_first = pair_grid > 0 ? 0 : 1;
+        return launch_chained(kernel, single_grid, cta_threads<kEpi, false>(), single_smem, stream, tmap_x, tmap_x64,
+                              tmap_w, a);
     }
     return cudaSuccess;
 }

@@ -12,8 +12,8 @@ static cudaError_t launch_pair_instance(int grid, size_t smem, cudaStream_t stre
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kernel<<<grid, 64 + 32 * pair_epilogue_warps<kEpi>(), smem, stream>>>(tmap_x, tmap_x64, tmap_w, args);
-    return cudaGetLastError();
+    return launch_chained(kernel, grid, 64 + 32 * pair_epilogue_warps<kEpi>(), smem, stream, tmap_x, tmap_x64, tmap_w,
+                          args);
 }
 
 cudaError_t launch_gemm_pair(int bn, int grid, size_t smem, cudaStream_t stream, const CUtensorMap& tmap_x,

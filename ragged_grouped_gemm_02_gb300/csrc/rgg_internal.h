@@ -6,11 +6,37 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 #include "rgg.h"
 #include "rgg_gemm.cuh"
 
 namespace rgg {
+
+// Every GEMM kernel is launched with programmatic stream serialisation: it
+// may become resident while the kernel ahead of it on the stream is still
+// running (its CTAs take SMs as that kernel's CTAs exit), and waits on the
+// device (griddepcontrol.wait) before its first global memory access.  Back
+// to back launches then hide most of the launch and CTA-dispatch latency.
+// Ahead of a copy or a memset, or a kernel launched without the attribute,
+// the launch is ordered as usual.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), int grid, int threads, size_t smem, cudaStream_t stream,
+                           Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
 
 // Grouped GEMM kernels, one translation unit per BM.  `bn` is 128, 192 or
 // 256.  tmap_x64 is X with a 64-row box (tail tiles of 128-row kernels).
