@@ -116,8 +116,10 @@ typedef struct rgg_options {
                                     planner's choice), -1 = off.  On: bm and bn must be 0 or 256, tail64
                                     must not be -1, walk_order is not used. */
     int mixed_pair_sms;          /* mixed launch: SMs given to the pair kernel (even; the 1-CTA kernel gets
-                                    the rest).  0 = split by the estimated work of each class (from
-                                    host_counts, else balanced experts), -1 = no pair kernel. */
+                                    the rest).  0 = split by the estimated work of each class: from
+                                    host_counts when given; else, with fixed walks, from the device offsets
+                                    (see rgg_plan_info.device_split), and with claims from balanced
+                                    experts.  -1 = no pair kernel. */
     int pair_min_rows;           /* mixed launch: smallest expert (rows) that runs on CTA pairs; 0 = 256 */
 } rgg_options;
 
@@ -146,6 +148,11 @@ typedef struct rgg_plan_info {
     int single_stages;           /* mixed launch: ring depth of the 1-CTA kernel */
     int single_smem_bytes;       /* mixed launch: dynamic shared memory per CTA of the 1-CTA kernel */
     int pair_min_rows;           /* mixed launch: smallest expert on CTA pairs */
+    int device_split;            /* mixed launch with fixed walks: 1 when the split of the SMs between the
+                                    two kernels is taken on the device from the offsets (no host_counts,
+                                    mixed_pair_sms 0): both kernels are launched over all the SMs (grid and
+                                    single_grid above), every CTA computes the same split, and the CTAs past
+                                    their kernel's share leave at once; else 0 */
 } rgg_plan_info;
 
 /*

@@ -70,7 +70,8 @@ class _PlanInfo(ctypes.Structure):
                 ("tmem_cols", ctypes.c_int), ("max_tiles", ctypes.c_int64), ("tail64", ctypes.c_int),
                 ("walk_order", ctypes.c_int), ("gather_mode", ctypes.c_int), ("workspace_bytes", ctypes.c_int64),
                 ("mixed", ctypes.c_int), ("single_grid", ctypes.c_int), ("single_stages", ctypes.c_int),
-                ("single_smem_bytes", ctypes.c_int), ("pair_min_rows", ctypes.c_int)]
+                ("single_smem_bytes", ctypes.c_int), ("pair_min_rows", ctypes.c_int),
+                ("device_split", ctypes.c_int)]
 
 
 _lock = threading.Lock()

@@ -88,6 +88,10 @@ struct Plan {
     int mixed = 0;
     int single_grid = 0, single_stages = 0, single_smem = 0;
     int pair_min_rows = 0;
+    // fixed walks only: both kernels launched over all `split_sms` SMs, each
+    // CTA computing the split from the device offsets (CTAs past their
+    // kernel's share leave at once)
+    int device_split = 0, split_sms = 0;
 };
 
 
@@ -114,19 +118,15 @@ int stages_that_fit(int smem_optin, uint32_t fixed, int64_t per_stage) {
 // The mixed launch (csrc/rgg_sched.cuh): experts of at least pair_min_rows
 // rows on CTA pairs in 256 x 256 tiles, the rest on single CTAs in 128 x 256
 // tiles, two kernels on disjoint SMs.  The split of the SMs follows the
-// estimated work of each class in SM-time, taken as the bytes each SM pulls
-// into shared memory per tile (the quantity that set the pace of both tile
-// shapes on a GB300): (128 + cols/2) per CTA of a pair tile (64 + cols/2 for
-// a tile of <= 128 rows), 128 + cols per 1-CTA tile (64 + cols for <= 64
-// rows), the pair tiles' count weighted by kPairCostFactor: on the skewed
-// 16k workload a pair tile's unit took 1.12 times a 1-CTA tile's (per-CTA
-// traces: 12.8 SM-us per 512 units against 8.6 per 384), and the split it
-// gives (88 of 152 SMs on pairs) was the measured best, 906 TFLOP/s (84: 876,
-// 80: 872, 92: 882, 100: 824).  With claims the kernels steal each other's
-// tiles when their own class runs out, so an inexact split costs only the
-// less efficient shape on the stolen tiles; the fixed walks depend on it.
-// Without host counts the experts are taken as balanced.
-constexpr double kPairCostFactor = 1.12;
+// estimated work of each class (mixed_pair_sms in rgg_sched.cuh; with it, 88
+// of 152 SMs on pairs for the skewed 16k workload, the measured best: 906
+// TFLOP/s against 876 for 84, 872 for 80, 882 for 92, 824 for 100).  With
+// claims the kernels steal each other's tiles when their own class runs out,
+// so an inexact split costs only the less efficient shape on the stolen
+// tiles; the fixed walks depend on it.  Without host counts the fixed walks
+// take the split from the device offsets (both kernels launched over all the
+// SMs; each CTA computes the same split, and those past their kernel's share
+// leave at once), claims take the experts as balanced.
 rgg_status plan_mixed(int grid_cap, int smem_optin, int E, int64_t M_tot, int N, const rgg_options* opt, Plan* out,
                       int mode) {
     const int want_bm = opt ? opt->bm : 0;
@@ -139,46 +139,32 @@ rgg_status plan_mixed(int grid_cap, int smem_optin, int E, int64_t M_tot, int N,
         return RGG_ERR_INVALID_ARG;
     if (want_psms < -1 || want_psms > grid_cap || (want_psms > 0 && want_psms % 2 != 0)) return RGG_ERR_INVALID_ARG;
     if (tile_bound(E, M_tot, N, 128, rgg::kMixedBN) >= (int64_t(1) << 31)) return RGG_ERR_UNSUPPORTED;
+    const bool host_counts = opt && opt->host_counts;
+    const bool device_split = (mode == 2 && want_psms == 0 && !host_counts && grid_cap >= 2);
     int pair_sms = 0;
     if (want_psms == -1) {
         pair_sms = 0;
     } else if (want_psms > 0) {
         pair_sms = want_psms;
     } else {
-        double cost_p = 0.0, cost_s = 0.0;
-        auto add_expert = [&](int64_t m, double weight) {
-            for (int64_t c0 = 0; c0 < N; c0 += rgg::kMixedBN) {
-                const int64_t cols = std::min<int64_t>(rgg::kMixedBN, N - c0);
-                if (m >= pmin) {
-                    const double pc = static_cast<double>(ceil_div(cols, 128) * 128);
-                    const int64_t rem = m % 256;
-                    cost_p += weight * ((m / 256) * 2.0 * (128 + pc / 2) +
-                                        (rem > 128 ? 2.0 * (128 + pc / 2) : rem > 0 ? 2.0 * (64 + pc / 2) : 0.0));
-                } else {
-                    const double sc = static_cast<double>(ceil_div(cols, 64) * 64);
-                    const int64_t rem = m % 128;
-                    cost_s += weight *
-                              ((m / 128) * (128 + sc) + (rem > 64 ? 128 + sc : rem > 0 ? 64 + sc : 0.0));
-                }
-            }
-        };
-        if (opt && opt->host_counts) {
-            for (int e = 0; e < E; ++e) add_expert(std::max<int64_t>(0, opt->host_counts[e]), 1.0);
+        const rgg::MixedColCosts cc = rgg::mixed_col_costs(N);
+        int64_t cost_p = 0, cost_s = 0;
+        if (host_counts) {
+            for (int e = 0; e < E; ++e) rgg::mixed_add_expert(cc, opt->host_counts[e], pmin, &cost_p, &cost_s);
         } else {
-            add_expert(M_tot / E, static_cast<double>(E));
+            int64_t cp = 0, cs = 0;
+            rgg::mixed_add_expert(cc, M_tot / E, pmin, &cp, &cs);
+            cost_p = cp * E;
+            cost_s = cs * E;
         }
-        cost_p *= kPairCostFactor;
-        if (cost_p <= 0.0) {
-            pair_sms = 0;
-        } else if (cost_s <= 0.0) {
-            pair_sms = grid_cap & ~1;
-        } else {
-            pair_sms = static_cast<int>(grid_cap * cost_p / (cost_p + cost_s) + 1.0) & ~1;
-            pair_sms = std::max(2, std::min(pair_sms, (grid_cap - 1) & ~1));
-        }
+        pair_sms = rgg::mixed_pair_sms(cost_p, cost_s, grid_cap);
     }
     pair_sms = std::min(pair_sms, grid_cap & ~1);
-    const int single = grid_cap - pair_sms;
+    int single = grid_cap - pair_sms;
+    if (device_split) {
+        pair_sms = grid_cap & ~1;
+        single = grid_cap;
+    }
     if (pair_sms == 0 && single == 0) return RGG_ERR_INVALID_ARG;
 
     // shared memory: each kernel keeps the offsets, both class prefixes and the tile queue
@@ -208,6 +194,8 @@ rgg_status plan_mixed(int grid_cap, int smem_optin, int E, int64_t M_tot, int N,
     out->single_stages = st_s;
     out->single_smem = smem_s;
     out->pair_min_rows = pmin;
+    out->device_split = device_split ? 1 : 0;
+    out->split_sms = grid_cap;
     return RGG_OK;
 }
 
@@ -349,6 +337,15 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     if (want_mixed == 0 && mixed_kind && pair && bn == 256 && walk == 4 && want_walk == 0 && want_tail != -1 &&
         (want_stages == 0))
         return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out, 1);
+    // Without host counts, experts that average one to three 256-row tiles
+    // (more than 64 rows, fewer than 768): the mixed launch with fixed walks,
+    // whose kernels take the split of the SMs from the device offsets, so a
+    // skewed routing still runs its large experts on pairs and its small ones
+    // on single CTAs while the counts never reach the host.  The plain op
+    // only, as below.
+    if (want_mixed == 0 && kind == 0 && !(opt && opt->host_counts) && avg > 64.0 && avg < 768.0 && want_bm == 0 &&
+        (want_bn == 0 || want_bn == 256) && want_walk == 0 && want_tail != -1 && want_stages == 0 && grid_cap >= 2)
+        return plan_mixed(grid_cap, smem_optin, E, M_tot, N, opt, out, 2);
     // A strong skew (host counts: the largest expert above four times the
     // mean) over experts that fill 128-row tiles: the large experts on CTA
     // pairs beside the small ones on single CTAs, each kernel walking its own
@@ -626,6 +623,8 @@ rgg_status host_grouped_gemm(int num_sms, int smem_optin, int32_t* status, const
         a.sched_singles = p.single_grid;
         a.sched_claims = (p.mixed == 1) ? 1 : 0;
         a.pair_min_rows = p.pair_min_rows;
+        a.sched_split = p.device_split;
+        a.split_sms = p.split_sms;
         GemmArgs as = a;
         as.stages = p.single_stages;
         cudaError_t err = launch_gemm_mixed(p.grid, p.smem_bytes, a, p.single_grid, p.single_smem, as, st, tx, tx64,
@@ -755,6 +754,7 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->single_stages = p.single_stages;
     out->single_smem_bytes = p.single_smem;
     out->pair_min_rows = p.pair_min_rows;
+    out->device_split = p.device_split;
     if (p.mixed) out->tmem_cols = 512;
     return RGG_OK;
 }
@@ -817,6 +817,8 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
         a.sched_singles = p.single_grid;
         a.sched_claims = (p.mixed == 1) ? 1 : 0;
         a.pair_min_rows = p.pair_min_rows;
+        a.sched_split = p.device_split;
+        a.split_sms = p.split_sms;
         rgg::GemmArgs as = a;
         as.stages = p.single_stages;
         cudaError_t err = rgg::launch_gemm_mixed_swiglu(p.grid, p.smem_bytes, a, p.single_grid, p.single_smem, as, st,

@@ -85,6 +85,13 @@ struct GemmArgs {
     int32_t sched_singles = 0;  // CTAs of the 1-CTA kernel (each takes its first class-S tile without a claim)
     int32_t sched_claims = 1;   // 0: each kernel walks its own class statically (no counters, no queue)
     int32_t pair_min_rows = kPairMinRowsDefault;
+    // Fixed walks only.  1: both kernels were launched over all split_sms
+    // SMs (the pair kernel on split_sms & ~1 of them); each CTA computes the
+    // split from the device offsets (mixed_pair_sms_from_offsets) and the
+    // clusters and CTAs past their kernel's share leave at once.  0: the
+    // launched grids are the split.
+    int32_t sched_split = 0;
+    int32_t split_sms = 0;
     // 1: the kernel waits for the grid before it on the stream before its
     // first global memory access (programmatic dependent launch, see
     // pdl_wait_prerequisites); 0 only for the mixed launch's 1-CTA kernel
@@ -431,16 +438,32 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
     }
     ClassLists L;
     int32_t T;
+    // mixed launch, fixed walks: clusters of the pair kernel and CTAs of this
+    // kernel that take part (this kernel's CTA k walks positions k, k + units, ...)
+    int32_t pair_units = 0, single_units = 0;
     if constexpr (kDyn) {
         // both class lists (class P in s_pre, class S in s_order)
         if (warp == 0) build_class_prefix_warp(s_off, s_pre, E, 256, args.n_tiles_n, args.pair_min_rows, 0x7fffffff);
         if (warp == 1) build_class_prefix_warp(s_off, s_order, E, 128, args.n_tiles_n, 0, args.pair_min_rows);
+        if (warp == 2 && args.sched_split) {
+            const int ps = mixed_pair_sms_from_offsets(s_off, E, kEpi == kEpiSwiGLU ? 2 * args.N : args.N,
+                                                       args.pair_min_rows, args.split_sms);
+            if (lane == 0) misc[2] = static_cast<uint32_t>(ps);
+        }
         __syncthreads();
         L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E], kOutN};
         T = L.nP + L.nS;
         if (T == 0) {
             if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);
             pdl_wait_prerequisites();
+            return;
+        }
+        pair_units = args.sched_split ? static_cast<int32_t>(misc[2]) / 2 : args.sched_pairs;
+        single_units = args.sched_split ? args.split_sms - static_cast<int32_t>(misc[2]) : args.sched_singles;
+        if (args.sched_split && static_cast<int32_t>(blockIdx.x) >= single_units) {
+            // past this kernel's share: leave (CTA 0 still keeps the grid from
+            // ending before the pair kernel)
+            if (blockIdx.x == 0) pdl_wait_prerequisites();
             return;
         }
     } else {
@@ -636,8 +659,8 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             };
             if (kDyn && !args.sched_claims) {
                 ClassWalk cw;
-                cw.init(L, false, args.sched_pairs > 0);
-                for (int32_t p = blockIdx.x; ok && p < cw.n_positions; p += gridDim.x) {
+                cw.init(L, false, pair_units > 0);
+                for (int32_t p = blockIdx.x; ok && p < cw.n_positions; p += single_units) {
                     const TileCoord c = cw.at(L, p);
                     if (c.rows > 0) produce(c);
                 }
@@ -727,8 +750,8 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
             };
             if (kDyn && !args.sched_claims) {
                 ClassWalk cw;
-                cw.init(L, false, args.sched_pairs > 0);
-                for (int32_t p = blockIdx.x; ok && p < cw.n_positions; p += gridDim.x) {
+                cw.init(L, false, pair_units > 0);
+                for (int32_t p = blockIdx.x; ok && p < cw.n_positions; p += single_units) {
                     const TileCoord c = cw.at(L, p);
                     if (c.rows > 0) mma_tile(c);
                 }
@@ -786,8 +809,8 @@ __global__ void __launch_bounds__(cta_threads<kEpi, kFp8>(), 1)
         };
         if (kDyn && !args.sched_claims) {
             ClassWalk cw;
-            cw.init(L, false, args.sched_pairs > 0);
-            for (int32_t p = blockIdx.x; p < cw.n_positions; p += gridDim.x) {
+            cw.init(L, false, pair_units > 0);
+            for (int32_t p = blockIdx.x; p < cw.n_positions; p += single_units) {
                 const TileCoord c = cw.at(L, p);
                 if (c.rows > 0 && !epi_tile(c)) break;
             }

@@ -137,10 +137,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     }
     ClassLists L;
     int32_t T;
+    // mixed launch, fixed walks: clusters of this kernel and CTAs of the
+    // 1-CTA kernel that take part (cluster k walks positions k, k + units, ...)
+    int32_t pair_units = 0, single_units = 0;
     if constexpr (kDyn) {
         // both class lists (class P in s_pre, class S in s_order)
         if (warp == 0) build_class_prefix_warp(s_off, s_pre, E, 256, args.n_tiles_n, args.pair_min_rows, 0x7fffffff);
         if (warp == 1) build_class_prefix_warp(s_off, s_order, E, 128, args.n_tiles_n, 0, args.pair_min_rows);
+        if (warp == 2 && args.sched_split) {
+            const int ps = mixed_pair_sms_from_offsets(s_off, E, kEpi == kEpiSwiGLU ? 2 * args.N : args.N,
+                                                       args.pair_min_rows, args.split_sms);
+            if (lane == 0) misc[2] = static_cast<uint32_t>(ps);
+        }
         __syncthreads();
         L = ClassLists{s_off, s_pre, s_order, E, args.n_tiles_n, s_pre[E], s_order[E], kOutN};
         T = L.nP + L.nS;
@@ -148,6 +156,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             if (threadIdx.x == 0 && args.sched_claims) sched_cta_done(args.sched, args.sched_total);
             return;
         }
+        pair_units = args.sched_split ? static_cast<int32_t>(misc[2]) / 2 : args.sched_pairs;
+        single_units = args.sched_split ? args.split_sms - static_cast<int32_t>(misc[2]) : args.sched_singles;
+        // past this kernel's share (both CTAs of the pair alike): leave
+        if (args.sched_split && static_cast<int32_t>(pair) >= pair_units) return;
     } else {
         if (warp == 0) build_tile_prefix_warp(s_off, s_pre, E, BM, args.n_tiles_n);
         __syncthreads();
@@ -270,8 +282,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             };
             if (kDyn && !args.sched_claims) {
                 ClassWalk cw;
-                cw.init(L, true, args.sched_singles > 0);
-                for (int32_t p = pair; ok && p < cw.n_positions; p += npairs) produce(cw.at(L, p));
+                cw.init(L, true, single_units > 0);
+                for (int32_t p = pair; ok && p < cw.n_positions; p += pair_units) produce(cw.at(L, p));
             } else if constexpr (kDyn) {
                 int qs = 0;
                 uint32_t qp = 0;
@@ -377,8 +389,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             };
             if (kDyn && !args.sched_claims) {
                 ClassWalk cw;
-                cw.init(L, true, args.sched_singles > 0);
-                for (int32_t p = pair; ok && p < cw.n_positions; p += npairs) mma_tile(cw.at(L, p));
+                cw.init(L, true, single_units > 0);
+                for (int32_t p = pair; ok && p < cw.n_positions; p += pair_units) mma_tile(cw.at(L, p));
             } else if constexpr (kDyn) {
                 int qs = 0;
                 uint32_t qp = 0;
@@ -493,8 +505,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
         };
         if (kDyn && !args.sched_claims) {
             ClassWalk cw;
-            cw.init(L, true, args.sched_singles > 0);
-            for (int32_t p = pair; p < cw.n_positions; p += npairs)
+            cw.init(L, true, single_units > 0);
+            for (int32_t p = pair; p < cw.n_positions; p += pair_units)
                 if (!epi_tile(cw.at(L, p))) break;
         } else if constexpr (kDyn) {
             int qs = 0;

@@ -53,6 +53,75 @@ constexpr int kMixedBN = 256;           // both classes: MMAs 256 columns wide (
                                         // fused gate-up: 128 gate + 128 up columns, 128 outputs)
 constexpr int kPairMinRowsDefault = 256;
 
+// The split of the SMs between the two kernels follows the estimated work of
+// each class in SM-time, taken as the bytes each SM pulls into shared memory
+// per tile (what set the pace of both tile shapes on a GB300): 2 (128 + c/2)
+// for a 256-row pair tile of c columns (c rounded up to 128; 2 (64 + c/2) for
+// a pair tile of <= 128 rows), 128 + c for a 128-row 1-CTA tile (c rounded up
+// to 64; 64 + c for <= 64 rows), pair tiles weighted by 112/100: on the
+// skewed 16k workload a pair tile's unit took 1.12 times a 1-CTA tile's
+// (per-CTA traces), and the split this gives there (88 of 152 SMs on pairs)
+// measured best.  Integer arithmetic, so the host planner (with the routed
+// counts) and the kernels (from the device offsets) agree exactly.
+struct MixedColCosts {
+    int64_t p_full, p_half, s_full, s_half;  // per expert M tile, summed over its N tiles
+};
+
+__host__ __device__ inline MixedColCosts mixed_col_costs(int N) {
+    MixedColCosts c = {0, 0, 0, 0};
+    for (int c0 = 0; c0 < N; c0 += kMixedBN) {
+        const int cols = (N - c0 < kMixedBN) ? N - c0 : kMixedBN;
+        const int64_t pc = ((cols + 127) / 128) * 128;
+        const int64_t sc = ((cols + 63) / 64) * 64;
+        c.p_full += 2 * (128 + pc / 2);
+        c.p_half += 2 * (64 + pc / 2);
+        c.s_full += 128 + sc;
+        c.s_half += 64 + sc;
+    }
+    return c;
+}
+
+// Adds expert rows m to the class costs.
+__host__ __device__ inline void mixed_add_expert(const MixedColCosts& c, int64_t m, int pair_min_rows, int64_t* cost_p,
+                                                 int64_t* cost_s) {
+    if (m <= 0) return;
+    if (m >= pair_min_rows) {
+        const int64_t rem = m % 256;
+        *cost_p += (m / 256) * c.p_full + (rem > 128 ? c.p_full : rem > 0 ? c.p_half : 0);
+    } else {
+        const int64_t rem = m % 128;
+        *cost_s += (m / 128) * c.s_full + (rem > 64 ? c.s_full : rem > 0 ? c.s_half : 0);
+    }
+}
+
+// SMs (even) for the pair kernel out of `sms`: all when there is no class-S
+// work, none when there is no class-P work, else the cost share rounded up to
+// an even count within [2, sms - 1].
+__host__ __device__ inline int mixed_pair_sms(int64_t cost_p, int64_t cost_s, int sms) {
+    if (cost_p <= 0) return 0;
+    if (cost_s <= 0) return sms & ~1;
+    const int64_t wp = 112 * cost_p, ws = 100 * cost_s;
+    int pair = static_cast<int>((static_cast<int64_t>(sms) * wp + wp + ws) / (wp + ws)) & ~1;
+    const int hi = (sms - 1) & ~1;
+    pair = pair < 2 ? 2 : pair;
+    return pair > hi ? hi : pair;
+}
+
+// The same split from the device offsets (one warp; lane 0 returns it).
+__device__ __forceinline__ int mixed_pair_sms_from_offsets(const int32_t* s_off, int E, int N, int pair_min_rows,
+                                                           int sms) {
+    const int lane = threadIdx.x & 31;
+    const MixedColCosts c = mixed_col_costs(N);
+    int64_t cp = 0, cs = 0;
+    for (int e = lane; e < E; e += 32) mixed_add_expert(c, s_off[e + 1] - s_off[e], pair_min_rows, &cp, &cs);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        cp += __shfl_xor_sync(0xffffffffu, cp, d);
+        cs += __shfl_xor_sync(0xffffffffu, cs, d);
+    }
+    return mixed_pair_sms(cp, cs, sms);
+}
+
 struct ClassLists {
     const int32_t* s_off;
     const int32_t* s_preP;  // class P prefix of 256-row tiles

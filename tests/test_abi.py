@@ -375,11 +375,18 @@ def test_plan_mixed_launch(lib):
     assert (p["grid"], p["single_grid"]) == (0, 152)
     p = rgg.rgg_plan(4, 256, 256, 512, host_counts=[100, 0, 300, 1], mixed=1, max_ctas=3)
     assert p["grid"] == 2 and p["single_grid"] == 1
-    # chosen by the planner: fixed walks for a strong skew over 128-row tiles (host counts only),
-    # claims for experts of three or more 256-row tiles; off for balanced mid-size experts,
-    # small groups, and without counts unless the experts average three 256-row tiles
+    # chosen by the planner: fixed walks for a strong skew over 128-row tiles (host counts), claims
+    # for experts of three or more 256-row tiles; off for balanced mid-size experts and small groups.
+    # Without counts, experts of one to three 256-row tiles on average take the fixed walks with the
+    # split from the device offsets (both kernels over all the SMs)
     assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=skew)["mixed"] == 2
-    assert rgg.rgg_plan(64, 16384, 1024, 2688)["mixed"] == 0
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=skew)["device_split"] == 0
+    p = rgg.rgg_plan(64, 16384, 1024, 2688)
+    assert (p["mixed"], p["device_split"], p["grid"], p["single_grid"]) == (2, 1, 152, 152)
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, max_ctas=9)
+    assert (p["mixed"], p["device_split"], p["grid"], p["single_grid"]) == (2, 1, 8, 9)
+    assert rgg.rgg_plan(64, 4096, 1024, 2688)["mixed"] == 0          # 64 rows per expert
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, op="swiglu")["mixed"] == 0
     assert rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=[256] * 64)["mixed"] == 0
     assert rgg.rgg_plan(64, 2048, 1024, 2688, host_counts=wl.workload_counts("skew2k"))["mixed"] == 0
     assert rgg.rgg_plan(32, 32768, 6144, 4096)["mixed"] == 1
@@ -388,9 +395,12 @@ def test_plan_mixed_launch(lib):
     assert rgg.rgg_plan(64, 16384, 1024, 1344, host_counts=skew, op="swiglu")["mixed"] == 0
     p = rgg.rgg_plan(64, 16384, 1024, 1344, host_counts=skew, op="swiglu", mixed=2)
     assert p["mixed"] == 2 and p["grid"] > 0 and p["single_grid"] > 0
-    # the fixed walks on request
+    # the fixed walks on request; an explicit split or claims keep the launched grids as the split
     p = rgg.rgg_plan(64, 16384, 1024, 2688, host_counts=skew, mixed=2, mixed_pair_sms=76)
     assert (p["mixed"], p["grid"], p["single_grid"]) == (2, 76, 76)
+    p = rgg.rgg_plan(64, 16384, 1024, 2688, mixed=2, mixed_pair_sms=76)
+    assert (p["mixed"], p["grid"], p["single_grid"], p["device_split"]) == (2, 76, 76, 0)
+    assert rgg.rgg_plan(64, 16384, 1024, 2688, mixed=1)["device_split"] == 0
 
 
 @pytest.mark.parametrize("kw,status", [(dict(bm=128), "INVALID_ARG"), (dict(bn=128), "INVALID_ARG"),

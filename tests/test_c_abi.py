@@ -38,10 +38,10 @@ static void plan(int E, int64_t M, int K, int N, const int32_t* counts, int op, 
     rgg_plan_info p;
     memset(&p, 0, sizeof(p));
     rgg_status s = rgg_plan(0, 0, E, M, K, N, &o, &p);
-    printf("%d %d %d %d %d %d %d %d %lld %d %d %d %lld %d %d %d %d %d\n", (int)s, p.bm, p.bn, p.bk, p.stages,
+    printf("%d %d %d %d %d %d %d %d %lld %d %d %d %lld %d %d %d %d %d %d\n", (int)s, p.bm, p.bn, p.bk, p.stages,
            p.grid, p.threads, p.smem_bytes, (long long)p.max_tiles, p.tail64, p.walk_order, p.gather_mode,
            (long long)p.workspace_bytes, p.mixed, p.single_grid, p.single_stages, p.single_smem_bytes,
-           p.pair_min_rows);
+           p.pair_min_rows, p.device_split);
 }
 
 int main(void) {
@@ -118,7 +118,7 @@ def test_c_program_sees_the_same_plans_as_python(c_output):
         p = rgg.rgg_plan(case["E"], case["M"], case["K"], case["N"], **kw)
         fields = ["bm", "bn", "bk", "stages", "grid", "threads", "smem_bytes", "max_tiles", "tail64", "walk_order",
                   "gather_mode", "workspace_bytes", "mixed", "single_grid", "single_stages", "single_smem_bytes",
-                  "pair_min_rows"]
+                  "pair_min_rows", "device_split"]
         assert vals[1:] == [p[f] for f in fields], (case, vals, p)
 
 

@@ -61,7 +61,8 @@ GEMM_OPTS = [dict(bm=64, bn=128), dict(bm=64, bn=256), dict(bm=128, bn=192), dic
              dict(bm=128, bn=256, tail64=-1), dict(bm=256, bn=128), dict(bm=256, bn=256), dict(walk_order=3),
              dict(walk_order=4, bm=256), dict(mixed=1), dict(mixed=1, mixed_pair_sms=-1),
              dict(mixed=1, mixed_pair_sms=2), dict(mixed=1, max_ctas=5), dict(mixed=2), dict(mixed=2, mixed_pair_sms=-1),
-             dict(mixed=2, mixed_pair_sms=4, max_ctas=7)]
+             dict(mixed=2, mixed_pair_sms=4, max_ctas=7), dict(mixed=2, host_counts=None),
+             dict(mixed=2, host_counts=None, max_ctas=7)]
 
 
 @pytest.mark.parametrize("opts", GEMM_OPTS, ids=[str(o) for o in GEMM_OPTS])
@@ -70,14 +71,16 @@ def test_grouped_gemm_edges(opts, K, integer):
     inp = wl.make_custom(EDGE_PAIRS, K=K, N=520, seed=171, integer_valued=integer, spare_rows=3)
     X, W = inp.X.cuda(), inp.W.cuda()
     Y = _canary(X.shape[0], 520)
-    rgg.rgg_grouped_gemm(X, W, torch.from_numpy(inp.offsets).cuda(), Y, check=True, host_counts=inp.counts, **opts)
+    kw = dict(host_counts=inp.counts)
+    kw.update(opts)  # host_counts=None: the split of a mixed launch from the device offsets
+    rgg.rgg_grouped_gemm(X, W, torch.from_numpy(inp.offsets).cuda(), Y, check=True, **kw)
     torch.cuda.synchronize()
     ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
     _check(Y.cpu(), ref, 0, int(inp.offsets[-1]), integer)
 
 
 @pytest.mark.parametrize("opts", [dict(bm=64, bn=128), dict(bm=128, bn=256), dict(bm=256, bn=256), dict(mixed=1),
-                                  dict(mixed=2, host_counts=True), dict(mixed=1, mixed_pair_sms=-1)])
+                                  dict(mixed=2, host_counts=True), dict(mixed=1, mixed_pair_sms=-1), dict(mixed=2)])
 def test_swiglu_edges(opts):
     inp = wl.make_custom(EDGE_PAIRS, K=264, N=2 * 520, seed=172, spare_rows=2)
     X, W = inp.X.cuda(), inp.W.cuda()

@@ -142,6 +142,57 @@ def test_bounded_wait_reports_timeout_and_context_survives(opts):
     _check(inp, _run(inp, mixed=mode, host_counts=inp.counts, **opts), exact=False)
 
 
+# the split of the SMs taken on the device from the offsets (fixed walks, no host counts): both
+# kernels launched over all the SMs, the CTAs past their kernel's share leave at once
+SPLIT_COUNTS = [COUNTS, [256] * 19, [16] * 19, [0] * 18 + [3000], [2000, 1] * 9 + [0], [0] * 19]
+
+
+@pytest.mark.parametrize("counts", SPLIT_COUNTS, ids=["mixed", "all-pairs", "all-single", "one", "alternating",
+                                                      "empty"])
+@pytest.mark.parametrize("max_ctas", [0, 2, 3, 9])
+def test_split_from_device_offsets(counts, max_ctas):
+    inp = wl.make_custom(counts, K=64, N=520, seed=169, integer_valued=True, spare_rows=5)
+    E, M = len(counts), int(inp.offsets[-1])
+    if M == 0:
+        pytest.skip("no rows: nothing to plan")
+    p = rgg.rgg_plan(E, M, 64, 520, mixed=2, max_ctas=max_ctas)
+    assert p["device_split"] == 1
+    _check(inp, _run(inp, mixed=2, max_ctas=max_ctas), exact=True)
+    # the same offsets again: the graph of a replayed step sees the split it planned
+    _check(inp, _run(inp, mixed=2, max_ctas=max_ctas), exact=True)
+
+
+def test_split_from_device_offsets_follows_new_routing_in_a_graph():
+    # one captured launch planned without counts, replayed on offsets of other shapes
+    K, N = 128, 392
+    shapes = [COUNTS, [16] * 19, [1500] + [10] * 18, [256] * 19]
+    inps = [wl.make_custom(c, K=K, N=N, seed=170 + i, spare_rows=0) for i, c in enumerate(shapes)]
+    M = max(int(i.offsets[-1]) for i in inps)
+    X = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    W = inps[0].W.cuda()
+    off = torch.zeros(len(COUNTS) + 1, dtype=torch.int32, device="cuda")
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    off.copy_(torch.from_numpy(inps[0].offsets))
+    rgg.rgg_grouped_gemm(X, W, off, Y, check=True, mixed=2)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        rgg.rgg_grouped_gemm(X, W, off, Y, mixed=2)
+    for inp in inps + inps[::-1]:
+        m = int(inp.offsets[-1])
+        X.zero_()
+        X[:m].copy_(inp.X[:m].cuda())
+        W.copy_(inp.W.cuda())
+        off.copy_(torch.from_numpy(inp.offsets))
+        Y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert rgg.rgg_query_status() == rgg.RGG_OK
+        ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
+        got = Y[:m].double().cpu().numpy()
+        err = np.abs(got - ref[:m])
+        assert (err <= RTOL * np.maximum(1.0, np.abs(ref[:m]))).all()
+
+
 def test_repeated_calls_and_graph_replay():
     # the counters are zeroed per call; a captured call (memset + pair kernel +
     # 1-CTA kernel launched after it) replays on new data
@@ -174,7 +225,8 @@ def test_full_size(name):
     ref = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
     X, W = inp.X.cuda(), inp.W.cuda()
     off = torch.from_numpy(inp.offsets).cuda()
-    for opts in (dict(host_counts=inp.counts, mixed=1), dict(mixed=1), dict(host_counts=inp.counts, mixed=2)):
+    for opts in (dict(host_counts=inp.counts, mixed=1), dict(mixed=1), dict(host_counts=inp.counts, mixed=2),
+                 dict(mixed=2)):
         Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device="cuda")
         rgg.rgg_grouped_gemm(X, W, off, Y, check=True, **opts)
         torch.cuda.synchronize()
