@@ -91,6 +91,8 @@ def parse_args():
                         "through its token index inside the kernel")
     p.add_argument("--profile", action="store_true",
                    help="for ncu: --warmup launches then one more, no timing, no CPU work after")
+    p.add_argument("--no-host-counts", action="store_true",
+                   help="with --profile: plan from the device offsets alone (no host counts)")
     return p.parse_args()
 
 
@@ -282,7 +284,7 @@ def run_profile(args):
     off = torch.from_numpy(inp.offsets).to(dev)
     Y = torch.empty(X.shape[0], W.shape[2], dtype=torch.bfloat16, device=dev)
     opts = dict(bm=args.bm, bn=args.bn, stages=args.stages, tail64=args.tail64,
-                walk_order=args.walk_order, host_counts=inp.counts)
+                walk_order=args.walk_order, host_counts=None if args.no_host_counts else inp.counts)
     if args.op in ("gemm", "swiglu"):
         opts.update(mixed=args.mixed, mixed_pair_sms=args.mixed_pair_sms)
     if args.op == "gather":
@@ -382,6 +384,9 @@ class Step:
             self.opts.update(mixed=args.mixed, mixed_pair_sms=args.mixed_pair_sms)
         self.plan_from = ("host-side routed counts (tile shape only)" if host_counts
                           else "device offsets only (no host counts)")
+        # the key of this launch's DRAM capture in profiles/dram_traffic.json
+        self.traffic_key = (workload if op == "gemm" else workload + "+" + op) + ("" if host_counts
+                                                                                 else " (device offsets)")
         if self.gather:
             self.opts["gather_mode"] = args.gather_mode
             # the two-pass mode's gathered rows, allocated once outside the timed region
@@ -520,7 +525,7 @@ def roofline_of(step, launch_ms, peaks):
                 "peak": tc_peak, "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     # the capture of this exact launch: the workload, and the op when it is not the plain GEMM
-    roof["traffic"] = measured_traffic(step.workload if op == "gemm" else step.workload + "+" + op)
+    roof["traffic"] = measured_traffic(step.traffic_key)
     roof["peak_source"] = peaks["source"] + (" bf16 x 2 (nominal fp8/bf16 ratio)" if op == "fp8" else "")
     roof["algorithmic_per_launch"] = {"flops": step.flops, "bytes": step.bytes}
     roof["launch_ms"] = round(launch_ms, 5)
