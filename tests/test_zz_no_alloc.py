@@ -48,19 +48,21 @@ def _call(lib, X, W, off, Y, status):
                                         status.data_ptr() if status is not None else None, stream)
 
 
-# the last case is planned as the mixed launch (large experts on CTA pairs with device-side tile
-# claims), whose claim counters also live in the fixed device array: two calls in a row check that
-# the first leaves them ready for the second
-@pytest.mark.parametrize("counts,K,N,spare", [([37, 0, 64, 155], 256, 512, 0),
-                                              ([500, 3, 0, 257, 1024, 77, 129, 2], 512, 520, 9),
-                                              ([16] * 32, 1024, 2048, 0),
-                                              ([1000, 1100, 900, 1100, 1050, 990, 1010, 1042], 256, 4096, 4)])
-def test_noalloc_matches_handle_entry_point_and_oracle_twice(lib, counts, K, N, spare):
+# The second case is planned as the mixed launch with fixed walks whose SM split is taken on the
+# device (no host counts), the last as the mixed launch with device-side tile claims, whose claim
+# counters also live in the fixed device array: two calls in a row check that the first leaves
+# them ready for the second.
+@pytest.mark.parametrize("counts,K,N,spare,mixed", [([37, 0, 64, 155], 256, 512, 0, 0),
+                                                    ([500, 3, 0, 257, 1024, 77, 129, 2], 512, 520, 9, 2),
+                                                    ([16] * 32, 1024, 2048, 0, 0),
+                                                    ([1000, 1100, 900, 1100, 1050, 990, 1010, 1042], 256, 4096,
+                                                     4, 1)])
+def test_noalloc_matches_handle_entry_point_and_oracle_twice(lib, counts, K, N, spare, mixed):
     inp = wl.make_custom(counts, K=K, N=N, seed=51, spare_rows=spare)
     X, W = inp.X.cuda(), inp.W.cuda()
     off = torch.from_numpy(inp.offsets).cuda()
     plan = rgg.rgg_plan(len(counts), X.shape[0], K, N)
-    assert plan["mixed"] == (1 if len(counts) == 8 and counts[0] == 1000 else 0)
+    assert plan["mixed"] == mixed
     handle = rgg.rgg_grouped_gemm(X, W, off, check=True).double().cpu().numpy()
     exact = oracle.grouped_gemm(wl.bf16_bits(inp.X), wl.bf16_bits(inp.W), inp.offsets)
     M_used = int(inp.offsets[-1])
