@@ -53,6 +53,14 @@ constexpr int kStatusBadOffsets = 4;
 constexpr int kStatusBadRowIndex = 7;
 constexpr int kStatusCapacity = 6;
 constexpr int kMaxStages = 16;
+// The CTA-pair kernel's static walk: the producer, which decodes every tile
+// it loads, leaves the tile's MMA instruction descriptor for the MMA thread in
+// a ring of kInfoSlots words in shared memory (slot = tile count mod
+// kInfoSlots), written before its arrive on the tile's first stage; the MMA
+// thread reads it after its wait on that stage (the arrive releases the
+// write), so it runs no decode of its own between two tiles.  The producer is
+// at most kMaxStages stages, so tiles, ahead: twice that many slots.
+constexpr int kInfoSlots = 2 * kMaxStages;
 constexpr int kThreads = 192;
 constexpr int kBK = 64;                  // K elements per stage = one 128-byte swizzle row
 constexpr uint64_t kDrainLimitNs = 2000000000ull;  // teardown waits for copies/MMAs already issued
@@ -119,8 +127,10 @@ __host__ __device__ inline SmemPlan smem_plan(int BM, int BN, int stages, int E,
     p.a_off = 0;
     p.b_off = p.a_off + stages * p.a_stage;
     p.bar_off = p.b_off + stages * p.b_stage;          // full[S], empty[S], acc_full[2], acc_empty[2], drain
-    p.misc_off = p.bar_off + 8u * (2u * stages + 5u);   // tmem base, abort flag (16 B reserved)
-    p.off_off = p.misc_off + 16u;
+    // misc: tmem base, abort flag, the mixed launch's SM split, one spare word,
+    // then the pair kernel's ring of kInfoSlots instruction descriptors
+    p.misc_off = p.bar_off + 8u * (2u * stages + 5u);
+    p.off_off = p.misc_off + 16u + 4u * kInfoSlots;
     p.pre_off = p.off_off + ex;
     p.ord_off = p.pre_off + ex;
     p.spre_off = p.ord_off + ((sorted || mixed) ? ex : 0u);

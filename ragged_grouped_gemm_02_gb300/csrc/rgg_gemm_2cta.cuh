@@ -113,6 +113,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     auto acce_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
     uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + sp.misc_off);
+    volatile uint32_t* info_ring = misc + 4;  // static walk: the leader's MMA instruction descriptors (kInfoSlots)
     int32_t* s_off = reinterpret_cast<int32_t*>(gbase + sp.off_off);
     int32_t* s_pre = reinterpret_cast<int32_t*>(gbase + sp.pre_off);
     int32_t* s_order = reinterpret_cast<int32_t*>(gbase + sp.ord_off);  // walk order 3; mixed: class S prefix
@@ -241,6 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             int st = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;
+            uint32_t n_produced = 0;  // tiles loaded: the slot of the next one in the descriptor ring
             bool ok = true;
             auto produce = [&](const TileCoord& c) {
                 (void)RGG_BOUNDS_OK(tile_ok(c.expert, c.row0, c.rows, c.col0, s_off, E, args.N), args.status);
@@ -260,7 +262,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                         break;
                     }
                     const uint32_t full_leader = map_to_rank(full_bar(st), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(st), tx_bytes);
+                    if (rank == 0) {
+                        // static walk: the MMA thread reads it after its wait on this stage (this
+                        // arrive releases it)
+                        if (!kDyn && kb == 0)
+                            info_ring[n_produced++ % kInfoSlots] =
+                                idesc_bf16_f32(half ? 128 : 256, pair_tile_cols<BN, kEpi>(c.col0, args.N), true);
+                        mbar_arrive_expect_tx(full_bar(st), tx_bytes);
+                    }
                     // the second CTA's rows may start past M_tot (a short tile at the end of X): the copy
                     // zero-fills them, so the row check allows one tile of overhang
                     if (RGG_BOUNDS_OK(x_box_ok(kb * Cfg::kKStage, a_row, args.K, args.M_tot + 128, 2), args.status))
@@ -351,9 +360,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
             int acc = 0;
             uint32_t acc_ph = 0;
             bool ok = true;
-            auto mma_tile = [&](const TileCoord& c) {
-                const uint32_t idesc = idesc_bf16_f32(half_tile(c) ? 128 : 256, pair_tile_cols<BN, kEpi>(c.col0, args.N),
-                                                      true);
+            uint32_t n_tiles = 0;  // tiles issued: the slot of the next one in the producer's descriptor ring
+            // One tile.  from_ring (the static walk): its instruction
+            // descriptor is the producer's ring entry, read once the tile's
+            // first stage has landed; else `idesc`, decoded here.
+            auto mma_tile = [&](uint32_t idesc, bool from_ring) {
                 if (!pair_wait_or_abort(acce_bar(acc), acc_ph ^ 1u, abort_flag, peer_flag, args.status,
                                         args.timeout_ns)) {
                     ok = false;
@@ -367,6 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                         return;
                     }
                     tc_fence_after_sync();
+                    if (kb == 0 && from_ring) idesc = info_ring[n_tiles % kInfoSlots];
                     const uint32_t a_st = a0 + st * sp.a_stage;
                     const uint32_t b_st = b0 + st * sp.b_stage;
 #pragma unroll
@@ -386,11 +398,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                     acc = 0;
                     acc_ph ^= 1u;
                 }
+                ++n_tiles;
             };
             if (kDyn && !args.sched_claims) {
                 ClassWalk cw;
                 cw.init(L, true, single_units > 0);
-                for (int32_t p = pair; ok && p < cw.n_positions; p += pair_units) mma_tile(cw.at(L, p));
+                for (int32_t p = pair; ok && p < cw.n_positions; p += pair_units) {
+                    const TileCoord c = cw.at(L, p);
+                    mma_tile(idesc_bf16_f32(half_tile(c) ? 128 : 256, pair_tile_cols<BN, kEpi>(c.col0, args.N), true),
+                             false);
+                }
             } else if constexpr (kDyn) {
                 int qs = 0;
                 uint32_t qp = 0;
@@ -401,10 +418,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                         break;
                     }
                     if (c.expert < 0) break;
-                    mma_tile(c);
+                    mma_tile(idesc_bf16_f32(half_tile(c) ? 128 : 256, pair_tile_cols<BN, kEpi>(c.col0, args.N), true),
+                             false);
                 }
             } else {
-                for (int32_t t = pair; ok && t < T; t += npairs) mma_tile(tile_at(t));
+                // every position of the walk is a tile: count them, take the descriptors from the ring
+                const int32_t b = static_cast<int32_t>(pair);  // < T: the others left after S1
+                const int32_t count = (T - b + static_cast<int32_t>(npairs) - 1) / static_cast<int32_t>(npairs);
+                for (int32_t i = 0; ok && i < count; ++i) mma_tile(0u, true);
             }
             if (!ok) {
                 mma_commit_pair(drain_bar, 0x1);
