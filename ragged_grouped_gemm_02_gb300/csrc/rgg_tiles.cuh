@@ -28,7 +28,7 @@ struct TileCoord {
 
 // Load off[0..E] into shared memory and check validity:
 // 0 <= off[0] <= off[1] <= ... <= off[E] <= M_tot.  Every thread of the
-// block must call this; returns the same verdict in every thread.
+// block must call this; returns the same answer in every thread.
 __device__ __forceinline__ bool load_and_check_offsets(const int32_t* __restrict__ g_off, int32_t* s_off, int E,
                                                        int64_t M_tot) {
     int bad = 0;
