@@ -403,6 +403,45 @@ def test_plan_mixed_launch(lib):
     assert rgg.rgg_plan(64, 16384, 1024, 2688, mixed=1)["device_split"] == 0
 
 
+def _mixed_split(counts, N, pmin, sms):
+    # The SM split of the mixed launch restated: per 256-column tile, 2 (128 + c/2) for a 256-row
+    # pair tile (c rounded up to 128; 2 (64 + c/2) for a pair tile of <= 128 rows), 128 + c for a
+    # 128-row 1-CTA tile (c rounded up to 64; 64 + c for <= 64 rows); pair work weighted 112/100;
+    # the pair share of the SMs rounded up to an even count within [2, sms - 1].
+    cp = cs = 0
+    for m in counts:
+        for c0 in range(0, N, 256):
+            cols = min(256, N - c0)
+            pc, sc = -(-cols // 128) * 128, -(-cols // 64) * 64
+            if m >= pmin:
+                r = m % 256
+                cp += (m // 256) * 2 * (128 + pc // 2) + (2 * (128 + pc // 2) if r > 128 else
+                                                          2 * (64 + pc // 2) if r > 0 else 0)
+            elif m > 0:
+                r = m % 128
+                cs += (m // 128) * (128 + sc) + ((128 + sc) if r > 64 else (64 + sc) if r > 0 else 0)
+    if cp == 0:
+        return 0
+    if cs == 0:
+        return sms & ~1
+    wp, ws = 112 * cp, 100 * cs
+    pair = ((sms * wp + wp + ws) // (wp + ws)) & ~1
+    return min(max(pair, 2), (sms - 1) & ~1)
+
+
+@pytest.mark.parametrize("counts,N,pmin", [("skew16k", 2688, 256), ("worklog_skew16k", 2688, 256),
+                                           ("skew16k", 2688, 512), ([300, 5, 70, 129, 1000, 0], 520, 256),
+                                           ([256] * 8 + [16] * 8, 4096, 256), ([16] * 32, 4096, 256),
+                                           ([1000] * 4, 136, 256)])
+@pytest.mark.parametrize("sms", [152, 9, 3])
+def test_plan_mixed_split_matches_its_cost_model(lib, counts, N, pmin, sms):
+    from ragged_grouped_gemm_02_gb300 import workloads as wl
+    c = [int(x) for x in (wl.workload_counts(counts) if isinstance(counts, str) else counts)]
+    p = rgg.rgg_plan(len(c), sum(c), 1024, N, host_counts=c, mixed=2, max_ctas=sms, pair_min_rows=pmin)
+    pair = min(_mixed_split(c, N, pmin, sms), sms & ~1)
+    assert (p["grid"], p["single_grid"], p["device_split"]) == (pair, sms - pair, 0)
+
+
 @pytest.mark.parametrize("kw,status", [(dict(bm=128), "INVALID_ARG"), (dict(bn=128), "INVALID_ARG"),
                                        (dict(tail64=-1), "INVALID_ARG"), (dict(mixed_pair_sms=3), "INVALID_ARG"),
                                        (dict(mixed_pair_sms=154), "INVALID_ARG"),
