@@ -55,8 +55,9 @@ def _close(got, ref):
         bad.shape[0], bad[0].tolist(), got[tuple(bad[0])], ref[tuple(bad[0])])
 
 
-@pytest.mark.parametrize("opts", [dict(), dict(bm=64, bn=128), dict(bm=128, bn=256), dict(bm=256, bn=256)],
-                         ids=["auto", "64x128", "128x256", "pair"])
+@pytest.mark.parametrize("opts", [dict(), dict(bm=64, bn=128), dict(bm=128, bn=256), dict(bm=256, bn=256),
+                                  dict(mixed=1), dict(mixed=2)],
+                         ids=["auto", "64x128", "128x256", "pair", "mixed-claims", "mixed-device-split"])
 def test_max_experts_bit_exact(opts):
     rng = np.random.default_rng(4096)
     counts = rng.integers(0, 6, 4096) * (rng.random(4096) < 0.6)
@@ -89,16 +90,19 @@ def _random_case(seed):
     K = int(rng.choice([64, 128, 200, 264, 512]))
     N = 8 * int(rng.integers(2, 96))
     choices = [dict(), dict(bm=64), dict(bm=128), dict(bm=256), dict(bm=128, bn=192), dict(bm=64, bn=128),
-               dict(bm=256, bn=128), dict(bm=128, tail64=-1), dict(bm=256, tail64=-1)]
+               dict(bm=256, bn=128), dict(bm=128, tail64=-1), dict(bm=256, tail64=-1), dict(mixed=1),
+               dict(mixed=2), dict(mixed=2, no_counts=True)]
     opts = dict(choices[int(rng.integers(len(choices)))])
-    walks = [0, 1, 2, 3, 4] if E <= 256 else [0, 1, 2, 4]
-    opts["walk_order"] = int(rng.choice(walks))
-    if rng.random() < 0.5:
+    if not opts.get("mixed"):
+        walks = [0, 1, 2, 3, 4] if E <= 256 else [0, 1, 2, 4]
+        opts["walk_order"] = int(rng.choice(walks))
+    no_counts = opts.pop("no_counts", False)  # the mixed launch's SM split from the device offsets
+    if rng.random() < 0.5 and not no_counts:
         opts["host_counts"] = counts
     return counts, K, N, opts
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(32))
 def test_random_configurations(seed):
     counts, K, N, opts = _random_case(seed)
     inp = wl.make_custom(counts, K=K, N=N, seed=2000 + seed, spare_rows=int(seed % 3) * 5)
