@@ -352,8 +352,8 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     // class (measured on the skewed 16k workload: 855-868 TFLOP/s for the
     // size-sorted 128 x 256 walk, 906 for the mixed launch with fixed walks,
     // 841 with claims, whose descriptor queue costs a few microseconds).  The
-    // plain op only: the fused gate-up op's pair tiles keep 256-row tails, and
-    // there it lost (867 -> 730 TFLOP/s).
+    // plain op only: on the fused gate-up op it runs level with the static
+    // 128 x 256 walk (870 against 868 TFLOP/s), not ahead.
     if (want_mixed == 0 && kind == 0 && skewed && bm == 128 && want_bm == 0 && (want_bn == 0 || want_bn == 256) &&
         want_walk == 0 && want_tail != -1 && want_stages == 0) {
         Plan mp;
@@ -746,7 +746,7 @@ rgg_status rgg_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, in
     out->max_tiles = p.max_tiles;
     out->tail64 = p.tail64;
     out->walk_order = p.walk_order;
-    if (swiglu && p.bm == 256) out->tail64 = 0;  // fused gate-up pairs keep 256-row tail tiles
+    if (swiglu && p.bm == 256 && p.bn != 256) out->tail64 = 0;  // 128-column gate-up pairs keep 256-row tails
     out->gather_mode = mode;
     out->workspace_bytes = prefers_two_pass ? gather_workspace_bytes(M_tot, K) : 0;
     out->mixed = p.mixed;
@@ -810,7 +810,7 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
     a.tail64 = p.tail64;
     a.walk_order = p.walk_order;
     if (p.mixed) {
-        // as for rgg_grouped_gemm's mixed launch; the pair kernel keeps 256-row tail tiles here
+        // as for rgg_grouped_gemm's mixed launch
         a.sched = h->d_status + 16;
         a.sched_total = p.grid + p.single_grid;
         a.sched_pairs = p.grid / 2;
@@ -829,7 +829,7 @@ rgg_status rgg_grouped_gemm_swiglu(rgg_handle* h, const void* X, const void* W13
         }
         return RGG_OK;
     }
-    if (p.bm == 256) a.tail64 = 0;  // the pair's 128-row tail layout splits gate and up across warps
+    if (p.bm == 256 && p.bn != 256) a.tail64 = 0;  // 128-column pairs: a 64-column panel cannot hold gate and up
     cudaError_t err = (p.bm == 256) ? rgg::launch_gemm_pair_swiglu(p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a)
                                     : rgg::launch_gemm_swiglu(p.bm, p.bn, p.grid, p.smem_bytes, st, tx, tx64, tw, a);
     return err == cudaSuccess ? RGG_OK : cuda_failure(err, "grouped_gemm_swiglu launch");

@@ -65,7 +65,13 @@ __device__ __forceinline__ bool pair_runs_as_128_rows(const GemmArgs& args, cons
 // BN/2 output columns; CTA 0 loads the BN/2 gate columns and CTA 1 the
 // matching BN/2 up columns as the two halves of B, so the M = 256 MMA leaves
 // [gate | up] side by side in each CTA's TMEM for that CTA's 128 rows, and the
-// epilogue writes silu(gate) * up.  Tail tiles run at M = 256 in this mode.
+// epilogue writes silu(gate) * up.  A tail tile of <= 128 rows (BN = 256)
+// runs as an M = 128 pair MMA, whose accumulator puts the first half of B's
+// columns in TMEM lanes 0-63 and the second half in lanes 64-127 (see the
+// epilogue); so that each lane holds a gate column and its up column, CTA r
+// then loads gate columns [64 r, 64 r + 64) and the matching up columns of
+// the tile, and lanes 0-63 / 64-127 produce output columns [0, 64) / [64, 128).
+// (BN = 128 keeps tails at M = 256: a 64-column panel cannot be split.)
 // Epilogue warps per CTA: four for plain bf16 outputs, eight (two per TMEM
 // lane quadrant, each on half of the columns) for the fused gate-up epilogue,
 // whose exponentials otherwise outlast the main loop (measured: uniform 845 ->
@@ -89,7 +95,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
     static_assert(!kDyn || BN == kMixedBN, "the mixed launch's pairs run 256-column MMAs");
     constexpr int BM = 256;  // rows per pair tile
     constexpr int kOutN = (kEpi == kEpiSwiGLU) ? BN / 2 : BN;  // output columns per tile
-    auto half_tile = [&](const TileCoord& c) { return kEpi == kEpiPlain && pair_runs_as_128_rows(args, c); };
+    auto half_tile = [&](const TileCoord& c) {
+        return (kEpi == kEpiPlain || BN == 256) && pair_runs_as_128_rows(args, c);
+    };
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
     const int warp = threadIdx.x >> 5;
@@ -275,13 +283,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                     if (RGG_BOUNDS_OK(x_box_ok(kb * Cfg::kKStage, a_row, args.K, args.M_tot + 128, 2), args.status))
                         tma_load_2d_pair(a0 + st * sp.a_stage, xmap, full_leader, kb * Cfg::kKStage, a_row);
 #pragma unroll
-                    for (int p = 0; p < Cfg::kPanels; ++p)
-                        if (p < np && RGG_BOUNDS_OK(w_box_ok(b_col + Cfg::kPanelN * p, kb * Cfg::kKStage, c.expert,
+                    for (int p = 0; p < Cfg::kPanels; ++p) {
+                        // a gate-up tail tile: panel 0 this CTA's 64 gate columns, panel 1 their up columns
+                        const int32_t wc = (kEpi == kEpiSwiGLU && half)
+                                               ? (p == 0 ? c.col0 : args.N + c.col0) +
+                                                     Cfg::kPanelN * static_cast<int32_t>(rank)
+                                               : b_col + Cfg::kPanelN * p;
+                        if (p < np && RGG_BOUNDS_OK(w_box_ok(wc, kb * Cfg::kKStage, c.expert,
                                                              kEpi == kEpiSwiGLU ? 2 * int64_t(args.N) : args.N,
                                                              args.K, E, 2, Cfg::kPanelN),
                                                     args.status))
-                            tma_load_3d_pair(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_leader,
-                                             b_col + Cfg::kPanelN * p, kb * Cfg::kKStage, c.expert);
+                            tma_load_3d_pair(b0 + st * sp.b_stage + p * Cfg::kPanelB, &tmap_w, full_leader, wc,
+                                             kb * Cfg::kKStage, c.expert);
+                    }
                     ++issued;
                     if (++st == S) {
                         st = 0;
@@ -474,10 +488,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * pair_epilo
                 const bool ld_ok = RGG_BOUNDS_OK(tmem_cols_ok(tcol, 32, Cfg::kTmemCols), args.status);
                 if (ld_ok) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(cc), v);
                 if constexpr (kEpi == kEpiSwiGLU) {
-                    // gate in columns [cc, cc+32), up in [kOutN + cc, kOutN + cc + 32)
+                    // gate in columns [cc, cc+32), up in [up_off + cc, up_off + cc + 32): kOutN
+                    // columns on (M = 256), half that on an M = 128 tail tile
+                    const int up_off = half ? kOutN / 2 : kOutN;
                     uint32_t u[32];
-                    const bool ldu_ok = RGG_BOUNDS_OK(tmem_cols_ok(tcol + kOutN, 32, Cfg::kTmemCols), args.status);
-                    if (ldu_ok) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kOutN + cc), u);
+                    const bool ldu_ok = RGG_BOUNDS_OK(tmem_cols_ok(tcol + up_off, 32, Cfg::kTmemCols), args.status);
+                    if (ldu_ok) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(up_off + cc), u);
                     tmem_ld_wait();
                     if (!ldu_ok)
                         for (int i = 0; i < 32; ++i) u[i] = 0u;
