@@ -325,11 +325,13 @@ def test_gather_null_handle_is_rejected_without_touching_cuda(lib):
         assert s == rgg.RGG_ERR_INVALID_ARG
 
 
-def test_plan_fused_gate_up_takes_pairs_without_tails(lib):
-    # balanced large groups: CTA pairs, 256-row tail tiles (the 128-row pair
-    # tail layout would split gate and up across warps); BN = 192 is refused
+def test_plan_fused_gate_up_pair_tails(lib):
+    # balanced large groups: CTA pairs; 256-column pair tiles run tails of <= 128 rows as M = 128
+    # pair MMAs (each CTA loads 64 gate columns and their up columns), 128-column ones keep
+    # 256-row tails (a 64-column panel cannot hold both); BN = 192 is refused
     p = rgg.rgg_plan(32, 32768, 6144, 2048, op="swiglu")
-    assert p["bm"] == 256 and p["bn"] in (128, 256) and p["tail64"] == 0
+    assert p["bm"] == 256 and p["bn"] == 256 and p["tail64"] == 1
+    assert rgg.rgg_plan(32, 32768, 6144, 2048, op="swiglu", bm=256, bn=128)["tail64"] == 0
     assert rgg.rgg_plan(64, 16384, 1024, 1344, op="swiglu")["bm"] == 256
     assert rgg.rgg_plan(64, 16384, 1024, 2688, op="gemm", bm=256)["tail64"] == 1
     assert rgg.rgg_plan(32, 512, 6144, 2048, op="swiglu")["bm"] == 64
