@@ -745,8 +745,9 @@ def run_ours(args):
         "eager": eager,
         "ramp": t["ramp"], "clocks": t["clocks"], "configs": configs,
         "gpu_launches": launches,
-        "gpu_launches_note": "kernels of this library launched in the timed regions: the headline's K steps "
-                             "plus each side configuration's K steps", "impl": "ours",
+        "gpu_launches_note": "kernels of this library launched in the timed regions behind the values: the "
+                             "headline's K steps plus each side configuration's K steps (the graph_replay and "
+                             "eager figures beside them launch as many again each)", "impl": "ours",
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
