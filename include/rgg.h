@@ -31,7 +31,16 @@
  *
  * Streams: every launching call is asynchronous on the given stream (a
  * cudaStream_t passed as void*; NULL is the legacy default stream).
- * rgg_grouped_gemm allocates nothing per call.
+ * rgg_grouped_gemm allocates nothing per call.  The GEMM kernels are
+ * launched with programmatic stream serialisation: one may become resident
+ * while the kernel ahead of it on the stream still runs, and waits on the
+ * device for that kernel to complete before touching any memory, so the
+ * usual stream order holds for its inputs and outputs.  Each lets the next
+ * launch on the stream start early in turn: a caller's kernel launched after
+ * it with programmatic serialisation must wait on the device
+ * (cudaGridDependencySynchronize) before reading the output, as that launch
+ * mode requires anyway; copies and kernels launched the usual way follow
+ * completion as always.
  */
 #ifndef RGG_H
 #define RGG_H
