@@ -276,6 +276,12 @@ rgg_status make_plan(int num_sms, int smem_optin, int E, int64_t M_tot, int K, i
     int bm = want_bm;
     int bn = want_bn;
     if (bm == 0 && avg <= 64.0) bm = 64;
+    // 64-row tiles without host counts: 256 columns.  The balanced estimate
+    // of the tile count can tip the wave model to 192 columns, which streams
+    // the weights in more, smaller tiles (measured on the skewed 2k workload
+    // planned from the device offsets: 64 x 192 170 TFLOP/s, 64 x 256 184.5,
+    // the host-count plan 184.7; decode already takes 256).
+    if (bm == 64 && bn == 0 && want_bm == 0 && !(opt && opt->host_counts)) bn = 256;
     {
         double best = 1e300;
         int best_bm = bm, best_bn = bn;
